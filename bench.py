@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark: routed tokens/s of one pooled-wave MoE layer forward on GB300.
+
+One step = one whole forward of the layer (router top-k, latent projection,
+fixed pooled-wave dispatch with both capacity caps, grouped SwiGLU experts,
+combine + up-projection + shared experts) over one batch of T synthetic
+tokens of the full-width 535B-A23B layer (d=6144, L=3072, 384 experts on 64
+logical ranks, top-8, 2 shared experts).  Inputs and weights are resident in
+HBM when the timed region starts; the weights (8.1 GB) exceed L2, so no
+separate L2 flush is done.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (a
+bounded token sample of the same workload per step, on the host cores).
+Under torchrun each rank runs an independent replica on its own batch
+(weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_routing_capacity_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "routed tokens/sec per MoE layer on 1 GB300"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="full", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="tokens per oracle sample (0: sized automatically)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def source_hash():
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "moe_routing_capacity_gb300", "csrc")
+    for f in sorted(os.listdir(src)):
+        h.update(open(os.path.join(src, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def kernel_work(name, cfg, plan, st):
+    """Algorithmic work of one launch: (amount, unit, bound)."""
+    T, d, L, E, k = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.top_k
+    H, Hs, ns = cfg.h_expert, cfg.h_shared, cfg.n_shared
+    kept = st["kept"]
+    sent = st["kept"] + st["dropped_recv"]
+    F = {
+        "gemm_router": 2.0 * T * d * E,
+        "gemm_latent": 2.0 * T * d * L,
+        "gemm_expert_gateup": 2.0 * kept * L * 2 * H,
+        "gemm_expert_down": 2.0 * kept * H * L,
+        "gemm_shared_gateup": 2.0 * T * d * 2 * ns * Hs,
+        "gemm_out": 2.0 * T * (L + ns * Hs) * d,
+    }
+    if name in F:
+        return F[name] / 1e12, "TFLOP", "tensor"
+    B = {
+        "router_topk": T * E * 4 + T * k * 8 + T,
+        # each token's z row read once, every sender-kept row written with its tag,
+        # plus the per-assignment decisions
+        "dispatch_pack": T * L * 2 + sent * (2 * L + 16) + T * k * (4 + 8 + 4 + 4 + 1) + kept * 4,
+        "dispatch_init": plan.pool_rows * 16 + E * plan.c_recv * 4,
+        # every kept expert row read once, c written once, slots and weights read
+        "combine": kept * L * 2 + T * L * 2 + T * k * 8,
+    }
+    if name in B:
+        return B[name] / 1e9, "GB", "hbm"
+    return None, None, "latency"
+
+
+class ClockSampler:
+    """nvidia-smi samples while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.p = None
+        self.index = index
+        if enabled:
+            try:
+                self.p = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except (OSError, FileNotFoundError):
+                self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(f[0]), max=float(f[1]), power=float(f[2]),
+                                 hw=f[4], hwt=f[5], swt=f[6], swp=f[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, nm in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(nm)
+        loaded = [r["sm"] for r in rows if r["power"] > 300] or [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def oracle_inputs(cfg_full, inputs_dev, n_tokens):
+    """Host copies of the inputs for an oracle run on the first n_tokens of
+    the batch (a layer of the same widths with T = n_tokens), widened to the
+    oracle's float64 once, outside any timing."""
+    import numpy as np
+    S = cfg_full.n_ranks
+    n = max(S, (n_tokens // S) * S)
+    # float64 expert weights need 4x their bf16 size in host memory; with less
+    # than that available they stay float32 and the oracle widens per expert
+    wide = np.float64 if 5 * sum(v.numel() * 8 for k, v in inputs_dev.items()
+                                 if v is not None and v.dim() == 3) < mem_available() \
+        else np.float32
+    host = {}
+    for key, v in inputs_dev.items():
+        if v is None:
+            host[key] = None
+        elif key == "x":
+            host[key] = v[:n].double().cpu().numpy()
+        elif v.dim() == 3:
+            a = np.empty(tuple(v.shape), dtype=wide)
+            for e in range(v.shape[0]):
+                a[e] = v[e].double().cpu().numpy()
+            host[key] = a
+        else:
+            host[key] = v.double().cpu().numpy()
+    return cfg_full.with_(T=n), host
+
+
+def mem_available() -> int:
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def time_oracle(cfg, host):
+    import oracle as O
+    t0 = time.perf_counter()
+    O.layer(cfg, host)
+    return time.perf_counter() - t0
+
+
+def cores_used():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    cfg = wl.CONFIGS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.make_inputs(cfg, dev)
+    total = args.steps + args.warmup
+    n_tok = args.cpu_sample or (64 if total > 8 else 256)
+    scfg, host = oracle_inputs(cfg, inp, n_tok)
+    del inp
+    n = scfg.T
+    times = []
+    for i in range(total):
+        t = time_oracle(scfg, host)
+        if i >= args.warmup:
+            times.append(t)
+    sec = sum(times)
+    value = n * len(times) / sec
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} sampled to {n} tokens per step, d={cfg.d_model}, "
+                   f"L={cfg.d_latent}, E={cfg.n_experts}, ranks={cfg.n_ranks}, k={cfg.top_k}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{n} tokens per step (T={n} layer of the same widths), "
+                                   f"{len(times)} timed steps, float64 NumPy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, rank, world, local_rank):
+    from moe_routing_capacity_gb300 import abi
+    from moe_routing_capacity_gb300.layer import PooledWaveMoE
+
+    cfg = wl.CONFIGS[args.workload]
+    if world > 1:
+        cfg = cfg.with_(seed=cfg.seed + 1000 * rank)
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(cfg, dev)
+    m = PooledWaveMoE(cfg, inp, dev)
+    x = inp["x"]
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        m.forward(x)
+    torch.cuda.synchronize()
+    assert int(m.status.item()) == 0, "device status word set during warm-up"
+    st = m.drop_stats()
+
+    # ---- timed region: device-resident inputs
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
+    time.sleep(0.3 if not args.no_clocks else 0.0)
+    n_kern = 16
+    abi.trace_begin((n_kern + 1) * args.steps + 8)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        abi.trace_mark(stream)
+        m.forward(x)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    trace = abi.trace_end()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    assert int(m.status.item()) == 0, "device status word set during the timed region"
+    value = world * cfg.T * args.steps / elapsed
+
+    # ---- per-kernel times from the trace (event after each launch)
+    per = {}
+    for name, ms in trace:
+        if name == "mark":
+            continue
+        d = per.setdefault(name, [0.0, 0])
+        d[0] += ms
+        d[1] += 1
+    pk = peaks()
+    kernels = {}
+    for name, (ms, n) in sorted(per.items(), key=lambda kv: -kv[1][0]):
+        work, unit, bound = kernel_work(name, cfg, m.plan, st)
+        ms_l = ms / n
+        e = {"ms_per_launch": round(ms_l, 4), "launches": n,
+             "share": round(ms / max(1e-9, sum(v[0] for v in per.values())), 4)}
+        if work is not None:
+            ach = work / (ms_l / 1e3)
+            peak = pk["bf16_sustained"] if bound == "tensor" else pk["hbm"]
+            e.update({"work_per_launch": work, "unit": unit + "/s", "achieved": round(ach, 2),
+                      "frac": round(ach / (peak if unit == "TFLOP" else peak), 4)})
+        kernels[name] = e
+    top = next(iter(kernels))
+    twork, tunit, tbound = kernel_work(top, cfg, m.plan, st)
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        rec = json.load(open(tp)).get(top)
+        if rec and rec.get("source_hash") == source_hash() and rec.get("workload") == cfg.name:
+            traffic = rec.get("dram_bytes_per_launch")
+    if twork is not None:
+        ach = kernels[top]["achieved"]
+        peak = pk["bf16_sustained"] if tbound == "tensor" else pk["hbm"]
+        roof = {"kernel": top, "bound": tbound, "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s" if tbound == "tensor" else "GB/s",
+                "frac": round(ach / peak, 4), "traffic": traffic,
+                "peak_source": pk["source"] + (" sustained bf16" if tbound == "tensor" else " HBM copy")}
+    else:
+        roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None,
+                "unit": None, "frac": None, "traffic": traffic}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        oh = torch.empty_like(m.out, device="cpu").pin_memory()
+        sh = torch.empty_like(m.stats, device="cpu").pin_memory()
+        xd = torch.empty_like(x)
+        for _ in range(2):
+            xd.copy_(xh, non_blocking=True)
+            m.forward(xd)
+            oh.copy_(m.out, non_blocking=True)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 20))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            xd.copy_(xh, non_blocking=True)
+            m.forward(xd)
+            oh.copy_(m.out, non_blocking=True)
+            sh.copy_(m.stats, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        el = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([el], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            el = float(t.item())
+        e2e = {"value": world * cfg.T * n_e2e / el, "unit": UNIT,
+               "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+               "d2h_bytes_per_step": oh.numel() * oh.element_size() + sh.numel() * 8,
+               "steps": n_e2e}
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok = args.cpu_sample or 4096
+        scfg, host = oracle_inputs(cfg, inp, n_tok)
+        n = scfg.T
+        sec = time_oracle(scfg, host)
+        del host
+        cpu = {"value": n / sec, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+               "sample": f"first {n} tokens of the batch as a T={n} layer of the same widths "
+                         f"({n // cfg.n_ranks} per source rank), one float64 NumPy pass, "
+                         f"{sec:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: T={cfg.T} tokens ({cfg.n_seqs} x {cfg.T // max(1, cfg.n_seqs)}), "
+                       f"d={cfg.d_model}, L={cfg.d_latent}, E={cfg.n_experts} on {cfg.n_ranks} logical ranks, "
+                       f"top-{cfg.top_k}, {cfg.n_waves} waves, {cfg.n_shared} shared (Hs={cfg.h_shared}), "
+                       f"H={cfg.h_expert}, cf {cfg.cf_send}/{cfg.cf_recv}",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (8.1 GB weights per step)"},
+            "drops": {"kept": st["kept"], "dropped_send": st["dropped_send"],
+                      "dropped_recv": st["dropped_recv"],
+                      "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
+            "gpu_launches": sum(v[1] for v in per.values()),
+            "roofline": roof, "kernels": kernels, "clocks": clk, "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_gb300(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * moe_pooled_wave.h -- C ABI of the GB300 (sm_103a) pooled-wave MoE layer.
+ *
+ * One MoE branch forward as the Marin 535B-A23B pages state it (lamjinlab,
+ * "Marin 開始公開訓練 535B 參數 MoE 模型", section 二 "稀疏模型的組織方式", and
+ * its Japanese edition, section 二): a router picks k of E routed experts per
+ * token; a latent projection compresses the routed activations (6144 -> 3072)
+ * before the exchange; each source keeps one fixed pool per destination rank,
+ * sent in W same-shape waves with the expert id packed into the payload row;
+ * a sender capacity factor bounds one source -> one destination, a receiver
+ * capacity factor bounds the rows of one local expert, and any assignment
+ * that overflows either buffer is dropped and counted; each destination runs
+ * its local experts on what it received; the outputs return, are combined,
+ * projected back to model width and added to the shared experts, which see
+ * every token.
+ *
+ * On one GPU the S source ranks and D = S destination ranks are regions of
+ * device memory: the pool is laid out destination-major, so the sender's pool
+ * *is* the receiver's buffer and the exchange is the pack scatter (and the
+ * return path the combine gather).
+ *
+ * Conventions for every entry point
+ *  - All tensor arguments are DEVICE pointers owned by the caller, row-major,
+ *    16-byte aligned, non-overlapping unless stated.  bf16 tensors are passed
+ *    as uint16_t (IEEE bfloat16 bit patterns).  Weights are stored
+ *    out-features-major ([out, in], as torch.nn.Linear does).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    only enqueues work: it never synchronises the host and never allocates
+ *    or frees memory.  Scratch space is caller-provided (sizes from moe_plan).
+ *  - Return value: MOE_OK (0) or a negative MOE_E* code.  Host-side argument
+ *    checks run before anything is enqueued; on error nothing is enqueued.
+ *    With T = 0 (an empty batch) every call returns MOE_OK without touching
+ *    its tensor pointers, which may then be NULL (moe_dispatch_pooled still
+ *    writes expert_count and stats).
+ *  - `status` is a caller-owned device int32.  A kernel whose bounded wait on
+ *    an on-chip barrier runs out writes MOE_ETIMEOUT there (first error wins)
+ *    and returns early; its outputs are then undefined.  The library never
+ *    clears it: zero it once and read it when convenient.
+ *  - Results are deterministic: identical inputs give identical bits,
+ *    including pool slots and drop decisions.
+ */
+#ifndef MOE_POOLED_WAVE_H
+#define MOE_POOLED_WAVE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK        0
+#define MOE_EINVAL   -1   /* bad sizes, divisibility, alignment or null pointer      */
+#define MOE_ENOSPC   -2   /* caller-provided scratch smaller than moe_plan asks for   */
+#define MOE_ECUDA    -3   /* a CUDA runtime/driver call failed (launch, tensor map)   */
+#define MOE_ETIMEOUT -4   /* a device-side bounded wait ran out (written to status)   */
+#define MOE_ENODEV   -5   /* the current device is not sm_103 (GB300)                 */
+
+/* Layer sizes.  S = D = n_ranks logical ranks; T must divide by n_ranks,
+ * n_experts by n_ranks, and (n_experts / n_ranks) by n_waves.  d_model,
+ * d_latent, h_expert and h_shared must be multiples of 8 (16-byte rows).
+ * Capacity factors are read to six decimals; a factor >= 1e6 or an infinity
+ * means "no cap". */
+typedef struct moe_config {
+    int64_t T;            /* tokens in the batch (may be 0)                          */
+    int32_t d_model;      /* d: token state width (6144 in the pages)                */
+    int32_t d_latent;     /* L: latent width crossing the exchange (3072)            */
+    int32_t n_experts;    /* E: routed experts (384)                                 */
+    int32_t n_ranks;      /* S = D: logical expert-parallel ranks (64)               */
+    int32_t top_k;        /* k: experts per token (8)                                */
+    int32_t n_waves;      /* W: same-shape waves (3)                                 */
+    int32_t n_shared;     /* n_s: shared experts (2); 0 allowed                      */
+    int32_t h_expert;     /* H: routed SwiGLU hidden size                            */
+    int32_t h_shared;     /* Hs: shared SwiGLU hidden size per shared expert         */
+    int32_t reserved;     /* must be 0                                               */
+    double  cf_send;      /* sender capacity factor (1.10)                           */
+    double  cf_recv;      /* receiver capacity factor (1.15)                         */
+} moe_config_t;
+
+/* Derived sizes (host-only computation).
+ * c_send = ceil(cf_send * (T/S) * k / (D * W)): rows of one (source,
+ *   destination, wave) slice -- the uniform expected load of that slice times
+ *   the factor.  c_recv = ceil(cf_recv * T * k / E): rows of one expert.
+ *   Both are clamped to the most rows that can ever arrive
+ *   ((T/S) * min(k, E/D/W) and T).
+ * Pool row of (dst, wave, src, slot) = ((dst*W + wave)*S + src)*c_send + slot;
+ *   wave w of a destination carries its local experts [w*E_w, (w+1)*E_w),
+ *   E_w = E/D/W. */
+typedef struct moe_plan {
+    int64_t tokens_per_rank;     /* T_s = T / S                                      */
+    int32_t experts_per_rank;    /* E_l = E / D                                      */
+    int32_t experts_per_wave;    /* E_w = E_l / W                                    */
+    int32_t c_send;              /* rows per (src, dst, wave) slice                  */
+    int32_t c_recv;              /* rows per expert                                  */
+    int64_t pool_rows;           /* D * W * S * c_send                               */
+    int64_t pool_row_bytes;      /* 2*L + 16: L bf16 payload + 16-byte tag           */
+    int64_t ws_dispatch_bytes;   /* scratch for moe_dispatch_pooled                  */
+    int64_t ws_ffn_bytes;        /* scratch for moe_expert_ffn_grouped (incl. h)     */
+    int64_t h_offset_bytes;      /* where h [E, c_recv, H] bf16 sits in ws_ffn       */
+} moe_plan_t;
+
+/* Pool row tag (the 16 bytes after the L payload values of every pool row).
+ * Filled slot: {expert, token, top-k rank, 0}.  Empty slot: {-1, -1, -1, 0}. */
+typedef struct moe_row_tag {
+    int32_t expert;
+    int32_t token;
+    int32_t rank;
+    int32_t reserved;
+} moe_row_tag_t;
+
+/* Drop accounting, written by moe_dispatch_pooled (device memory). */
+typedef struct moe_drop_stats {
+    int64_t assignments;    /* T * k                                                 */
+    int64_t kept;           /* assignments that reach an expert                      */
+    int64_t dropped_send;   /* over the (src, dst, wave) slice capacity              */
+    int64_t dropped_recv;   /* sender-kept but over the expert's capacity            */
+    int32_t max_send_fill;  /* fullest (src, dst, wave) slice, rows                  */
+    int32_t max_expert_rows;/* fullest expert, rows                                  */
+    int32_t status;         /* MOE_OK or a device-side error code                    */
+    int32_t reserved;
+} moe_drop_stats_t;
+
+/* Sizes and scratch requirements; checks the config.  Host only. */
+int moe_plan(const moe_config_t* cfg, moe_plan_t* plan);
+
+/* Router: logits = x Wr^T (+ bias), then per token the k largest logits
+ * (descending; equal logits -> lower expert id first), gate weights = softmax
+ * over the k selected logits, and a near-tie flag.
+ *   x      [T, d] bf16        Wr [E, d] bf16        bias [E] fp32 or NULL
+ *   logits [T, E] fp32 (out)  idx [T, k] int32 (out)  w [T, k] fp32 (out)
+ *   tie    [T] uint8 (out): bit 0 = k-th and (k+1)-th logits closer than
+ *          float(1e-4); bit 1 = two adjacent selected logits closer than that.
+ * Source: lamjinlab zh-HK section 二 (eight experts per token); the bias is
+ * the quantile-balancing bias added to the router logits (devpress.csdn.net,
+ * appendix A.2).  Tensor cores: tcgen05 GEMM; top-k: one warp per token. */
+int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* Wr,
+                    const float* bias, float* logits, int32_t* idx, float* w,
+                    uint8_t* tie, int32_t* status, void* stream);
+
+/* Dense projection out[M, N] = bf16(in[M, K] W[N, K]^T), fp32 accumulation.
+ * Used for the latent down-projection z = x W_ld^T (lamjinlab zh-HK section
+ * 二: 6144 -> 3072 before the exchange).  K and N multiples of 8. */
+int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K, int32_t N,
+                    uint16_t* out, int32_t* status, void* stream);
+
+/* Fixed pooled-wave dispatch (lamjinlab zh-HK section 二: one fixed pool per
+ * destination, W same-shape waves, expert id in the payload row, the two
+ * capacity factors, drops counted separately).  Priority: token ascending,
+ * then top-k rank ascending.  Sender stage per (src, dst, wave) slice, then
+ * receiver stage per expert over the sender-kept rows in the same order.
+ *   z           [T, L] bf16      idx [T, k] int32 (each row: distinct experts)
+ *   ws          scratch, >= plan.ws_dispatch_bytes
+ *   pool        [pool_rows, L + 8] uint16: payload z[t] for every
+ *               sender-kept assignment, tag (moe_row_tag_t) on every row
+ *   slot_of     [T, k] int32: pool row of a kept assignment, else -1
+ *   drop        [T, k] uint8: 0 kept, 1 dropped by the sender cap,
+ *               2 dropped by the receiver cap
+ *   expert_rows [E, c_recv] int32: pool rows of expert e in arrival order,
+ *               -1 after expert_count[e]
+ *   expert_count[E] int32        stats: moe_drop_stats_t (device)
+ * Out-of-range expert ids in idx give MOE_EINVAL in stats->status and leave
+ * the outputs undefined. */
+int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                        void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
+                        uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
+                        moe_drop_stats_t* stats, void* stream);
+
+/* Grouped SwiGLU experts on the received rows: for expert e and r <
+ * expert_count[e], with X = payload of pool row expert_rows[e][r]:
+ *   h = bf16(silu(X Wg_e^T) * (X Wu_e^T)),  Y = bf16(h Wd_e^T)
+ * and Y is written to ypool at that same pool row (the return path keeps the
+ * slot).  Rows of ypool that no expert computes are left untouched.
+ *   Wg, Wu [E, H, L] bf16     Wd [E, L, H] bf16     ypool [pool_rows, L] bf16
+ *   ws     scratch, >= plan.ws_ffn_bytes (holds h at plan.h_offset_bytes)
+ * The pages give each receiver its local experts (section 二) but no
+ * activation; the SwiGLU form and the hidden size are the workload's. */
+int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
+                           const int32_t* expert_rows, const int32_t* expert_count,
+                           const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                           void* ws, size_t ws_bytes, uint16_t* ypool, int32_t* status,
+                           void* stream);
+
+/* Return path, weighted combine, up-projection and shared experts:
+ *   c[t]   = bf16(sum over kept j, in j order, of w[t,j] * ypool[slot_of[t,j]])
+ *   a      = bf16(silu(x Wsg_s^T) * (x Wsu_s^T)) for each shared expert s,
+ *            concatenated along the hidden axis: [T, n_s*Hs]
+ *   out    = bf16(c W_lu^T + sum_s a_s Wsd_s^T)     (fp32 accumulation)
+ * Dropped assignments contribute nothing and weights are not renormalised;
+ * the shared experts see every token (lamjinlab zh-HK sections 二 and 四).
+ *   ypool [pool_rows, L]  slot_of [T, k]  w [T, k] fp32  W_lu [d, L]  x [T, d]
+ *   Wsg, Wsu [n_s, Hs, d]  Wsd [n_s, d, Hs]
+ *   c [T, L] bf16 (out)  a [T, n_s*Hs] bf16 (out)  out [T, d] bf16 (out) */
+int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* slot_of,
+                const float* w, const uint16_t* W_lu, const uint16_t* x,
+                const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
+                uint16_t* c, uint16_t* a, uint16_t* out, int32_t* status, void* stream);
+
+/* Kernel timing trace (instrumentation; the pages define no such operation).
+ * moe_trace_begin(n) creates n CUDA events (timing enabled) owned by the
+ *   library and turns tracing on; from then on every kernel the library
+ *   launches is followed by a cudaEventRecord of the next event on the same
+ *   stream, until n events are used.  n = 0 frees the events.  Host only,
+ *   process-wide; do not trace while capturing a CUDA graph.
+ * moe_trace_mark(stream) records the next event with the name "mark".
+ * moe_trace_end() turns tracing off and returns the number of events used.
+ * moe_trace_event(i, &name, &ms) waits for event i and returns the name of
+ *   the kernel it follows and the milliseconds since event i-1 (0 for i=0).
+ *   name points to a static string. */
+int moe_trace_begin(int n);
+int moe_trace_mark(void* stream);
+int moe_trace_end(void);
+int moe_trace_event(int i, const char** name, float* ms_since_prev);
+
+/* Human-readable name of a MOE_* code (static string). */
+const char* moe_strerror(int code);
+
+/* ABI version: 1. */
+int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_POOLED_WAVE_H */

@@ -1,0 +1,207 @@
+"""ctypes binding of ``libmoe_pooled_wave.so`` (the C ABI in
+``include/moe_pooled_wave.h``).
+
+Argument marshalling only: each function takes torch tensors, checks dtype,
+device and contiguity, and passes raw pointers, sizes and the current CUDA
+stream to the C entry point of the same name.  Every step of the layer runs
+in the library's kernels; if the library is missing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_pooled_wave.so")
+
+MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2, -3, -4, -5
+
+# Every entry point the header declares (checked by the tests).
+EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_dispatch_pooled",
+           "moe_expert_ffn_grouped", "moe_combine", "moe_trace_begin", "moe_trace_mark",
+           "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d_model", ctypes.c_int32), ("d_latent", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("n_ranks", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("n_waves", ctypes.c_int32),
+                ("n_shared", ctypes.c_int32), ("h_expert", ctypes.c_int32),
+                ("h_shared", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("cf_send", ctypes.c_double), ("cf_recv", ctypes.c_double)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("tokens_per_rank", ctypes.c_int64), ("experts_per_rank", ctypes.c_int32),
+                ("experts_per_wave", ctypes.c_int32), ("c_send", ctypes.c_int32),
+                ("c_recv", ctypes.c_int32), ("pool_rows", ctypes.c_int64),
+                ("pool_row_bytes", ctypes.c_int64), ("ws_dispatch_bytes", ctypes.c_int64),
+                ("ws_ffn_bytes", ctypes.c_int64), ("h_offset_bytes", ctypes.c_int64)]
+
+
+class DropStats(ctypes.Structure):
+    _fields_ = [("assignments", ctypes.c_int64), ("kept", ctypes.c_int64),
+                ("dropped_send", ctypes.c_int64), ("dropped_recv", ctypes.c_int64),
+                ("max_send_fill", ctypes.c_int32), ("max_expert_rows", ctypes.c_int32),
+                ("status", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+STATS_WORDS = ctypes.sizeof(DropStats) // 8    # int64 words of a stats record
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m moe_routing_capacity_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        pc = ctypes.POINTER(Config)
+        L.moe_plan.argtypes = [pc, ctypes.POINTER(Plan)]
+        L.moe_router_topk.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_latent_proj.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp]
+        L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+        L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_strerror.argtypes = [ctypes.c_int]
+        L.moe_strerror.restype = ctypes.c_char_p
+        L.moe_abi_version.argtypes = []
+        L.moe_trace_begin.argtypes = [ctypes.c_int]
+        L.moe_trace_mark.argtypes = [vp]
+        L.moe_trace_end.argtypes = []
+        L.moe_trace_event.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                      ctypes.POINTER(ctypes.c_float)]
+        for n in EXPORTS:
+            if n != "moe_strerror":
+                getattr(L, n).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().moe_strerror(code).decode()
+
+
+def make_config(cfg) -> Config:
+    """C config from any object with the layer-size attributes."""
+    return Config(cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.n_ranks, cfg.top_k,
+                  cfg.n_waves, cfg.n_shared, cfg.h_expert, cfg.h_shared, 0,
+                  float(cfg.cf_send), float(cfg.cf_recv))
+
+
+def plan(cfg) -> Plan:
+    p = Plan()
+    rc = lib().moe_plan(ctypes.byref(make_config(cfg)), ctypes.byref(p))
+    if rc:
+        raise MoeError("moe_plan", rc)
+    return p
+
+
+def _ptr(t, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError("tensor required")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError("tensors must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc:
+        raise MoeError(fn, rc)
+
+
+bf16, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+
+def router_topk(cfg, x, Wr, bias, logits, idx, w, tie, status, stream=None):
+    _check("moe_router_topk", lib().moe_router_topk(
+        ctypes.byref(make_config(cfg)), _ptr(x, bf16), _ptr(Wr, bf16),
+        _ptr(bias, f32, allow_none=True), _ptr(logits, f32), _ptr(idx, i32), _ptr(w, f32),
+        _ptr(tie, u8), _ptr(status, i32), _stream(stream)))
+
+
+def latent_proj(inp, W, out, status, stream=None):
+    M, K = inp.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(out.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _check("moe_latent_proj", lib().moe_latent_proj(
+        _ptr(inp, bf16), _ptr(W, bf16), M, K, N, _ptr(out, bf16), _ptr(status, i32),
+        _stream(stream)))
+
+
+def dispatch_pooled(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
+                    stream=None):
+    _check("moe_dispatch_pooled", lib().moe_dispatch_pooled(
+        ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
+        ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
+        _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(stats, torch.int64),
+        _stream(stream)))
+
+
+def expert_ffn_grouped(cfg, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ypool, status,
+                       stream=None):
+    _check("moe_expert_ffn_grouped", lib().moe_expert_ffn_grouped(
+        ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16), _ptr(expert_rows, i32),
+        _ptr(expert_count, i32), _ptr(Wg, bf16), _ptr(Wu, bf16), _ptr(Wd, bf16),
+        _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32), _stream(stream)))
+
+
+def combine(cfg, ypool, slot_of, w, W_lu, x, Wsg, Wsu, Wsd, c, a, out, status, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        ctypes.byref(make_config(cfg)), _ptr(ypool, bf16), _ptr(slot_of, i32), _ptr(w, f32),
+        _ptr(W_lu, bf16), _ptr(x, bf16), _ptr(Wsg, bf16), _ptr(Wsu, bf16), _ptr(Wsd, bf16),
+        _ptr(c, bf16), _ptr(a, bf16, allow_none=True), _ptr(out, bf16), _ptr(status, i32),
+        _stream(stream)))
+
+
+def stats_dict(stats_tensor) -> dict:
+    """Decode a moe_drop_stats_t record held in an int64 tensor of STATS_WORDS."""
+    raw = bytes(stats_tensor.detach().cpu().numpy().tobytes())
+    s = DropStats.from_buffer_copy(raw)
+    return {f: getattr(s, f) for f, _ in DropStats._fields_}
+
+
+# ---------------------------------------------------------------- timing trace
+
+def trace_begin(n: int):
+    _check("moe_trace_begin", lib().moe_trace_begin(n))
+
+
+def trace_mark(stream=None):
+    _check("moe_trace_mark", lib().moe_trace_mark(_stream(stream)))
+
+
+def trace_end() -> list:
+    """Stop tracing; return [(kernel name, ms since the previous event)]."""
+    n = lib().moe_trace_end()
+    out = []
+    name = ctypes.c_char_p()
+    ms = ctypes.c_float()
+    for i in range(n):
+        _check("moe_trace_event", lib().moe_trace_event(i, ctypes.byref(name), ctypes.byref(ms)))
+        out.append((name.value.decode(), float(ms.value)))
+    return out

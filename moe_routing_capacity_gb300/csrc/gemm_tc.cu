@@ -1,0 +1,541 @@
+// gemm_tc.cu -- the layer's dense contractions on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in TMEM, operands staged in shared memory
+// by TMA or, for gathered expert rows, by cp.async).
+//
+// One persistent kernel template serves every contraction of the layer:
+//   router logits      x [T,d] . Wr [E,d]^T               -> fp32 (+ bias)
+//   latent down-proj   x [T,d] . W_ld [L,d]^T             -> bf16 z
+//   shared gate/up     x [T,d] . [Wsg | Wsu]^T            -> bf16 silu(g)*u
+//   up-proj + shared   [c | a_0 | a_1] . [W_lu | Wsd_0 | Wsd_1]^T -> bf16 out
+//   expert gate/up     pool rows of expert e (gathered) . [Wg_e | Wu_e]^T -> h_e
+//   expert down        h_e . Wd_e^T  -> Y, scattered back to the pool rows
+//
+// CTA = 128 x BN output tile, K in blocks of 64 (one 128-byte swizzle row).
+// Warp roles: warp 0 issues TMA loads (one elected lane), warp 1 issues
+// tcgen05.mma (one lane), warp 2 owns the TMEM allocation, warps 4-7 run the
+// epilogue (warp 4+q reads TMEM lanes 32q..32q+31), and for gathered A
+// warps 8-11 copy one A row each with cp.async.  Two TMEM accumulators let the
+// epilogue of tile i overlap the main loop of tile i+1.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
+
+template <int BN>
+struct TileCfg {
+    static constexpr int B_STAGE_BYTES = BN * BK * 2;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES =
+        1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + BAR_BYTES;
+};
+
+struct KParams {
+    CUtensorMap mapA[4];
+    CUtensorMap mapB[4];
+    CUtensorMap mapBup;
+    int nseg;
+    int seg_kb[5];          // k-block prefix over segments
+    long long M;
+    int N;
+    int K0;                 // K of segment 0 (gather bound)
+    int n_tiles_n;
+    int m_tiles;            // dense tile rows
+    const int2* tile_list;
+    const int* tile_count;
+    const int* rowmap;
+    const int* counts;
+    int rowmap_ld;
+    const uint16_t* gather_src;
+    long long gather_pitch;
+    void* out;
+    long long ldo;
+    long long out_gstride;
+    const float* bias;
+    int* status;
+};
+
+template <int AMODE>
+__device__ __forceinline__ int num_tiles(const KParams& p) {
+    if (AMODE == A_DENSE) return p.m_tiles * p.n_tiles_n;
+    return (*reinterpret_cast<const volatile int*>(p.tile_count)) * p.n_tiles_n;
+}
+
+template <int AMODE>
+__device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& m0, int& nb) {
+    const int entry = tile / p.n_tiles_n;
+    nb = tile - entry * p.n_tiles_n;
+    if (AMODE == A_DENSE) {
+        g = 0;
+        m0 = entry * BM;
+    } else {
+        const int2 te = p.tile_list[entry];
+        g = te.x;
+        m0 = te.y;
+    }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+template <int BN, int AMODE, int EPI>
+__global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
+    gemm_tc_kernel(const __grid_constant__ KParams p) {
+    using C = TileCfg<BN>;
+    constexpr int STAGES = C::STAGES;
+    constexpr bool B3D = (AMODE != A_DENSE);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sbase = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sA = sbase;
+    uint8_t* sB = sbase + STAGES * A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], AMODE == A_GATHER ? 1 + 128 : 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < p.nseg; ++s) {
+            tma_prefetch_map(&p.mapB[s]);
+            if (AMODE != A_GATHER) tma_prefetch_map(&p.mapA[s]);
+        }
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int kb_total = p.seg_kb[p.nseg];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const int ntiles = num_tiles<AMODE>(p);
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed = 0;        // stages ever armed (bit mask)
+            uint32_t last_par = 0;     // parity of each stage's last armed phase
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                int g, m0, nb;
+                decode_tile<AMODE>(p, tile, g, m0, nb);
+                int seg = 0;
+                for (int kb = 0; kb < kb_total; ++kb) {
+                    while (kb >= p.seg_kb[seg + 1]) ++seg;
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const int kx = (kb - p.seg_kb[seg]) * BK;
+                    const uint32_t a_dst = smem_u32(sA + stage * A_STAGE_BYTES);
+                    const uint32_t b_dst = smem_u32(sB + stage * C::B_STAGE_BYTES);
+                    const uint32_t bytes =
+                        C::B_STAGE_BYTES + (AMODE == A_GATHER ? 0u : (uint32_t)A_STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    armed |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (AMODE == A_DENSE) tma_load_2d(a_dst, &p.mapA[seg], &full[stage], kx, m0);
+                    if (AMODE == A_GROUPED)
+                        tma_load_3d(a_dst, &p.mapA[seg], &full[stage], kx, m0, g);
+                    if (EPI == EPI_SWIGLU) {
+                        const int n_half = nb * (BN / 2);
+                        const uint32_t b_dst2 = b_dst + (BN / 2) * BK * 2;
+                        if (B3D) {
+                            tma_load_3d(b_dst, &p.mapB[0], &full[stage], kx, n_half, g);
+                            tma_load_3d(b_dst2, &p.mapBup, &full[stage], kx, n_half, g);
+                        } else {
+                            tma_load_2d(b_dst, &p.mapB[0], &full[stage], kx, n_half);
+                            tma_load_2d(b_dst2, &p.mapBup, &full[stage], kx, n_half);
+                        }
+                    } else {
+                        if (B3D)
+                            tma_load_3d(b_dst, &p.mapB[seg], &full[stage], kx, nb * BN, g);
+                        else
+                            tma_load_2d(b_dst, &p.mapB[seg], &full[stage], kx, nb * BN);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok || *abort_flag) {
+                // Unwinding: let every armed load land before the CTA exits.
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed >> s & 1u) {
+                        volatile int no_abort = 0;
+                        mbar_wait(&full[s], (last_par >> s) & 1u, &no_abort, nullptr,
+                                  20000000ull);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const int ntiles = num_tiles<AMODE>(p);
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            uint32_t stage = 0, phase = 0;
+            uint32_t acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < kb_total; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_k_sw128(smem_u32(sA + stage * A_STAGE_BYTES));
+                    const uint64_t bd = sdesc_k_sw128(smem_u32(sB + stage * C::B_STAGE_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                                 (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // Every MMA this CTA issued must finish before TMEM is released.
+            mma_commit(done);
+            volatile int no_abort = 0;
+            mbar_wait(done, 0, &no_abort, p.status);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp - 4;
+        const int r_local = q * 32 + lane;
+        const int ntiles = num_tiles<AMODE>(p);
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            int g, m0, nb;
+            decode_tile<AMODE>(p, tile, g, m0, nb);
+            if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+            const int m = m0 + r_local;
+            bool row_ok;
+            long long orow;
+            if (AMODE == A_DENSE) {
+                row_ok = m < p.M;
+                orow = m;
+            } else {
+                row_ok = m < p.counts[g];
+                orow = m;
+                if (EPI == EPI_SCATTER && row_ok)
+                    orow = p.rowmap[static_cast<long long>(g) * p.rowmap_ld + m];
+            }
+            if (EPI == EPI_F32) {
+                float* out = reinterpret_cast<float*>(p.out) + orow * p.ldo;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + c * 32, r);
+                    const int col0 = nb * BN + c * 32;
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int col = col0 + i;
+                            if (col < p.N) {
+                                float v = __uint_as_float(r[i]);
+                                if (p.bias) v += p.bias[col];
+                                out[col] = v;
+                            }
+                        }
+                    }
+                }
+            } else if (EPI == EPI_SWIGLU) {
+                uint16_t* out = reinterpret_cast<uint16_t*>(p.out) +
+                                static_cast<long long>(g) * p.out_gstride + orow * p.ldo;
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld32(tl + c * 32, gr);
+                    tmem_ld32(tl + BN / 2 + c * 32, ur);
+                    const int col0 = nb * (BN / 2) + c * 32;
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float h0 = silu_f(__uint_as_float(gr[2 * i])) *
+                                             __uint_as_float(ur[2 * i]);
+                            const float h1 = silu_f(__uint_as_float(gr[2 * i + 1])) *
+                                             __uint_as_float(ur[2 * i + 1]);
+                            pk[i] = pack_bf16x2(h0, h1);
+                        }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (col0 + 8 * v < p.N)
+                                *reinterpret_cast<uint4*>(out + col0 + 8 * v) =
+                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                               pk[4 * v + 3]);
+                    }
+                }
+            } else {   // EPI_BF16 / EPI_SCATTER
+                uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + orow * p.ldo;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + c * 32, r);
+                    const int col0 = nb * BN + c * 32;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + 8 * v < p.N) {
+                                const uint4 pk = make_uint4(
+                                    pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                                    pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                    pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                    pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+                                *reinterpret_cast<uint4*>(out + col0 + 8 * v) = pk;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    } else if (AMODE == A_GATHER && warp >= 8) {
+        // ------------------------------------------------------------ row gather (A)
+        constexpr int LAG = STAGES - 2;     // k-blocks in flight per thread
+        const int r = threadIdx.x - 256;    // tile row owned by this thread
+        const int ntiles = num_tiles<AMODE>(p);
+        uint32_t stage = 0, phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            int g, m0, nb;
+            decode_tile<AMODE>(p, tile, g, m0, nb);
+            const int m = m0 + r;
+            const bool valid = m < p.counts[g];
+            const uint16_t* src =
+                p.gather_src +
+                (valid ? static_cast<long long>(p.rowmap[static_cast<long long>(g) * p.rowmap_ld + m]) *
+                             p.gather_pitch
+                       : 0ll);
+            for (int kb = 0; kb < kb_total; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = smem_u32(sA + stage * A_STAGE_BYTES) + r * 128;
+                const int k0 = kb * BK;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int kc = k0 + c * 8;
+                    const uint32_t nbytes = (valid && kc < p.K0) ? 16u : 0u;
+                    cp_async_16(dst + ((c ^ (r & 7)) << 4), src + (nbytes ? kc : 0), nbytes);
+                }
+                cp_async_commit();
+                if (it >= LAG) {
+                    cp_async_wait<LAG>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[(it - LAG) % STAGES]);
+                }
+                ++it;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (int i = (it > LAG ? it - LAG : 0); i < it; ++i) mbar_arrive(&full[i % STAGES]);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ==================================================================== host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle, box {64, box_rows[, 1]}; out-of-range
+// elements read as zero.  dims/strides in elements (innermost first).
+static int make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_el, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return MOE_ECUDA;
+    cuuint64_t gdim[3], gstr[2];
+    cuuint32_t box[3], est[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) gdim[i] = dims[i];
+    for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_el[i] * 2;
+    box[0] = BK;
+    box[1] = box_rows;
+    box[2] = 1;
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstr,
+                     box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
+}
+
+static int map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld,
+                 uint32_t box_rows) {
+    const uint64_t dims[2] = {cols, rows};
+    const uint64_t str[1] = {ld};
+    return make_map(m, base, 2, dims, str, box_rows);
+}
+
+static int map3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t groups,
+                 uint64_t ld, uint64_t gstride, uint32_t box_rows) {
+    const uint64_t dims[3] = {cols, rows, groups};
+    const uint64_t str[2] = {ld, gstride};
+    return make_map(m, base, 3, dims, str, box_rows);
+}
+
+template <int BN, int AMODE, int EPI>
+static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
+    using C = TileCfg<BN>;
+    auto kern = gemm_tc_kernel<BN, AMODE, EPI>;
+    // Attribute setting is per device; cheap and idempotent, done every launch.
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+        return MOE_ECUDA;
+    kern<<<grid, AMODE == A_GATHER ? 384 : 256, C::SMEM_BYTES, st>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
+
+template <int BN, int AMODE, int EPI>
+static int launch_traced(const KParams& p, int grid, cudaStream_t st, const char* name) {
+    const int rc = launch_inst<BN, AMODE, EPI>(p, grid, st);
+    if (rc == MOE_OK) trace_after(st, name ? name : "gemm");
+    return rc;
+}
+
+int gemm_launch(const GemmDesc& d, cudaStream_t st) {
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    if (d.nseg < 1 || d.nseg > 4 || (d.bn != 128 && d.bn != 256)) return MOE_EINVAL;
+
+    KParams p;
+    std::memset(&p, 0, sizeof(p));
+    const uint32_t b_box = (d.epi == EPI_SWIGLU) ? d.bn / 2 : d.bn;
+    p.nseg = d.nseg;
+    p.seg_kb[0] = 0;
+    for (int s = 0; s < d.nseg; ++s) {
+        const GemmSeg& g = d.seg[s];
+        if (g.K <= 0 || (g.K % 8)) return MOE_EINVAL;
+        p.seg_kb[s + 1] = p.seg_kb[s] + (g.K + BK - 1) / BK;
+        if (d.a_mode == A_DENSE) {
+            if ((rc = map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM))) return rc;
+            if ((rc = map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box))) return rc;
+        } else {
+            if (d.a_mode == A_GROUPED &&
+                (rc = map3d(&p.mapA[s], g.A, g.K, d.rows_per_group, d.groups, g.lda, d.a_gstride,
+                            BM)))
+                return rc;
+            if ((rc = map3d(&p.mapB[s], g.B, g.K, d.b_rows, d.groups, g.ldb, d.b_gstride, b_box)))
+                return rc;
+        }
+    }
+    if (d.epi == EPI_SWIGLU) {
+        if (d.nseg != 1 || !d.B_up) return MOE_EINVAL;
+        if (d.a_mode == A_DENSE)
+            rc = map2d(&p.mapBup, d.B_up, d.seg[0].K, d.b_rows, d.seg[0].ldb, b_box);
+        else
+            rc = map3d(&p.mapBup, d.B_up, d.seg[0].K, d.b_rows, d.groups, d.seg[0].ldb,
+                       d.b_gstride, b_box);
+        if (rc) return rc;
+    }
+    p.M = d.M;
+    p.N = d.N;
+    p.K0 = d.seg[0].K;
+    const int n_per_tile = (d.epi == EPI_SWIGLU) ? d.bn / 2 : d.bn;
+    p.n_tiles_n = (d.N + n_per_tile - 1) / n_per_tile;
+    p.m_tiles = static_cast<int>((d.M + BM - 1) / BM);
+    p.tile_list = reinterpret_cast<const int2*>(d.tile_list);
+    p.tile_count = d.tile_count;
+    p.rowmap = d.rowmap;
+    p.counts = d.counts;
+    p.rowmap_ld = d.rowmap_ld;
+    p.gather_src = d.gather_src;
+    p.gather_pitch = d.gather_pitch;
+    p.out = d.out;
+    p.ldo = d.ldo;
+    p.out_gstride = d.out_gstride;
+    p.bias = d.bias;
+    p.status = d.status;
+
+    int tiles = (d.a_mode == A_DENSE) ? p.m_tiles * p.n_tiles_n : d.max_tiles * p.n_tiles_n;
+    if (tiles <= 0) return MOE_OK;
+    const int grid = tiles < sms ? tiles : sms;
+
+    const int key = d.bn * 100 + d.a_mode * 10 + d.epi;
+    switch (key) {
+        case 128 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<128, A_DENSE, EPI_F32>(p, grid, st, d.name);
+        case 256 * 100 + A_DENSE * 10 + EPI_BF16: return launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
+        case 256 * 100 + A_DENSE * 10 + EPI_SWIGLU: return launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
+        case 256 * 100 + A_GATHER * 10 + EPI_SWIGLU: return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);
+        case 256 * 100 + A_GROUPED * 10 + EPI_SCATTER: return launch_traced<256, A_GROUPED, EPI_SCATTER>(p, grid, st, d.name);
+        default: return MOE_EINVAL;
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,113 @@
+// internal.h -- host-side interfaces between the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_pooled_wave.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- device
+
+// Checks that the current device is an sm_103 part and returns its SM count.
+int current_device(int* device, int* num_sms);
+
+// Kernel timing trace: after each launch the library calls trace_after(),
+// which records the next trace event on that stream when tracing is on.
+void trace_after(cudaStream_t stream, const char* kernel_name);
+
+// ---------------------------------------------------------------- GEMM engine
+
+enum AMode : int {
+    A_DENSE = 0,    // A [M, K] row-major, TMA 2D tiles
+    A_GROUPED = 1,  // A [G, rows, K], TMA 3D tiles (group = expert)
+    A_GATHER = 2,   // A rows gathered by index from a pitched row store (cp.async)
+};
+
+enum EpiMode : int {
+    EPI_F32 = 0,      // fp32 out (+ optional per-column bias)
+    EPI_BF16 = 1,     // bf16 out
+    EPI_SWIGLU = 2,   // accumulator = [gate | up] halves -> bf16(silu(gate) * up)
+    EPI_SCATTER = 3,  // bf16 out to rows given by a row map
+};
+
+struct GemmSeg {        // one K segment of the contraction: A_s [M, K_s] . B_s [N, K_s]^T
+    const void* A;      // bf16
+    int64_t lda;        // elements between A rows
+    const void* B;      // bf16
+    int64_t ldb;        // elements between B rows
+    int K;
+};
+
+// out = sum_s A_s B_s^T with one of the epilogues above.  For EPI_SWIGLU the
+// B operand of segment 0 is the gate weight and B_up the up weight (same
+// shape); N then counts hidden units.  Grouped modes take the tile list
+// (int2 {group, m0}) and its length from device memory.
+struct GemmDesc {
+    int a_mode;
+    int epi;
+    int bn;                 // 128 or 256
+    int64_t M;              // dense: rows of A/out
+    int N;                  // output columns (hidden units for SWIGLU)
+    int nseg;
+    GemmSeg seg[4];
+    const void* B_up;
+    // grouped geometry
+    int groups;
+    int rows_per_group;     // rows of one group in a grouped A / in the row map
+    int64_t a_gstride;      // elements between groups of A (A_GROUPED)
+    int64_t b_gstride;      // elements between groups of B (and B_up)
+    int b_rows;             // rows of one group's B (N extent of the weight)
+    const int32_t* tile_list;
+    const int32_t* tile_count;
+    int max_tiles;          // upper bound of the tile list length
+    const int32_t* rowmap;  // [groups, rowmap_ld]
+    const int32_t* counts;  // [groups]
+    int rowmap_ld;
+    const uint16_t* gather_src;
+    int64_t gather_pitch;   // elements between gathered rows
+    int64_t gather_rows;    // rows in the gather source
+    // epilogue
+    void* out;
+    int64_t ldo;
+    int64_t out_gstride;    // elements between groups of out (grouped SWIGLU)
+    const float* bias;
+    int32_t* status;
+    const char* name;       // kernel name for the timing trace
+};
+
+int gemm_launch(const GemmDesc& d, cudaStream_t stream);
+
+// ---------------------------------------------------------------- routing kernels
+
+int launch_topk(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
+                uint8_t* tie, cudaStream_t stream);
+
+struct DispatchGeom {
+    int64_t T;
+    int k, E, S, D, W, E_l, E_w, L;
+    int64_t T_s;
+    int c_send, c_recv;
+    int64_t pool_rows;
+};
+
+// Scratch layout of moe_dispatch_pooled.
+struct DispatchWs {
+    size_t send_row_off, rloc_off, cnt_se_off, base_se_off, demand_off, total;
+};
+DispatchWs dispatch_ws_layout(const DispatchGeom& g);
+
+int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
+                    uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
+                    int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream);
+
+// Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
+int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
+                       int32_t* tile_count, cudaStream_t stream);
+
+int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
+                   int L, uint16_t* c, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,513 @@
+// route.cu -- the bandwidth- and latency-bound steps of the layer:
+//   router top-k        one warp per token, warp-shuffle arg-max rounds
+//   dispatch            sender slots and receiver ranks (warp-aggregated
+//                       counting, deterministic prefix sums), drops counted,
+//                       payload rows packed into the fixed pools
+//   combine             the return gather: per token, weighted sum of its
+//                       kept expert rows
+//   tile list           {expert, m0} work items of the grouped expert GEMMs
+#include <climits>
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ==================================================================== top-k
+
+constexpr float kTieEps = 1e-4f;
+
+template <int PER>   // logits per lane: E <= 32 * PER
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int64_t T,
+                                                   int E, int k, int32_t* __restrict__ idx,
+                                                   float* __restrict__ w,
+                                                   uint8_t* __restrict__ tie) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float* row = logits + t * E;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(row + e) : 0.0f;
+    }
+    uint32_t live = 0;   // bit i: entry i still a candidate
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        if (lane + 32 * i < E) live |= 1u << i;
+
+    float my_v = 0.0f;   // lane j keeps round j's winner
+    int my_e = 0;
+    float next_v = 0.0f; // the (k+1)-th largest logit
+    const int rounds = k < E ? k + 1 : k;
+    for (int rd = 0; rd < rounds; ++rd) {
+        // best live entry of this lane: largest value, lowest expert id on ties
+        float bv = -INFINITY;
+        int be = INT_MAX;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if ((live >> i & 1u) && (bi < 0 || v[i] > bv)) {
+                bv = v[i];
+                be = lane + 32 * i;
+                bi = i;
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (rd < k) {
+            if (lane == rd) {
+                my_v = bv;
+                my_e = be;
+            }
+            if ((be & 31) == lane) live &= ~(1u << (be >> 5));
+        } else {
+            next_v = bv;
+        }
+    }
+    // softmax over the selected logits (lane 0 holds the largest)
+    const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    // near ties: exact differences in double against float(1e-4)
+    const float nb_v = __shfl_down_sync(0xffffffffu, my_v, 1);
+    const bool inner = (lane + 1 < k) &&
+                       (static_cast<double>(my_v) - static_cast<double>(nb_v) <
+                        static_cast<double>(kTieEps));
+    const unsigned inner_any = __ballot_sync(0xffffffffu, inner);
+    const float last_v = __shfl_sync(0xffffffffu, my_v, k - 1);
+    if (lane < k) {
+        idx[t * k + lane] = my_e;
+        w[t * k + lane] = ex / sum;
+    }
+    if (lane == 0) {
+        uint8_t f = inner_any ? 2 : 0;
+        if (k < E && static_cast<double>(last_v) - static_cast<double>(next_v) <
+                         static_cast<double>(kTieEps))
+            f |= 1;
+        tie[t] = f;
+    }
+}
+
+int launch_topk(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
+                uint8_t* tie, cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    const int per = (E + 31) / 32;
+    const int tpb = 256;
+    const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+#define MOE_TOPK(P)                                                              \
+    topk_kernel<P><<<grid, tpb, 0, st>>>(logits, T, E, k, idx, w, tie);        \
+    break;
+    switch (per <= 4 ? 4 : per <= 8 ? 8 : per <= 12 ? 12 : per <= 16 ? 16 : 32) {
+        case 4: MOE_TOPK(4)
+        case 8: MOE_TOPK(8)
+        case 12: MOE_TOPK(12)
+        case 16: MOE_TOPK(16)
+        default: MOE_TOPK(32)
+    }
+#undef MOE_TOPK
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "router_topk");
+    return MOE_OK;
+}
+
+// ==================================================================== dispatch
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+DispatchWs dispatch_ws_layout(const DispatchGeom& g) {
+    DispatchWs w;
+    size_t o = 0;
+    const size_t n = static_cast<size_t>(g.T) * g.k;
+    w.send_row_off = o;  o = align256(o + n * sizeof(int64_t));
+    w.rloc_off = o;      o = align256(o + n * sizeof(int32_t));
+    w.cnt_se_off = o;    o = align256(o + static_cast<size_t>(g.S) * g.E * sizeof(int32_t));
+    w.base_se_off = o;   o = align256(o + static_cast<size_t>(g.S) * g.E * sizeof(int32_t));
+    w.demand_off = o;    o = align256(o + static_cast<size_t>(g.S) * g.D * g.W * sizeof(int32_t));
+    w.total = o;
+    return w;
+}
+
+// Reset the stats, write the empty tag into every pool row and -1 into the
+// expert row lists.
+__global__ void dispatch_init_kernel(DispatchGeom g, uint16_t* __restrict__ pool,
+                                     int32_t* __restrict__ expert_rows,
+                                     moe_drop_stats_t* __restrict__ stats) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (tid == 0) {
+        stats->assignments = g.T * g.k;
+        stats->kept = 0;
+        stats->dropped_send = 0;
+        stats->dropped_recv = 0;
+        stats->max_send_fill = 0;
+        stats->max_expert_rows = 0;
+        stats->status = 0;
+        stats->reserved = 0;
+    }
+    const int64_t pitch = g.L + 8;
+    for (int64_t r = tid; r < g.pool_rows; r += nthr)
+        *reinterpret_cast<int4*>(pool + r * pitch + g.L) = make_int4(-1, -1, -1, 0);
+    const int64_t ne = static_cast<int64_t>(g.E) * g.c_recv;
+    for (int64_t i = tid; i < ne; i += nthr) expert_rows[i] = -1;
+}
+
+// Sender stage and the per-source half of the receiver stage.  One warp per
+// source rank walks that source's assignments in priority order, 32 at a
+// time.  Lanes with the same (destination, wave) key find each other with
+// __match_any_sync; each gets slot = count so far + its rank among the
+// group, and the group's lowest lane advances the count (a warp-aggregated
+// increment of a counter the warp owns, so the result is deterministic).
+// The same is done per expert over the sender-kept lanes, giving each kept
+// row its rank among this source's rows for that expert.
+__global__ void __launch_bounds__(128) dispatch_send_kernel(DispatchGeom g,
+                                                            const int32_t* __restrict__ idx,
+                                                            int64_t* __restrict__ send_row,
+                                                            int32_t* __restrict__ rloc,
+                                                            int32_t* __restrict__ cnt_se,
+                                                            int32_t* __restrict__ demand,
+                                                            moe_drop_stats_t* __restrict__ stats) {
+    extern __shared__ int32_t sh[];
+    const int warps = blockDim.x >> 5;
+    const int wib = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.x * warps + wib;
+    const int nkey = g.D * g.W;
+    int32_t* cnt_key = sh + wib * (nkey + g.E);
+    int32_t* cnt_e = cnt_key + nkey;
+    for (int i = lane; i < nkey + g.E; i += 32) cnt_key[i] = 0;
+    __syncwarp();
+    if (s >= g.S) return;
+
+    const unsigned lt = (1u << lane) - 1u;
+    const int64_t n = g.T_s * g.k;
+    const int64_t first = static_cast<int64_t>(s) * n;   // flat (t, j) index of this source
+    int64_t dropped = 0;
+    bool bad = false;
+    for (int64_t base = 0; base < n; base += 32) {
+        const int64_t i = base + lane;
+        const bool valid = i < n;
+        int e = valid ? idx[first + i] : 0;
+        if (valid && (e < 0 || e >= g.E)) {
+            bad = true;
+            e = 0;
+        }
+        const int dst = e / g.E_l;
+        const int wv = (e - dst * g.E_l) / g.E_w;
+        const int key = dst * g.W + wv;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? key : -1 - lane);
+        const int before = __popc(peers & lt);
+        const int cnt0 = valid ? cnt_key[key] : 0;
+        __syncwarp();
+        if (valid && before == 0) cnt_key[key] = cnt0 + __popc(peers);
+        __syncwarp();
+        const int slot = cnt0 + before;
+        const bool kept = valid && slot < g.c_send;
+        const unsigned epeers = __match_any_sync(0xffffffffu, kept ? e : -1 - lane);
+        const int ebefore = __popc(epeers & lt);
+        const int ecnt0 = kept ? cnt_e[e] : 0;
+        __syncwarp();
+        if (kept && ebefore == 0) cnt_e[e] = ecnt0 + __popc(epeers);
+        __syncwarp();
+        if (valid) {
+            const int64_t row =
+                (static_cast<int64_t>(key) * g.S + s) * g.c_send + slot;
+            send_row[first + i] = kept ? row : -1;
+            rloc[first + i] = kept ? ecnt0 + ebefore : -1;
+            if (!kept) ++dropped;
+        }
+    }
+    __syncwarp();
+    for (int e = lane; e < g.E; e += 32) cnt_se[static_cast<int64_t>(s) * g.E + e] = cnt_e[e];
+    int maxfill = 0;
+    for (int key = lane; key < nkey; key += 32) {
+        const int d = cnt_key[key];
+        demand[static_cast<int64_t>(s) * nkey + key] = d;
+        maxfill = max(maxfill, min(d, g.c_send));
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        maxfill = max(maxfill, __shfl_xor_sync(0xffffffffu, maxfill, off));
+        dropped += __shfl_xor_sync(0xffffffffu, dropped, off);
+    }
+    const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&stats->dropped_send),
+                  static_cast<unsigned long long>(dropped));
+        atomicMax(&stats->max_send_fill, maxfill);
+        if (any_bad) atomicCAS(&stats->status, 0, MOE_EINVAL);
+    }
+}
+
+// Receiver stage, per expert: exclusive prefix over sources of the kept
+// counts (sources hold contiguous token ranges, so source order is priority
+// order); count = min(total, c_recv).
+__global__ void dispatch_recv_scan_kernel(DispatchGeom g, const int32_t* __restrict__ cnt_se,
+                                          int32_t* __restrict__ base_se,
+                                          int32_t* __restrict__ expert_count,
+                                          moe_drop_stats_t* __restrict__ stats) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    long long kept = 0, over = 0;
+    int cnt = 0;
+    if (e < g.E) {
+        int run = 0;
+        for (int s = 0; s < g.S; ++s) {
+            base_se[static_cast<int64_t>(s) * g.E + e] = run;
+            run += cnt_se[static_cast<int64_t>(s) * g.E + e];
+        }
+        cnt = min(run, g.c_recv);
+        expert_count[e] = cnt;
+        kept = cnt;
+        over = run - cnt;
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        kept += __shfl_xor_sync(0xffffffffu, kept, off);
+        over += __shfl_xor_sync(0xffffffffu, over, off);
+        cnt = max(cnt, __shfl_xor_sync(0xffffffffu, cnt, off));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&stats->kept),
+                  static_cast<unsigned long long>(kept));
+        atomicAdd(reinterpret_cast<unsigned long long*>(&stats->dropped_recv),
+                  static_cast<unsigned long long>(over));
+        atomicMax(&stats->max_expert_rows, cnt);
+    }
+}
+
+// Final decisions and the pack, one warp per token: the token's latent row
+// is read once into registers (16-byte loads) and written with 16-byte
+// stores to each of its sender-kept pool rows, followed by the row's tag.
+template <int CH>   // 16-byte chunks per lane per column block
+__global__ void __launch_bounds__(256) dispatch_pack_kernel(
+    DispatchGeom g, const uint16_t* __restrict__ z, const int32_t* __restrict__ idx,
+    const int64_t* __restrict__ send_row, const int32_t* __restrict__ rloc,
+    const int32_t* __restrict__ base_se, uint16_t* __restrict__ pool,
+    int32_t* __restrict__ slot_of, uint8_t* __restrict__ drop, int32_t* __restrict__ expert_rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= g.T) return;
+    const int64_t s = t / g.T_s;
+    const int64_t pitch = g.L + 8;
+    // lane j < k owns assignment (t, j)
+    int64_t row = -1;
+    int e = 0;
+    if (lane < g.k) {
+        const int64_t a = t * g.k + lane;
+        e = idx[a];
+        row = send_row[a];
+        int32_t so = -1;
+        uint8_t dr = 1;
+        if (row >= 0 && e >= 0 && e < g.E) {
+            const int r = base_se[s * g.E + e] + rloc[a];
+            if (r < g.c_recv) {
+                expert_rows[static_cast<int64_t>(e) * g.c_recv + r] = static_cast<int32_t>(row);
+                so = static_cast<int32_t>(row);
+                dr = 0;
+            } else {
+                dr = 2;
+            }
+        }
+        slot_of[a] = so;
+        drop[a] = dr;
+    }
+    const int nchunk = g.L / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(z + t * g.L);
+    for (int cb = 0; cb < nchunk; cb += 32 * CH) {
+        uint4 v[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int ch = cb + lane + 32 * c;
+            if (ch < nchunk) v[c] = __ldg(src + ch);
+        }
+        for (int j = 0; j < g.k; ++j) {
+            const int64_t rj = __shfl_sync(0xffffffffu, row, j);
+            if (rj < 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(pool + rj * pitch);
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int ch = cb + lane + 32 * c;
+                if (ch < nchunk) dst[ch] = v[c];
+            }
+        }
+    }
+    if (lane < g.k && row >= 0)
+        *reinterpret_cast<int4*>(pool + row * pitch + g.L) =
+            make_int4(e, static_cast<int>(t), lane, 0);
+}
+
+int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
+                    uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
+                    int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t st) {
+    const DispatchWs L = dispatch_ws_layout(g);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int64_t* send_row = reinterpret_cast<int64_t*>(w + L.send_row_off);
+    int32_t* rloc = reinterpret_cast<int32_t*>(w + L.rloc_off);
+    int32_t* cnt_se = reinterpret_cast<int32_t*>(w + L.cnt_se_off);
+    int32_t* base_se = reinterpret_cast<int32_t*>(w + L.base_se_off);
+    int32_t* demand = reinterpret_cast<int32_t*>(w + L.demand_off);
+
+    dispatch_init_kernel<<<1024, 256, 0, st>>>(g, pool, expert_rows, stats);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_init");
+    // counters of one source: D*W keys + E experts, in shared memory
+    const size_t per_warp = static_cast<size_t>(g.D * g.W + g.E) * sizeof(int32_t);
+    int warps = 4;
+    while (warps > 1 && per_warp * warps > 96 * 1024) warps >>= 1;
+    const size_t shm = per_warp * warps;
+    if (shm > 200 * 1024) return MOE_EINVAL;
+    if (shm > 48 * 1024 &&
+        cudaFuncSetAttribute(dispatch_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(shm)) != cudaSuccess)
+        return MOE_ECUDA;
+    dispatch_send_kernel<<<(g.S + warps - 1) / warps, 32 * warps, shm, st>>>(
+        g, idx, send_row, rloc, cnt_se, demand, stats);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_send");
+    dispatch_recv_scan_kernel<<<(g.E + 127) / 128, 128, 0, st>>>(g, cnt_se, base_se, expert_count,
+                                                                  stats);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_recv_scan");
+    if (g.T == 0) return MOE_OK;
+    const unsigned grid = static_cast<unsigned>((g.T + 7) / 8);
+    const int nchunk = g.L / 8;
+    if (nchunk <= 32 * 4)
+        dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
+                                                       slot_of, drop, expert_rows);
+    else
+        dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
+                                                        slot_of, drop, expert_rows);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_pack");
+    return MOE_OK;
+}
+
+// ==================================================================== tile list
+
+// One CTA: per expert ceil(count/bm) row tiles, exclusive prefix over
+// experts, entries {e, m0} in expert order.
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ counts,
+                                                           int E, int bm,
+                                                           int2* __restrict__ tiles,
+                                                           int32_t* __restrict__ tile_count) {
+    __shared__ int warp_sum[32];
+    __shared__ int carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const int mt = e < E ? (counts[e] + bm - 1) / bm : 0;
+        int incl = mt;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sum[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int ws = lane < (int)(blockDim.x >> 5) ? warp_sum[lane] : 0;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ws, off);
+                if (lane >= off) ws += y;
+            }
+            warp_sum[lane] = ws;
+        }
+        __syncthreads();
+        const int excl = carry + (wid ? warp_sum[wid - 1] : 0) + incl - mt;
+        for (int i = 0; i < mt; ++i) tiles[excl + i] = make_int2(e, i * bm);
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = excl + mt;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *tile_count = carry;
+}
+
+int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
+                       int32_t* tile_count, cudaStream_t st) {
+    build_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, bm, reinterpret_cast<int2*>(tile_list),
+                                           tile_count);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "build_tiles");
+    return MOE_OK;
+}
+
+// ==================================================================== combine
+
+// The return path, one warp per token: c[t] = bf16(sum_j w[t,j] Y[slot_of[t,j]])
+// over kept j in j order, fp32 accumulation, 16-byte loads of the rows.
+template <int CH>
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ ypool,
+                                                      const int32_t* __restrict__ slot_of,
+                                                      const float* __restrict__ w, int64_t T,
+                                                      int k, int L, uint16_t* __restrict__ c) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int32_t my_row = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        my_row = slot_of[t * k + lane];
+        my_w = w[t * k + lane];
+    }
+    const int nchunk = L / 8;
+    uint4* dst = reinterpret_cast<uint4*>(c + t * L);
+    for (int cb = 0; cb < nchunk; cb += 32 * CH) {
+        float acc[CH][8];
+#pragma unroll
+        for (int q = 0; q < CH; ++q)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[q][i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+            const float wj = __shfl_sync(0xffffffffu, my_w, j);
+            if (r < 0) continue;
+            const uint4* src = reinterpret_cast<const uint4*>(ypool + static_cast<int64_t>(r) * L);
+#pragma unroll
+            for (int q = 0; q < CH; ++q) {
+                const int ch = cb + lane + 32 * q;
+                if (ch < nchunk) {
+                    const uint4 v = __ldg(src + ch);
+                    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        acc[q][2 * h] = fmaf(wj, bf16_lo(u[h]), acc[q][2 * h]);
+                        acc[q][2 * h + 1] = fmaf(wj, bf16_hi(u[h]), acc[q][2 * h + 1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < CH; ++q) {
+            const int ch = cb + lane + 32 * q;
+            if (ch < nchunk)
+                dst[ch] = make_uint4(pack_bf16x2(acc[q][0], acc[q][1]),
+                                     pack_bf16x2(acc[q][2], acc[q][3]),
+                                     pack_bf16x2(acc[q][4], acc[q][5]),
+                                     pack_bf16x2(acc[q][6], acc[q][7]));
+        }
+    }
+}
+
+int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
+                   int L, uint16_t* c, cudaStream_t st) {
+    if (T == 0) return MOE_OK;
+    const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+    if (L / 8 <= 32 * 4)
+        combine_kernel<4><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c);
+    else
+        combine_kernel<6><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "combine");
+    return MOE_OK;
+}
+
+}  // namespace moe

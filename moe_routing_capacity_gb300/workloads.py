@@ -116,7 +116,7 @@ def _normal_bf16(shape, std: float, g: torch.Generator, dev: torch.device,
                  chunk_dim0: int | None = None) -> torch.Tensor:
     out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     n0 = shape[0]
-    step = n0 if chunk_dim0 is None else max(1, chunk_dim0)
+    step = max(1, n0 if chunk_dim0 is None else chunk_dim0)
     for a in range(0, n0, step):
         b = min(n0, a + step)
         blk = torch.randn((b - a,) + tuple(shape[1:]), generator=g, device=dev,

@@ -399,8 +399,8 @@ def layer(cfg, t: dict, gate_w=None) -> dict:
     z = latent_down(t["x"], t["W_ld"])
     disp = dispatch(idx, p)
     payload, tags = pack_pool(z, idx, disp, p)
-    Wg, Wu, Wd = _f64(t["Wg"]), _f64(t["Wu"]), _f64(t["Wd"])
-    Y = experts_forward(lambda rows: payload[np.asarray(rows)], disp, Wg, Wu, Wd)
+    # expert weights are widened to float64 one expert at a time (inside expert_ffn)
+    Y = experts_forward(lambda rows: payload[np.asarray(rows)], disp, t["Wg"], t["Wu"], t["Wd"])
     L = z.shape[1]
     c = combine(lambda r: Y[r], disp["slot_of"], w, L)
     a = shared_act(t["x"], t["Wsg"], t["Wsu"])

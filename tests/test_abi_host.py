@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI library (no GPU needed): it builds, loads and
+exports every entry point the header declares; its plan (capacities, pool
+size) equals the oracle's; invalid configurations are rejected."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import oracle as O
+from moe_routing_capacity_gb300 import abi
+from moe_routing_capacity_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_pooled_wave.h")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    if not os.path.exists(abi.LIB_PATH):
+        from moe_routing_capacity_gb300 import build
+        build.build()
+    return abi.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, re.M)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(abi.EXPORTS) == _declared()
+
+
+def test_library_exports_every_declared_symbol():
+    L = abi.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert L.moe_abi_version() == 1
+
+
+def test_struct_sizes():
+    assert ctypes.sizeof(abi.Config) == 64
+    assert ctypes.sizeof(abi.Plan) == 64
+    assert ctypes.sizeof(abi.DropStats) == 48
+    assert abi.STATS_WORDS == 6
+
+
+def test_strerror_names_every_code():
+    for c in (abi.MOE_OK, abi.MOE_EINVAL, abi.MOE_ENOSPC, abi.MOE_ECUDA, abi.MOE_ETIMEOUT,
+              abi.MOE_ENODEV):
+        assert abi.strerror(c) != "unknown error"
+    assert abi.strerror(-99) == "unknown error"
+
+
+@pytest.mark.parametrize("cfg", list(wl.CONFIGS.values()), ids=lambda c: c.name)
+def test_plan_matches_oracle(cfg):
+    p, q = abi.plan(cfg), O.make_plan(cfg)
+    assert (p.c_send, p.c_recv, p.pool_rows) == (q.c_send, q.c_recv, q.pool_rows)
+    assert p.tokens_per_rank == q.T_s and p.experts_per_rank == q.E_l
+    assert p.experts_per_wave == q.E_w
+    assert p.pool_row_bytes == 2 * cfg.d_latent + 16
+    assert p.h_offset_bytes % 16 == 0
+    assert p.ws_ffn_bytes >= p.h_offset_bytes + cfg.n_experts * p.c_recv * cfg.h_expert * 2
+
+
+def _small(**kw):
+    base = dict(name="s", T=64, d_model=64, d_latent=32, n_experts=12, n_ranks=2, top_k=2,
+                n_waves=3, n_shared=1, h_expert=32, h_shared=32)
+    base.update(kw)
+    return wl.LayerConfig(**base)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(cf_send=1.1, cf_recv=1.1), dict(cf_send=0.01, cf_recv=0.01),
+    dict(cf_send=float("inf"), cf_recv=float("inf")), dict(cf_send=1.5, cf_recv=1.25),
+    dict(T=0), dict(top_k=1), dict(n_waves=1), dict(n_waves=2, n_experts=8),
+    dict(T=75, n_ranks=1, n_experts=3, n_waves=3, cf_send=1.1, cf_recv=1.1),
+    dict(T=200, n_ranks=4, n_experts=24, top_k=5, cf_send=1.37, cf_recv=0.93),
+])
+def test_plan_matches_oracle_edge_cases(kw):
+    cfg = _small(**kw)
+    p, q = abi.plan(cfg), O.make_plan(cfg)
+    assert (p.c_send, p.c_recv, p.pool_rows) == (q.c_send, q.c_recv, q.pool_rows)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=63),                     # T not divisible by the ranks
+    dict(n_experts=13),             # E not divisible by the ranks
+    dict(n_experts=8, n_waves=3),   # E/ranks not divisible by the waves
+    dict(d_model=60),               # rows not 16-byte multiples
+    dict(d_latent=36), dict(h_expert=20), dict(h_shared=12),
+    dict(top_k=0), dict(top_k=13), dict(top_k=33, n_experts=64),
+    dict(n_shared=4), dict(cf_send=0.0), dict(cf_recv=-1.0), dict(cf_send=float("nan")),
+    dict(n_experts=2048, n_ranks=2, n_waves=1, top_k=2),
+])
+def test_plan_rejects_invalid(kw):
+    cfg = _small(**kw)
+    with pytest.raises(abi.MoeError) as ei:
+        abi.plan(cfg)
+    assert ei.value.code == abi.MOE_EINVAL
+
+
+def test_entry_points_validate_before_touching_the_gpu():
+    """Null pointers and short scratch are refused on the host, before any
+    device call (these run without a GPU)."""
+    L = abi.lib()
+    c = abi.make_config(_small())
+    cp = ctypes.byref(c)
+    n = None
+    assert L.moe_router_topk(cp, n, n, n, n, n, n, n, n, n) == abi.MOE_EINVAL
+    assert L.moe_latent_proj(n, n, 4, 8, 8, n, n, n) == abi.MOE_EINVAL
+    assert L.moe_latent_proj(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 12, 8,
+                             ctypes.c_void_p(16), ctypes.c_void_p(16), n) == abi.MOE_EINVAL
+    assert L.moe_dispatch_pooled(cp, n, n, n, 0, n, n, n, n, n, n, n) == abi.MOE_EINVAL
+    p = abi.plan(_small())
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.moe_dispatch_pooled(cp, fake, fake, fake, p.ws_dispatch_bytes - 1, fake, fake, fake,
+                                 fake, fake, fake, n) == abi.MOE_ENOSPC
+    assert L.moe_expert_ffn_grouped(cp, fake, fake, fake, fake, fake, fake, fake,
+                                    p.ws_ffn_bytes - 1, fake, fake, n) == abi.MOE_ENOSPC
+    assert L.moe_combine(cp, n, n, n, n, n, n, n, n, n, n, n, n, n) == abi.MOE_EINVAL
+    bad = abi.make_config(_small(T=63))
+    assert L.moe_plan(ctypes.byref(bad), ctypes.byref(abi.Plan())) == abi.MOE_EINVAL
+
+
+def test_capacity_uses_decimal_factor():
+    # 1.1 * 50 is 55 exactly; a float ceil would say 56
+    cfg = _small(T=75, n_ranks=1, n_experts=3, n_waves=3, top_k=2, cf_send=1.1, cf_recv=1.1)
+    p = abi.plan(cfg)
+    assert (p.c_send, p.c_recv) == (55, 55)
+    assert not math.isclose(1.1 * 50, 55.0, rel_tol=0, abs_tol=0)
