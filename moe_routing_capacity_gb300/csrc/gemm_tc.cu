@@ -14,8 +14,10 @@
 // Warp roles: warp 0 issues TMA loads (one elected lane), warp 1 issues
 // tcgen05.mma (one lane), warp 2 owns the TMEM allocation, warps 4-7 run the
 // epilogue (warp 4+q reads TMEM lanes 32q..32q+31), and for gathered A
-// warps 8-11 copy one A row each with cp.async.  Two TMEM accumulators let the
-// epilogue of tile i overlap the main loop of tile i+1.
+// warps 8-11 copy the tile's 128 rows (indices from the expert's row list)
+// with cp.async, eight threads per 128-byte row segment so every global
+// access is a full, coalesced line.  Two TMEM accumulators let the epilogue
+// of tile i overlap the main loop of tile i+1.
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -343,8 +345,14 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         }
     } else if (AMODE == A_GATHER && warp >= 8) {
         // ------------------------------------------------------------ row gather (A)
-        constexpr int LAG = STAGES - 2;     // k-blocks in flight per thread
-        const int r = threadIdx.x - 256;    // tile row owned by this thread
+        // Thread t copies 16-byte chunk c = t % 8 of tile rows t/8 + 16 i,
+        // i = 0..7: a warp instruction moves four whole 128-byte row segments.
+        // Each thread keeps LAG k-blocks of copies in flight, then waits for
+        // the oldest, fences them into the async proxy and signals the stage.
+        constexpr int LAG = STAGES - 2;
+        const int t = threadIdx.x - 256;
+        const int c = t & 7;
+        const int rg = t >> 3;
         const int ntiles = num_tiles<AMODE>(p);
         uint32_t stage = 0, phase = 0;
         int it = 0;
@@ -352,25 +360,31 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
             int g, m0, nb;
             decode_tile<AMODE>(p, tile, g, m0, nb);
-            const int m = m0 + r;
-            const bool valid = m < p.counts[g];
-            const uint16_t* src =
-                p.gather_src +
-                (valid ? static_cast<long long>(p.rowmap[static_cast<long long>(g) * p.rowmap_ld + m]) *
-                             p.gather_pitch
-                       : 0ll);
+            const int cnt = p.counts[g];
+            const int* rl = p.rowmap + static_cast<long long>(g) * p.rowmap_ld;
+            const uint16_t* src[8];
+            uint32_t valid = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int m = m0 + rg + 16 * i;
+                const bool v = m < cnt;
+                valid |= (v ? 1u : 0u) << i;
+                src[i] = p.gather_src + (v ? static_cast<long long>(rl[m]) * p.gather_pitch : 0ll) +
+                         c * 8;
+            }
             for (int kb = 0; kb < kb_total; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t dst = smem_u32(sA + stage * A_STAGE_BYTES) + r * 128;
-                const int k0 = kb * BK;
+                const uint32_t dst =
+                    smem_u32(sA + stage * A_STAGE_BYTES) + ((c ^ (rg & 7)) << 4);
+                const int kc = kb * BK;
+                const bool kin = kc + c * 8 < p.K0;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int kc = k0 + c * 8;
-                    const uint32_t nbytes = (valid && kc < p.K0) ? 16u : 0u;
-                    cp_async_16(dst + ((c ^ (r & 7)) << 4), src + (nbytes ? kc : 0), nbytes);
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t nbytes = ((valid >> i & 1u) && kin) ? 16u : 0u;
+                    cp_async_16(dst + (rg + 16 * i) * 128, src[i] + (nbytes ? kc : 0), nbytes);
                 }
                 cp_async_commit();
                 if (it >= LAG) {

@@ -45,9 +45,11 @@ def check_close(name: str, got, want, report: dict | None = None):
     assert rel <= REL_L2, f"{name}: relative L2 {rel:.3g} > {REL_L2}"
 
 
-def tie_margin_ok(logits32: np.ndarray, k: int, idx_o: np.ndarray, slack: float = 1e-5):
-    """Tokens whose oracle gaps (adjacent top-(k+1) logits) all sit at least
-    `slack` away from the near-tie threshold, so the flag cannot flip."""
+def tie_margin_ok(logits32: np.ndarray, k: int, idx_o: np.ndarray, slack: float):
+    """Tokens whose oracle gaps (adjacent top-(k+1) logits) all sit more than
+    `slack` away from the near-tie threshold, so the flag cannot flip.  With
+    logits that differ by at most err, a gap moves by at most 2*err: callers
+    pass slack = 2*err (plus a hair)."""
     l = logits32.astype(np.float64)
     order = np.argsort(-l, axis=1, kind="stable")[:, : min(k + 1, l.shape[1])]
     top = np.take_along_axis(l, order, axis=1)

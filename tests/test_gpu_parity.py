@@ -54,7 +54,8 @@ def compare_full(cfg, inp, report=None):
     tie = _np(m.tie)
     clear = ref["tie"] == 0
     assert (idx[clear] == ref["idx"][clear]).all(), "top-k ids differ away from near-ties"
-    stable = tie_margin_ok(ref["logits"], cfg.top_k, ref["idx"])
+    lerr = float(np.abs(lg - ref["logits"]).max())
+    stable = tie_margin_ok(ref["logits"], cfg.top_k, ref["idx"], 2 * lerr + 1e-7)
     assert (tie[stable] == ref["tie"][stable]).all(), "near-tie flags differ"
     same_route = clear | (idx == ref["idx"]).all(axis=1)
     check_close("w", _np(m.gate_w)[same_route], ref["w"][same_route], report)
@@ -194,7 +195,9 @@ def test_results_are_deterministic():
     for _ in range(2):
         m.forward(x)
         torch.cuda.synchronize()
-        outs.append([t.clone() for t in (m.idx, m.slot_of, m.drop, m.expert_rows, m.pool,
-                                          m.ypool, m.out)])
+        # bit patterns (rows no expert writes hold whatever was there, NaNs included)
+        outs.append([t.clone().view(torch.uint8) for t in (m.idx, m.slot_of, m.drop,
+                                                            m.expert_rows, m.pool, m.ypool,
+                                                            m.out)])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
