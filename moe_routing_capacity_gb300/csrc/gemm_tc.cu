@@ -31,14 +31,19 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 
-template <int BN>
+// Shared-memory rings: A stages (128 x 64 bf16, 16 KB) and B stages (BN x 64
+// bf16) have their own depths.  Gathered A (cp.async, latency-bound) gets a
+// deeper ring than the TMA-fed B.
+template <int BN, int AMODE>
 struct TileCfg {
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int B_STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int A_STAGES = (AMODE == A_GATHER) ? 6 : B_STAGES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES =
-        1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + BAR_BYTES;
+        1024 + A_STAGES * A_STAGE_BYTES + B_STAGES * B_STAGE_BYTES + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct KParams {
@@ -91,19 +96,22 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 template <int BN, int AMODE, int EPI>
 __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     gemm_tc_kernel(const __grid_constant__ KParams p) {
-    using C = TileCfg<BN>;
-    constexpr int STAGES = C::STAGES;
+    using C = TileCfg<BN, AMODE>;
+    constexpr int AST = C::A_STAGES;
+    constexpr int BST = C::B_STAGES;
     constexpr bool B3D = (AMODE != A_DENSE);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sbase = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sA = sbase;
-    uint8_t* sB = sbase + STAGES * A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * C::B_STAGE_BYTES);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
+    uint8_t* sB = sbase + AST * A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + BST * C::B_STAGE_BYTES);
+    uint64_t* fullA = bars;
+    uint64_t* emptyA = fullA + AST;
+    uint64_t* fullB = emptyA + AST;
+    uint64_t* emptyB = fullB + BST;
+    uint64_t* tfull = emptyB + BST;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -113,9 +121,13 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], AMODE == A_GATHER ? 1 + 128 : 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < AST; ++s) {
+            mbar_init(&fullA[s], AMODE == A_GATHER ? 128 : 1);
+            mbar_init(&emptyA[s], 1);
+        }
+        for (int s = 0; s < BST; ++s) {
+            mbar_init(&fullB[s], 1);
+            mbar_init(&emptyB[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -145,9 +157,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const int ntiles = num_tiles<AMODE>(p);
-            uint32_t stage = 0, phase = 0;
-            uint32_t armed = 0;        // stages ever armed (bit mask)
-            uint32_t last_par = 0;     // parity of each stage's last armed phase
+            uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
+            uint32_t armedA = 0, parA = 0, armedB = 0, parB = 0;   // for unwinding
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
                 int g, m0, nb;
@@ -155,51 +166,64 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 int seg = 0;
                 for (int kb = 0; kb < kb_total; ++kb) {
                     while (kb >= p.seg_kb[seg + 1]) ++seg;
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                    const int kx = (kb - p.seg_kb[seg]) * BK;
+                    if (AMODE != A_GATHER) {
+                        if (!mbar_wait(&emptyA[sa], pa ^ 1u, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t a_dst = smem_u32(sA + sa * A_STAGE_BYTES);
+                        mbar_arrive_expect_tx(&fullA[sa], A_STAGE_BYTES);
+                        armedA |= 1u << sa;
+                        parA = (parA & ~(1u << sa)) | (pa << sa);
+                        if (AMODE == A_DENSE)
+                            tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], kx, m0);
+                        else
+                            tma_load_3d(a_dst, &p.mapA[seg], &fullA[sa], kx, m0, g);
+                        if (++sa == AST) {
+                            sa = 0;
+                            pa ^= 1u;
+                        }
+                    }
+                    if (!mbar_wait(&emptyB[sb], pb ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
-                    const int kx = (kb - p.seg_kb[seg]) * BK;
-                    const uint32_t a_dst = smem_u32(sA + stage * A_STAGE_BYTES);
-                    const uint32_t b_dst = smem_u32(sB + stage * C::B_STAGE_BYTES);
-                    const uint32_t bytes =
-                        C::B_STAGE_BYTES + (AMODE == A_GATHER ? 0u : (uint32_t)A_STAGE_BYTES);
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    armed |= 1u << stage;
-                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                    if (AMODE == A_DENSE) tma_load_2d(a_dst, &p.mapA[seg], &full[stage], kx, m0);
-                    if (AMODE == A_GROUPED)
-                        tma_load_3d(a_dst, &p.mapA[seg], &full[stage], kx, m0, g);
+                    const uint32_t b_dst = smem_u32(sB + sb * C::B_STAGE_BYTES);
+                    mbar_arrive_expect_tx(&fullB[sb], C::B_STAGE_BYTES);
+                    armedB |= 1u << sb;
+                    parB = (parB & ~(1u << sb)) | (pb << sb);
                     if (EPI == EPI_SWIGLU) {
                         const int n_half = nb * (BN / 2);
                         const uint32_t b_dst2 = b_dst + (BN / 2) * BK * 2;
                         if (B3D) {
-                            tma_load_3d(b_dst, &p.mapB[0], &full[stage], kx, n_half, g);
-                            tma_load_3d(b_dst2, &p.mapBup, &full[stage], kx, n_half, g);
+                            tma_load_3d(b_dst, &p.mapB[0], &fullB[sb], kx, n_half, g);
+                            tma_load_3d(b_dst2, &p.mapBup, &fullB[sb], kx, n_half, g);
                         } else {
-                            tma_load_2d(b_dst, &p.mapB[0], &full[stage], kx, n_half);
-                            tma_load_2d(b_dst2, &p.mapBup, &full[stage], kx, n_half);
+                            tma_load_2d(b_dst, &p.mapB[0], &fullB[sb], kx, n_half);
+                            tma_load_2d(b_dst2, &p.mapBup, &fullB[sb], kx, n_half);
                         }
                     } else {
                         if (B3D)
-                            tma_load_3d(b_dst, &p.mapB[seg], &full[stage], kx, nb * BN, g);
+                            tma_load_3d(b_dst, &p.mapB[seg], &fullB[sb], kx, nb * BN, g);
                         else
-                            tma_load_2d(b_dst, &p.mapB[seg], &full[stage], kx, nb * BN);
+                            tma_load_2d(b_dst, &p.mapB[seg], &fullB[sb], kx, nb * BN);
                     }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (++sb == BST) {
+                        sb = 0;
+                        pb ^= 1u;
                     }
                 }
             }
             if (!ok || *abort_flag) {
-                // Unwinding: let every armed load land before the CTA exits.
-                for (int s = 0; s < STAGES; ++s)
-                    if (armed >> s & 1u) {
-                        volatile int no_abort = 0;
-                        mbar_wait(&full[s], (last_par >> s) & 1u, &no_abort, nullptr,
-                                  20000000ull);
-                    }
+                // Unwinding: let every armed TMA load land before the CTA exits.
+                volatile int no_abort = 0;
+                for (int s = 0; s < BST; ++s)
+                    if (armedB >> s & 1u)
+                        mbar_wait(&fullB[s], (parB >> s) & 1u, &no_abort, nullptr, 20000000ull);
+                for (int s = 0; s < AST; ++s)
+                    if (armedA >> s & 1u)
+                        mbar_wait(&fullA[s], (parA >> s) & 1u, &no_abort, nullptr, 20000000ull);
             }
         }
     } else if (warp == 1) {
@@ -207,7 +231,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         if (lane == 0) {
             const int ntiles = num_tiles<AMODE>(p);
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-            uint32_t stage = 0, phase = 0;
+            uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
@@ -215,21 +239,27 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < kb_total; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+                    if (!mbar_wait(&fullA[sa], pa, abort_flag, p.status) ||
+                        !mbar_wait(&fullB[sb], pb, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_k_sw128(smem_u32(sA + stage * A_STAGE_BYTES));
-                    const uint64_t bd = sdesc_k_sw128(smem_u32(sB + stage * C::B_STAGE_BYTES));
+                    const uint64_t ad = sdesc_k_sw128(smem_u32(sA + sa * A_STAGE_BYTES));
+                    const uint64_t bd = sdesc_k_sw128(smem_u32(sB + sb * C::B_STAGE_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
                                  (kb | kk) != 0 ? 1u : 0u);
-                    mma_commit(&empty[stage]);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    mma_commit(&emptyA[sa]);
+                    mma_commit(&emptyB[sb]);
+                    if (++sa == AST) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++sb == BST) {
+                        sb = 0;
+                        pb ^= 1u;
                     }
                 }
                 if (!ok) break;
@@ -348,37 +378,48 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         // Thread t copies 16-byte chunk c = t % 8 of tile rows t/8 + 16 i,
         // i = 0..7: a warp instruction moves four whole 128-byte row segments.
         // Each thread keeps LAG k-blocks of copies in flight, then waits for
-        // the oldest, fences them into the async proxy and signals the stage.
-        constexpr int LAG = STAGES - 2;
+        // the oldest, fences them into the async proxy and signals its stage.
+        // LAG = A_STAGES - 2 leaves the MMA one stage of slack, so a stage is
+        // never signalled behind a wait for the slot two blocks ahead.  The
+        // next tile's row indices are fetched while this tile streams.
+        constexpr int LAG = AST - 2;
         const int t = threadIdx.x - 256;
         const int c = t & 7;
         const int rg = t >> 3;
         const int ntiles = num_tiles<AMODE>(p);
-        uint32_t stage = 0, phase = 0;
+        uint32_t sa = 0, pa = 0;
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        int nxt_row[8];
+        int nxt_cnt = 0;
+        auto fetch_rows = [&](int tile) {
             int g, m0, nb;
             decode_tile<AMODE>(p, tile, g, m0, nb);
-            const int cnt = p.counts[g];
-            const int* rl = p.rowmap + static_cast<long long>(g) * p.rowmap_ld;
+            nxt_cnt = p.counts[g] - m0;   // valid rows of the tile, from its first
+            const int* rl = p.rowmap + static_cast<long long>(g) * p.rowmap_ld + m0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int m = rg + 16 * i;
+                nxt_row[i] = m < nxt_cnt ? rl[m] : 0;
+            }
+        };
+        if (static_cast<int>(blockIdx.x) < ntiles) fetch_rows(blockIdx.x);
+        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
             const uint16_t* src[8];
             uint32_t valid = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int m = m0 + rg + 16 * i;
-                const bool v = m < cnt;
+                const bool v = rg + 16 * i < nxt_cnt;
                 valid |= (v ? 1u : 0u) << i;
-                src[i] = p.gather_src + (v ? static_cast<long long>(rl[m]) * p.gather_pitch : 0ll) +
-                         c * 8;
+                src[i] = p.gather_src + static_cast<long long>(nxt_row[i]) * p.gather_pitch + c * 8;
             }
+            if (tile + static_cast<int>(gridDim.x) < ntiles) fetch_rows(tile + gridDim.x);
             for (int kb = 0; kb < kb_total; ++kb) {
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                if (!mbar_wait(&emptyA[sa], pa ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t dst =
-                    smem_u32(sA + stage * A_STAGE_BYTES) + ((c ^ (rg & 7)) << 4);
+                const uint32_t dst = smem_u32(sA + sa * A_STAGE_BYTES) + ((c ^ (rg & 7)) << 4);
                 const int kc = kb * BK;
                 const bool kin = kc + c * 8 < p.K0;
 #pragma unroll
@@ -390,18 +431,18 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 if (it >= LAG) {
                     cp_async_wait<LAG>();
                     fence_proxy_async_smem();
-                    mbar_arrive(&full[(it - LAG) % STAGES]);
+                    mbar_arrive(&fullA[(it - LAG) % AST]);
                 }
                 ++it;
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (++sa == AST) {
+                    sa = 0;
+                    pa ^= 1u;
                 }
             }
         }
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        for (int i = (it > LAG ? it - LAG : 0); i < it; ++i) mbar_arrive(&full[i % STAGES]);
+        for (int i = (it > LAG ? it - LAG : 0); i < it; ++i) mbar_arrive(&fullA[i % AST]);
     }
 
     tc_fence_before();
@@ -465,7 +506,7 @@ static int map3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 
 template <int BN, int AMODE, int EPI>
 static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, AMODE>;
     auto kern = gemm_tc_kernel<BN, AMODE, EPI>;
     // Attribute setting is per device; cheap and idempotent, done every launch.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
