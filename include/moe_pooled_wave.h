@@ -165,6 +165,34 @@ int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_
                         uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
                         moe_drop_stats_t* stats, void* stream);
 
+/* moe_dispatch_pooled for callers that cannot allocate device memory.  The
+ * paper has no counterpart: it is a way of calling the dispatch above.
+ * Some callers cannot cudaMalloc: a host application that reserves the
+ * device's memory up front and forbids later allocations, code on a
+ * latency-critical path where an allocation's implicit device
+ * synchronisation is not acceptable, or a plug-in that is handed tensors but
+ * no allocator.  This entry point takes the same arguments as
+ * moe_dispatch_pooled minus the scratch, and uses instead a fixed array of
+ * MOE_DISPATCH_NOALLOC_SCRATCH_BYTES in device memory that the library
+ * defines (every GPU that loads the library holds it until the process
+ * exits).  It allocates nothing and calls no allocating routine.
+ *  - Limit: a configuration whose plan.ws_dispatch_bytes exceeds the array
+ *    is rejected with MOE_ENOSPC before anything is enqueued (8 MiB covers
+ *    T*k up to about 678,000 assignments at E=384, 64 ranks, 3 waves).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches
+ *    it; make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the
+ *    last call's contents.  Nothing in it needs to start at zero (each call
+ *    writes every word before reading it), but calls whose work overlaps on
+ *    the GPU (different streams without ordering between them) race on it.
+ * Outputs and errors are those of moe_dispatch_pooled. */
+#define MOE_DISPATCH_NOALLOC_SCRATCH_BYTES (8u << 20)
+int moe_dispatch_pooled_noalloc(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                                uint16_t* pool, int32_t* slot_of, uint8_t* drop,
+                                int32_t* expert_rows, int32_t* expert_count,
+                                moe_drop_stats_t* stats, void* stream);
+
 /* Grouped SwiGLU experts on the received rows: for expert e and r <
  * expert_count[e], with X = payload of pool row expert_rows[e][r]:
  *   h = bf16(silu(X Wg_e^T) * (X Wu_e^T)),  Y = bf16(h Wd_e^T)

@@ -20,7 +20,7 @@ MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2,
 
 # Every entry point the header declares (checked by the tests).
 EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_dispatch_pooled",
-           "moe_expert_ffn_grouped", "moe_combine", "moe_trace_begin", "moe_trace_mark",
+           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
 
 
@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.moe_router_topk.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_latent_proj.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp]
         L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
         L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_strerror.argtypes = [ctypes.c_int]
@@ -160,6 +161,19 @@ def dispatch_pooled(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_co
         ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
         _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(stats, torch.int64),
         _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def dispatch_pooled_noalloc(cfg, z, idx, pool, slot_of, drop, expert_rows, expert_count, stats,
+                            stream=None):
+    """moe_dispatch_pooled with the library's fixed scratch array instead of a
+    caller-provided one (for callers that cannot allocate device memory)."""
+    _check("moe_dispatch_pooled_noalloc", lib().moe_dispatch_pooled_noalloc(
+        ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32),
+        _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8), _ptr(expert_rows, i32),
+        _ptr(expert_count, i32), _ptr(stats, torch.int64), _stream(stream)))
 
 
 def expert_ffn_grouped(cfg, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ypool, status,
