@@ -32,30 +32,34 @@ def _sources():
     return sorted(os.path.join(SRC, f) for f in os.listdir(SRC) if f.endswith(".cu"))
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, out_dir: str = OUT, extra=()) -> tuple[str, str]:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(OUT, exist_ok=True)
+def build(verbose: bool = False, lib_path: str = LIB, extra_flags=()) -> str:
+    """Compile and link.  ``lib_path`` and ``extra_flags`` (e.g. -D tuning
+    macros) let a variant be built somewhere else without touching the
+    package's own library."""
+    out_dir = OUT if lib_path == LIB else os.path.splitext(lib_path)[0] + "_obj"
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(_compile, srcs))
+        results = list(ex.map(lambda f: _compile(f, out_dir, tuple(extra_flags)), srcs))
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

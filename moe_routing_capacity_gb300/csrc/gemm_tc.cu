@@ -34,11 +34,30 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 // Shared-memory rings: A stages (128 x 64 bf16, 16 KB) and B stages (BN x 64
 // bf16) have their own depths.  Gathered A (cp.async, latency-bound) gets a
 // deeper ring than the TMA-fed B.
+#ifndef MOE_GATHER_A_STAGES
+#define MOE_GATHER_A_STAGES 6
+#endif
+#ifndef MOE_GATHER_B_STAGES
+#define MOE_GATHER_B_STAGES 4
+#endif
+#ifndef MOE_GROUPED_A_STAGES
+#define MOE_GROUPED_A_STAGES 4
+#endif
+#ifndef MOE_GROUPED_B_STAGES
+#define MOE_GROUPED_B_STAGES 4
+#endif
+
 template <int BN, int AMODE>
 struct TileCfg {
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
-    static constexpr int B_STAGES = (BN == 256) ? 4 : 6;
-    static constexpr int A_STAGES = (AMODE == A_GATHER) ? 6 : B_STAGES;
+    static constexpr int B_STAGES = (BN != 256)              ? 6
+                                    : (AMODE == A_GATHER)    ? MOE_GATHER_B_STAGES
+                                    : (AMODE == A_GROUPED)   ? MOE_GROUPED_B_STAGES
+                                                             : 4;
+    static constexpr int A_STAGES = (AMODE == A_GATHER)    ? MOE_GATHER_A_STAGES
+                                    : (AMODE == A_GROUPED) ? MOE_GROUPED_A_STAGES
+                                                           : B_STAGES;
+    static_assert(AMODE != A_GATHER || A_STAGES >= 3, "the gather needs LAG >= 1");
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES =

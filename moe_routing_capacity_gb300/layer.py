@@ -63,19 +63,21 @@ class PooledWaveMoE:
                                self.w["Wg"], self.w["Wu"], self.w["Wd"], self.ws_ffn, self.ypool,
                                self.status, stream)
 
-    def combine(self, x, stream=None):
+    def combine(self, x, out=None, stream=None):
         abi.combine(self.cfg, self.ypool, self.slot_of, self.gate_w, self.w["W_lu"], x,
                     self.w["Wsg"], self.w["Wsu"], self.w["Wsd"], self.c,
-                    self.a if self.cfg.n_shared else None, self.out, self.status, stream)
+                    self.a if self.cfg.n_shared else None,
+                    self.out if out is None else out, self.status, stream)
 
-    def forward(self, x, stream=None):
-        """Enqueue the whole layer on ``stream``; returns the output buffer."""
+    def forward(self, x, out=None, stream=None):
+        """Enqueue the whole layer on ``stream``; returns the output tensor
+        (``out`` if given, else the layer's own output buffer)."""
         self.route(x, stream)
         self.latent(x, stream)
         self.dispatch(stream)
         self.experts(stream)
-        self.combine(x, stream)
-        return self.out
+        self.combine(x, out, stream)
+        return self.out if out is None else out
 
     # -- views ------------------------------------------------------------
     def pool_payload(self):
@@ -87,3 +89,57 @@ class PooledWaveMoE:
 
     def drop_stats(self) -> dict:
         return abi.stats_dict(self.stats)
+
+
+class HostPipeline:
+    """Runs host-resident batches through a layer with the copies overlapped.
+
+    Batch i's host->device copy runs on its own stream while batch i-1
+    computes and batch i-2's output (and drop statistics) copy back on a third
+    stream; ``depth`` device buffers per direction keep the three in flight.
+    Host tensors should be pinned for the copies to be asynchronous.
+    """
+
+    def __init__(self, layer: "PooledWaveMoE", depth: int = 2):
+        self.m = layer
+        self.depth = depth
+        cfg, dev = layer.cfg, layer.device
+        self.xd = [torch.empty(cfg.T, cfg.d_model, dtype=torch.bfloat16, device=dev)
+                   for _ in range(depth)]
+        self.od = [torch.empty(cfg.T, cfg.d_model, dtype=torch.bfloat16, device=dev)
+                   for _ in range(depth)]
+        self.sd = [torch.empty_like(layer.stats) for _ in range(depth)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.comp = torch.cuda.current_stream(dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(depth)]     # x[b] landed
+        self.ev_done = [torch.cuda.Event() for _ in range(depth)]   # layer read x[b], wrote out[b]
+        self.ev_out = [torch.cuda.Event() for _ in range(depth)]    # out[b] copied back
+        self.i = 0
+
+    def submit(self, x_host, out_host, stats_host=None):
+        """Enqueue one batch: x_host -> layer -> out_host (all asynchronous)."""
+        b = self.i % self.depth
+        m = self.m
+        if self.i >= self.depth:
+            self.h2d.wait_event(self.ev_done[b])      # x[b] no longer read
+        with torch.cuda.stream(self.h2d):
+            self.xd[b].copy_(x_host, non_blocking=True)
+            self.ev_in[b].record(self.h2d)
+        self.comp.wait_event(self.ev_in[b])
+        if self.i >= self.depth:
+            self.comp.wait_event(self.ev_out[b])     # out[b] copied back
+        m.forward(self.xd[b], out=self.od[b], stream=self.comp)
+        self.sd[b].copy_(m.stats, non_blocking=True)
+        self.ev_done[b].record(self.comp)
+        self.d2h.wait_event(self.ev_done[b])
+        with torch.cuda.stream(self.d2h):
+            out_host.copy_(self.od[b], non_blocking=True)
+            if stats_host is not None:
+                stats_host.copy_(self.sd[b], non_blocking=True)
+            self.ev_out[b].record(self.d2h)
+        self.i += 1
+
+    def synchronize(self):
+        for ev in self.ev_out:
+            ev.synchronize()

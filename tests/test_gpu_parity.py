@@ -201,3 +201,29 @@ def test_results_are_deterministic():
                                                             m.out)])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def test_host_pipeline_matches_forward():
+    """Host batches through the overlapped-copy runner give the same bits as
+    the plain forward on device-resident inputs."""
+    from moe_routing_capacity_gb300.layer import HostPipeline
+    cfg = wl.TINY.with_(seed=24, T=512, n_ranks=4)
+    inp = wl.make_inputs(cfg, "cpu")
+    m = PooledWaveMoE(cfg, inp, "cuda")
+    g = torch.Generator().manual_seed(9)
+    xs = [torch.randn(cfg.T, cfg.d_model, generator=g).to(torch.bfloat16).pin_memory()
+          for _ in range(5)]
+    want = []
+    for xh in xs:
+        m.forward(xh.cuda())
+        torch.cuda.synchronize()
+        want.append((m.out.cpu().clone(), m.stats.cpu().clone()))
+    pipe = HostPipeline(m, depth=2)
+    outs = [torch.empty(cfg.T, cfg.d_model, dtype=torch.bfloat16).pin_memory() for _ in xs]
+    sts = [torch.empty(m.stats.numel(), dtype=torch.int64).pin_memory() for _ in xs]
+    for xh, oh, sh in zip(xs, outs, sts):
+        pipe.submit(xh, oh, sh)
+    pipe.synchronize()
+    for (wo, ws), oh, sh in zip(want, outs, sts):
+        assert torch.equal(oh.view(torch.int16), wo.view(torch.int16))
+        assert torch.equal(sh, ws)
