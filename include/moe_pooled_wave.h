@@ -132,7 +132,8 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* plan);
  *          float(1e-4); bit 1 = two adjacent selected logits closer than that.
  * Source: lamjinlab zh-HK section 二 (eight experts per token); the bias is
  * the quantile-balancing bias added to the router logits (devpress.csdn.net,
- * appendix A.2).  Tensor cores: tcgen05 GEMM; top-k: one warp per token. */
+ * appendix A.2).  Tensor cores: tcgen05 GEMM (one 128 x 384 tile per 128
+ * tokens when E <= 384); top-k: one warp per token (k <= 32). */
 int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* Wr,
                     const float* bias, float* logits, int32_t* idx, float* w,
                     uint8_t* tie, int32_t* status, void* stream);

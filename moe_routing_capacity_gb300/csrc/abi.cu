@@ -222,8 +222,6 @@ int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* 
     GemmDesc d;
     std::memset(&d, 0, sizeof(d));
     d.a_mode = A_DENSE;
-    d.epi = EPI_F32;
-    d.bn = 128;
     d.M = G.g.T;
     d.N = G.g.E;
     d.nseg = 1;
@@ -233,6 +231,10 @@ int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* 
     d.ldo = G.g.E;
     d.bias = bias;
     d.status = status;
+    d.epi = EPI_F32;
+    // E <= 384: one 128 x 384 tile per 128 tokens (a single wave of CTAs at
+    // the workloads' sizes); wider routers use 128 x 128 tiles
+    d.bn = G.g.E <= 384 ? 384 : 128;
     d.name = "gemm_router";
     if ((rc = gemm_launch(d, st))) return rc;
     return launch_topk(logits, G.g.T, G.g.E, G.g.k, idx, w, tie, st);

@@ -50,7 +50,8 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 template <int BN, int AMODE>
 struct TileCfg {
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
-    static constexpr int B_STAGES = (BN != 256)              ? 6
+    static constexpr int B_STAGES = (BN == 384)              ? 3
+                                    : (BN != 256)            ? 6
                                     : (AMODE == A_GATHER)    ? MOE_GATHER_B_STAGES
                                     : (AMODE == A_GROUPED)   ? MOE_GROUPED_B_STAGES
                                                              : 4;
@@ -58,7 +59,10 @@ struct TileCfg {
                                     : (AMODE == A_GROUPED) ? MOE_GROUPED_A_STAGES
                                                            : B_STAGES;
     static_assert(AMODE != A_GATHER || A_STAGES >= 3, "the gather needs LAG >= 1");
-    static constexpr int TMEM_COLS = 2 * BN;
+    // two accumulators (double buffering) when they fit in the 512 TMEM
+    // columns; the 384-wide router tile gets one
+    static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
+    static constexpr int TMEM_COLS = (BN <= 256) ? 2 * BN : 512;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES =
         1024 + A_STAGES * A_STAGE_BYTES + B_STAGES * B_STAGE_BYTES + BAR_BYTES;
@@ -222,6 +226,11 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                             tma_load_2d(b_dst, &p.mapB[0], &fullB[sb], kx, n_half);
                             tma_load_2d(b_dst2, &p.mapBup, &fullB[sb], kx, n_half);
                         }
+                    } else if (BN == 384) {
+#pragma unroll
+                        for (int h = 0; h < 3; ++h)
+                            tma_load_2d(b_dst + h * 128 * BK * 2, &p.mapB[seg], &fullB[sb], kx,
+                                        nb * BN + h * 128);
                     } else {
                         if (B3D)
                             tma_load_3d(b_dst, &p.mapB[seg], &fullB[sb], kx, nb * BN, g);
@@ -249,7 +258,9 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const int ntiles = num_tiles<AMODE>(p);
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            constexpr int N0 = BN <= 256 ? BN : 256;          // first MMA's N
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, N0);
+            constexpr uint32_t idesc_hi = idesc_bf16_f32(BM, BN > 256 ? BN - 256 : 16);
             uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
@@ -267,9 +278,13 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     const uint64_t ad = sdesc_k_sw128(smem_u32(sA + sa * A_STAGE_BYTES));
                     const uint64_t bd = sdesc_k_sw128(smem_u32(sB + sb * C::B_STAGE_BYTES));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
+                    for (int kk = 0; kk < BK / 16; ++kk) {
                         mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
                                  (kb | kk) != 0 ? 1u : 0u);
+                        if (BN > 256)   // columns 256.. from B rows 256.. (32 KB further)
+                            mma_bf16(d_tmem + 256, ad + 2u * kk, bd + (32768u >> 4) + 2u * kk,
+                                     idesc_hi, (kb | kk) != 0 ? 1u : 0u);
+                    }
                     mma_commit(&emptyA[sa]);
                     mma_commit(&emptyB[sb]);
                     if (++sa == AST) {
@@ -283,7 +298,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
-                if (++acc == 2) {
+                if (++acc == C::NACC) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -387,7 +402,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
-            if (++acc == 2) {
+            if (++acc == C::NACC) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -546,11 +561,13 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
     if (rc) return rc;
-    if (d.nseg < 1 || d.nseg > 4 || (d.bn != 128 && d.bn != 256)) return MOE_EINVAL;
+    if (d.nseg < 1 || d.nseg > 4 || (d.bn != 128 && d.bn != 256 && d.bn != 384))
+        return MOE_EINVAL;
+    if (d.bn == 384 && (d.epi != EPI_F32 || d.a_mode != A_DENSE)) return MOE_EINVAL;
 
     KParams p;
     std::memset(&p, 0, sizeof(p));
-    const uint32_t b_box = (d.epi == EPI_SWIGLU) ? d.bn / 2 : d.bn;
+    const uint32_t b_box = (d.epi == EPI_SWIGLU || d.bn == 384) ? 128 : d.bn;
     p.nseg = d.nseg;
     p.seg_kb[0] = 0;
     for (int s = 0; s < d.nseg; ++s) {
@@ -604,6 +621,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     const int key = d.bn * 100 + d.a_mode * 10 + d.epi;
     switch (key) {
         case 128 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<128, A_DENSE, EPI_F32>(p, grid, st, d.name);
+        case 384 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<384, A_DENSE, EPI_F32>(p, grid, st, d.name);
         case 256 * 100 + A_DENSE * 10 + EPI_BF16: return launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
         case 256 * 100 + A_DENSE * 10 + EPI_SWIGLU: return launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
         case 256 * 100 + A_GATHER * 10 + EPI_SWIGLU: return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);

@@ -48,7 +48,7 @@ struct GemmSeg {        // one K segment of the contraction: A_s [M, K_s] . B_s 
 struct GemmDesc {
     int a_mode;
     int epi;
-    int bn;                 // 128 or 256
+    int bn;                 // 128, 256, or 384 (fp32 epilogue only: two MMAs, N=256+128)
     int64_t M;              // dense: rows of A/out
     int N;                  // output columns (hidden units for SWIGLU)
     int nseg;

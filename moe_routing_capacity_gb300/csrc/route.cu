@@ -162,76 +162,142 @@ __global__ void dispatch_init_kernel(DispatchGeom g, uint16_t* __restrict__ pool
     for (int64_t i = tid; i < ne; i += nthr) expert_rows[i] = -1;
 }
 
-// Sender stage and the per-source half of the receiver stage.  One warp per
-// source rank walks that source's assignments in priority order, 32 at a
-// time.  Lanes with the same (destination, wave) key find each other with
-// __match_any_sync; each gets slot = count so far + its rank among the
-// group, and the group's lowest lane advances the count (a warp-aggregated
-// increment of a counter the warp owns, so the result is deterministic).
-// The same is done per expert over the sender-kept lanes, giving each kept
-// row its rank among this source's rows for that expert.
-__global__ void __launch_bounds__(128) dispatch_send_kernel(DispatchGeom g,
-                                                            const int32_t* __restrict__ idx,
-                                                            int64_t* __restrict__ send_row,
-                                                            int32_t* __restrict__ rloc,
-                                                            int32_t* __restrict__ cnt_se,
-                                                            int32_t* __restrict__ demand,
-                                                            moe_drop_stats_t* __restrict__ stats) {
-    extern __shared__ int32_t sh[];
-    const int warps = blockDim.x >> 5;
-    const int wib = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int s = blockIdx.x * warps + wib;
-    const int nkey = g.D * g.W;
-    int32_t* cnt_key = sh + wib * (nkey + g.E);
-    int32_t* cnt_e = cnt_key + nkey;
-    for (int i = lane; i < nkey + g.E; i += 32) cnt_key[i] = 0;
-    __syncwarp();
-    if (s >= g.S) return;
+// Sender stage and the per-source half of the receiver stage, one CTA per
+// source rank.  The source's assignments are taken in priority order in
+// rounds of at most SEND_WARPS x 32 x SEND_PER_LANE; a round is split evenly
+// over the warps (in multiples of 32) and warp w holds its contiguous slice in
+// registers.  Slots are exact ranks in priority order,
+// obtained without atomics on shared counts:
+//   pass 1  each warp counts its slice per (destination, wave) key: lanes with
+//           the same key find each other with __match_any_sync and the
+//           group's lowest lane adds the group size to the warp's counter;
+//   scan    per key, an exclusive prefix over warps (plus the rounds before)
+//           gives each warp's first slot -- a deterministic prefix sum;
+//   pass 2  slot = warp base + rank within the group so far; kept if
+//           slot < c_send; kept rows are counted per expert the same way;
+//   scan    per expert, prefix over warps;
+//   pass 3  each kept row's rank among this source's kept rows for its expert.
+constexpr int SEND_WARPS = 16;
+constexpr int SEND_PER_LANE = 16;
 
+__global__ void __launch_bounds__(SEND_WARPS * 32) dispatch_send_kernel(
+    DispatchGeom g, const int32_t* __restrict__ idx, int64_t* __restrict__ send_row,
+    int32_t* __restrict__ rloc, int32_t* __restrict__ cnt_se, int32_t* __restrict__ demand,
+    moe_drop_stats_t* __restrict__ stats) {
+    extern __shared__ int32_t sh[];
+    const int nkey = g.D * g.W;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const unsigned lt = (1u << lane) - 1u;
+    int32_t* cnt_key = sh;                              // [SEND_WARPS][nkey]
+    int32_t* cnt_e = cnt_key + SEND_WARPS * nkey;       // [SEND_WARPS][E]
+    int32_t* run_key = cnt_e + SEND_WARPS * g.E;        // [nkey] totals of earlier rounds
+    int32_t* run_e = run_key + nkey;                    // [E]
+    for (int i = threadIdx.x; i < nkey + g.E; i += blockDim.x) run_key[i] = 0;
+
+    const int s = blockIdx.x;
     const int64_t n = g.T_s * g.k;
-    const int64_t first = static_cast<int64_t>(s) * n;   // flat (t, j) index of this source
+    const int64_t first = static_cast<int64_t>(s) * n;
     int64_t dropped = 0;
     bool bad = false;
-    for (int64_t base = 0; base < n; base += 32) {
-        const int64_t i = base + lane;
-        const bool valid = i < n;
-        int e = valid ? idx[first + i] : 0;
-        if (valid && (e < 0 || e >= g.E)) {
-            bad = true;
-            e = 0;
+    constexpr int ROUND = SEND_WARPS * 32 * SEND_PER_LANE;
+    for (int64_t base = 0; base < n; base += ROUND) {
+        const int64_t rn = n - base < ROUND ? n - base : ROUND;       // items this round
+        const int per_warp = static_cast<int>((rn + SEND_WARPS * 32 - 1) / (SEND_WARPS * 32)) * 32;
+        const int64_t wbase = base + static_cast<int64_t>(warp) * per_warp;
+        const int64_t wend = (wbase + per_warp < base + rn) ? wbase + per_warp : base + rn;
+        int e[SEND_PER_LANE];
+#pragma unroll
+        for (int i = 0; i < SEND_PER_LANE; ++i) {
+            const int64_t a = wbase + 32 * i + lane;
+            e[i] = a < wend ? idx[first + a] : -1;
+            if (a < wend && (e[i] < 0 || e[i] >= g.E)) {
+                bad = true;
+                e[i] = 0;
+            }
         }
-        const int dst = e / g.E_l;
-        const int wv = (e - dst * g.E_l) / g.E_w;
-        const int key = dst * g.W + wv;
-        const unsigned peers = __match_any_sync(0xffffffffu, valid ? key : -1 - lane);
-        const int before = __popc(peers & lt);
-        const int cnt0 = valid ? cnt_key[key] : 0;
+        int32_t* my_key = cnt_key + warp * nkey;
+        int32_t* my_e = cnt_e + warp * g.E;
+        for (int i = lane; i < nkey; i += 32) my_key[i] = 0;
+        for (int i = lane; i < g.E; i += 32) my_e[i] = 0;
         __syncwarp();
-        if (valid && before == 0) cnt_key[key] = cnt0 + __popc(peers);
-        __syncwarp();
-        const int slot = cnt0 + before;
-        const bool kept = valid && slot < g.c_send;
-        const unsigned epeers = __match_any_sync(0xffffffffu, kept ? e : -1 - lane);
-        const int ebefore = __popc(epeers & lt);
-        const int ecnt0 = kept ? cnt_e[e] : 0;
-        __syncwarp();
-        if (kept && ebefore == 0) cnt_e[e] = ecnt0 + __popc(epeers);
-        __syncwarp();
-        if (valid) {
-            const int64_t row =
-                (static_cast<int64_t>(key) * g.S + s) * g.c_send + slot;
-            send_row[first + i] = kept ? row : -1;
-            rloc[first + i] = kept ? ecnt0 + ebefore : -1;
-            if (!kept) ++dropped;
+        // pass 1: per-warp key counts
+#pragma unroll
+        for (int i = 0; i < SEND_PER_LANE; ++i) {
+            if (i * 32 >= per_warp) break;
+            const bool v = e[i] >= 0;
+            const int dst = e[i] / g.E_l;
+            const int key = dst * g.W + (e[i] - dst * g.E_l) / g.E_w;
+            const unsigned peers = __match_any_sync(0xffffffffu, v ? key : -1 - lane);
+            if (v && (peers & lt) == 0) my_key[key] += __popc(peers);
+            __syncwarp();
         }
+        __syncthreads();
+        for (int key = threadIdx.x; key < nkey; key += blockDim.x) {
+            int acc = run_key[key];
+            for (int w = 0; w < SEND_WARPS; ++w) {
+                const int c = cnt_key[w * nkey + key];
+                cnt_key[w * nkey + key] = acc;
+                acc += c;
+            }
+            run_key[key] = acc;
+        }
+        __syncthreads();
+        // pass 2: slots, sender decisions, per-warp counts of kept rows per expert
+        uint32_t kept_mask = 0;
+#pragma unroll
+        for (int i = 0; i < SEND_PER_LANE; ++i) {
+            if (i * 32 >= per_warp) break;
+            const bool v = e[i] >= 0;
+            const int dst = e[i] / g.E_l;
+            const int key = dst * g.W + (e[i] - dst * g.E_l) / g.E_w;
+            const unsigned peers = __match_any_sync(0xffffffffu, v ? key : -1 - lane);
+            const int slot = (v ? my_key[key] : 0) + __popc(peers & lt);
+            __syncwarp();
+            if (v && (peers & lt) == 0) my_key[key] += __popc(peers);
+            const bool kept = v && slot < g.c_send;
+            const unsigned epeers = __match_any_sync(0xffffffffu, kept ? e[i] : -1 - lane);
+            if (kept && (epeers & lt) == 0) my_e[e[i]] += __popc(epeers);
+            __syncwarp();
+            if (v) {
+                const int64_t a = wbase + 32 * i + lane;
+                send_row[first + a] =
+                    kept ? (static_cast<int64_t>(key) * g.S + s) * g.c_send + slot : -1;
+                if (!kept) ++dropped;
+            }
+            kept_mask |= (kept ? 1u : 0u) << i;
+        }
+        __syncthreads();
+        for (int ex = threadIdx.x; ex < g.E; ex += blockDim.x) {
+            int acc = run_e[ex];
+            for (int w = 0; w < SEND_WARPS; ++w) {
+                const int c = cnt_e[w * g.E + ex];
+                cnt_e[w * g.E + ex] = acc;
+                acc += c;
+            }
+            run_e[ex] = acc;
+        }
+        __syncthreads();
+        // pass 3: rank among this source's kept rows of the same expert
+#pragma unroll
+        for (int i = 0; i < SEND_PER_LANE; ++i) {
+            if (i * 32 >= per_warp) break;
+            const bool kept = kept_mask >> i & 1u;
+            const unsigned epeers = __match_any_sync(0xffffffffu, kept ? e[i] : -1 - lane);
+            const int r = (kept ? my_e[e[i]] : 0) + __popc(epeers & lt);
+            __syncwarp();
+            if (kept && (epeers & lt) == 0) my_e[e[i]] += __popc(epeers);
+            __syncwarp();
+            const int64_t a = wbase + 32 * i + lane;
+            if (e[i] >= 0) rloc[first + a] = kept ? r : -1;
+        }
+        __syncthreads();
     }
-    __syncwarp();
-    for (int e = lane; e < g.E; e += 32) cnt_se[static_cast<int64_t>(s) * g.E + e] = cnt_e[e];
+    for (int ex = threadIdx.x; ex < g.E; ex += blockDim.x)
+        cnt_se[static_cast<int64_t>(s) * g.E + ex] = run_e[ex];
     int maxfill = 0;
-    for (int key = lane; key < nkey; key += 32) {
-        const int d = cnt_key[key];
+    for (int key = threadIdx.x; key < nkey; key += blockDim.x) {
+        const int d = run_key[key];
         demand[static_cast<int64_t>(s) * nkey + key] = d;
         maxfill = max(maxfill, min(d, g.c_send));
     }
@@ -241,8 +307,9 @@ __global__ void __launch_bounds__(128) dispatch_send_kernel(DispatchGeom g,
     }
     const unsigned any_bad = __ballot_sync(0xffffffffu, bad);
     if (lane == 0) {
-        atomicAdd(reinterpret_cast<unsigned long long*>(&stats->dropped_send),
-                  static_cast<unsigned long long>(dropped));
+        if (dropped)
+            atomicAdd(reinterpret_cast<unsigned long long*>(&stats->dropped_send),
+                      static_cast<unsigned long long>(dropped));
         atomicMax(&stats->max_send_fill, maxfill);
         if (any_bad) atomicCAS(&stats->status, 0, MOE_EINVAL);
     }
@@ -358,18 +425,17 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
     dispatch_init_kernel<<<1024, 256, 0, st>>>(g, pool, expert_rows, stats);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_init");
-    // counters of one source: D*W keys + E experts, in shared memory
-    const size_t per_warp = static_cast<size_t>(g.D * g.W + g.E) * sizeof(int32_t);
-    int warps = 4;
-    while (warps > 1 && per_warp * warps > 96 * 1024) warps >>= 1;
-    const size_t shm = per_warp * warps;
+    // per-warp counters plus running totals: (SEND_WARPS + 1) x (D*W + E) ints;
+    // D*W <= E <= 1024, so at most 139 KB
+    const size_t shm =
+        static_cast<size_t>(SEND_WARPS + 1) * (g.D * g.W + g.E) * sizeof(int32_t);
     if (shm > 200 * 1024) return MOE_EINVAL;
     if (shm > 48 * 1024 &&
         cudaFuncSetAttribute(dispatch_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(shm)) != cudaSuccess)
         return MOE_ECUDA;
-    dispatch_send_kernel<<<(g.S + warps - 1) / warps, 32 * warps, shm, st>>>(
-        g, idx, send_row, rloc, cnt_se, demand, stats);
+    dispatch_send_kernel<<<g.S, SEND_WARPS * 32, shm, st>>>(g, idx, send_row, rloc, cnt_se,
+                                                            demand, stats);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_send");
     dispatch_recv_scan_kernel<<<(g.E + 127) / 128, 128, 0, st>>>(g, cnt_se, base_se, expert_count,

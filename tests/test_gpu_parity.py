@@ -130,6 +130,9 @@ def test_tiny_layer_matches_oracle():
     dict(seed=19, top_k=6, cf_send=1.0, cf_recv=1.0),
     dict(seed=20, T=1024, n_ranks=8, n_experts=48, top_k=4, d_model=256, d_latent=128,
          h_expert=256, h_shared=128),
+    dict(seed=25, n_experts=768, top_k=2),      # E > 384: router GEMM + separate top-k kernel
+    dict(seed=26, n_experts=48, top_k=20),      # k > 16: same fallback
+    dict(seed=27, n_experts=384, n_ranks=4, top_k=16, cf_send=2.0, cf_recv=2.0),
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()) or "tiny")
 def test_small_variants_match_oracle(kw):
     cfg = wl.TINY.with_(**kw)
