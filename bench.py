@@ -80,6 +80,7 @@ def kernel_work(name, cfg, plan, st):
     F = {
         "gemm_router": 2.0 * T * d * E,
         "gemm_latent": 2.0 * T * d * L,
+        "gemm_latent_router": 2.0 * T * d * (L + E),
         "gemm_expert_gateup": 2.0 * kept * L * 2 * H,
         "gemm_expert_down": 2.0 * kept * H * L,
         "gemm_shared_gateup": 2.0 * T * d * 2 * ns * Hs,

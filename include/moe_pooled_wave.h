@@ -144,6 +144,17 @@ int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* 
 int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K, int32_t N,
                     uint16_t* out, int32_t* status, void* stream);
 
+/* moe_router_topk and moe_latent_proj(x, W_ld) in one pass over x: both read
+ * the token states (lamjinlab zh-HK section 二: the router picks the experts,
+ * the latent projection compresses the routed activations), so one GEMM
+ * computes [z | logits] = x [W_ld | Wr]^T, its column tiles writing z (bf16)
+ * or logits (fp32 + bias), followed by the top-k kernel.  Same outputs, with
+ * the same layouts and the same bits, as the two calls; z [T, L] bf16 is the
+ * extra output.  When L is not a multiple of 256 it runs the two calls. */
+int moe_route_project(const moe_config_t* cfg, const uint16_t* x, const uint16_t* Wr,
+                      const float* bias, const uint16_t* W_ld, float* logits, int32_t* idx,
+                      float* w, uint8_t* tie, uint16_t* z, int32_t* status, void* stream);
+
 /* Fixed pooled-wave dispatch (lamjinlab zh-HK section 二: one fixed pool per
  * destination, W same-shape waves, expert id in the payload row, the two
  * capacity factors, drops counted separately).  Priority: token ascending,

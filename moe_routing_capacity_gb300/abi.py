@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe_pooled_wave.so")
 MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2, -3, -4, -5
 
 # Every entry point the header declares (checked by the tests).
-EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_dispatch_pooled",
+EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project",
+           "moe_dispatch_pooled",
            "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
 
@@ -72,6 +73,7 @@ def lib() -> ctypes.CDLL:
         L.moe_plan.argtypes = [pc, ctypes.POINTER(Plan)]
         L.moe_router_topk.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_latent_proj.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp]
+        L.moe_route_project.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
         L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
@@ -152,6 +154,13 @@ def latent_proj(inp, W, out, status, stream=None):
     _check("moe_latent_proj", lib().moe_latent_proj(
         _ptr(inp, bf16), _ptr(W, bf16), M, K, N, _ptr(out, bf16), _ptr(status, i32),
         _stream(stream)))
+
+
+def route_project(cfg, x, Wr, bias, W_ld, logits, idx, w, tie, z, status, stream=None):
+    _check("moe_route_project", lib().moe_route_project(
+        ctypes.byref(make_config(cfg)), _ptr(x, bf16), _ptr(Wr, bf16),
+        _ptr(bias, f32, allow_none=True), _ptr(W_ld, bf16), _ptr(logits, f32), _ptr(idx, i32),
+        _ptr(w, f32), _ptr(tie, u8), _ptr(z, bf16), _ptr(status, i32), _stream(stream)))
 
 
 def dispatch_pooled(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,

@@ -240,6 +240,45 @@ int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* 
     return launch_topk(logits, G.g.T, G.g.E, G.g.k, idx, w, tie, st);
 }
 
+int moe_route_project(const moe_config_t* cfg, const uint16_t* x, const uint16_t* Wr,
+                      const float* bias, const uint16_t* W_ld, float* logits, int32_t* idx,
+                      float* w, uint8_t* tie, uint16_t* z, int32_t* status, void* stream) {
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    if (G.g.T == 0) return MOE_OK;
+    if (!x || !Wr || !W_ld || !logits || !idx || !w || !tie || !z || !status) return MOE_EINVAL;
+    if (!aligned16(x) || !aligned16(Wr) || !aligned16(W_ld) || !aligned16(z)) return MOE_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (G.g.L % 256) {   // no whole latent tiles: the two separate passes
+        if ((rc = moe_router_topk(cfg, x, Wr, bias, logits, idx, w, tie, status, stream))) return rc;
+        return moe_latent_proj(x, W_ld, G.g.T, G.d, G.g.L, z, status, stream);
+    }
+    GemmDesc d;
+    std::memset(&d, 0, sizeof(d));
+    d.a_mode = A_DENSE;
+    d.epi = EPI_SPLIT;
+    d.bn = 256;
+    d.M = G.g.T;
+    d.N = G.g.L;
+    d.nseg = 1;
+    d.seg[0] = GemmSeg{x, G.d, W_ld, G.d, G.d};
+    d.b_rows = G.g.L;
+    d.B_up = Wr;
+    d.b2_rows = G.g.E;
+    d.nsplit = G.g.L / 256;
+    d.N2 = G.g.E;
+    d.out = z;
+    d.ldo = G.g.L;
+    d.out2 = logits;
+    d.ldo2 = G.g.E;
+    d.bias = bias;
+    d.status = status;
+    d.name = "gemm_latent_router";
+    if ((rc = gemm_launch(d, st))) return rc;
+    return launch_topk(logits, G.g.T, G.g.E, G.g.k, idx, w, tie, st);
+}
+
 int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K, int32_t N,
                     uint16_t* out, int32_t* status, void* stream) {
     if (M < 0 || K <= 0 || N <= 0 || K % 8 || N % 8) return MOE_EINVAL;

@@ -92,6 +92,10 @@ struct KParams {
     long long out_gstride;
     const float* bias;
     int* status;
+    int nsplit;
+    int N2;
+    void* out2;
+    long long ldo2;
 };
 
 template <int AMODE>
@@ -226,6 +230,11 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                             tma_load_2d(b_dst, &p.mapB[0], &fullB[sb], kx, n_half);
                             tma_load_2d(b_dst2, &p.mapBup, &fullB[sb], kx, n_half);
                         }
+                    } else if (EPI == EPI_SPLIT) {
+                        if (nb < p.nsplit)
+                            tma_load_2d(b_dst, &p.mapB[0], &fullB[sb], kx, nb * BN);
+                        else
+                            tma_load_2d(b_dst, &p.mapBup, &fullB[sb], kx, (nb - p.nsplit) * BN);
                     } else if (BN == 384) {
 #pragma unroll
                         for (int h = 0; h < 3; ++h)
@@ -332,7 +341,42 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 if (EPI == EPI_SCATTER && row_ok)
                     orow = p.rowmap[static_cast<long long>(g) * p.rowmap_ld + m];
             }
-            if (EPI == EPI_F32) {
+            if (EPI == EPI_SPLIT && nb >= p.nsplit) {
+                float* out = reinterpret_cast<float*>(p.out2) + orow * p.ldo2;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + c * 32, r);
+                    const int col0 = (nb - p.nsplit) * BN + c * 32;
+                    if (row_ok && col0 < p.N2) {
+                        if (col0 + 32 <= p.N2 && (p.ldo2 & 3) == 0) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                float4 f;
+                                f.x = __uint_as_float(r[4 * v]);
+                                f.y = __uint_as_float(r[4 * v + 1]);
+                                f.z = __uint_as_float(r[4 * v + 2]);
+                                f.w = __uint_as_float(r[4 * v + 3]);
+                                if (p.bias) {
+                                    const float4 b = *reinterpret_cast<const float4*>(p.bias + col0 + 4 * v);
+                                    f.x += b.x; f.y += b.y; f.z += b.z; f.w += b.w;
+                                }
+                                *reinterpret_cast<float4*>(out + col0 + 4 * v) = f;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const int col = col0 + i;
+                                if (col < p.N2) {
+                                    float v = __uint_as_float(r[i]);
+                                    if (p.bias) v += p.bias[col];
+                                    out[col] = v;
+                                }
+                            }
+                        }
+                    }
+                }
+            } else if (EPI == EPI_F32) {
                 float* out = reinterpret_cast<float*>(p.out) + orow * p.ldo;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -586,6 +630,11 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
                 return rc;
         }
     }
+    if (d.epi == EPI_SPLIT) {
+        if (d.nseg != 1 || !d.B_up || d.a_mode != A_DENSE || d.N != d.nsplit * d.bn)
+            return MOE_EINVAL;
+        if ((rc = map2d(&p.mapBup, d.B_up, d.seg[0].K, d.b2_rows, d.seg[0].ldb, b_box))) return rc;
+    }
     if (d.epi == EPI_SWIGLU) {
         if (d.nseg != 1 || !d.B_up) return MOE_EINVAL;
         if (d.a_mode == A_DENSE)
@@ -600,6 +649,13 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.K0 = d.seg[0].K;
     const int n_per_tile = (d.epi == EPI_SWIGLU) ? d.bn / 2 : d.bn;
     p.n_tiles_n = (d.N + n_per_tile - 1) / n_per_tile;
+    if (d.epi == EPI_SPLIT) {
+        p.nsplit = d.nsplit;
+        p.N2 = d.N2;
+        p.out2 = d.out2;
+        p.ldo2 = d.ldo2;
+        p.n_tiles_n = d.nsplit + (d.N2 + d.bn - 1) / d.bn;
+    }
     p.m_tiles = static_cast<int>((d.M + BM - 1) / BM);
     p.tile_list = reinterpret_cast<const int2*>(d.tile_list);
     p.tile_count = d.tile_count;
@@ -622,6 +678,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     switch (key) {
         case 128 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<128, A_DENSE, EPI_F32>(p, grid, st, d.name);
         case 384 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<384, A_DENSE, EPI_F32>(p, grid, st, d.name);
+        case 256 * 100 + A_DENSE * 10 + EPI_SPLIT: return launch_traced<256, A_DENSE, EPI_SPLIT>(p, grid, st, d.name);
         case 256 * 100 + A_DENSE * 10 + EPI_BF16: return launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
         case 256 * 100 + A_DENSE * 10 + EPI_SWIGLU: return launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
         case 256 * 100 + A_GATHER * 10 + EPI_SWIGLU: return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);

@@ -31,6 +31,8 @@ enum EpiMode : int {
     EPI_BF16 = 1,     // bf16 out
     EPI_SWIGLU = 2,   // accumulator = [gate | up] halves -> bf16(silu(gate) * up)
     EPI_SCATTER = 3,  // bf16 out to rows given by a row map
+    EPI_SPLIT = 4,    // column tiles < nsplit: bf16 out (B = seg 0); the rest: fp32
+                      // out2 + bias (B = B_up), e.g. latent projection + router
 };
 
 struct GemmSeg {        // one K segment of the contraction: A_s [M, K_s] . B_s [N, K_s]^T
@@ -76,6 +78,12 @@ struct GemmDesc {
     const float* bias;
     int32_t* status;
     const char* name;       // kernel name for the timing trace
+    // EPI_SPLIT: second output
+    int nsplit;             // column tiles of the first output (N = nsplit * bn)
+    int N2;                 // columns of the second output
+    void* out2;
+    int64_t ldo2;
+    int b2_rows;            // rows of the second B (B_up)
 };
 
 int gemm_launch(const GemmDesc& d, cudaStream_t stream);

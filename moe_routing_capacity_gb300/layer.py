@@ -3,8 +3,8 @@
 ``PooledWaveMoE`` owns every buffer the C ABI asks the caller for (allocated
 once through PyTorch's caching allocator) and runs the layer as
 
-    moe_router_topk -> moe_latent_proj -> moe_dispatch_pooled
-        -> moe_expert_ffn_grouped -> moe_combine
+    moe_route_project (= moe_router_topk + moe_latent_proj in one pass over x)
+        -> moe_dispatch_pooled -> moe_expert_ffn_grouped -> moe_combine
 
 on one CUDA stream, with no host synchronisation, so the whole forward can be
 captured in a CUDA graph.  Intermediates stay readable as attributes.
@@ -69,11 +69,16 @@ class PooledWaveMoE:
                     self.a if self.cfg.n_shared else None,
                     self.out if out is None else out, self.status, stream)
 
+    def route_and_latent(self, x, stream=None):
+        """Router top-k and latent projection in one pass over x."""
+        abi.route_project(self.cfg, x, self.w["Wr"], self.w.get("bias"), self.w["W_ld"],
+                          self.logits, self.idx, self.gate_w, self.tie, self.z, self.status,
+                          stream)
+
     def forward(self, x, out=None, stream=None):
         """Enqueue the whole layer on ``stream``; returns the output tensor
         (``out`` if given, else the layer's own output buffer)."""
-        self.route(x, stream)
-        self.latent(x, stream)
+        self.route_and_latent(x, stream)
         self.dispatch(stream)
         self.experts(stream)
         self.combine(x, out, stream)

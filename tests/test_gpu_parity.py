@@ -230,3 +230,24 @@ def test_host_pipeline_matches_forward():
     for (wo, ws), oh, sh in zip(want, outs, sts):
         assert torch.equal(oh.view(torch.int16), wo.view(torch.int16))
         assert torch.equal(sh, ws)
+
+
+@pytest.mark.parametrize("E", [48, 384, 768])
+def test_route_project_equals_separate_calls(E):
+    """The one-pass router + latent projection gives the same bits as
+    moe_router_topk followed by moe_latent_proj."""
+    from moe_routing_capacity_gb300 import abi
+    cfg = wl.TINY.with_(seed=28, T=640, n_ranks=4, d_model=384, d_latent=512, n_experts=E,
+                        top_k=8 if E > 48 else 4, bias_kind="zipf")
+    inp = wl.make_inputs(cfg, "cuda")
+    a = PooledWaveMoE(cfg, inp, "cuda")
+    b = PooledWaveMoE(cfg, inp, "cuda")
+    x = inp["x"]
+    a.route_and_latent(x)
+    b.route(x)
+    b.latent(x)
+    torch.cuda.synchronize()
+    for name in ("logits", "idx", "gate_w", "tie", "z"):
+        ta, tb = getattr(a, name), getattr(b, name)
+        assert torch.equal(ta.view(torch.uint8), tb.view(torch.uint8)), name
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
