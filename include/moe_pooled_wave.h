@@ -235,6 +235,21 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
                 const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
                 uint16_t* c, uint16_t* a, uint16_t* out, int32_t* status, void* stream);
 
+/* Quantile-balancing bias update (devpress.csdn.net, section 四 and appendix
+ * A.2): a global histogram H counts how often each expert was selected;
+ * f_e = H[e] / sum(H); b_e = -alpha * (f_e - 1/E); the bias is added to the
+ * router logits from the next batch on, without gradient.
+ *   idx   [T, k] int32: this batch's top-k selections (before capacity drops)
+ *   hist  [E] int64 (in/out): the histogram; this batch's counts are added.
+ *         It accumulates over every call since the caller last zeroed it, so
+ *         the caller chooses the window of batches.
+ *   bias  [E] fp32 (out): the new bias; 0 everywhere while H is empty.  It
+ *         may be the buffer moe_router_topk reads: calls on the same stream
+ *         then route the next batch with it.
+ * The second reading on the pages (a "10,000-bin" histogram) is not built. */
+int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,
+                       float* bias, void* stream);
+
 /* Kernel timing trace (instrumentation; the pages define no such operation).
  * moe_trace_begin(n) creates n CUDA events (timing enabled) owned by the
  *   library and turns tracing on; from then on every kernel the library

@@ -21,7 +21,7 @@ MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2,
 # Every entry point the header declares (checked by the tests).
 EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project",
            "moe_dispatch_pooled",
-           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_combine", "moe_trace_begin", "moe_trace_mark",
+           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
 
 
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
         L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         L.moe_abi_version.argtypes = []
@@ -191,6 +192,12 @@ def expert_ffn_grouped(cfg, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ypo
         ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16), _ptr(expert_rows, i32),
         _ptr(expert_count, i32), _ptr(Wg, bf16), _ptr(Wu, bf16), _ptr(Wd, bf16),
         _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32), _stream(stream)))
+
+
+def balance_update(cfg, idx, hist, alpha, bias, stream=None):
+    _check("moe_balance_update", lib().moe_balance_update(
+        ctypes.byref(make_config(cfg)), _ptr(idx, i32), _ptr(hist, torch.int64),
+        float(alpha), _ptr(bias, f32), _stream(stream)))
 
 
 def combine(cfg, ypool, slot_of, w, W_lu, x, Wsg, Wsu, Wsd, c, a, out, status, stream=None):

@@ -401,6 +401,20 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
     return gemm_launch(d2, st);
 }
 
+int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,
+                       float* bias, void* stream) {
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    if (!hist || !bias || (G.g.T > 0 && !idx) || !(alpha == alpha)) return MOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(hist) & 7u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+        return MOE_EINVAL;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    return launch_balance_update(idx, G.g.T * G.g.k, G.g.E, hist, alpha, bias,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* slot_of,
                 const float* w, const uint16_t* W_lu, const uint16_t* x, const uint16_t* Wsg,
                 const uint16_t* Wsu, const uint16_t* Wsd, uint16_t* c, uint16_t* a,

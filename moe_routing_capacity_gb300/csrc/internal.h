@@ -115,6 +115,10 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
 int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
                        int32_t* tile_count, cudaStream_t stream);
 
+// Quantile-balancing bias update: hist += counts of idx; bias from hist.
+int launch_balance_update(const int32_t* idx, int64_t n, int E, int64_t* hist, float alpha,
+                          float* bias, cudaStream_t stream);
+
 int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
                    int L, uint16_t* c, cudaStream_t stream);
 

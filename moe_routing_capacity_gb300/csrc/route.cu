@@ -6,6 +6,7 @@
 //   combine             the return gather: per token, weighted sum of its
 //                       kept expert rows
 //   tile list           {expert, m0} work items of the grouped expert GEMMs
+#include <algorithm>
 #include <climits>
 #include <cstdio>
 
@@ -503,6 +504,61 @@ int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
                                            tile_count);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "build_tiles");
+    return MOE_OK;
+}
+
+// ==================================================================== balancing bias
+
+// Per-expert counts of this batch's top-k selections, added to the caller's
+// histogram: a shared-memory histogram per CTA, then one global add per
+// expert and CTA (integer adds, so the result does not depend on order).
+__global__ void __launch_bounds__(1024) balance_hist_kernel(const int32_t* __restrict__ idx,
+                                                            int64_t n, int E,
+                                                            unsigned long long* __restrict__ hist) {
+    extern __shared__ unsigned int hcount[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hcount[e] = 0;
+    __syncthreads();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int e = idx[i];
+        if (e >= 0 && e < E) atomicAdd(&hcount[e], 1u);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (hcount[e]) atomicAdd(&hist[e], static_cast<unsigned long long>(hcount[e]));
+}
+
+// bias[e] = -alpha * (hist[e] / sum(hist) - 1/E), 0 for an empty histogram.
+__global__ void __launch_bounds__(1024) balance_bias_kernel(const int64_t* __restrict__ hist,
+                                                            int E, float alpha,
+                                                            float* __restrict__ bias) {
+    __shared__ long long part[32];
+    long long s = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s += hist[e];
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += part[w];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const double f = total > 0 ? static_cast<double>(hist[e]) / static_cast<double>(total)
+                                   : 1.0 / E;
+        bias[e] = static_cast<float>(-static_cast<double>(alpha) * (f - 1.0 / E));
+    }
+}
+
+int launch_balance_update(const int32_t* idx, int64_t n, int E, int64_t* hist, float alpha,
+                          float* bias, cudaStream_t st) {
+    if (n > 0) {
+        const int grid = static_cast<int>(std::min<int64_t>((n + 1023) / 1024, 152));
+        balance_hist_kernel<<<grid, 1024, E * sizeof(unsigned int), st>>>(
+            idx, n, E, reinterpret_cast<unsigned long long*>(hist));
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "balance_hist");
+    }
+    balance_bias_kernel<<<1, 1024, 0, st>>>(hist, E, alpha, bias);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "balance_bias");
     return MOE_OK;
 }
 

@@ -17,7 +17,12 @@ from . import abi
 
 
 class PooledWaveMoE:
-    def __init__(self, cfg, weights: dict, device="cuda"):
+    """``balance_alpha``: if set, after each batch's routing the
+    quantile-balancing bias is recomputed from the running selection
+    histogram (``self.hist``) into the router bias, so it applies from the
+    next batch on."""
+
+    def __init__(self, cfg, weights: dict, device="cuda", balance_alpha=None):
         self.cfg = cfg
         self.plan = abi.plan(cfg)
         self.device = torch.device(device)
@@ -45,6 +50,11 @@ class PooledWaveMoE:
         self.a = e(T, max(1, cfg.n_shared * cfg.h_shared), dt=torch.bfloat16)
         self.out = e(T, d, dt=torch.bfloat16)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.balance_alpha = balance_alpha
+        if balance_alpha is not None:
+            if self.w.get("bias") is None:
+                self.w["bias"] = torch.zeros(E, dtype=torch.float32, device=dev)
+            self.hist = torch.zeros(E, dtype=torch.int64, device=dev)
 
     # -- the five steps -------------------------------------------------
     def route(self, x, stream=None):
@@ -79,6 +89,9 @@ class PooledWaveMoE:
         """Enqueue the whole layer on ``stream``; returns the output tensor
         (``out`` if given, else the layer's own output buffer)."""
         self.route_and_latent(x, stream)
+        if self.balance_alpha is not None:
+            abi.balance_update(self.cfg, self.idx, self.hist, self.balance_alpha,
+                               self.w["bias"], stream)
         self.dispatch(stream)
         self.experts(stream)
         self.combine(x, out, stream)

@@ -41,7 +41,7 @@ import numpy as np
 __all__ = [
     "bf16_round", "silu", "Plan", "make_plan", "router_logits", "router_topk",
     "latent_down", "placement", "dispatch", "pack_pool", "expert_ffn",
-    "experts_forward", "combine", "shared_act", "output", "layer",
+    "experts_forward", "combine", "shared_act", "output", "layer", "balance_update",
     "TIE_EPS", "EMPTY_TAG", "DROP_KEPT", "DROP_SEND", "DROP_RECV",
 ]
 
@@ -381,6 +381,28 @@ def output(c, a, W_lu, Wsd) -> np.ndarray:
     for s in range(Wsd.shape[0]):
         acc = acc + a[:, s * Hs:(s + 1) * Hs] @ Wsd[s].T
     return bf16_round(acc)
+
+
+# ---------------------------------------------------------------- balancing bias
+
+def balance_update(idx, hist, alpha: float, n_experts: int):
+    """Quantile-balancing bias for the next step.
+
+    [CSDN] appendix A.2: a global histogram H counts how often each expert
+    was selected; f_i = H[i] / sum(H); b_i = -alpha * (f_i - 1/E), added to
+    the router logits from the next batch on (no gradient).  [CSDN] sec. 四
+    describes the same update.  Reading: H counts top-k selections (before
+    capacity drops), accumulated over the batches since the caller last
+    cleared it (the caller's window); with an empty histogram b = 0.
+    Returns (new histogram, bias) as (int64, float64) arrays.
+    """
+    idx = np.asarray(idx, dtype=np.int64).reshape(-1)
+    h = np.asarray(hist, dtype=np.int64) + np.bincount(idx, minlength=n_experts)
+    total = int(h.sum())
+    if total == 0:
+        return h, np.zeros(n_experts)
+    f = h / total
+    return h, -alpha * (f - 1.0 / n_experts)
 
 
 # ---------------------------------------------------------------- layer

@@ -416,3 +416,34 @@ def test_skewed_bias_raises_drops():
     d0 = r0["disp"]["stats"]["dropped_send"] + r0["disp"]["stats"]["dropped_recv"]
     d1 = r1["disp"]["stats"]["dropped_send"] + r1["disp"]["stats"]["dropped_recv"]
     assert d1 > 2 * d0
+
+
+# ------------------------------------------------------------------ balancing bias
+
+def test_balance_update_closed_form():
+    # 4 experts; selections 0,0,0,1,1,2 (expert 3 never): H = [3, 2, 1, 0],
+    # f = [1/2, 1/3, 1/6, 0], b = -alpha (f - 1/4)
+    idx = np.array([[0, 1], [0, 2], [0, 1]])
+    h, b = O.balance_update(idx, np.zeros(4, dtype=np.int64), 0.5, 4)
+    assert h.tolist() == [3, 2, 1, 0]
+    np.testing.assert_allclose(b, [-0.5 * (1/2 - 1/4), -0.5 * (1/3 - 1/4),
+                                   -0.5 * (1/6 - 1/4), -0.5 * (0 - 1/4)], rtol=1e-15)
+    # accumulates over batches
+    h2, b2 = O.balance_update(np.array([[3, 2]]), h, 0.5, 4)
+    assert h2.tolist() == [3, 2, 2, 1]
+    np.testing.assert_allclose(b2, -0.5 * (np.array([3, 2, 2, 1]) / 8 - 0.25), rtol=1e-15)
+
+
+def test_balance_update_invariants():
+    rng = np.random.default_rng(9)
+    E = 24
+    idx = _random_routing(rng, 500, E, 4)
+    h, b = O.balance_update(idx, np.zeros(E, dtype=np.int64), 0.01, E)
+    assert h.sum() == 500 * 4
+    assert abs(b.sum()) < 1e-15                      # sum_i (f_i - 1/E) = 0
+    assert ((b < 0) == (h > h.sum() / E)).all()      # over-selected experts pushed down
+    flat = np.tile(np.arange(E), 10).reshape(-1, 4)  # perfectly balanced selections
+    _, b0 = O.balance_update(flat, np.zeros(E, dtype=np.int64), 1.0, E)
+    np.testing.assert_allclose(b0, 0.0, atol=1e-17)
+    _, bz = O.balance_update(np.zeros((0, 4), dtype=np.int64), np.zeros(E, dtype=np.int64), 1.0, E)
+    assert (bz == 0).all()
