@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-dropless", action="store_true",
+                    help="skip timing the dropless ragged variant")
     return ap.parse_args()
 
 
@@ -362,6 +364,38 @@ def run_gb300(args, rank, world, local_rank):
                "steps": n_e2e, "timer": "host wall clock around the submitted steps",
                "overlap": "H2D / compute / D2H on three streams, double-buffered"}
 
+    # ---- the dropless ragged variant on the same batch: the cost of removing drops
+    dropless = None
+    if not args.no_dropless:
+        md = PooledWaveMoE(cfg, inp, dev, dropless=True)
+        for _ in range(args.warmup):
+            md.forward(x)
+        torch.cuda.synchronize()
+        nd = max(3, min(args.steps, 100))
+        abi.trace_begin((n_kern + 1) * nd + 8)
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(nd):
+            abi.trace_mark(stream)
+            md.forward(x)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dtr = abi.trace_end()
+        assert int(md.status.item()) == 0
+        dms = d0.elapsed_time(d1) / nd
+        dper = {}
+        for name, ms in dtr:
+            if name != "mark":
+                dper.setdefault(name, []).append(ms)
+        dst = md.drop_stats()
+        dropless = {"value": world * cfg.T / (dms / 1e3), "unit": UNIT, "ms_per_step": dms,
+                    "steps": nd, "pool_rows": md.plan.pool_rows,
+                    "kept": dst["kept"], "capped_kept": st["kept"],
+                    "expert_ffn_ms": round(sum(sum(v) for k2, v in dper.items()
+                                               if k2.startswith("gemm_expert")) / nd, 4)}
+        del md
+
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -392,6 +426,7 @@ def run_gb300(args, rank, world, local_rank):
                       "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
             "gpu_launches": sum(v[1] for v in per.values()),
             "roofline": roof, "kernels": kernels, "clocks": clk, "e2e": e2e,
+            "dropless": dropless,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

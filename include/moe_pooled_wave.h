@@ -205,6 +205,33 @@ int moe_dispatch_pooled_noalloc(const moe_config_t* cfg, const uint16_t* z, cons
                                 int32_t* expert_rows, int32_t* expert_count,
                                 moe_drop_stats_t* stats, void* stream);
 
+/* Dropless ragged variant: the pages' fallback should drops stay too high
+ * (lamjinlab zh-HK section 四, "a ragged all-to-all without drops").  No
+ * capacity factor applies; every assignment is kept.  The pool keeps the
+ * destination-major order (destination, wave, source, priority), but each
+ * (source, destination, wave) block holds exactly the rows routed there, so
+ * the pool has T*k rows and no empty slot.
+ * moe_plan_ragged: as moe_plan with pool_rows = T*k, c_send = c_recv = 0
+ *   (no caps) and the ragged scratch sizes.
+ * moe_dispatch_ragged: outputs as moe_dispatch_pooled, except
+ *   expert_offsets [E+1] int32: expert e's rows are
+ *   expert_rows[expert_offsets[e] .. expert_offsets[e+1]) (flat [T*k] int32,
+ *   priority order); expert_count [E] = the differences; drop is all 0 and
+ *   slot_of >= 0 everywhere.
+ * moe_expert_ffn_ragged: moe_expert_ffn_grouped over those row lists; h
+ *   [T*k, H] sits at plan.h_offset_bytes of ws with expert e's rows from
+ *   expert_offsets[e].  ypool [T*k, L].  moe_combine applies unchanged. */
+int moe_plan_ragged(const moe_config_t* cfg, moe_plan_t* plan);
+int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                        void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
+                        uint8_t* drop, int32_t* expert_offsets, int32_t* expert_rows,
+                        int32_t* expert_count, moe_drop_stats_t* stats, void* stream);
+int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
+                          const int32_t* expert_offsets, const int32_t* expert_rows,
+                          const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                          const uint16_t* Wd, void* ws, size_t ws_bytes, uint16_t* ypool,
+                          int32_t* status, void* stream);
+
 /* Grouped SwiGLU experts on the received rows: for expert e and r <
  * expert_count[e], with X = payload of pool row expert_rows[e][r]:
  *   h = bf16(silu(X Wg_e^T) * (X Wu_e^T)),  Y = bf16(h Wd_e^T)

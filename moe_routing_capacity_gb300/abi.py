@@ -21,7 +21,8 @@ MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2,
 # Every entry point the header declares (checked by the tests).
 EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project",
            "moe_dispatch_pooled",
-           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update", "moe_combine", "moe_trace_begin", "moe_trace_mark",
+           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update",
+           "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
 
 
@@ -79,6 +80,9 @@ def lib() -> ctypes.CDLL:
         L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
         L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
+        L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
+        L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         L.moe_abi_version.argtypes = []
@@ -110,6 +114,14 @@ def plan(cfg) -> Plan:
     rc = lib().moe_plan(ctypes.byref(make_config(cfg)), ctypes.byref(p))
     if rc:
         raise MoeError("moe_plan", rc)
+    return p
+
+
+def plan_ragged(cfg) -> Plan:
+    p = Plan()
+    rc = lib().moe_plan_ragged(ctypes.byref(make_config(cfg)), ctypes.byref(p))
+    if rc:
+        raise MoeError("moe_plan_ragged", rc)
     return p
 
 
@@ -192,6 +204,24 @@ def expert_ffn_grouped(cfg, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ypo
         ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16), _ptr(expert_rows, i32),
         _ptr(expert_count, i32), _ptr(Wg, bf16), _ptr(Wu, bf16), _ptr(Wd, bf16),
         _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32), _stream(stream)))
+
+
+def dispatch_ragged(cfg, z, idx, ws, pool, slot_of, drop, expert_offsets, expert_rows,
+                    expert_count, stats, stream=None):
+    _check("moe_dispatch_ragged", lib().moe_dispatch_ragged(
+        ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
+        ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
+        _ptr(expert_offsets, i32), _ptr(expert_rows, i32), _ptr(expert_count, i32),
+        _ptr(stats, torch.int64), _stream(stream)))
+
+
+def expert_ffn_ragged(cfg, pool, expert_offsets, expert_rows, expert_count, Wg, Wu, Wd, ws,
+                      ypool, status, stream=None):
+    _check("moe_expert_ffn_ragged", lib().moe_expert_ffn_ragged(
+        ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16), _ptr(expert_offsets, i32),
+        _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(Wg, bf16), _ptr(Wu, bf16),
+        _ptr(Wd, bf16), _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32),
+        _stream(stream)))
 
 
 def balance_update(cfg, idx, hist, alpha, bias, stream=None):

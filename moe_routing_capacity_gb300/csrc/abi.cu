@@ -97,6 +97,7 @@ static int make_geom(const moe_config_t* c, Geom* out) {
     if (c->T > (1ll << 31) / c->top_k) return MOE_EINVAL;
 
     DispatchGeom& g = out->g;
+    g.ragged = 0;
     g.T = c->T;
     g.k = c->top_k;
     g.E = c->n_experts;
@@ -133,6 +134,30 @@ static int make_geom(const moe_config_t* c, Geom* out) {
     const size_t tiles_bytes = align_up(max_mt * 8 + 16, 1024);
     p.h_offset_bytes = static_cast<int64_t>(tiles_bytes);
     p.ws_ffn_bytes = static_cast<int64_t>(tiles_bytes + static_cast<size_t>(g.E) * g.c_recv * out->H * 2);
+    return MOE_OK;
+}
+
+// The dropless ragged layout: no caps, a pool of exactly T*k rows, h stored
+// flat with each expert's rows at its offset.
+static int make_geom_ragged(const moe_config_t* c, Geom* out) {
+    int rc = make_geom(c, out);
+    if (rc) return rc;
+    DispatchGeom& g = out->g;
+    const int64_t n = g.T * g.k;
+    if (n > INT32_MAX / 2) return MOE_EINVAL;
+    g.ragged = 1;
+    g.c_send = INT32_MAX;   // never binds
+    g.c_recv = INT32_MAX;
+    g.pool_rows = n;
+    moe_plan_t& p = out->plan;
+    p.c_send = 0;
+    p.c_recv = 0;
+    p.pool_rows = n;
+    p.ws_dispatch_bytes = static_cast<int64_t>(dispatch_ws_layout(g).total);
+    const size_t max_mt = static_cast<size_t>(n / 128 + g.E);
+    const size_t tiles_bytes = align_up(max_mt * 8 + 16, 1024);
+    p.h_offset_bytes = static_cast<int64_t>(tiles_bytes);
+    p.ws_ffn_bytes = static_cast<int64_t>(tiles_bytes + static_cast<size_t>(n) * out->H * 2);
     return MOE_OK;
 }
 
@@ -320,6 +345,113 @@ int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_
     if ((rc = current_device(&dev, &sms))) return rc;
     return launch_dispatch(G.g, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
                            static_cast<cudaStream_t>(stream));
+}
+
+int moe_plan_ragged(const moe_config_t* cfg, moe_plan_t* plan) {
+    if (!plan) return MOE_EINVAL;
+    Geom G;
+    const int rc = make_geom_ragged(cfg, &G);
+    if (rc) return rc;
+    *plan = G.plan;
+    return MOE_OK;
+}
+
+int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx, void* ws,
+                        size_t ws_bytes, uint16_t* pool, int32_t* slot_of, uint8_t* drop,
+                        int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
+                        moe_drop_stats_t* stats, void* stream) {
+    Geom G;
+    int rc = make_geom_ragged(cfg, &G);
+    if (rc) return rc;
+    if (!stats || !expert_count || !expert_offsets || !ws ||
+        (G.g.T > 0 && (!z || !idx || !slot_of || !drop || !pool || !expert_rows)))
+        return MOE_EINVAL;
+    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || !aligned16(ws)) return MOE_EINVAL;
+    if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    return launch_dispatch_ragged(G.g, z, idx, ws, pool, slot_of, drop, expert_offsets,
+                                  expert_rows, expert_count, stats,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
+                          const int32_t* expert_offsets, const int32_t* expert_rows,
+                          const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                          const uint16_t* Wd, void* ws, size_t ws_bytes, uint16_t* ypool,
+                          int32_t* status, void* stream) {
+    Geom G;
+    int rc = make_geom_ragged(cfg, &G);
+    if (rc) return rc;
+    const DispatchGeom& g = G.g;
+    if (g.pool_rows == 0) return MOE_OK;
+    if (!pool || !expert_offsets || !expert_rows || !expert_count || !Wg || !Wu || !Wd || !ws ||
+        !ypool || !status)
+        return MOE_EINVAL;
+    if (!aligned16(pool) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) ||
+        !aligned16(ypool) || !aligned16(ws))
+        return MOE_EINVAL;
+    if (ws_bytes < static_cast<size_t>(G.plan.ws_ffn_bytes)) return MOE_ENOSPC;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    int32_t* tiles = reinterpret_cast<int32_t*>(wsb);
+    const int max_mt = static_cast<int>(g.pool_rows / 128 + g.E);
+    int32_t* tile_count = reinterpret_cast<int32_t*>(wsb + static_cast<size_t>(max_mt) * 8);
+    uint16_t* h = reinterpret_cast<uint16_t*>(wsb + G.plan.h_offset_bytes);
+    if ((rc = launch_build_tiles(expert_count, g.E, 128, tiles, tile_count, st))) return rc;
+    const int L = g.L, H = G.H;
+    const int n = static_cast<int>(g.pool_rows);
+
+    GemmDesc d1;
+    std::memset(&d1, 0, sizeof(d1));
+    d1.a_mode = A_GATHER;
+    d1.epi = EPI_SWIGLU;
+    d1.bn = 256;
+    d1.N = H;
+    d1.nseg = 1;
+    d1.seg[0] = GemmSeg{nullptr, 0, Wg, L, L};
+    d1.B_up = Wu;
+    d1.groups = g.E;
+    d1.b_rows = H;
+    d1.b_gstride = static_cast<int64_t>(H) * L;
+    d1.tile_list = tiles;
+    d1.tile_count = tile_count;
+    d1.max_tiles = max_mt;
+    d1.rowmap = expert_rows;
+    d1.counts = expert_count;
+    d1.goff = expert_offsets;
+    d1.gather_src = pool;
+    d1.gather_pitch = L + 8;
+    d1.gather_rows = n;
+    d1.out = h;
+    d1.ldo = H;
+    d1.status = status;
+    d1.name = "gemm_expert_gateup";
+    if ((rc = gemm_launch(d1, st))) return rc;
+
+    GemmDesc d2;
+    std::memset(&d2, 0, sizeof(d2));
+    d2.a_mode = A_GROUPED;
+    d2.epi = EPI_SCATTER;
+    d2.bn = 256;
+    d2.N = L;
+    d2.nseg = 1;
+    d2.seg[0] = GemmSeg{h, H, Wd, H, H};
+    d2.groups = g.E;
+    d2.rows_per_group = n;   // with goff: rows of the flat h
+    d2.b_rows = L;
+    d2.b_gstride = static_cast<int64_t>(L) * H;
+    d2.tile_list = tiles;
+    d2.tile_count = tile_count;
+    d2.max_tiles = max_mt;
+    d2.rowmap = expert_rows;
+    d2.counts = expert_count;
+    d2.goff = expert_offsets;
+    d2.out = ypool;
+    d2.ldo = L;
+    d2.status = status;
+    d2.name = "gemm_expert_down";
+    return gemm_launch(d2, st);
 }
 
 int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,

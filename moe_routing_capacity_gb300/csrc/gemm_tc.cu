@@ -84,6 +84,7 @@ struct KParams {
     const int* tile_count;
     const int* rowmap;
     const int* counts;
+    const int* goff;        // optional per-group first row (ragged groups)
     int rowmap_ld;
     const uint16_t* gather_src;
     long long gather_pitch;
@@ -205,6 +206,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         parA = (parA & ~(1u << sa)) | (pa << sa);
                         if (AMODE == A_DENSE)
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], kx, m0);
+                        else if (p.goff)   // ragged groups: rows of one flat 2-D matrix
+                            tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], kx, p.goff[g] + m0);
                         else
                             tma_load_3d(a_dst, &p.mapA[seg], &fullA[sa], kx, m0, g);
                         if (++sa == AST) {
@@ -339,7 +342,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 row_ok = m < p.counts[g];
                 orow = m;
                 if (EPI == EPI_SCATTER && row_ok)
-                    orow = p.rowmap[static_cast<long long>(g) * p.rowmap_ld + m];
+                    orow = p.rowmap[(p.goff ? static_cast<long long>(p.goff[g])
+                                            : static_cast<long long>(g) * p.rowmap_ld) + m];
             }
             if (EPI == EPI_SPLIT && nb >= p.nsplit) {
                 float* out = reinterpret_cast<float*>(p.out2) + orow * p.ldo2;
@@ -397,7 +401,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 }
             } else if (EPI == EPI_SWIGLU) {
                 uint16_t* out = reinterpret_cast<uint16_t*>(p.out) +
-                                static_cast<long long>(g) * p.out_gstride + orow * p.ldo;
+                                (p.goff ? (p.goff[g] + orow) * p.ldo
+                                        : static_cast<long long>(g) * p.out_gstride + orow * p.ldo);
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t gr[32], ur[32];
@@ -474,7 +479,9 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             int g, m0, nb;
             decode_tile<AMODE>(p, tile, g, m0, nb);
             nxt_cnt = p.counts[g] - m0;   // valid rows of the tile, from its first
-            const int* rl = p.rowmap + static_cast<long long>(g) * p.rowmap_ld + m0;
+            const int* rl = p.rowmap + m0 +
+                            (p.goff ? static_cast<long long>(p.goff[g])
+                                    : static_cast<long long>(g) * p.rowmap_ld);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int m = rg + 16 * i;
@@ -622,7 +629,10 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
             if ((rc = map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM))) return rc;
             if ((rc = map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box))) return rc;
         } else {
-            if (d.a_mode == A_GROUPED &&
+            if (d.a_mode == A_GROUPED && d.goff &&
+                (rc = map2d(&p.mapA[s], g.A, g.K, d.rows_per_group, g.lda, BM)))
+                return rc;   // ragged: rows_per_group = rows of the whole flat matrix
+            if (d.a_mode == A_GROUPED && !d.goff &&
                 (rc = map3d(&p.mapA[s], g.A, g.K, d.rows_per_group, d.groups, g.lda, d.a_gstride,
                             BM)))
                 return rc;
@@ -661,6 +671,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.tile_count = d.tile_count;
     p.rowmap = d.rowmap;
     p.counts = d.counts;
+    p.goff = d.goff;
     p.rowmap_ld = d.rowmap_ld;
     p.gather_src = d.gather_src;
     p.gather_pitch = d.gather_pitch;

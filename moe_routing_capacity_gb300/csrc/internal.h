@@ -65,8 +65,10 @@ struct GemmDesc {
     const int32_t* tile_list;
     const int32_t* tile_count;
     int max_tiles;          // upper bound of the tile list length
-    const int32_t* rowmap;  // [groups, rowmap_ld]
+    const int32_t* rowmap;  // [groups, rowmap_ld], or flat with goff
     const int32_t* counts;  // [groups]
+    const int32_t* goff;    // optional [groups]: first row of each group in a flat
+                            // (ragged) row map, grouped A and grouped SwiGLU output
     int rowmap_ld;
     const uint16_t* gather_src;
     int64_t gather_pitch;   // elements between gathered rows
@@ -99,17 +101,24 @@ struct DispatchGeom {
     int64_t T_s;
     int c_send, c_recv;
     int64_t pool_rows;
+    int ragged;   // 1: dropless ragged layout (no caps, pool of T*k rows)
 };
 
-// Scratch layout of moe_dispatch_pooled.
+// Scratch layout of moe_dispatch_pooled (and of the ragged dispatch, which
+// adds the block offsets).
 struct DispatchWs {
-    size_t send_row_off, rloc_off, cnt_se_off, base_se_off, demand_off, total;
+    size_t send_row_off, rloc_off, cnt_se_off, base_se_off, demand_off, blk_off_off, total;
 };
 DispatchWs dispatch_ws_layout(const DispatchGeom& g);
 
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
                     int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream);
+
+int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
+                           uint16_t* pool, int32_t* slot_of, uint8_t* drop,
+                           int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
+                           moe_drop_stats_t* stats, cudaStream_t stream);
 
 // Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
 int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,

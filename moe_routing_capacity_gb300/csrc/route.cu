@@ -135,6 +135,8 @@ DispatchWs dispatch_ws_layout(const DispatchGeom& g) {
     w.cnt_se_off = o;    o = align256(o + static_cast<size_t>(g.S) * g.E * sizeof(int32_t));
     w.base_se_off = o;   o = align256(o + static_cast<size_t>(g.S) * g.E * sizeof(int32_t));
     w.demand_off = o;    o = align256(o + static_cast<size_t>(g.S) * g.D * g.W * sizeof(int32_t));
+    w.blk_off_off = o;
+    if (g.ragged) o = align256(o + (static_cast<size_t>(g.S) * g.D * g.W + 1) * sizeof(int32_t));
     w.total = o;
     return w;
 }
@@ -156,6 +158,7 @@ __global__ void dispatch_init_kernel(DispatchGeom g, uint16_t* __restrict__ pool
         stats->status = 0;
         stats->reserved = 0;
     }
+    if (g.ragged) return;   // every row and every list entry gets written
     const int64_t pitch = g.L + 8;
     for (int64_t r = tid; r < g.pool_rows; r += nthr)
         *reinterpret_cast<int4*>(pool + r * pitch + g.L) = make_int4(-1, -1, -1, 0);
@@ -262,8 +265,11 @@ __global__ void __launch_bounds__(SEND_WARPS * 32) dispatch_send_kernel(
             __syncwarp();
             if (v) {
                 const int64_t a = wbase + 32 * i + lane;
+                // capped: the pool row; ragged: (block, slot in block), resolved
+                // once the block offsets are known
+                const int64_t blk = static_cast<int64_t>(key) * g.S + s;
                 send_row[first + a] =
-                    kept ? (static_cast<int64_t>(key) * g.S + s) * g.c_send + slot : -1;
+                    !kept ? -1 : g.ragged ? (blk << 32) | slot : blk * g.c_send + slot;
                 if (!kept) ++dropped;
             }
             kept_mask |= (kept ? 1u : 0u) << i;
@@ -359,7 +365,8 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
     DispatchGeom g, const uint16_t* __restrict__ z, const int32_t* __restrict__ idx,
     const int64_t* __restrict__ send_row, const int32_t* __restrict__ rloc,
     const int32_t* __restrict__ base_se, uint16_t* __restrict__ pool,
-    int32_t* __restrict__ slot_of, uint8_t* __restrict__ drop, int32_t* __restrict__ expert_rows) {
+    int32_t* __restrict__ slot_of, uint8_t* __restrict__ drop, int32_t* __restrict__ expert_rows,
+    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ eoff) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= g.T) return;
@@ -372,12 +379,15 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
         const int64_t a = t * g.k + lane;
         e = idx[a];
         row = send_row[a];
+        if (g.ragged && row >= 0) row = blk_off[row >> 32] + (row & 0xffffffffll);
         int32_t so = -1;
         uint8_t dr = 1;
         if (row >= 0 && e >= 0 && e < g.E) {
             const int r = base_se[s * g.E + e] + rloc[a];
             if (r < g.c_recv) {
-                expert_rows[static_cast<int64_t>(e) * g.c_recv + r] = static_cast<int32_t>(row);
+                const int64_t at = g.ragged ? static_cast<int64_t>(eoff[e]) + r
+                                            : static_cast<int64_t>(e) * g.c_recv + r;
+                expert_rows[at] = static_cast<int32_t>(row);
                 so = static_cast<int32_t>(row);
                 dr = 0;
             } else {
@@ -448,10 +458,115 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
     const int nchunk = g.L / 8;
     if (nchunk <= 32 * 4)
         dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
-                                                       slot_of, drop, expert_rows);
+                                                       slot_of, drop, expert_rows, nullptr,
+                                                       nullptr);
     else
         dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
-                                                        slot_of, drop, expert_rows);
+                                                        slot_of, drop, expert_rows, nullptr,
+                                                        nullptr);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_pack");
+    return MOE_OK;
+}
+
+// ==================================================================== ragged offsets
+
+// Exclusive prefix over `n` values read through `get(i)`, written to
+// out[0..n] (out[n] = total), by one CTA of 1024 threads in chunks.
+template <typename Get>
+__device__ void block_exclusive_scan(int n, Get get, int32_t* __restrict__ out) {
+    __shared__ int warp_sum[32];
+    __shared__ int carry;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
+        const int v = i < n ? get(i) : 0;
+        int incl = v;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sum[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ws, off);
+                if (lane >= off) ws += y;
+            }
+            warp_sum[lane] = ws;
+        }
+        __syncthreads();
+        const int excl = carry + (wid ? warp_sum[wid - 1] : 0) + incl - v;
+        if (i < n) out[i] = excl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = excl + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[n] = carry;
+}
+
+// Ragged pool blocks in (destination, wave, source) order: block b = key*S + s
+// holds demand[s][key] rows and starts at the exclusive prefix of the counts;
+// expert e's rows start at the prefix of the expert totals.
+__global__ void __launch_bounds__(1024) ragged_offsets_kernel(DispatchGeom g,
+                                                              const int32_t* __restrict__ demand,
+                                                              const int32_t* __restrict__ counts,
+                                                              int32_t* __restrict__ blk_off,
+                                                              int32_t* __restrict__ eoff) {
+    const int nkey = g.D * g.W;
+    block_exclusive_scan(nkey * g.S, [&](int b) { return demand[(b % g.S) * nkey + b / g.S]; },
+                         blk_off);
+    __syncthreads();
+    block_exclusive_scan(g.E, [&](int e) { return counts[e]; }, eoff);
+}
+
+int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
+                           uint16_t* pool, int32_t* slot_of, uint8_t* drop,
+                           int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
+                           moe_drop_stats_t* stats, cudaStream_t st) {
+    const DispatchWs L = dispatch_ws_layout(g);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int64_t* send_row = reinterpret_cast<int64_t*>(w + L.send_row_off);
+    int32_t* rloc = reinterpret_cast<int32_t*>(w + L.rloc_off);
+    int32_t* cnt_se = reinterpret_cast<int32_t*>(w + L.cnt_se_off);
+    int32_t* base_se = reinterpret_cast<int32_t*>(w + L.base_se_off);
+    int32_t* demand = reinterpret_cast<int32_t*>(w + L.demand_off);
+    int32_t* blk_off = reinterpret_cast<int32_t*>(w + L.blk_off_off);
+
+    dispatch_init_kernel<<<1, 32, 0, st>>>(g, pool, expert_rows, stats);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_init");
+    const size_t shm =
+        static_cast<size_t>(SEND_WARPS + 1) * (g.D * g.W + g.E) * sizeof(int32_t);
+    if (shm > 200 * 1024) return MOE_EINVAL;
+    if (shm > 48 * 1024 &&
+        cudaFuncSetAttribute(dispatch_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(shm)) != cudaSuccess)
+        return MOE_ECUDA;
+    dispatch_send_kernel<<<g.S, SEND_WARPS * 32, shm, st>>>(g, idx, send_row, rloc, cnt_se,
+                                                            demand, stats);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_send");
+    dispatch_recv_scan_kernel<<<(g.E + 127) / 128, 128, 0, st>>>(g, cnt_se, base_se, expert_count,
+                                                                  stats);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "dispatch_recv_scan");
+    ragged_offsets_kernel<<<1, 1024, 0, st>>>(g, demand, expert_count, blk_off, expert_offsets);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "ragged_offsets");
+    if (g.T == 0) return MOE_OK;
+    const unsigned grid = static_cast<unsigned>((g.T + 7) / 8);
+    if (g.L / 8 <= 32 * 4)
+        dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
+                                                       slot_of, drop, expert_rows, blk_off,
+                                                       expert_offsets);
+    else
+        dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
+                                                        slot_of, drop, expert_rows, blk_off,
+                                                        expert_offsets);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_pack");
     return MOE_OK;

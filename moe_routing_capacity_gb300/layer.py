@@ -22,9 +22,11 @@ class PooledWaveMoE:
     histogram (``self.hist``) into the router bias, so it applies from the
     next batch on."""
 
-    def __init__(self, cfg, weights: dict, device="cuda", balance_alpha=None):
+    def __init__(self, cfg, weights: dict, device="cuda", balance_alpha=None,
+                 dropless=False):
         self.cfg = cfg
-        self.plan = abi.plan(cfg)
+        self.dropless = dropless
+        self.plan = abi.plan_ragged(cfg) if dropless else abi.plan(cfg)
         self.device = torch.device(device)
         dev = self.device
         T, d, L, E, k = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.top_k
@@ -41,7 +43,11 @@ class PooledWaveMoE:
         self.pool = e(p.pool_rows, L + 8, dt=torch.int16)
         self.slot_of = e(T, k, dt=torch.int32)
         self.drop = e(T, k, dt=torch.uint8)
-        self.expert_rows = e(E, p.c_recv, dt=torch.int32)
+        if dropless:    # flat row list with per-expert offsets
+            self.expert_rows = e(T * k, dt=torch.int32)
+            self.expert_offsets = e(E + 1, dt=torch.int32)
+        else:
+            self.expert_rows = e(E, p.c_recv, dt=torch.int32)
         self.expert_count = e(E, dt=torch.int32)
         self.stats = torch.zeros(abi.STATS_WORDS, dtype=torch.int64, device=dev)
         self.ws_ffn = e(max(1, p.ws_ffn_bytes), dt=torch.uint8)
@@ -65,13 +71,24 @@ class PooledWaveMoE:
         abi.latent_proj(x, self.w["W_ld"], self.z, self.status, stream)
 
     def dispatch(self, stream=None):
-        abi.dispatch_pooled(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool, self.slot_of,
-                            self.drop, self.expert_rows, self.expert_count, self.stats, stream)
+        if self.dropless:
+            abi.dispatch_ragged(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
+                                self.slot_of, self.drop, self.expert_offsets, self.expert_rows,
+                                self.expert_count, self.stats, stream)
+        else:
+            abi.dispatch_pooled(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
+                                self.slot_of, self.drop, self.expert_rows, self.expert_count,
+                                self.stats, stream)
 
     def experts(self, stream=None):
-        abi.expert_ffn_grouped(self.cfg, self.pool, self.expert_rows, self.expert_count,
-                               self.w["Wg"], self.w["Wu"], self.w["Wd"], self.ws_ffn, self.ypool,
-                               self.status, stream)
+        if self.dropless:
+            abi.expert_ffn_ragged(self.cfg, self.pool, self.expert_offsets, self.expert_rows,
+                                  self.expert_count, self.w["Wg"], self.w["Wu"], self.w["Wd"],
+                                  self.ws_ffn, self.ypool, self.status, stream)
+        else:
+            abi.expert_ffn_grouped(self.cfg, self.pool, self.expert_rows, self.expert_count,
+                                   self.w["Wg"], self.w["Wu"], self.w["Wd"], self.ws_ffn,
+                                   self.ypool, self.status, stream)
 
     def combine(self, x, out=None, stream=None):
         abi.combine(self.cfg, self.ypool, self.slot_of, self.gate_w, self.w["W_lu"], x,

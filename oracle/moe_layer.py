@@ -42,6 +42,7 @@ __all__ = [
     "bf16_round", "silu", "Plan", "make_plan", "router_logits", "router_topk",
     "latent_down", "placement", "dispatch", "pack_pool", "expert_ffn",
     "experts_forward", "combine", "shared_act", "output", "layer", "balance_update",
+    "dispatch_ragged", "layer_ragged",
     "TIE_EPS", "EMPTY_TAG", "DROP_KEPT", "DROP_SEND", "DROP_RECV",
 ]
 
@@ -381,6 +382,69 @@ def output(c, a, W_lu, Wsd) -> np.ndarray:
     for s in range(Wsd.shape[0]):
         acc = acc + a[:, s * Hs:(s + 1) * Hs] @ Wsd[s].T
     return bf16_round(acc)
+
+
+# ---------------------------------------------------------------- dropless ragged dispatch
+
+def dispatch_ragged(idx, p: Plan) -> dict:
+    """Dropless ragged dispatch, the pages' fallback if drops stay too high.
+
+    [LJ-HK] sec. 四: a ragged all-to-all without drops.  Reading: the same
+    destination-major pool order (destination, wave, source, priority), but
+    each (source, destination, wave) block holds exactly the rows routed
+    there, so blocks start at the exclusive prefix of the counts and the pool
+    has T*k rows; nothing is dropped; expert e's rows, in priority order,
+    are expert_rows[expert_offsets[e] : expert_offsets[e+1]].
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape
+    e = idx.reshape(-1)
+    tok = np.repeat(np.arange(T), k)
+    src = tok // p.T_s if p.T_s else tok
+    dst, _, wv = placement(e, p)
+    gkey = (dst * p.W + wv) * p.S + src                  # block order in the pool
+    slot = _rank_within_key(gkey)
+    counts = np.bincount(gkey, minlength=p.D * p.W * p.S)
+    block_start = np.r_[0, np.cumsum(counts)[:-1]]
+    row = block_start[gkey] + slot
+    r = _rank_within_key(e)
+    ecount = np.bincount(e, minlength=p.E)
+    eoff = np.r_[0, np.cumsum(ecount)]
+    expert_rows = np.full(T * k, -1, dtype=np.int64)
+    expert_rows[eoff[e] + r] = row
+    return dict(slot_of=row.reshape(T, k).astype(np.int32), send_row=row.reshape(T, k),
+                drop=np.zeros((T, k), dtype=np.uint8), expert_offsets=eoff.astype(np.int32),
+                expert_rows=expert_rows.astype(np.int32), count=ecount.astype(np.int32),
+                block_counts=counts.reshape(p.D, p.W, p.S),
+                stats=dict(assignments=T * k, kept=T * k, dropped_send=0, dropped_recv=0))
+
+
+def layer_ragged(cfg, t: dict) -> dict:
+    """The whole layer with the dropless ragged dispatch."""
+    p = make_plan(cfg)
+    l32 = router_logits(t["x"], t["Wr"], t.get("bias"))
+    idx, w, tie = router_topk(l32, cfg.top_k)
+    z = latent_down(t["x"], t["W_ld"])
+    disp = dispatch_ragged(idx, p)
+    T, k = idx.shape
+    payload = np.full((T * k, z.shape[1]), np.nan)
+    tags = np.tile(np.array(EMPTY_TAG, dtype=np.int32), (T * k, 1))
+    for tt in range(T):
+        for j in range(k):
+            rr = disp["slot_of"][tt, j]
+            payload[rr] = z[tt]
+            tags[rr] = (idx[tt, j], tt, j, 0)
+    Y = {}
+    for e in range(p.E):
+        rows = disp["expert_rows"][disp["expert_offsets"][e]:disp["expert_offsets"][e + 1]]
+        if rows.size:
+            for rr, y in zip(rows, expert_ffn(payload[rows], t["Wg"][e], t["Wu"][e], t["Wd"][e])):
+                Y[int(rr)] = y
+    c = combine(lambda rr: Y[rr], disp["slot_of"], w, z.shape[1])
+    a = shared_act(t["x"], t["Wsg"], t["Wsu"])
+    out = output(c, a, t["W_lu"], t["Wsd"])
+    return dict(plan=p, logits=l32, idx=idx, w=w, tie=tie, z=z, disp=disp, payload=payload,
+                tags=tags, Y=Y, c=c, a=a, out=out)
 
 
 # ---------------------------------------------------------------- balancing bias

@@ -94,3 +94,28 @@ def dispatch_rules_hold(idx: np.ndarray, slot_of, drop, expert_rows, count, plan
         assert count[e] == len(rr)
         assert list(expert_rows[e, : len(rr)]) == rr
         assert (expert_rows[e, len(rr):] == -1).all()
+
+
+def ragged_rules_hold(idx: np.ndarray, slot_of, expert_offsets, expert_rows, count, plan):
+    """Property check of a dropless ragged dispatch for the routing it was
+    given: the pool is a permutation of 0..T*k-1 ordered by (destination,
+    wave, source) blocks in priority order, and each expert's list holds its
+    rows in priority order."""
+    T, k = idx.shape
+    p = plan
+    keys = []
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            dst, q = e // p.E_l, e % p.E_l
+            keys.append(((dst, q // p.E_w, t // p.T_s), t, j))
+    for r, (_, t, j) in enumerate(sorted(keys)):
+        assert slot_of[t, j] == r, (t, j)
+    per = {}
+    for t in range(T):
+        for j in range(k):
+            per.setdefault(int(idx[t, j]), []).append(int(slot_of[t, j]))
+    for e in range(p.E):
+        rows = per.get(e, [])
+        assert count[e] == len(rows)
+        assert list(expert_rows[expert_offsets[e]:expert_offsets[e + 1]]) == rows

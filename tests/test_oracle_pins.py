@@ -447,3 +447,48 @@ def test_balance_update_invariants():
     np.testing.assert_allclose(b0, 0.0, atol=1e-17)
     _, bz = O.balance_update(np.zeros((0, 4), dtype=np.int64), np.zeros(E, dtype=np.int64), 1.0, E)
     assert (bz == 0).all()
+
+
+# ------------------------------------------------------------------ dropless ragged dispatch
+
+@pytest.mark.parametrize("seed", range(6))
+def test_ragged_dispatch_structure(seed):
+    rng = np.random.default_rng(200 + seed)
+    cfg = _cfg(T=96, n_ranks=4, n_experts=24, top_k=3, n_waves=[1, 3][seed % 2])
+    p = O.make_plan(cfg)
+    idx = _random_routing(rng, cfg.T, cfg.n_experts, cfg.top_k)
+    if seed >= 3:
+        idx[:, 0] = 0                      # everyone also picks expert 0 (kept anyway)
+        idx = np.stack([np.r_[0, rng.choice(np.arange(1, 24), 2, replace=False)] for _ in range(96)])
+    d = O.dispatch_ragged(idx, p)
+    rows = d["slot_of"].reshape(-1)
+    assert sorted(rows.tolist()) == list(range(cfg.T * cfg.top_k))      # a permutation: no gaps
+    assert (d["drop"] == 0).all()
+    # brute force: rows grouped by (dst, wave, src) in that order, priority inside
+    prio = [(t, j) for t in range(cfg.T) for j in range(cfg.top_k)]
+    def blk(tj):
+        e = int(idx[tj]); dst = e // p.E_l; wv = (e % p.E_l) // p.E_w
+        return (dst, wv, tj[0] // p.T_s)
+    order = sorted(prio, key=lambda tj: (blk(tj), tj))
+    for r, tj in enumerate(order):
+        assert d["slot_of"][tj] == r
+    for e in range(p.E):
+        mine = [d["slot_of"][tj] for tj in prio if idx[tj] == e]
+        got = d["expert_rows"][d["expert_offsets"][e]:d["expert_offsets"][e + 1]]
+        assert got.tolist() == mine
+
+
+def test_ragged_layer_equals_unbounded_capped_layer():
+    """Without caps nothing drops in either layout, so every token's result
+    is the same whether the pools are padded (cf = inf) or ragged."""
+    cfg = wl.TINY.with_(cf_send=float("inf"), cf_recv=float("inf"))
+    t = _tiny_inputs(cfg)
+    a = O.layer(cfg, t)
+    b = O.layer_ragged(cfg, t)
+    assert a["disp"]["stats"]["kept"] == b["disp"]["stats"]["kept"] == cfg.T * cfg.top_k
+    np.testing.assert_array_equal(a["c"], b["c"])
+    np.testing.assert_array_equal(a["out"], b["out"])
+    for tt in range(cfg.T):
+        for j in range(cfg.top_k):
+            np.testing.assert_array_equal(a["Y"][int(a["disp"]["slot_of"][tt, j])],
+                                          b["Y"][int(b["disp"]["slot_of"][tt, j])])
