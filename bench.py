@@ -200,6 +200,19 @@ def time_oracle(cfg, host):
     return time.perf_counter() - t0
 
 
+def replica_throughput(elapsed_s: float, tokens_per_step: int, steps: int, dev):
+    """Whole-job throughput of independent replicas: every rank ran `steps`
+    steps of `tokens_per_step` tokens; the job took as long as the slowest
+    rank.  Returns (tokens/s over all ranks, max elapsed seconds)."""
+    import torch.distributed as dist
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    if world > 1:
+        t = torch.tensor([elapsed_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+    return world * tokens_per_step * steps / elapsed_s, elapsed_s
+
+
 def cores_used():
     for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(v, "").isdigit():
@@ -209,9 +222,15 @@ def cores_used():
 
 # ------------------------------------------------------------------ arms
 
+def reference_runs_on(rank: int) -> bool:
+    """The reference arm (the CPU oracle) runs on rank 0 only; other ranks
+    exit without work."""
+    return rank == 0
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm (rank 0 only)."""
-    if rank != 0:
+    if not reference_runs_on(rank):
         return
     cfg = wl.CONFIGS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -284,11 +303,8 @@ def run_gb300(args, rank, world, local_rank):
     elapsed = ev0.elapsed_time(ev1) / 1e3
     if world > 1:
         torch.distributed.barrier()
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    value, elapsed = replica_throughput(elapsed, cfg.T, args.steps, dev)
     assert int(m.status.item()) == 0, "device status word set during the timed region"
-    value = world * cfg.T * args.steps / elapsed
 
     # ---- per-kernel times from the trace (event after each launch)
     per = {}
@@ -353,12 +369,9 @@ def run_gb300(args, rank, world, local_rank):
         pipe.synchronize()
         torch.cuda.synchronize()
         el = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([el], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            el = float(t.item())
+        e2e_value, el = replica_throughput(el, cfg.T, n_e2e, dev)
         assert int(m.status.item()) == 0
-        e2e = {"value": world * cfg.T * n_e2e / el, "unit": UNIT,
+        e2e = {"value": e2e_value, "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": oh[0].numel() * oh[0].element_size() + sh[0].numel() * 8,
                "steps": n_e2e, "timer": "host wall clock around the submitted steps",
