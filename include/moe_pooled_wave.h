@@ -144,6 +144,20 @@ int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* 
 int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K, int32_t N,
                     uint16_t* out, int32_t* status, void* stream);
 
+/* General bf16 product on the tensor cores with fp32 accumulation (the
+ * building block of the layer's backward pass, whose products over the token
+ * axis read their operands MN-major):
+ *   out[m, n] = sum_k A(m, k) * B(n, k),  m < M, n < N, k < K
+ *   A(m, k) = A[m*lda + k] if a_mn == 0 (A stored [M, K]),
+ *             A[k*lda + m] if a_mn == 1 (A stored [K, M]);
+ *   B(n, k) = B[n*ldb + k] if b_mn == 0, B[k*ldb + n] if b_mn == 1;
+ *   out [M, N] row-major with leading dimension ldo, bf16 (out_f32 = 0,
+ *   N % 8 == 0) or fp32 (out_f32 = 1).
+ * K, lda, ldb multiples of 8; pointers 16-byte aligned. */
+int moe_matmul(const uint16_t* A, int a_mn, int64_t lda, const uint16_t* B, int b_mn,
+               int64_t ldb, int64_t M, int32_t N, int32_t K, void* out, int out_f32, int64_t ldo,
+               int32_t* status, void* stream);
+
 /* moe_router_topk and moe_latent_proj(x, W_ld) in one pass over x: both read
  * the token states (lamjinlab zh-HK section 二: the router picks the experts,
  * the latent projection compresses the routed activations), so one GEMM

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_pooled_wave.so")
 MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2, -3, -4, -5
 
 # Every entry point the header declares (checked by the tests).
-EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project",
+EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project", "moe_matmul",
            "moe_dispatch_pooled",
            "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update",
            "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.moe_router_topk.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_latent_proj.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp]
         L.moe_route_project.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.moe_matmul.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, i64, i32, i32, vp,
+                                 ctypes.c_int, i64, vp, vp]
         L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
         L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
@@ -166,6 +168,16 @@ def latent_proj(inp, W, out, status, stream=None):
         raise ValueError("shape mismatch")
     _check("moe_latent_proj", lib().moe_latent_proj(
         _ptr(inp, bf16), _ptr(W, bf16), M, K, N, _ptr(out, bf16), _ptr(status, i32),
+        _stream(stream)))
+
+
+def matmul(A, B, M, N, K, out, status, a_mn=False, b_mn=False, stream=None):
+    """out[M, N] = sum_k A(m, k) B(n, k); A stored [M, K] (or [K, M] if a_mn),
+    B stored [N, K] (or [K, N] if b_mn); out bf16 or fp32, row-major."""
+    lda, ldb = A.shape[1], B.shape[1]
+    _check("moe_matmul", lib().moe_matmul(
+        _ptr(A, bf16), int(bool(a_mn)), lda, _ptr(B, bf16), int(bool(b_mn)), ldb, M, N, K,
+        _ptr(out), int(out.dtype == torch.float32), out.shape[1], _ptr(status, i32),
         _stream(stream)))
 
 

@@ -327,6 +327,36 @@ int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K,
     return gemm_launch(d, static_cast<cudaStream_t>(stream));
 }
 
+int moe_matmul(const uint16_t* A, int a_mn, int64_t lda, const uint16_t* B, int b_mn,
+               int64_t ldb, int64_t M, int32_t N, int32_t K, void* out, int out_f32, int64_t ldo,
+               int32_t* status, void* stream) {
+    if (M < 0 || N <= 0 || K <= 0 || lda <= 0 || ldb <= 0 || ldo < N) return MOE_EINVAL;
+    if (lda % 8 || ldb % 8 || (out_f32 ? ldo % 4 : ldo % 8) || (!out_f32 && N % 8))
+        return MOE_EINVAL;
+    if ((!a_mn && lda < K) || (a_mn && lda < M) || (!b_mn && ldb < K) || (b_mn && ldb < N))
+        return MOE_EINVAL;
+    if (M == 0) return MOE_OK;
+    if (!A || !B || !out || !status || !aligned16(A) || !aligned16(B) || !aligned16(out))
+        return MOE_EINVAL;
+    GemmDesc d;
+    std::memset(&d, 0, sizeof(d));
+    d.a_mode = A_DENSE;
+    d.epi = out_f32 ? EPI_F32 : EPI_BF16;
+    d.a_mn = a_mn ? 1 : 0;
+    d.b_mn = b_mn ? 1 : 0;
+    d.bn = 256;
+    d.M = M;
+    d.N = N;
+    d.nseg = 1;
+    d.seg[0] = GemmSeg{A, lda, B, ldb, K};
+    d.b_rows = N;
+    d.out = out;
+    d.ldo = ldo;
+    d.status = status;
+    d.name = "gemm_matmul";
+    return gemm_launch(d, static_cast<cudaStream_t>(stream));
+}
+
 int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx, void* ws,
                         size_t ws_bytes, uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                         int32_t* expert_rows, int32_t* expert_count, moe_drop_stats_t* stats,

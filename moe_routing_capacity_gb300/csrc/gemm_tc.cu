@@ -121,13 +121,20 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-template <int BN, int AMODE, int EPI>
+// MAJ bit 0: A is MN-major (stored [K, M], M contiguous); bit 1: B is
+// MN-major (stored [K, N]).  MN-major tiles arrive as 64 x 64 TMA boxes, one
+// per 64 M/N elements, 8 KB apart.
+template <int BN, int AMODE, int EPI, int MAJ>
 __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     gemm_tc_kernel(const __grid_constant__ KParams p) {
     using C = TileCfg<BN, AMODE>;
     constexpr int AST = C::A_STAGES;
     constexpr int BST = C::B_STAGES;
     constexpr bool B3D = (AMODE != A_DENSE);
+    constexpr bool A_MN = (MAJ & 1) != 0;
+    constexpr bool B_MN = (MAJ & 2) != 0;
+    static_assert(!A_MN || AMODE == A_DENSE, "MN-major A: dense TMA tiles only");
+    static_assert(!B_MN || (BN <= 256 && EPI != EPI_SPLIT), "MN-major B: plain tiles only");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -204,7 +211,10 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         mbar_arrive_expect_tx(&fullA[sa], A_STAGE_BYTES);
                         armedA |= 1u << sa;
                         parA = (parA & ~(1u << sa)) | (pa << sa);
-                        if (AMODE == A_DENSE)
+                        if (A_MN) {
+                            tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], m0, kx);
+                            tma_load_2d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, kx);
+                        } else if (AMODE == A_DENSE)
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], kx, m0);
                         else if (p.goff)   // ragged groups: rows of one flat 2-D matrix
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], kx, p.goff[g] + m0);
@@ -223,7 +233,21 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     mbar_arrive_expect_tx(&fullB[sb], C::B_STAGE_BYTES);
                     armedB |= 1u << sb;
                     parB = (parB & ~(1u << sb)) | (pb << sb);
-                    if (EPI == EPI_SWIGLU) {
+                    if (B_MN) {
+                        // BN/64 boxes of 64 N x 64 K; SwiGLU: gate then up halves
+#pragma unroll
+                        for (int h = 0; h < BN / 64; ++h) {
+                            const bool up = EPI == EPI_SWIGLU && h >= BN / 128;
+                            const int n = EPI == EPI_SWIGLU
+                                              ? nb * (BN / 2) + (h % (BN / 128)) * 64
+                                              : nb * BN + h * 64;
+                            const CUtensorMap* mp = up ? &p.mapBup : &p.mapB[seg];
+                            if (B3D)
+                                tma_load_3d(b_dst + h * 8192, mp, &fullB[sb], n, kx, g);
+                            else
+                                tma_load_2d(b_dst + h * 8192, mp, &fullB[sb], n, kx);
+                        }
+                    } else if (EPI == EPI_SWIGLU) {
                         const int n_half = nb * (BN / 2);
                         const uint32_t b_dst2 = b_dst + (BN / 2) * BK * 2;
                         if (B3D) {
@@ -271,8 +295,12 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         if (lane == 0) {
             const int ntiles = num_tiles<AMODE>(p);
             constexpr int N0 = BN <= 256 ? BN : 256;          // first MMA's N
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, N0);
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, N0, A_MN, B_MN);
             constexpr uint32_t idesc_hi = idesc_bf16_f32(BM, BN > 256 ? BN - 256 : 16);
+            // descriptor step per 16-wide K slice: 32 B along a K-major row,
+            // 16 rows of 128 B down an MN-major box
+            constexpr uint32_t a_step = A_MN ? (2048u >> 4) : (32u >> 4);
+            constexpr uint32_t b_step = B_MN ? (2048u >> 4) : (32u >> 4);
             uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
@@ -287,11 +315,13 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_k_sw128(smem_u32(sA + sa * A_STAGE_BYTES));
-                    const uint64_t bd = sdesc_k_sw128(smem_u32(sB + sb * C::B_STAGE_BYTES));
+                    const uint32_t a_s = smem_u32(sA + sa * A_STAGE_BYTES);
+                    const uint32_t b_s = smem_u32(sB + sb * C::B_STAGE_BYTES);
+                    const uint64_t ad = A_MN ? sdesc_mn_sw128(a_s) : sdesc_k_sw128(a_s);
+                    const uint64_t bd = B_MN ? sdesc_mn_sw128(b_s) : sdesc_k_sw128(b_s);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                        mma_bf16(d_tmem, ad + a_step * kk, bd + b_step * kk, idesc,
                                  (kb | kk) != 0 ? 1u : 0u);
                         if (BN > 256)   // columns 256.. from B rows 256.. (32 KB further)
                             mma_bf16(d_tmem + 256, ad + 2u * kk, bd + (32768u >> 4) + 2u * kk,
@@ -589,10 +619,10 @@ static int map3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
     return make_map(m, base, 3, dims, str, box_rows);
 }
 
-template <int BN, int AMODE, int EPI>
+template <int BN, int AMODE, int EPI, int MAJ = 0>
 static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
     using C = TileCfg<BN, AMODE>;
-    auto kern = gemm_tc_kernel<BN, AMODE, EPI>;
+    auto kern = gemm_tc_kernel<BN, AMODE, EPI, MAJ>;
     // Attribute setting is per device; cheap and idempotent, done every launch.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
         cudaSuccess)
@@ -601,9 +631,9 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
-template <int BN, int AMODE, int EPI>
+template <int BN, int AMODE, int EPI, int MAJ = 0>
 static int launch_traced(const KParams& p, int grid, cudaStream_t st, const char* name) {
-    const int rc = launch_inst<BN, AMODE, EPI>(p, grid, st);
+    const int rc = launch_inst<BN, AMODE, EPI, MAJ>(p, grid, st);
     if (rc == MOE_OK) trace_after(st, name ? name : "gemm");
     return rc;
 }
@@ -626,8 +656,20 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         if (g.K <= 0 || (g.K % 8)) return MOE_EINVAL;
         p.seg_kb[s + 1] = p.seg_kb[s] + (g.K + BK - 1) / BK;
         if (d.a_mode == A_DENSE) {
-            if ((rc = map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM))) return rc;
-            if ((rc = map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box))) return rc;
+            if (d.a_mn)   // [K, M] storage: 64 x 64 boxes, M inner
+                rc = map2d(&p.mapA[s], g.A, d.M, g.K, g.lda, 64);
+            else
+                rc = map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM);
+            if (rc) return rc;
+            if (d.b_mn)
+                rc = map2d(&p.mapB[s], g.B, d.b_rows, g.K, g.ldb, 64);
+            else
+                rc = map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box);
+            if (rc) return rc;
+        } else if (d.b_mn) {
+            if (d.a_mode == A_GROUPED || d.a_mn) return MOE_EINVAL;
+            if ((rc = map3d(&p.mapB[s], g.B, d.b_rows, g.K, d.groups, g.ldb, d.b_gstride, 64)))
+                return rc;
         } else {
             if (d.a_mode == A_GROUPED && d.goff &&
                 (rc = map2d(&p.mapA[s], g.A, g.K, d.rows_per_group, g.lda, BM)))
@@ -647,7 +689,12 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     }
     if (d.epi == EPI_SWIGLU) {
         if (d.nseg != 1 || !d.B_up) return MOE_EINVAL;
-        if (d.a_mode == A_DENSE)
+        if (d.b_mn && d.a_mode == A_DENSE)
+            rc = map2d(&p.mapBup, d.B_up, d.b_rows, d.seg[0].K, d.seg[0].ldb, 64);
+        else if (d.b_mn)
+            rc = map3d(&p.mapBup, d.B_up, d.b_rows, d.seg[0].K, d.groups, d.seg[0].ldb,
+                       d.b_gstride, 64);
+        else if (d.a_mode == A_DENSE)
             rc = map2d(&p.mapBup, d.B_up, d.seg[0].K, d.b_rows, d.seg[0].ldb, b_box);
         else
             rc = map3d(&p.mapBup, d.B_up, d.seg[0].K, d.b_rows, d.groups, d.seg[0].ldb,
@@ -685,15 +732,27 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     if (tiles <= 0) return MOE_OK;
     const int grid = tiles < sms ? tiles : sms;
 
-    const int key = d.bn * 100 + d.a_mode * 10 + d.epi;
+    if ((d.a_mn || d.b_mn) && (d.bn != 256 || d.epi == EPI_SPLIT)) return MOE_EINVAL;
+    const int maj = (d.a_mn ? 1 : 0) | (d.b_mn ? 2 : 0);
+    const int key = ((d.bn * 10 + d.a_mode) * 10 + d.epi) * 10 + maj;
+#define MOE_K(BN_, AM_, EP_, MJ_) ((((BN_) * 10 + (AM_)) * 10 + (EP_)) * 10 + (MJ_))
     switch (key) {
-        case 128 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<128, A_DENSE, EPI_F32>(p, grid, st, d.name);
-        case 384 * 100 + A_DENSE * 10 + EPI_F32: return launch_traced<384, A_DENSE, EPI_F32>(p, grid, st, d.name);
-        case 256 * 100 + A_DENSE * 10 + EPI_SPLIT: return launch_traced<256, A_DENSE, EPI_SPLIT>(p, grid, st, d.name);
-        case 256 * 100 + A_DENSE * 10 + EPI_BF16: return launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
-        case 256 * 100 + A_DENSE * 10 + EPI_SWIGLU: return launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
-        case 256 * 100 + A_GATHER * 10 + EPI_SWIGLU: return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);
-        case 256 * 100 + A_GROUPED * 10 + EPI_SCATTER: return launch_traced<256, A_GROUPED, EPI_SCATTER>(p, grid, st, d.name);
+        case MOE_K(128, A_DENSE, EPI_F32, 0): return launch_traced<128, A_DENSE, EPI_F32>(p, grid, st, d.name);
+        case MOE_K(384, A_DENSE, EPI_F32, 0): return launch_traced<384, A_DENSE, EPI_F32>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_SPLIT, 0): return launch_traced<256, A_DENSE, EPI_SPLIT>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_BF16, 0): return launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_SWIGLU, 0): return launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
+        case MOE_K(256, A_GATHER, EPI_SWIGLU, 0): return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);
+        case MOE_K(256, A_GROUPED, EPI_SCATTER, 0): return launch_traced<256, A_GROUPED, EPI_SCATTER>(p, grid, st, d.name);
+        // MN-major operands (general products, the backward pass)
+        case MOE_K(256, A_DENSE, EPI_BF16, 1): return launch_traced<256, A_DENSE, EPI_BF16, 1>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_BF16, 2): return launch_traced<256, A_DENSE, EPI_BF16, 2>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_BF16, 3): return launch_traced<256, A_DENSE, EPI_BF16, 3>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_F32, 0): return launch_traced<256, A_DENSE, EPI_F32, 0>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_F32, 1): return launch_traced<256, A_DENSE, EPI_F32, 1>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_F32, 2): return launch_traced<256, A_DENSE, EPI_F32, 2>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_F32, 3): return launch_traced<256, A_DENSE, EPI_F32, 3>(p, grid, st, d.name);
+#undef MOE_K
         default: return MOE_EINVAL;
     }
 }

@@ -50,6 +50,8 @@ struct GemmSeg {        // one K segment of the contraction: A_s [M, K_s] . B_s 
 struct GemmDesc {
     int a_mode;
     int epi;
+    int a_mn;               // 1: A stored [K, M] (M contiguous) instead of [M, K]
+    int b_mn;               // 1: B stored [K, N] instead of [N, K]
     int bn;                 // 128, 256, or 384 (fp32 epilogue only: two MMAs, N=256+128)
     int64_t M;              // dense: rows of A/out
     int N;                  // output columns (hidden units for SWIGLU)
