@@ -42,7 +42,7 @@ __all__ = [
     "bf16_round", "silu", "Plan", "make_plan", "router_logits", "router_topk",
     "latent_down", "placement", "dispatch", "pack_pool", "expert_ffn",
     "experts_forward", "combine", "shared_act", "output", "layer", "balance_update",
-    "dispatch_ragged", "layer_ragged",
+    "dispatch_ragged", "layer_ragged", "layer_backward", "silu_grad", "exact",
     "TIE_EPS", "EMPTY_TAG", "DROP_KEPT", "DROP_SEND", "DROP_RECV",
 ]
 
@@ -142,8 +142,9 @@ def make_plan(cfg) -> Plan:
 
 # ---------------------------------------------------------------- router
 
-def router_logits(x, Wr, bias=None) -> np.ndarray:
-    """l = x Wr^T + bias, exact in float64, then rounded to float32.
+def router_logits(x, Wr, bias=None, dtype=np.float32) -> np.ndarray:
+    """l = x Wr^T + bias, exact in float64, then rounded to float32 (``dtype``;
+    float64 keeps it exact).
 
     [LJ-HK] sec. 二: the router picks experts per token; [CSDN] appendix A.2:
     the balancing bias is added to the router logits.
@@ -151,10 +152,10 @@ def router_logits(x, Wr, bias=None) -> np.ndarray:
     l = _f64(x) @ _f64(Wr).T
     if bias is not None:
         l = l + _f64(bias)[None, :]
-    return l.astype(np.float32)
+    return l.astype(dtype)
 
 
-def router_topk(l32, k: int, eps: float = TIE_EPS):
+def router_topk(l32, k: int, eps: float = TIE_EPS, dtype=np.float32):
     """Top-k experts per token, softmax gate weights and near-tie flags.
 
     [LJ-HK] sec. 二: the router selects eight experts for each token.
@@ -165,7 +166,7 @@ def router_topk(l32, k: int, eps: float = TIE_EPS):
     logits differ by less than eps (the *order*, hence the drop priority, is
     fragile).  Differences are exact (float64 of float32 values).
     """
-    l = np.asarray(l32, dtype=np.float32).astype(np.float64)
+    l = np.asarray(l32, dtype=dtype).astype(np.float64)
     T, E = l.shape
     order = np.argsort(-l, axis=1, kind="stable")
     idx = order[:, :k].astype(np.int32)
@@ -184,10 +185,10 @@ def router_topk(l32, k: int, eps: float = TIE_EPS):
 
 # ---------------------------------------------------------------- latent
 
-def latent_down(x, W_ld) -> np.ndarray:
+def latent_down(x, W_ld, rnd=bf16_round) -> np.ndarray:
     """z = bf16(x W_ld^T).  [LJ-HK] sec. 二: a latent projection compresses
     the routed activations from 6144 to 3072 values before the exchange."""
-    return bf16_round(_f64(x) @ _f64(W_ld).T)
+    return rnd(_f64(x) @ _f64(W_ld).T)
 
 
 # ---------------------------------------------------------------- dispatch
@@ -305,7 +306,7 @@ def pack_pool(z, idx, disp: dict, p: Plan, rows=None):
 
 # ---------------------------------------------------------------- experts
 
-def expert_ffn(X, Wg_e, Wu_e, Wd_e) -> np.ndarray:
+def expert_ffn(X, Wg_e, Wu_e, Wd_e, rnd=bf16_round) -> np.ndarray:
     """One routed expert on its rows: Y = bf16(bf16(silu(X Wg^T) * (X Wu^T)) Wd^T).
 
     [LJ-HK] sec. 二 / [CSDN] sec. 四: each receiver runs its local experts on
@@ -314,11 +315,11 @@ def expert_ffn(X, Wg_e, Wu_e, Wd_e) -> np.ndarray:
     X = _f64(X)
     g = X @ _f64(Wg_e).T
     u = X @ _f64(Wu_e).T
-    h = bf16_round(silu(g) * u)
-    return bf16_round(h @ _f64(Wd_e).T)
+    h = rnd(silu(g) * u)
+    return rnd(h @ _f64(Wd_e).T)
 
 
-def experts_forward(payload_of_row, disp: dict, Wg, Wu, Wd, experts=None) -> dict:
+def experts_forward(payload_of_row, disp: dict, Wg, Wu, Wd, experts=None, rnd=bf16_round) -> dict:
     """Y for every computed pool row: {row: Y[row]} over experts' kept rows.
 
     ``payload_of_row(rows) -> X`` returns the pool payload of those rows."""
@@ -329,7 +330,7 @@ def experts_forward(payload_of_row, disp: dict, Wg, Wu, Wd, experts=None) -> dic
         if n == 0:
             continue
         rows = disp["expert_rows"][e, :n]
-        Y = expert_ffn(payload_of_row(rows), Wg[e], Wu[e], Wd[e])
+        Y = expert_ffn(payload_of_row(rows), Wg[e], Wu[e], Wd[e], rnd)
         for r, y in zip(rows, Y):
             out[int(r)] = y
     return out
@@ -337,7 +338,7 @@ def experts_forward(payload_of_row, disp: dict, Wg, Wu, Wd, experts=None) -> dic
 
 # ---------------------------------------------------------------- combine
 
-def combine(Y_of_row, slot_of, w, L: int, tokens=None) -> np.ndarray:
+def combine(Y_of_row, slot_of, w, L: int, tokens=None, rnd=bf16_round) -> np.ndarray:
     """c[t] = bf16(sum over kept j, in j order, of w[t,j] * Y[slot_of[t,j]]).
 
     [LJ-HK] sec. 二: expert outputs come back to their tokens and are
@@ -355,22 +356,22 @@ def combine(Y_of_row, slot_of, w, L: int, tokens=None) -> np.ndarray:
             if r >= 0:
                 acc = acc + w[t, j] * _f64(Y_of_row(r))
         c.append(acc)
-    return bf16_round(np.stack(c)) if c else np.zeros((0, L))
+    return rnd(np.stack(c)) if c else np.zeros((0, L))
 
 
 # ---------------------------------------------------------------- output
 
-def shared_act(x, Wsg, Wsu) -> np.ndarray:
+def shared_act(x, Wsg, Wsu, rnd=bf16_round) -> np.ndarray:
     """Shared-expert activations a_s = bf16(silu(x Wsg_s^T) * (x Wsu_s^T)),
     concatenated over s along the hidden axis.  [LJ-HK] sec. 二: two shared
     experts stay local and process every token."""
     x = _f64(x)
     Wsg, Wsu = _f64(Wsg), _f64(Wsu)
-    parts = [bf16_round(silu(x @ Wsg[s].T) * (x @ Wsu[s].T)) for s in range(Wsg.shape[0])]
+    parts = [rnd(silu(x @ Wsg[s].T) * (x @ Wsu[s].T)) for s in range(Wsg.shape[0])]
     return np.concatenate(parts, axis=1) if parts else np.zeros((x.shape[0], 0))
 
 
-def output(c, a, W_lu, Wsd) -> np.ndarray:
+def output(c, a, W_lu, Wsd, rnd=bf16_round) -> np.ndarray:
     """out = bf16(c W_lu^T + sum_s a_s Wsd_s^T).
 
     [LJ-HK] sec. 二: the routed output is projected back to model width and
@@ -381,7 +382,7 @@ def output(c, a, W_lu, Wsd) -> np.ndarray:
     Hs = Wsd.shape[2] if Wsd.ndim == 3 else 0
     for s in range(Wsd.shape[0]):
         acc = acc + a[:, s * Hs:(s + 1) * Hs] @ Wsd[s].T
-    return bf16_round(acc)
+    return rnd(acc)
 
 
 # ---------------------------------------------------------------- dropless ragged dispatch
@@ -447,6 +448,120 @@ def layer_ragged(cfg, t: dict) -> dict:
                 tags=tags, Y=Y, c=c, a=a, out=out)
 
 
+# ---------------------------------------------------------------- backward pass
+
+def silu_grad(g) -> np.ndarray:
+    """d silu / dg = sigmoid(g) * (1 + g * (1 - sigmoid(g)))."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    return sig * (1.0 + g * (1.0 - sig))
+
+
+def layer_backward(cfg, t: dict, fwd: dict, dout, rnd=bf16_round) -> dict:
+    """Gradients of the layer output with respect to x and every weight.
+
+    The pages give the forward only (the 250,691 tokens/s they report is a
+    training step); this is its derivative, step by step in reverse:
+      out = c W_lu^T + sum_s a_s Wsd_s^T      -> dc, da_s, dW_lu, dWsd_s
+      a_s = silu(x Wsg_s^T) * (x Wsu_s^T)     -> dgs, dus, dWsg, dWsu
+      c_t = sum_kept w_tj Y_row               -> dY_row = w_tj dc_t, dw_tj = <dc_t, Y_row>
+      Y = h Wd^T, h = silu(g) u, g/u = X Wg^T / X Wu^T  (per expert)
+                                              -> dh, dg, du, dX, dWd, dWg, dWu
+      X_row = z_t (for every kept row)        -> dz_t = sum_kept dX_row
+      z = x W_ld^T                            -> dW_ld
+      w = softmax(l_selected), l = x Wr^T + b -> dl (zero off the selection), dWr
+      x feeds z, l and the shared experts     -> dx
+    The balancing bias gets no gradient (stop-gradient, [CSDN] appendix A.2).
+    `rnd` is applied where the tensors are kept in bf16 (dc, da, dY, dh, dg,
+    du, dX, dz, dl, dx); weight gradients stay float64.  Pre-activations g/u
+    are recomputed in float64 from the stored inputs.
+    """
+    x = _f64(t["x"])
+    W_lu, Wsd = _f64(t["W_lu"]), _f64(t["Wsd"])
+    Wsg, Wsu = _f64(t["Wsg"]), _f64(t["Wsu"])
+    dout = _f64(dout)
+    p = fwd["plan"]
+    T, k = fwd["idx"].shape
+    L = W_lu.shape[1]
+    ns, Hs = Wsd.shape[0], (Wsd.shape[2] if Wsd.ndim == 3 else 0)
+    c, a = fwd["c"], fwd["a"]
+    g_ = {}
+    dc = rnd(dout @ W_lu)
+    g_["W_lu"] = dout.T @ c
+    dgs, dus = np.zeros((T, ns * Hs)), np.zeros((T, ns * Hs))
+    g_["Wsd"] = np.zeros_like(Wsd)
+    g_["Wsg"], g_["Wsu"] = np.zeros_like(Wsg), np.zeros_like(Wsu)
+    for s_ in range(ns):
+        sl = slice(s_ * Hs, (s_ + 1) * Hs)
+        da = rnd(dout @ Wsd[s_])
+        g_["Wsd"][s_] = dout.T @ a[:, sl]
+        gs, us = x @ Wsg[s_].T, x @ Wsu[s_].T
+        dgs[:, sl] = rnd(da * us * silu_grad(gs))
+        dus[:, sl] = rnd(da * silu(gs))
+        g_["Wsg"][s_] = dgs[:, sl].T @ x
+        g_["Wsu"][s_] = dus[:, sl].T @ x
+    # combine
+    slot_of, w = fwd["disp"]["slot_of"], fwd["w"]
+    dY, dw = {}, np.zeros((T, k))
+    for tt in range(T):
+        for j in range(k):
+            r = int(slot_of[tt, j])
+            if r >= 0:
+                dY[r] = rnd(w[tt, j] * dc[tt])
+                dw[tt, j] = dc[tt] @ fwd["Y"][r]
+    # experts
+    Wg, Wu, Wd = t["Wg"], t["Wu"], t["Wd"]
+    g_["Wg"] = np.zeros(np.shape(Wg))
+    g_["Wu"] = np.zeros(np.shape(Wu))
+    g_["Wd"] = np.zeros(np.shape(Wd))
+    dX = {}
+    disp = fwd["disp"]
+    lists = ([disp["expert_rows"][e, :disp["count"][e]] for e in range(p.E)]
+             if "expert_offsets" not in disp else
+             [disp["expert_rows"][disp["expert_offsets"][e]:disp["expert_offsets"][e + 1]]
+              for e in range(p.E)])
+    for e in range(p.E):
+        rows = lists[e]
+        if rows.size == 0:
+            continue
+        X = fwd["payload"][rows]
+        Wg_e, Wu_e, Wd_e = _f64(Wg[e]), _f64(Wu[e]), _f64(Wd[e])
+        gg, uu = X @ Wg_e.T, X @ Wu_e.T
+        h = rnd(silu(gg) * uu)
+        dYe = np.stack([dY[int(r)] for r in rows])
+        dh = rnd(dYe @ Wd_e)
+        g_["Wd"][e] = dYe.T @ h
+        dg = rnd(dh * uu * silu_grad(gg))
+        du = rnd(dh * silu(gg))
+        g_["Wg"][e] = dg.T @ X
+        g_["Wu"][e] = du.T @ X
+        dXe = rnd(dg @ Wg_e + du @ Wu_e)
+        for r, v in zip(rows, dXe):
+            dX[int(r)] = v
+    dz = np.zeros((T, L))
+    for tt in range(T):
+        for j in range(k):
+            r = int(slot_of[tt, j])
+            if r >= 0:
+                dz[tt] += dX[r]
+    dz = rnd(dz)
+    g_["W_ld"] = dz.T @ x
+    # router: softmax over the selected logits
+    dl_sel = w * (dw - (w * dw).sum(axis=1, keepdims=True))
+    dl = np.zeros((T, p.E))
+    np.put_along_axis(dl, fwd["idx"].astype(np.int64), dl_sel, axis=1)
+    dl = rnd(dl)
+    g_["Wr"] = dl.T @ x
+    dx = dz @ _f64(t["W_ld"]) + dl @ _f64(t["Wr"])
+    for s_ in range(ns):
+        sl = slice(s_ * Hs, (s_ + 1) * Hs)
+        dx = dx + dgs[:, sl] @ Wsg[s_] + dus[:, sl] @ Wsu[s_]
+    g_["x"] = rnd(dx)
+    g_.update(dc=dc, dY=dY, dw=dw, dX=dX, dz=dz, dl=dl, dgs=dgs, dus=dus)
+    return g_
+
+
 # ---------------------------------------------------------------- balancing bias
 
 def balance_update(idx, hist, alpha: float, n_experts: int):
@@ -471,25 +586,33 @@ def balance_update(idx, hist, alpha: float, n_experts: int):
 
 # ---------------------------------------------------------------- layer
 
-def layer(cfg, t: dict, gate_w=None) -> dict:
+def exact(a) -> np.ndarray:
+    """No rounding: the precision policy of a float64-throughout layer."""
+    return np.asarray(a, dtype=np.float64)
+
+
+def layer(cfg, t: dict, gate_w=None, rnd=bf16_round) -> dict:
     """The whole layer on one batch, every intermediate kept.
 
     ``t`` holds the inputs (x, Wr, bias, W_ld, Wg, Wu, Wd, W_lu, Wsg, Wsu,
     Wsd).  ``gate_w`` optionally overrides the gate weights (used by tests
-    that zero the routed path)."""
+    that zero the routed path).  ``rnd`` is the storage rounding (bf16 by
+    default; ``exact`` gives a float64-throughout layer, logits included)."""
     p = make_plan(cfg)
-    l32 = router_logits(t["x"], t["Wr"], t.get("bias"))
-    idx, w, tie = router_topk(l32, cfg.top_k)
+    ldt = np.float64 if rnd is exact else np.float32
+    l32 = router_logits(t["x"], t["Wr"], t.get("bias"), dtype=ldt)
+    idx, w, tie = router_topk(l32, cfg.top_k, dtype=ldt)
     if gate_w is not None:
         w = np.asarray(gate_w, dtype=np.float64)
-    z = latent_down(t["x"], t["W_ld"])
+    z = latent_down(t["x"], t["W_ld"], rnd)
     disp = dispatch(idx, p)
     payload, tags = pack_pool(z, idx, disp, p)
     # expert weights are widened to float64 one expert at a time (inside expert_ffn)
-    Y = experts_forward(lambda rows: payload[np.asarray(rows)], disp, t["Wg"], t["Wu"], t["Wd"])
+    Y = experts_forward(lambda rows: payload[np.asarray(rows)], disp, t["Wg"], t["Wu"], t["Wd"],
+                        rnd=rnd)
     L = z.shape[1]
-    c = combine(lambda r: Y[r], disp["slot_of"], w, L)
-    a = shared_act(t["x"], t["Wsg"], t["Wsu"])
-    out = output(c, a, t["W_lu"], t["Wsd"])
+    c = combine(lambda r: Y[r], disp["slot_of"], w, L, rnd=rnd)
+    a = shared_act(t["x"], t["Wsg"], t["Wsu"], rnd)
+    out = output(c, a, t["W_lu"], t["Wsd"], rnd)
     return dict(plan=p, logits=l32, idx=idx, w=w, tie=tie, z=z, disp=disp,
                 payload=payload, tags=tags, Y=Y, c=c, a=a, out=out)

@@ -492,3 +492,53 @@ def test_ragged_layer_equals_unbounded_capped_layer():
         for j in range(cfg.top_k):
             np.testing.assert_array_equal(a["Y"][int(a["disp"]["slot_of"][tt, j])],
                                           b["Y"][int(b["disp"]["slot_of"][tt, j])])
+
+
+# ------------------------------------------------------------------ backward pass
+
+def test_backward_matches_central_differences():
+    """Every gradient of the float64 (rounding-free) layer against central
+    differences of the forward: d<out, dout>/dparam at random entries."""
+    cfg = _cfg(T=16, n_ranks=2, n_experts=6, top_k=2, n_waves=3, n_shared=2, h_expert=8,
+               h_shared=8, cf_send=float("inf"), cf_recv=float("inf"))
+    t = {k: (v.double().numpy() if v is not None else None)
+         for k, v in wl.make_inputs(cfg.with_(seed=5), "cpu").items()}
+    fwd = O.layer(cfg, t, rnd=O.exact)
+    rng = np.random.default_rng(11)
+    dout = rng.standard_normal(fwd["out"].shape)
+    g = O.layer_backward(cfg, t, fwd, dout, rnd=O.exact)
+
+    def loss(tt):
+        r = O.layer(cfg, tt, rnd=O.exact)
+        assert (r["idx"] == fwd["idx"]).all()            # no selection change within +-eps
+        return (r["out"] * dout).sum()
+
+    for name in ["x", "Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Wsd"]:
+        for _ in range(4):
+            idx = tuple(int(rng.integers(0, n)) for n in t[name].shape)
+            tt = {k: (v.copy() if v is not None else None) for k, v in t.items()}
+            eps = 1e-5
+            tt[name][idx] += eps
+            up = loss(tt)
+            tt[name][idx] -= 2 * eps
+            down = loss(tt)
+            fd = (up - down) / (2 * eps)
+            assert abs(fd - g[name][idx]) <= 1e-6 * (1 + abs(fd)), (name, idx, fd, g[name][idx])
+
+
+def test_backward_dropped_assignments_get_no_expert_gradient():
+    """A dropped assignment contributes nothing forward, so its expert and
+    gate-weight gradients vanish; the shared path still gets its gradient."""
+    cfg = _cfg(T=32, n_ranks=2, n_experts=6, top_k=2, cf_send=0.01, cf_recv=0.01)
+    t = {k: (v.double().numpy() if v is not None else None)
+         for k, v in wl.make_inputs(cfg.with_(seed=6), "cpu").items()}
+    fwd = O.layer(cfg, t)
+    dout = np.ones(fwd["out"].shape)
+    g = O.layer_backward(cfg, t, fwd, dout)
+    dropped = fwd["disp"]["slot_of"] < 0
+    assert dropped.any()
+    assert (g["dw"][dropped] == 0).all()
+    never = np.setdiff1d(np.arange(6), fwd["idx"][~dropped])
+    for e in never:
+        assert (g["Wd"][e] == 0).all() and (g["Wg"][e] == 0).all()
+    assert np.abs(g["Wsg"]).sum() > 0
