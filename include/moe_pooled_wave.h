@@ -276,6 +276,51 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
                 const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
                 uint16_t* c, uint16_t* a, uint16_t* out, int32_t* status, void* stream);
 
+/* Backward pass of the layer (capped layout).  The pages give the forward
+ * only; the throughput they quote is a training step, so this is the
+ * forward's derivative, step by step in reverse: output layer, shared
+ * experts (their gate/up recomputed), combine (dY = w dc, dw = <dc, Y>),
+ * routed experts (gate/up recomputed; dh, dg, du, dX, weight gradients), the
+ * return of dX to the tokens (dz), the latent projection, the router
+ * (softmax over the selected logits; the balancing bias is stop-gradient)
+ * and dx.  Storage precision: activation gradients bf16 (dc, da, dY, dh, dg,
+ * du, dX, dz, dlogits, dx), weight gradients fp32, all products accumulate
+ * in fp32.
+ * moe_backward_plan: byte offsets of the intermediates inside the scratch
+ *   and its total size (layout->total).
+ * moe_layer_backward: inputs are the forward's inputs and the tensors its
+ *   calls produced (idx, w, pool, slot_of, expert_rows, expert_count, h =
+ *   ws_ffn + plan.h_offset_bytes, ypool, c, a), plus dout [T, d] bf16.
+ *   Weight gradients are written (not accumulated) in the weights' own
+ *   layouts: dWr [E, d], dW_ld [L, d], dWg, dWu [E, H, L], dWd [E, L, H],
+ *   dW_lu [d, L], dWsg, dWsu [n_s, Hs, d], dWsd [n_s, d, Hs], all fp32;
+ *   dx [T, d] bf16.  The rows of h past each expert's count are set to zero
+ *   (they were never written by the forward).  All device pointers,
+ *   16-byte aligned; scratch ws of at least layout.total bytes. */
+typedef struct moe_backward_ws {
+    int64_t dc, da, dgs, dus, dw, dypool, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles;
+    int64_t total;
+} moe_backward_ws_t;
+
+typedef struct moe_backward_args {
+    const uint16_t *x, *Wr, *W_ld, *Wg, *Wu, *Wd, *W_lu, *Wsg, *Wsu, *Wsd;
+    const int32_t* idx;
+    const float* w;
+    const uint16_t* pool;
+    const int32_t *slot_of, *expert_rows, *expert_count;
+    uint16_t* h;
+    const uint16_t *ypool, *c, *a;
+    const uint16_t* dout;
+    uint16_t* dx;
+    float *dWr, *dW_ld, *dWg, *dWu, *dWd, *dW_lu, *dWsg, *dWsu, *dWsd;
+    void* ws;
+    size_t ws_bytes;
+    int32_t* status;
+} moe_backward_args_t;
+
+int moe_backward_plan(const moe_config_t* cfg, moe_backward_ws_t* layout);
+int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* args, void* stream);
+
 /* Quantile-balancing bias update (devpress.csdn.net, section 四 and appendix
  * A.2): a global histogram H counts how often each expert was selected;
  * f_e = H[e] / sum(H); b_e = -alpha * (f_e - 1/E); the bias is added to the

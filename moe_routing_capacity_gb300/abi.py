@@ -22,7 +22,8 @@ MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2,
 EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project", "moe_matmul",
            "moe_dispatch_pooled",
            "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update",
-           "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
+           "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged",
+           "moe_backward_plan", "moe_layer_backward", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
 
 
@@ -58,6 +59,24 @@ class DropStats(ctypes.Structure):
 
 STATS_WORDS = ctypes.sizeof(DropStats) // 8    # int64 words of a stats record
 
+BWD_WS_FIELDS = ("dc", "da", "dgs", "dus", "dw", "dypool", "dxpool", "dh", "dg", "du", "xe", "dye",
+                 "dz", "dlogits", "tiles", "total")
+
+
+class BackwardWs(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_int64) for f in BWD_WS_FIELDS]
+
+
+BWD_ARG_FIELDS = ("x", "Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Wsd", "idx", "w",
+                  "pool", "slot_of", "expert_rows", "expert_count", "h", "ypool", "c", "a",
+                  "dout", "dx", "dWr", "dW_ld", "dWg", "dWu", "dWd", "dW_lu", "dWsg", "dWsu",
+                  "dWsd", "ws")
+
+
+class BackwardArgs(ctypes.Structure):
+    _fields_ = ([(f, ctypes.c_void_p) for f in BWD_ARG_FIELDS] +
+                [("ws_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p)])
+
 _lib = None
 
 
@@ -85,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
         L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+        L.moe_backward_plan.argtypes = [pc, ctypes.POINTER(BackwardWs)]
+        L.moe_layer_backward.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         L.moe_abi_version.argtypes = []
@@ -277,3 +298,26 @@ def trace_end() -> list:
         _check("moe_trace_event", lib().moe_trace_event(i, ctypes.byref(name), ctypes.byref(ms)))
         out.append((name.value.decode(), float(ms.value)))
     return out
+
+
+# ---------------------------------------------------------------- backward pass
+
+def backward_plan(cfg) -> BackwardWs:
+    w = BackwardWs()
+    _check("moe_backward_plan", lib().moe_backward_plan(ctypes.byref(make_config(cfg)),
+                                                        ctypes.byref(w)))
+    return w
+
+
+def layer_backward(cfg, tensors: dict, ws, status, stream=None):
+    """tensors: every BackwardArgs field by name (torch tensors, or None for
+    the shared-expert ones when there are none)."""
+    args = BackwardArgs()
+    for f in BWD_ARG_FIELDS:
+        t = tensors.get(f)
+        setattr(args, f, None if t is None else t.data_ptr())
+    args.ws = ws.data_ptr()
+    args.ws_bytes = ws.numel()
+    args.status = status.data_ptr()
+    _check("moe_layer_backward", lib().moe_layer_backward(
+        ctypes.byref(make_config(cfg)), ctypes.byref(args), _stream(stream)))

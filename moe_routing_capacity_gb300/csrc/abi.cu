@@ -577,6 +577,47 @@ int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* his
                                  static_cast<cudaStream_t>(stream));
 }
 
+int moe_backward_plan(const moe_config_t* cfg, moe_backward_ws_t* layout) {
+    if (!layout) return MOE_EINVAL;
+    Geom G;
+    const int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    const BackwardWs w = backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns);
+    layout->dc = w.dc; layout->da = w.da; layout->dgs = w.dgs; layout->dus = w.dus;
+    layout->dw = w.dw; layout->dypool = w.dypool; layout->dxpool = w.dxpool; layout->dh = w.dh;
+    layout->dg = w.dg; layout->du = w.du; layout->xe = w.xe; layout->dye = w.dye;
+    layout->dz = w.dz; layout->dlogits = w.dlogits; layout->tiles = w.tiles;
+    layout->total = w.total;
+    return MOE_OK;
+}
+
+int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, void* stream) {
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    if (!a) return MOE_EINVAL;
+    if (G.g.T == 0) return MOE_OK;
+    const void* need[] = {a->x, a->Wr, a->W_ld, a->Wg, a->Wu, a->Wd, a->W_lu, a->idx, a->w,
+                          a->pool, a->slot_of, a->expert_rows, a->expert_count, a->h, a->ypool,
+                          a->c, a->dout, a->dx, a->dWr, a->dW_ld, a->dWg, a->dWu, a->dWd,
+                          a->dW_lu, a->ws, a->status};
+    for (const void* ptr : need)
+        if (!ptr) return MOE_EINVAL;
+    if (G.ns > 0 && (!a->Wsg || !a->Wsu || !a->Wsd || !a->a || !a->dWsg || !a->dWsu || !a->dWsd))
+        return MOE_EINVAL;
+    const void* al16[] = {a->x, a->Wr, a->W_ld, a->Wg, a->Wu, a->Wd, a->W_lu, a->pool, a->h,
+                          a->ypool, a->c, a->dout, a->dx, a->dWr, a->dW_ld, a->dWg, a->dWu,
+                          a->dWd, a->dW_lu, a->ws};
+    for (const void* ptr : al16)
+        if (!aligned16(ptr)) return MOE_EINVAL;
+    if (G.g.pool_rows == 0 || G.g.c_recv == 0) return MOE_EINVAL;
+    const BackwardWs w = backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns);
+    if (a->ws_bytes < w.total) return MOE_ENOSPC;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    return launch_backward(G.g, G.d, G.H, G.Hs, G.ns, *a, static_cast<cudaStream_t>(stream));
+}
+
 int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* slot_of,
                 const float* w, const uint16_t* W_lu, const uint16_t* x, const uint16_t* Wsg,
                 const uint16_t* Wsu, const uint16_t* Wsd, uint16_t* c, uint16_t* a,

@@ -1,0 +1,336 @@
+// backward.cu -- gradients of the layer (the pages report a training-step
+// throughput; this is the derivative of the forward, step by step in reverse):
+//   out = c W_lu^T + sum_s a_s Wsd_s^T   -> dc, da, dW_lu, dWsd
+//   a = silu(x Wsg^T) (x Wsu^T)          -> dgs, dus (g/u recomputed), dWsg, dWsu
+//   c_t = sum_kept w_tj Y_row            -> dY_row = w dc_t, dw_tj = <dc_t, Y_row>
+//   per expert: Y = h Wd^T, h = silu(g) u, g/u = X Wg^T / X Wu^T
+//                                        -> dh, dg, du, dX, dWd, dWg, dWu
+//   X_row = z_t                          -> dz_t = sum_kept dX_row (the return of the
+//                                           exchange, in reverse)
+//   z = x W_ld^T                         -> dW_ld
+//   w = softmax(selected logits)         -> dlogits, dWr
+//   x                                    -> dx
+// Every product runs on the tcgen05 GEMM engine; products over the token or
+// row axis read their operands MN-major.
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// dY[slot] = bf16(w_tj dc_t) for kept (t, j); dw_tj = <dc_t, Y[slot]> (fp32).
+// One warp per token; dc_t is read once into registers.
+template <int CH>
+__global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ dc,
+                                                          const uint16_t* __restrict__ ypool,
+                                                          const int32_t* __restrict__ slot_of,
+                                                          const float* __restrict__ w, int64_t T,
+                                                          int k, int L, uint16_t* __restrict__ dy,
+                                                          float* __restrict__ dw) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int32_t my_row = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        my_row = slot_of[t * k + lane];
+        my_w = w[t * k + lane];
+    }
+    const int nchunk = L / 8;
+    float dot_mine = 0.0f;   // lane j keeps dw for assignment j
+    for (int j = 0; j < k; ++j) {
+        const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+        const float wj = __shfl_sync(0xffffffffu, my_w, j);
+        float dot = 0.0f;
+        if (r >= 0) {
+            const uint4* yrow = reinterpret_cast<const uint4*>(ypool + static_cast<int64_t>(r) * L);
+            uint4* drow = reinterpret_cast<uint4*>(dy + static_cast<int64_t>(r) * L);
+            const uint4* crow = reinterpret_cast<const uint4*>(dc + t * L);
+            for (int ch = lane; ch < nchunk; ch += 32) {
+                const uint4 cv = __ldg(crow + ch);
+                const uint4 yv = __ldg(yrow + ch);
+                const uint32_t cu[4] = {cv.x, cv.y, cv.z, cv.w};
+                const uint32_t yu[4] = {yv.x, yv.y, yv.z, yv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float c0 = bf16_lo(cu[h]), c1 = bf16_hi(cu[h]);
+                    dot = fmaf(c0, bf16_lo(yu[h]), dot);
+                    dot = fmaf(c1, bf16_hi(yu[h]), dot);
+                    o[h] = pack_bf16x2(wj * c0, wj * c1);
+                }
+                drow[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        if (lane == j) dot_mine = r >= 0 ? dot : 0.0f;
+    }
+    if (lane < k) dw[t * k + lane] = dot_mine;
+}
+
+// dlogits[t, e] = bf16(w_j (dw_j - sum_i w_i dw_i)) for e = idx[t, j], else 0.
+__global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restrict__ idx,
+                                                         const float* __restrict__ w,
+                                                         const float* __restrict__ dw, int64_t T,
+                                                         int k, int E,
+                                                         uint16_t* __restrict__ dlogits) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_e = -1;
+    float my_w = 0.0f, my_dw = 0.0f;
+    if (lane < k) {
+        my_e = idx[t * k + lane];
+        my_w = w[t * k + lane];
+        my_dw = dw[t * k + lane];
+    }
+    float s = my_w * my_dw;
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const float my_dl = my_w * (my_dw - s);
+    uint16_t* row = dlogits + t * E;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        float v = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, my_e, j);
+            const float dj = __shfl_sync(0xffffffffu, my_dl, j);
+            if (ej == e) v = dj;
+        }
+        if (e < E) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(v);
+            row[e] = *reinterpret_cast<const uint16_t*>(&b);
+        }
+    }
+}
+
+// dst[e][r][0:L] = src[rows[e][r]][0:L] for r < count[e], zeros up to c_recv.
+__global__ void __launch_bounds__(256) gather_expert_rows_kernel(
+    const uint16_t* __restrict__ src, int64_t pitch, const int32_t* __restrict__ rows,
+    const int32_t* __restrict__ count, int E, int c_recv, int L, uint16_t* __restrict__ dst) {
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (wid >= static_cast<int64_t>(E) * c_recv) return;
+    const int e = static_cast<int>(wid / c_recv);
+    const int r = static_cast<int>(wid - static_cast<int64_t>(e) * c_recv);
+    uint4* d = reinterpret_cast<uint4*>(dst + wid * L);
+    const int nchunk = L / 8;
+    if (r < count[e]) {
+        const uint4* sp = reinterpret_cast<const uint4*>(
+            src + static_cast<int64_t>(rows[static_cast<int64_t>(e) * c_recv + r]) * pitch);
+        for (int ch = lane; ch < nchunk; ch += 32) d[ch] = __ldg(sp + ch);
+    } else {
+        for (int ch = lane; ch < nchunk; ch += 32) d[ch] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Rows r >= count[e] of a [E, c_recv, W] buffer set to zero.
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(uint16_t* __restrict__ buf,
+                                                            const int32_t* __restrict__ count,
+                                                            int E, int c_recv, int W) {
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (wid >= static_cast<int64_t>(E) * c_recv) return;
+    const int e = static_cast<int>(wid / c_recv);
+    const int r = static_cast<int>(wid - static_cast<int64_t>(e) * c_recv);
+    if (r < count[e]) return;
+    uint4* d = reinterpret_cast<uint4*>(buf + wid * W);
+    for (int ch = lane; ch < W / 8; ch += 32) d[ch] = make_uint4(0, 0, 0, 0);
+}
+
+static size_t al(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
+
+BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int ns) {
+    BackwardWs w;
+    size_t o = 0;
+    const size_t T = static_cast<size_t>(g.T), L = g.L, E = g.E, cr = g.c_recv;
+    const size_t P = static_cast<size_t>(g.pool_rows), HS = static_cast<size_t>(ns) * Hs;
+    w.dc = o;       o = al(o + T * L * 2);
+    w.da = o;       o = al(o + T * HS * 2);
+    w.dgs = o;      o = al(o + T * HS * 2);
+    w.dus = o;      o = al(o + T * HS * 2);
+    w.dw = o;       o = al(o + T * g.k * 4);
+    w.dypool = o;   o = al(o + P * L * 2);
+    w.dxpool = o;   o = al(o + P * L * 2);
+    w.dh = o;       o = al(o + E * cr * H * 2);
+    w.dg = o;       o = al(o + E * cr * H * 2);
+    w.du = o;       o = al(o + E * cr * H * 2);
+    w.xe = o;       o = al(o + E * cr * L * 2);
+    w.dye = o;      o = al(o + E * cr * L * 2);
+    w.dz = o;       o = al(o + T * L * 2);
+    w.dlogits = o;  o = al(o + T * E * 2);
+    w.tiles = o;    o = al(o + (E * ((cr + 127) / 128)) * 8 + 16);
+    w.total = o;
+    (void)d;
+    return w;
+}
+
+int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
+                    const moe_backward_args_t& a, cudaStream_t st) {
+    const BackwardWs L_ = backward_ws_layout(g, d, H, Hs, ns);
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
+    uint16_t *dc = bf(L_.dc), *da = bf(L_.da), *dgs = bf(L_.dgs), *dus = bf(L_.dus);
+    uint16_t *dyp = bf(L_.dypool), *dxp = bf(L_.dxpool), *dh = bf(L_.dh), *dg = bf(L_.dg),
+             *du = bf(L_.du), *xe = bf(L_.xe), *dye = bf(L_.dye), *dz = bf(L_.dz),
+             *dl = bf(L_.dlogits);
+    float* dw = reinterpret_cast<float*>(ws + L_.dw);
+    int32_t* tiles = reinterpret_cast<int32_t*>(ws + L_.tiles);
+    const int64_t T = g.T;
+    const int L = g.L, E = g.E, k = g.k, cr = g.c_recv;
+    const int HS = ns * Hs;
+    int rc;
+    auto mm = [&](GemmDesc& q, const char* name) {
+        q.status = a.status;
+        q.name = name;
+        return gemm_launch(q, st);
+    };
+    GemmDesc q;
+    // ---- output layer: dc = dout W_lu, da_s = dout Wsd_s
+    std::memset(&q, 0, sizeof(q));
+    q.a_mode = A_DENSE; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
+    q.M = T; q.N = L; q.nseg = 1; q.seg[0] = GemmSeg{a.dout, d, a.W_lu, L, d}; q.b_rows = L;
+    q.out = dc; q.ldo = L;
+    if ((rc = mm(q, "bwd_gemm_dc"))) return rc;
+    for (int s = 0; s < ns; ++s) {
+        std::memset(&q, 0, sizeof(q));
+        q.a_mode = A_DENSE; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
+        q.M = T; q.N = Hs; q.nseg = 1;
+        q.seg[0] = GemmSeg{a.dout, d, a.Wsd + static_cast<size_t>(s) * d * Hs, Hs, d};
+        q.b_rows = Hs; q.out = da + static_cast<size_t>(s) * Hs; q.ldo = HS;
+        if ((rc = mm(q, "bwd_gemm_da"))) return rc;
+    }
+    // ---- weight gradients of the output layer (products over tokens)
+    std::memset(&q, 0, sizeof(q));
+    q.a_mode = A_DENSE; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
+    q.M = d; q.N = L; q.nseg = 1; q.seg[0] = GemmSeg{a.dout, d, a.c, L, static_cast<int>(T)};
+    q.b_rows = L; q.out = a.dW_lu; q.ldo = L;
+    if ((rc = mm(q, "bwd_gemm_dW_lu"))) return rc;
+    for (int s = 0; s < ns; ++s) {
+        std::memset(&q, 0, sizeof(q));
+        q.a_mode = A_DENSE; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
+        q.M = d; q.N = Hs; q.nseg = 1;
+        q.seg[0] = GemmSeg{a.dout, d, a.a + static_cast<size_t>(s) * Hs, HS, static_cast<int>(T)};
+        q.b_rows = Hs; q.out = a.dWsd + static_cast<size_t>(s) * d * Hs; q.ldo = Hs;
+        if ((rc = mm(q, "bwd_gemm_dWsd"))) return rc;
+    }
+    // ---- shared experts: recompute g/u, SwiGLU backward, weight gradients
+    if (ns > 0) {
+        std::memset(&q, 0, sizeof(q));
+        q.a_mode = A_DENSE; q.epi = EPI_SWIGLU_BWD; q.bn = 256;
+        q.M = T; q.N = HS; q.nseg = 1; q.seg[0] = GemmSeg{a.x, d, a.Wsg, d, d};
+        q.B_up = a.Wsu; q.b_rows = HS; q.aux = da; q.out = dgs; q.out2 = dus; q.ldo = HS;
+        if ((rc = mm(q, "bwd_gemm_shared_swiglu"))) return rc;
+        for (int which = 0; which < 2; ++which) {
+            std::memset(&q, 0, sizeof(q));
+            q.a_mode = A_DENSE; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
+            q.M = HS; q.N = d; q.nseg = 1;
+            q.seg[0] = GemmSeg{which ? dus : dgs, HS, a.x, d, static_cast<int>(T)};
+            q.b_rows = d; q.out = which ? a.dWsu : a.dWsg; q.ldo = d;
+            if ((rc = mm(q, "bwd_gemm_dWshared"))) return rc;
+        }
+    }
+    // ---- combine backward (the return path in reverse)
+    {
+        const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+        if (L / 8 <= 32 * 4)
+            combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, a.w, T, k, L, dyp, dw);
+        else
+            combine_bwd_kernel<12><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, a.w, T, k, L, dyp, dw);
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "bwd_combine");
+    }
+    // ---- experts
+    const int max_mt = E * ((cr + 127) / 128);
+    int32_t* tile_count = tiles + 2 * max_mt;
+    if ((rc = launch_build_tiles(a.expert_count, E, 128, tiles, tile_count, st))) return rc;
+    std::memset(&q, 0, sizeof(q));   // dh = dY Wd_e (rows of dY gathered by the expert lists)
+    q.a_mode = A_GATHER; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
+    q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{nullptr, 0, a.Wd, H, L};
+    q.groups = E; q.rows_per_group = cr; q.b_rows = H;
+    q.b_gstride = static_cast<int64_t>(L) * H;
+    q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
+    q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+    q.gather_src = dyp; q.gather_pitch = L; q.gather_rows = g.pool_rows;
+    q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
+    if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
+    const size_t ghs = static_cast<size_t>(E) * cr * H * 2;
+    if (cudaMemsetAsync(dg, 0, ghs, st) != cudaSuccess || cudaMemsetAsync(du, 0, ghs, st) != cudaSuccess)
+        return MOE_ECUDA;
+    std::memset(&q, 0, sizeof(q));   // recompute g/u of the received rows, SwiGLU backward
+    q.a_mode = A_GATHER; q.epi = EPI_SWIGLU_BWD; q.bn = 256;
+    q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{nullptr, 0, a.Wg, L, L};
+    q.B_up = a.Wu; q.groups = E; q.rows_per_group = cr; q.b_rows = H;
+    q.b_gstride = static_cast<int64_t>(H) * L;
+    q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
+    q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+    q.gather_src = a.pool; q.gather_pitch = L + 8; q.gather_rows = g.pool_rows;
+    q.aux = dh; q.out = dg; q.out2 = du; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
+    if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
+    std::memset(&q, 0, sizeof(q));   // dX = dg Wg_e + du Wu_e, back to the pool rows
+    q.a_mode = A_GROUPED; q.epi = EPI_SCATTER; q.bn = 256; q.b_mn = 1;
+    q.N = L; q.nseg = 2;
+    q.seg[0] = GemmSeg{dg, H, a.Wg, L, H};
+    q.seg[1] = GemmSeg{du, H, a.Wu, L, H};
+    q.groups = E; q.rows_per_group = cr; q.a_gstride = static_cast<int64_t>(cr) * H;
+    q.b_rows = L; q.b_gstride = static_cast<int64_t>(H) * L;
+    q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
+    q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+    q.out = dxp; q.ldo = L;
+    if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
+    {   // per-expert contiguous, zero-padded copies of X and dY for the weight gradients
+        const int64_t nw = static_cast<int64_t>(E) * cr;
+        const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
+        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, L + 8, a.expert_rows, a.expert_count, E, cr, L, xe);
+        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(dyp, L, a.expert_rows, a.expert_count, E, cr, L, dye);
+        zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "bwd_gather_rows");
+    }
+    auto wgrad = [&](const uint16_t* A, int M, const uint16_t* B, int N, float* out, const char* nm) {
+        std::memset(&q, 0, sizeof(q));   // out_e[M, N] = A_e^T B_e over the expert's rows
+        q.a_mode = A_GROUPED; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
+        q.M = M; q.N = N; q.nseg = 1; q.seg[0] = GemmSeg{A, M, B, N, cr};
+        q.groups = E; q.uniform_groups = E;
+        q.a_gstride = static_cast<int64_t>(cr) * M; q.b_rows = N;
+        q.b_gstride = static_cast<int64_t>(cr) * N;
+        q.out = out; q.ldo = N; q.out_gstride = static_cast<int64_t>(M) * N;
+        return mm(q, nm);
+    };
+    if ((rc = wgrad(dye, L, a.h, H, a.dWd, "bwd_gemm_dWd"))) return rc;
+    if ((rc = wgrad(dg, H, xe, L, a.dWg, "bwd_gemm_dWg"))) return rc;
+    if ((rc = wgrad(du, H, xe, L, a.dWu, "bwd_gemm_dWu"))) return rc;
+    // ---- return of the gradients to the tokens, latent projection
+    if ((rc = launch_combine(dxp, a.slot_of, nullptr, T, k, L, dz, st))) return rc;
+    std::memset(&q, 0, sizeof(q));
+    q.a_mode = A_DENSE; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
+    q.M = L; q.N = d; q.nseg = 1; q.seg[0] = GemmSeg{dz, L, a.x, d, static_cast<int>(T)};
+    q.b_rows = d; q.out = a.dW_ld; q.ldo = d;
+    if ((rc = mm(q, "bwd_gemm_dW_ld"))) return rc;
+    // ---- router
+    {
+        const unsigned grid = static_cast<unsigned>((T + 7) / 8);
+        router_bwd_kernel<<<grid, 256, 0, st>>>(a.idx, a.w, dw, T, k, E, dl);
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "bwd_router");
+    }
+    std::memset(&q, 0, sizeof(q));
+    q.a_mode = A_DENSE; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
+    q.M = E; q.N = d; q.nseg = 1; q.seg[0] = GemmSeg{dl, E, a.x, d, static_cast<int>(T)};
+    q.b_rows = d; q.out = a.dWr; q.ldo = d;
+    if ((rc = mm(q, "bwd_gemm_dWr"))) return rc;
+    // ---- dx = dz W_ld + dlogits Wr + dgs Wsg + dus Wsu (one product, four K segments)
+    std::memset(&q, 0, sizeof(q));
+    q.a_mode = A_DENSE; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
+    q.M = T; q.N = d; q.nseg = ns > 0 ? 4 : 2;
+    q.seg[0] = GemmSeg{dz, L, a.W_ld, d, L};
+    q.seg[1] = GemmSeg{dl, E, a.Wr, d, E};
+    if (ns > 0) {
+        q.seg[2] = GemmSeg{dgs, HS, a.Wsg, d, HS};
+        q.seg[3] = GemmSeg{dus, HS, a.Wsu, d, HS};
+    }
+    q.b_rows = d; q.out = a.dx; q.ldo = d;
+    return mm(q, "bwd_gemm_dx");
+}
+
+}  // namespace moe

@@ -97,11 +97,14 @@ struct KParams {
     int N2;
     void* out2;
     long long ldo2;
+    const uint16_t* aux;
+    int uniform_groups;
 };
 
 template <int AMODE>
 __device__ __forceinline__ int num_tiles(const KParams& p) {
     if (AMODE == A_DENSE) return p.m_tiles * p.n_tiles_n;
+    if (p.uniform_groups) return p.uniform_groups * p.m_tiles * p.n_tiles_n;
     return (*reinterpret_cast<const volatile int*>(p.tile_count)) * p.n_tiles_n;
 }
 
@@ -112,6 +115,9 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
     if (AMODE == A_DENSE) {
         g = 0;
         m0 = entry * BM;
+    } else if (p.uniform_groups) {
+        g = entry / p.m_tiles;
+        m0 = (entry - g * p.m_tiles) * BM;
     } else {
         const int2 te = p.tile_list[entry];
         g = te.x;
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     constexpr bool B3D = (AMODE != A_DENSE);
     constexpr bool A_MN = (MAJ & 1) != 0;
     constexpr bool B_MN = (MAJ & 2) != 0;
-    static_assert(!A_MN || AMODE == A_DENSE, "MN-major A: dense TMA tiles only");
+    static_assert(!A_MN || AMODE != A_GATHER, "MN-major A: TMA tiles only");
     static_assert(!B_MN || (BN <= 256 && EPI != EPI_SPLIT), "MN-major B: plain tiles only");
 
     extern __shared__ uint8_t smem_raw[];
@@ -211,9 +217,12 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         mbar_arrive_expect_tx(&fullA[sa], A_STAGE_BYTES);
                         armedA |= 1u << sa;
                         parA = (parA & ~(1u << sa)) | (pa << sa);
-                        if (A_MN) {
+                        if (A_MN && AMODE == A_DENSE) {
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], m0, kx);
                             tma_load_2d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, kx);
+                        } else if (A_MN) {
+                            tma_load_3d(a_dst, &p.mapA[seg], &fullA[sa], m0, kx, g);
+                            tma_load_3d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, kx, g);
                         } else if (AMODE == A_DENSE)
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], kx, m0);
                         else if (p.goff)   // ragged groups: rows of one flat 2-D matrix
@@ -237,17 +246,17 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         // BN/64 boxes of 64 N x 64 K; SwiGLU: gate then up halves
 #pragma unroll
                         for (int h = 0; h < BN / 64; ++h) {
-                            const bool up = EPI == EPI_SWIGLU && h >= BN / 128;
-                            const int n = EPI == EPI_SWIGLU
-                                              ? nb * (BN / 2) + (h % (BN / 128)) * 64
-                                              : nb * BN + h * 64;
+                            constexpr bool PAIR = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD;
+                            const bool up = PAIR && h >= BN / 128;
+                            const int n = PAIR ? nb * (BN / 2) + (h % (BN / 128)) * 64
+                                               : nb * BN + h * 64;
                             const CUtensorMap* mp = up ? &p.mapBup : &p.mapB[seg];
                             if (B3D)
                                 tma_load_3d(b_dst + h * 8192, mp, &fullB[sb], n, kx, g);
                             else
                                 tma_load_2d(b_dst + h * 8192, mp, &fullB[sb], n, kx);
                         }
-                    } else if (EPI == EPI_SWIGLU) {
+                    } else if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
                         const int n_half = nb * (BN / 2);
                         const uint32_t b_dst2 = b_dst + (BN / 2) * BK * 2;
                         if (B3D) {
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             const int m = m0 + r_local;
             bool row_ok;
             long long orow;
-            if (AMODE == A_DENSE) {
+            if (AMODE == A_DENSE || p.uniform_groups) {
                 row_ok = m < p.M;
                 orow = m;
             } else {
@@ -375,6 +384,13 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     orow = p.rowmap[(p.goff ? static_cast<long long>(p.goff[g])
                                             : static_cast<long long>(g) * p.rowmap_ld) + m];
             }
+            // element offset of this row in the output (and in aux / out2):
+            // dense or scattered rows, or row m of group g
+            const long long obase =
+                (AMODE == A_DENSE || EPI == EPI_SCATTER)
+                    ? orow * p.ldo
+                    : (p.goff ? (p.goff[g] + orow) * p.ldo
+                              : static_cast<long long>(g) * p.out_gstride + orow * p.ldo);
             if (EPI == EPI_SPLIT && nb >= p.nsplit) {
                 float* out = reinterpret_cast<float*>(p.out2) + orow * p.ldo2;
 #pragma unroll 1
@@ -411,7 +427,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     }
                 }
             } else if (EPI == EPI_F32) {
-                float* out = reinterpret_cast<float*>(p.out) + orow * p.ldo;
+                float* out = reinterpret_cast<float*>(p.out) + obase;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -429,10 +445,49 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         }
                     }
                 }
+            } else if (EPI == EPI_SWIGLU_BWD) {
+                // recomputed g (columns 0..BN/2) and u (BN/2..BN) of hidden units
+                // nb*BN/2 + c; incoming dh; dg = dh u silu'(g), du = dh silu(g)
+                uint16_t* dgo = reinterpret_cast<uint16_t*>(p.out) + obase;
+                uint16_t* duo = reinterpret_cast<uint16_t*>(p.out2) + obase;
+                const uint16_t* dhi = p.aux + obase;
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld32(tl + c * 32, gr);
+                    tmem_ld32(tl + BN / 2 + c * 32, ur);
+                    const int col0 = nb * (BN / 2) + c * 32;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = col0 + 8 * v;
+                            if (col >= p.N) continue;
+                            const uint4 hv = *reinterpret_cast<const uint4*>(dhi + col);
+                            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+                            uint32_t pg[4], pu[4];
+#pragma unroll
+                            for (int q2 = 0; q2 < 4; ++q2) {
+                                float dg2[2], du2[2];
+#pragma unroll
+                                for (int e2 = 0; e2 < 2; ++e2) {
+                                    const int i = 8 * v + 2 * q2 + e2;
+                                    const float gg = __uint_as_float(gr[i]);
+                                    const float uu = __uint_as_float(ur[i]);
+                                    const float dh = e2 ? bf16_hi(hw[q2]) : bf16_lo(hw[q2]);
+                                    const float sig = 1.0f / (1.0f + expf(-gg));
+                                    dg2[e2] = dh * uu * (sig * (1.0f + gg * (1.0f - sig)));
+                                    du2[e2] = dh * (gg * sig);
+                                }
+                                pg[q2] = pack_bf16x2(dg2[0], dg2[1]);
+                                pu[q2] = pack_bf16x2(du2[0], du2[1]);
+                            }
+                            *reinterpret_cast<uint4*>(dgo + col) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+                            *reinterpret_cast<uint4*>(duo + col) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+                        }
+                    }
+                }
             } else if (EPI == EPI_SWIGLU) {
-                uint16_t* out = reinterpret_cast<uint16_t*>(p.out) +
-                                (p.goff ? (p.goff[g] + orow) * p.ldo
-                                        : static_cast<long long>(g) * p.out_gstride + orow * p.ldo);
+                uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + obase;
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t gr[32], ur[32];
@@ -458,7 +513,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     }
                 }
             } else {   // EPI_BF16 / EPI_SCATTER
-                uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + orow * p.ldo;
+                uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + obase;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -648,47 +703,53 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
 
     KParams p;
     std::memset(&p, 0, sizeof(p));
-    const uint32_t b_box = (d.epi == EPI_SWIGLU || d.bn == 384) ? 128 : d.bn;
+    // gate/up pairs load two 128-row halves, the 384-wide router tile three
+    // 128-row thirds; everything else one box of bn rows (K-major B)
+    const bool pair = d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD;
+    const uint32_t b_box = (pair || d.bn == 384) ? 128 : d.bn;
+    {   // every stage must receive exactly the bytes its barrier expects
+        const uint32_t loads = d.b_mn ? d.bn / 64 : pair ? 2 : d.bn == 384 ? 3 : 1;
+        const uint32_t box_rows = d.b_mn ? 64 : b_box;
+        if (loads * box_rows * BK * 2 != static_cast<uint32_t>(d.bn) * BK * 2) return MOE_EINVAL;
+    }
     p.nseg = d.nseg;
     p.seg_kb[0] = 0;
     for (int s = 0; s < d.nseg; ++s) {
         const GemmSeg& g = d.seg[s];
-        if (g.K <= 0 || (g.K % 8)) return MOE_EINVAL;
+        // the row gather copies 16-byte chunks of K; TMA tiles take any K
+        if (g.K <= 0 || (d.a_mode == A_GATHER && g.K % 8)) return MOE_EINVAL;
         p.seg_kb[s + 1] = p.seg_kb[s] + (g.K + BK - 1) / BK;
-        if (d.a_mode == A_DENSE) {
-            if (d.a_mn)   // [K, M] storage: 64 x 64 boxes, M inner
-                rc = map2d(&p.mapA[s], g.A, d.M, g.K, g.lda, 64);
-            else
-                rc = map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM);
-            if (rc) return rc;
-            if (d.b_mn)
-                rc = map2d(&p.mapB[s], g.B, d.b_rows, g.K, g.ldb, 64);
-            else
-                rc = map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box);
-            if (rc) return rc;
-        } else if (d.b_mn) {
-            if (d.a_mode == A_GROUPED || d.a_mn) return MOE_EINVAL;
-            if ((rc = map3d(&p.mapB[s], g.B, d.b_rows, g.K, d.groups, g.ldb, d.b_gstride, 64)))
-                return rc;
-        } else {
-            if (d.a_mode == A_GROUPED && d.goff &&
-                (rc = map2d(&p.mapA[s], g.A, g.K, d.rows_per_group, g.lda, BM)))
-                return rc;   // ragged: rows_per_group = rows of the whole flat matrix
-            if (d.a_mode == A_GROUPED && !d.goff &&
-                (rc = map3d(&p.mapA[s], g.A, g.K, d.rows_per_group, d.groups, g.lda, d.a_gstride,
-                            BM)))
-                return rc;
-            if ((rc = map3d(&p.mapB[s], g.B, g.K, d.b_rows, d.groups, g.ldb, d.b_gstride, b_box)))
-                return rc;
-        }
+        // A: [M, K] K-major or [K, M] MN-major; grouped: one such matrix per group
+        if (d.a_mode == A_DENSE)
+            rc = d.a_mn ? map2d(&p.mapA[s], g.A, d.M, g.K, g.lda, 64)
+                        : map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM);
+        else if (d.a_mode == A_GROUPED && d.goff)
+            rc = d.a_mn ? MOE_EINVAL : map2d(&p.mapA[s], g.A, g.K, d.rows_per_group, g.lda, BM);
+        else if (d.a_mode == A_GROUPED)
+            rc = d.a_mn ? map3d(&p.mapA[s], g.A, d.M, g.K, d.groups, g.lda, d.a_gstride, 64)
+                        : map3d(&p.mapA[s], g.A, g.K, d.rows_per_group, d.groups, g.lda,
+                                d.a_gstride, BM);
+        else
+            rc = d.a_mn ? MOE_EINVAL : MOE_OK;   // gathered rows: no map
+        if (rc) return rc;
+        // B: [N, K] K-major or [K, N] MN-major; grouped modes: per group
+        if (d.a_mode == A_DENSE)
+            rc = d.b_mn ? map2d(&p.mapB[s], g.B, d.b_rows, g.K, g.ldb, 64)
+                        : map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box);
+        else
+            rc = d.b_mn ? map3d(&p.mapB[s], g.B, d.b_rows, g.K, d.groups, g.ldb, d.b_gstride, 64)
+                        : map3d(&p.mapB[s], g.B, g.K, d.b_rows, d.groups, g.ldb, d.b_gstride,
+                                b_box);
+        if (rc) return rc;
     }
     if (d.epi == EPI_SPLIT) {
         if (d.nseg != 1 || !d.B_up || d.a_mode != A_DENSE || d.N != d.nsplit * d.bn)
             return MOE_EINVAL;
         if ((rc = map2d(&p.mapBup, d.B_up, d.seg[0].K, d.b2_rows, d.seg[0].ldb, b_box))) return rc;
     }
-    if (d.epi == EPI_SWIGLU) {
+    if (d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD) {
         if (d.nseg != 1 || !d.B_up) return MOE_EINVAL;
+        if (d.epi == EPI_SWIGLU_BWD && (!d.aux || !d.out2)) return MOE_EINVAL;
         if (d.b_mn && d.a_mode == A_DENSE)
             rc = map2d(&p.mapBup, d.B_up, d.b_rows, d.seg[0].K, d.seg[0].ldb, 64);
         else if (d.b_mn)
@@ -704,7 +765,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.M = d.M;
     p.N = d.N;
     p.K0 = d.seg[0].K;
-    const int n_per_tile = (d.epi == EPI_SWIGLU) ? d.bn / 2 : d.bn;
+    const int n_per_tile = (d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD) ? d.bn / 2 : d.bn;
     p.n_tiles_n = (d.N + n_per_tile - 1) / n_per_tile;
     if (d.epi == EPI_SPLIT) {
         p.nsplit = d.nsplit;
@@ -727,8 +788,13 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.out_gstride = d.out_gstride;
     p.bias = d.bias;
     p.status = d.status;
+    p.aux = static_cast<const uint16_t*>(d.aux);
+    p.uniform_groups = d.uniform_groups;
+    if (d.epi == EPI_SWIGLU_BWD) p.out2 = d.out2;
 
-    int tiles = (d.a_mode == A_DENSE) ? p.m_tiles * p.n_tiles_n : d.max_tiles * p.n_tiles_n;
+    int tiles = (d.a_mode == A_DENSE) ? p.m_tiles * p.n_tiles_n
+                : d.uniform_groups     ? d.uniform_groups * p.m_tiles * p.n_tiles_n
+                                       : d.max_tiles * p.n_tiles_n;
     if (tiles <= 0) return MOE_OK;
     const int grid = tiles < sms ? tiles : sms;
 
@@ -752,6 +818,12 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         case MOE_K(256, A_DENSE, EPI_F32, 1): return launch_traced<256, A_DENSE, EPI_F32, 1>(p, grid, st, d.name);
         case MOE_K(256, A_DENSE, EPI_F32, 2): return launch_traced<256, A_DENSE, EPI_F32, 2>(p, grid, st, d.name);
         case MOE_K(256, A_DENSE, EPI_F32, 3): return launch_traced<256, A_DENSE, EPI_F32, 3>(p, grid, st, d.name);
+        // backward pass
+        case MOE_K(256, A_DENSE, EPI_SWIGLU_BWD, 0): return launch_traced<256, A_DENSE, EPI_SWIGLU_BWD, 0>(p, grid, st, d.name);
+        case MOE_K(256, A_GATHER, EPI_SWIGLU_BWD, 0): return launch_traced<256, A_GATHER, EPI_SWIGLU_BWD, 0>(p, grid, st, d.name);
+        case MOE_K(256, A_GATHER, EPI_BF16, 2): return launch_traced<256, A_GATHER, EPI_BF16, 2>(p, grid, st, d.name);
+        case MOE_K(256, A_GROUPED, EPI_SCATTER, 2): return launch_traced<256, A_GROUPED, EPI_SCATTER, 2>(p, grid, st, d.name);
+        case MOE_K(256, A_GROUPED, EPI_F32, 3): return launch_traced<256, A_GROUPED, EPI_F32, 3>(p, grid, st, d.name);
 #undef MOE_K
         default: return MOE_EINVAL;
     }

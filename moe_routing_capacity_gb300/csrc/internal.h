@@ -33,6 +33,8 @@ enum EpiMode : int {
     EPI_SCATTER = 3,  // bf16 out to rows given by a row map
     EPI_SPLIT = 4,    // column tiles < nsplit: bf16 out (B = seg 0); the rest: fp32
                       // out2 + bias (B = B_up), e.g. latent projection + router
+    EPI_SWIGLU_BWD = 5,  // accumulator = [gate | up] (recomputed); with the incoming
+                         // gradient dh (aux, bf16): out = dh u silu'(g), out2 = dh silu(g)
 };
 
 struct GemmSeg {        // one K segment of the contraction: A_s [M, K_s] . B_s [N, K_s]^T
@@ -82,7 +84,10 @@ struct GemmDesc {
     const float* bias;
     int32_t* status;
     const char* name;       // kernel name for the timing trace
-    // EPI_SPLIT: second output
+    const void* aux;        // EPI_SWIGLU_BWD: incoming gradient, addressed like out
+    int uniform_groups;     // > 0: grouped tiles over `groups` groups of M rows each
+                            // (no tile list), e.g. per-expert weight gradients
+    // EPI_SPLIT: second output (EPI_SWIGLU_BWD: out2 = du, addressed like out)
     int nsplit;             // column tiles of the first output (N = nsplit * bn)
     int N2;                 // columns of the second output
     void* out2;
@@ -126,10 +131,19 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
 int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
                        int32_t* tile_count, cudaStream_t stream);
 
+// Backward pass: scratch layout (byte offsets) and launch sequence.
+struct BackwardWs {
+    size_t dc, da, dgs, dus, dw, dypool, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles, total;
+};
+BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int ns);
+int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
+                    const moe_backward_args_t& a, cudaStream_t stream);
+
 // Quantile-balancing bias update: hist += counts of idx; bias from hist.
 int launch_balance_update(const int32_t* idx, int64_t n, int E, int64_t* hist, float alpha,
                           float* bias, cudaStream_t stream);
 
+// c[t] = bf16(sum over kept j of w[t,j] ypool[slot_of[t,j]]); w == nullptr: weights 1.
 int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
                    int L, uint16_t* c, cudaStream_t stream);
 

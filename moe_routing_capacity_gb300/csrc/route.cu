@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     float my_w = 0.0f;
     if (lane < k) {
         my_row = slot_of[t * k + lane];
-        my_w = w[t * k + lane];
+        my_w = w ? w[t * k + lane] : 1.0f;   // no weights: plain sum (gradient return)
     }
     const int nchunk = L / 8;
     uint4* dst = reinterpret_cast<uint4*>(c + t * L);

@@ -114,6 +114,43 @@ class PooledWaveMoE:
         self.combine(x, out, stream)
         return self.out if out is None else out
 
+    def backward(self, x, dout, stream=None) -> dict:
+        """Gradients of the last forward with respect to x and every weight,
+        for the upstream gradient dout [T, d] (capped layout only).  Returns
+        {"x": dx (bf16), "Wr": ..., ...} with fp32 weight gradients."""
+        if self.dropless:
+            raise NotImplementedError("the backward pass covers the capped layout")
+        cfg, dev = self.cfg, self.device
+        T, d, L, E, H = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.h_expert
+        ns, Hs = cfg.n_shared, cfg.h_shared
+        if not hasattr(self, "bwd_ws"):
+            self.bwd_layout = abi.backward_plan(cfg)
+            self.bwd_ws = torch.empty(max(1, self.bwd_layout.total), dtype=torch.uint8, device=dev)
+            f = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
+            self.grads = {"x": torch.empty(T, d, dtype=torch.bfloat16, device=dev),
+                          "Wr": f(E, d), "W_ld": f(L, d), "Wg": f(E, H, L), "Wu": f(E, H, L),
+                          "Wd": f(E, L, H), "W_lu": f(d, L), "Wsg": f(ns, Hs, d),
+                          "Wsu": f(ns, Hs, d), "Wsd": f(ns, d, Hs)}
+        hoff = self.plan.h_offset_bytes
+        h = self.ws_ffn[hoff:hoff + E * self.plan.c_recv * H * 2].view(torch.bfloat16)
+        g = self.grads
+        tensors = dict(x=x, Wr=self.w["Wr"], W_ld=self.w["W_ld"], Wg=self.w["Wg"], Wu=self.w["Wu"],
+                       Wd=self.w["Wd"], W_lu=self.w["W_lu"], Wsg=self.w["Wsg"], Wsu=self.w["Wsu"],
+                       Wsd=self.w["Wsd"], idx=self.idx, w=self.gate_w, pool=self.pool,
+                       slot_of=self.slot_of, expert_rows=self.expert_rows,
+                       expert_count=self.expert_count, h=h, ypool=self.ypool, c=self.c,
+                       a=self.a if ns else None, dout=dout, dx=g["x"], dWr=g["Wr"],
+                       dW_ld=g["W_ld"], dWg=g["Wg"], dWu=g["Wu"], dWd=g["Wd"], dW_lu=g["W_lu"],
+                       dWsg=g["Wsg"] if ns else None, dWsu=g["Wsu"] if ns else None,
+                       dWsd=g["Wsd"] if ns else None)
+        abi.layer_backward(cfg, tensors, self.bwd_ws, self.status, stream)
+        return g
+
+    def backward_intermediate(self, name):
+        """A view of one backward intermediate in the scratch (tests)."""
+        off = getattr(self.bwd_layout, name)
+        return self.bwd_ws[off:]
+
     # -- views ------------------------------------------------------------
     def pool_payload(self):
         return self.pool[:, : self.cfg.d_latent].view(torch.bfloat16)

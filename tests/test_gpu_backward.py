@@ -1,0 +1,72 @@
+"""GPU parity of the layer's backward pass against the oracle's derivative
+(which the CPU suite pins with central finite differences)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from moe_routing_capacity_gb300 import workloads as wl
+from moe_routing_capacity_gb300.layer import PooledWaveMoE
+
+from helpers import check_close
+
+pytestmark = pytest.mark.gpu
+
+
+def check_grad(name, got, want, report):
+    """fp32 weight gradients: sums over many tokens of bf16-stored activation
+    gradients, so the bound scales with the gradient: elementwise
+    |err| <= 2e-2 * max|want|, relative L2 <= 1e-2."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, name
+    assert np.isfinite(got).all(), name
+    scale = float(np.abs(want).max()) or 1.0
+    err = np.abs(got - want)
+    rel = float(np.linalg.norm(got - want) / (np.linalg.norm(want) or 1.0))
+    report[name] = dict(max_err_over_scale=float(err.max() / scale), rel_l2=rel)
+    assert err.max() <= 2e-2 * scale, (name, err.max(), scale)
+    assert rel <= 1e-2, (name, rel)
+
+
+def run(cfg, seed_dout=3):
+    inp = wl.make_inputs(cfg, "cpu")
+    host = {k: (v.float().numpy() if v is not None else None) for k, v in inp.items()}
+    fwd = O.layer(cfg, host)
+    m = PooledWaveMoE(cfg, inp, "cuda")
+    x = inp["x"].cuda()
+    m.forward(x)
+    torch.cuda.synchronize()
+    assert (m.idx.cpu().numpy() == fwd["idx"]).all(), "choose a seed without near-tie flips"
+    assert (m.drop.cpu().numpy() == fwd["disp"]["drop"]).all()
+    g = torch.Generator().manual_seed(seed_dout)
+    dout = torch.randn(cfg.T, cfg.d_model, generator=g).to(torch.bfloat16)
+    grads = m.backward(x, dout.cuda())
+    torch.cuda.synchronize()
+    assert int(m.status.item()) == 0
+    ref = O.layer_backward(cfg, host, fwd, dout.float().numpy())
+    rep = {}
+    check_close("dx", grads["x"].float().cpu().numpy(), ref["x"], rep)
+    for name in ("Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu"):
+        check_grad("d" + name, grads[name].cpu().numpy(), ref[name], rep)
+    if cfg.n_shared:
+        for name in ("Wsg", "Wsu", "Wsd"):
+            check_grad("d" + name, grads[name].cpu().numpy(), ref[name], rep)
+    return m, ref, rep
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(seed=51, T=200, n_ranks=4, d_model=136, d_latent=72, h_expert=136, h_shared=72),
+    dict(seed=52, top_k=4, cf_send=0.6, cf_recv=0.8),          # many drops
+    dict(seed=53, n_shared=0),
+    dict(seed=54, n_shared=2, T=512, top_k=1),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()) or "tiny")
+def test_backward_small(kw):
+    _, _, rep = run(wl.TINY.with_(**kw))
+    print(rep)
+
+
+def test_backward_mid():
+    _, _, rep = run(wl.MID)
+    print(rep)
