@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-dropless", action="store_true",
                     help="skip timing the dropless ragged variant")
+    ap.add_argument("--no-train", action="store_true",
+                    help="skip timing forward + backward (one training step of the layer)")
     return ap.parse_args()
 
 
@@ -409,6 +411,41 @@ def run_gb300(args, rank, world, local_rank):
                                                if k2.startswith("gemm_expert")) / nd, 4)}
         del md
 
+    # ---- one training step of the layer: forward + backward on the same batch
+    train = None
+    if not args.no_train:
+        g = torch.Generator(device=dev).manual_seed(7)
+        dout = torch.randn(cfg.T, cfg.d_model, generator=g, device=dev).to(torch.bfloat16)
+        for _ in range(2):
+            m.forward(x)
+            m.backward(x, dout)
+        torch.cuda.synchronize()
+        assert int(m.status.item()) == 0, "device status word set in the backward"
+        nt = max(3, min(args.steps, 30))
+        abi.trace_begin(64 * nt + 8)
+        t0e = torch.cuda.Event(enable_timing=True)
+        t1e = torch.cuda.Event(enable_timing=True)
+        t0e.record(stream)
+        for _ in range(nt):
+            abi.trace_mark(stream)
+            m.forward(x)
+            m.backward(x, dout)
+        t1e.record(stream)
+        torch.cuda.synchronize()
+        ttr = abi.trace_end()
+        assert int(m.status.item()) == 0
+        tms = t0e.elapsed_time(t1e) / nt
+        bwd = sum(ms for n, ms in ttr if n.startswith("bwd_")) / nt
+        tv, _ = replica_throughput(tms / 1e3, cfg.T, 1, dev)
+        # GEMM work of the backward: twice the forward's, plus the gate/up
+        # recomputes (routed and shared)
+        fwd_tf = sum(kernel_work(n, cfg, m.plan, st)[0] or 0.0 for n in per
+                     if kernel_work(n, cfg, m.plan, st)[2] == "tensor")
+        train = {"value": tv, "unit": UNIT, "ms_per_step": tms, "steps": nt,
+                 "backward_ms": round(bwd, 4),
+                 "forward_tflop": round(fwd_tf, 3),
+                 "note": "forward + backward of the layer; weight gradients fp32"}
+
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,7 +476,7 @@ def run_gb300(args, rank, world, local_rank):
                       "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
             "gpu_launches": sum(v[1] for v in per.values()),
             "roofline": roof, "kernels": kernels, "clocks": clk, "e2e": e2e,
-            "dropless": dropless,
+            "dropless": dropless, "train_step": train,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
