@@ -47,7 +47,7 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 #define MOE_GROUPED_B_STAGES 4
 #endif
 
-template <int BN, int AMODE>
+template <int BN, int AMODE, int EPI>
 struct TileCfg {
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
     static constexpr int B_STAGES = (BN == 384)              ? 3
@@ -64,8 +64,11 @@ struct TileCfg {
     static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
     static constexpr int TMEM_COLS = (BN <= 256) ? 2 * BN : 512;
     static constexpr int BAR_BYTES = 256;
+    // fp32 output: each epilogue warp stages a 32 x 32 block in shared memory
+    // so that the global stores run along rows (full 128-byte lines)
+    static constexpr int STG_BYTES = (EPI == EPI_F32) ? 4 * 32 * 32 * 4 : 0;
     static constexpr int SMEM_BYTES =
-        1024 + A_STAGES * A_STAGE_BYTES + B_STAGES * B_STAGE_BYTES + BAR_BYTES;
+        1024 + A_STAGES * A_STAGE_BYTES + B_STAGES * B_STAGE_BYTES + BAR_BYTES + STG_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -133,7 +136,7 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 template <int BN, int AMODE, int EPI, int MAJ>
 __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     gemm_tc_kernel(const __grid_constant__ KParams p) {
-    using C = TileCfg<BN, AMODE>;
+    using C = TileCfg<BN, AMODE, EPI>;
     constexpr int AST = C::A_STAGES;
     constexpr int BST = C::B_STAGES;
     constexpr bool B3D = (AMODE != A_DENSE);
@@ -427,23 +430,57 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     }
                 }
             } else if (EPI == EPI_F32) {
-                float* out = reinterpret_cast<float*>(p.out) + obase;
+                // Lane i holds row 32q + i.  Each 32-column block goes through
+                // shared memory (16-byte chunks XOR-swizzled by row, so both
+                // the row-wise writes and the column-wise reads are free of
+                // bank conflicts); then lane l stores columns 4(l%8)..+3 of
+                // rows 4j + l/8: one warp store covers four whole rows.
+                float4* stg = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(bars) +
+                                                        C::BAR_BYTES) + q * 256;
+                float* out = reinterpret_cast<float*>(p.out);
+                const int rsub = lane >> 3, csub = lane & 7;
+                long long rbase[8];
+                uint32_t rok = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    rbase[j] = __shfl_sync(0xffffffffu, obase, 4 * j + rsub);
+                    rok |= (__shfl_sync(0xffffffffu, row_ok ? 1 : 0, 4 * j + rsub) ? 1u : 0u) << j;
+                }
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tl + c * 32, r);
-                    const int col0 = nb * BN + c * 32;
-                    if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int col = col0 + i;
-                            if (col < p.N) {
-                                float v = __uint_as_float(r[i]);
-                                if (p.bias) v += p.bias[col];
-                                out[col] = v;
-                            }
+                    for (int v = 0; v < 8; ++v)
+                        stg[lane * 8 + (v ^ (lane & 7))] =
+                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    __syncwarp();
+                    const int col = nb * BN + c * 32 + 4 * csub;
+                    float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p.bias) {
+                        if (col + 0 < p.N) bv.x = p.bias[col + 0];
+                        if (col + 1 < p.N) bv.y = p.bias[col + 1];
+                        if (col + 2 < p.N) bv.z = p.bias[col + 2];
+                        if (col + 3 < p.N) bv.w = p.bias[col + 3];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = 4 * j + rsub;
+                        float4 f = stg[rr * 8 + (csub ^ (rr & 7))];
+                        f.x += bv.x; f.y += bv.y; f.z += bv.z; f.w += bv.w;
+                        if (!(rok >> j & 1u) || col >= p.N) continue;
+                        float* dst = out + rbase[j] + col;
+                        if (col + 4 <= p.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                            *reinterpret_cast<float4*>(dst) = f;
+                        } else {
+                            dst[0] = f.x;
+                            if (col + 1 < p.N) dst[1] = f.y;
+                            if (col + 2 < p.N) dst[2] = f.z;
+                            if (col + 3 < p.N) dst[3] = f.w;
                         }
                     }
+                    __syncwarp();
                 }
             } else if (EPI == EPI_SWIGLU_BWD) {
                 // recomputed g (columns 0..BN/2) and u (BN/2..BN) of hidden units
@@ -676,7 +713,7 @@ static int map3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 
 template <int BN, int AMODE, int EPI, int MAJ = 0>
 static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
-    using C = TileCfg<BN, AMODE>;
+    using C = TileCfg<BN, AMODE, EPI>;
     auto kern = gemm_tc_kernel<BN, AMODE, EPI, MAJ>;
     // Attribute setting is per device; cheap and idempotent, done every launch.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=

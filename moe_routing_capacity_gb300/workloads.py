@@ -81,7 +81,13 @@ FULL = LayerConfig("full", T=16384, d_model=6144, d_latent=3072, n_experts=384, 
 SKEW = FULL.with_(name="skew", bias_kind="zipf")
 LONG = FULL.with_(name="long", T=65536, seed=3, x_kind="ar1", n_seqs=1)
 
-CONFIGS = {c.name: c for c in (TINY, MID, FULL, SKEW, LONG)}
+# The full-width layer's per-expert shapes (d=6144, L=3072, H=1024, top-8,
+# 6 experts a rank, about 340 received rows per expert) on 96 experts and 16
+# ranks with T=4096: the expert GEMMs run in the same regime on a few GB of
+# device memory, small enough for multi-pass profiler captures.
+SLICE = FULL.with_(name="full_slice", T=4096, n_experts=96, n_ranks=16, seed=4, n_seqs=1)
+
+CONFIGS = {c.name: c for c in (TINY, MID, FULL, SKEW, LONG, SLICE)}
 
 # Inputs with fewer elements than this are drawn on the host (so CPU-only and
 # GPU test runs see identical values); larger ones are drawn on the target
