@@ -287,7 +287,10 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
  * du, dX, dz, dlogits, dx), weight gradients fp32, all products accumulate
  * in fp32.
  * moe_backward_plan: byte offsets of the intermediates inside the scratch
- *   and its total size (layout->total).
+ *   and its total size (layout->total).  Among them: dY and X of the routed
+ *   experts in per-expert row order ([E, c_recv, L], dye and xe), rowinv
+ *   (int32 per pool row: e * c_recv + r for the r-th row of expert e), dX in
+ *   pool row order (dxpool) and dh, dg, du ([E, c_recv, H]).
  * moe_layer_backward: inputs are the forward's inputs and the tensors its
  *   calls produced (idx, w, pool, slot_of, expert_rows, expert_count, h =
  *   ws_ffn + plan.h_offset_bytes, ypool, c, a), plus dout [T, d] bf16.
@@ -298,7 +301,7 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
  *   (they were never written by the forward).  All device pointers,
  *   16-byte aligned; scratch ws of at least layout.total bytes. */
 typedef struct moe_backward_ws {
-    int64_t dc, da, dgs, dus, dw, dypool, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles;
+    int64_t dc, da, dgs, dus, dw, rowinv, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles;
     int64_t total;
 } moe_backward_ws_t;
 

@@ -59,7 +59,7 @@ class DropStats(ctypes.Structure):
 
 STATS_WORDS = ctypes.sizeof(DropStats) // 8    # int64 words of a stats record
 
-BWD_WS_FIELDS = ("dc", "da", "dgs", "dus", "dw", "dypool", "dxpool", "dh", "dg", "du", "xe", "dye",
+BWD_WS_FIELDS = ("dc", "da", "dgs", "dus", "dw", "rowinv", "dxpool", "dh", "dg", "du", "xe", "dye",
                  "dz", "dlogits", "tiles", "total")
 
 

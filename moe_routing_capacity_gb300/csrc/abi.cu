@@ -584,7 +584,7 @@ int moe_backward_plan(const moe_config_t* cfg, moe_backward_ws_t* layout) {
     if (rc) return rc;
     const BackwardWs w = backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns);
     layout->dc = w.dc; layout->da = w.da; layout->dgs = w.dgs; layout->dus = w.dus;
-    layout->dw = w.dw; layout->dypool = w.dypool; layout->dxpool = w.dxpool; layout->dh = w.dh;
+    layout->dw = w.dw; layout->rowinv = w.rowinv; layout->dxpool = w.dxpool; layout->dh = w.dh;
     layout->dg = w.dg; layout->du = w.du; layout->xe = w.xe; layout->dye = w.dye;
     layout->dz = w.dz; layout->dlogits = w.dlogits; layout->tiles = w.tiles;
     layout->total = w.total;

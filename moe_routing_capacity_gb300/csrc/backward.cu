@@ -19,33 +19,37 @@
 
 namespace moe {
 
-// dY[slot] = bf16(w_tj dc_t) for kept (t, j); dw_tj = <dc_t, Y[slot]> (fp32).
-// One warp per token; dc_t is read once into registers.
+// dY = bf16(w_tj dc_t) for kept (t, j), written to the assignment's row in
+// the per-expert layout (rowinv of its pool slot); dw_tj = <dc_t, Y[slot]>
+// (fp32).  One warp per token.
 template <int CH>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ dc,
                                                           const uint16_t* __restrict__ ypool,
                                                           const int32_t* __restrict__ slot_of,
+                                                          const int32_t* __restrict__ rowinv,
                                                           const float* __restrict__ w, int64_t T,
                                                           int k, int L, uint16_t* __restrict__ dy,
                                                           float* __restrict__ dw) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    int32_t my_row = -1;
+    int32_t my_row = -1, my_dst = 0;
     float my_w = 0.0f;
     if (lane < k) {
         my_row = slot_of[t * k + lane];
         my_w = w[t * k + lane];
+        if (my_row >= 0) my_dst = rowinv[my_row];
     }
     const int nchunk = L / 8;
     float dot_mine = 0.0f;   // lane j keeps dw for assignment j
     for (int j = 0; j < k; ++j) {
         const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+        const int32_t rd = __shfl_sync(0xffffffffu, my_dst, j);
         const float wj = __shfl_sync(0xffffffffu, my_w, j);
         float dot = 0.0f;
         if (r >= 0) {
             const uint4* yrow = reinterpret_cast<const uint4*>(ypool + static_cast<int64_t>(r) * L);
-            uint4* drow = reinterpret_cast<uint4*>(dy + static_cast<int64_t>(r) * L);
+            uint4* drow = reinterpret_cast<uint4*>(dy + static_cast<int64_t>(rd) * L);
             const uint4* crow = reinterpret_cast<const uint4*>(dc + t * L);
             for (int ch = lane; ch < nchunk; ch += 32) {
                 const uint4 cv = __ldg(crow + ch);
@@ -104,6 +108,18 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restri
     }
 }
 
+// rowinv[rows[e][r]] = e * c_recv + r for r < count[e]: where each kept pool
+// row sits in the per-expert layout.
+__global__ void __launch_bounds__(256) row_inverse_kernel(const int32_t* __restrict__ rows,
+                                                          const int32_t* __restrict__ count, int E,
+                                                          int c_recv, int32_t* __restrict__ rowinv) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(E) * c_recv) return;
+    const int e = static_cast<int>(i / c_recv);
+    const int r = static_cast<int>(i - static_cast<int64_t>(e) * c_recv);
+    if (r < count[e]) rowinv[rows[i]] = static_cast<int32_t>(i);
+}
+
 // dst[e][r][0:L] = src[rows[e][r]][0:L] for r < count[e], zeros up to c_recv.
 __global__ void __launch_bounds__(256) gather_expert_rows_kernel(
     const uint16_t* __restrict__ src, int64_t pitch, const int32_t* __restrict__ rows,
@@ -150,7 +166,7 @@ BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int n
     w.dgs = o;      o = al(o + T * HS * 2);
     w.dus = o;      o = al(o + T * HS * 2);
     w.dw = o;       o = al(o + T * g.k * 4);
-    w.dypool = o;   o = al(o + P * L * 2);
+    w.rowinv = o;   o = al(o + P * 4);
     w.dxpool = o;   o = al(o + P * L * 2);
     w.dh = o;       o = al(o + E * cr * H * 2);
     w.dg = o;       o = al(o + E * cr * H * 2);
@@ -171,7 +187,8 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
     uint16_t *dc = bf(L_.dc), *da = bf(L_.da), *dgs = bf(L_.dgs), *dus = bf(L_.dus);
-    uint16_t *dyp = bf(L_.dypool), *dxp = bf(L_.dxpool), *dh = bf(L_.dh), *dg = bf(L_.dg),
+    int32_t* rowinv = reinterpret_cast<int32_t*>(ws + L_.rowinv);
+    uint16_t *dxp = bf(L_.dxpool), *dh = bf(L_.dh), *dg = bf(L_.dg),
              *du = bf(L_.du), *xe = bf(L_.xe), *dye = bf(L_.dye), *dz = bf(L_.dz),
              *dl = bf(L_.dlogits);
     float* dw = reinterpret_cast<float*>(ws + L_.dw);
@@ -230,13 +247,21 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
             if ((rc = mm(q, "bwd_gemm_dWshared"))) return rc;
         }
     }
-    // ---- combine backward (the return path in reverse)
+    // ---- combine backward (the return path in reverse): dY straight into the
+    // per-expert layout, whose rows past each expert's count are zero
     {
+        const int64_t nw = static_cast<int64_t>(E) * cr;
+        const unsigned g_inv = static_cast<unsigned>((nw + 255) / 256);
+        const unsigned g_pad = static_cast<unsigned>((nw + 7) / 8);
+        row_inverse_kernel<<<g_inv, 256, 0, st>>>(a.expert_rows, a.expert_count, E, cr, rowinv);
+        zero_pad_rows_kernel<<<g_pad, 256, 0, st>>>(dye, a.expert_count, E, cr, L);
         const unsigned grid = static_cast<unsigned>((T + 7) / 8);
         if (L / 8 <= 32 * 4)
-            combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, a.w, T, k, L, dyp, dw);
+            combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
+                                                         L, dye, dw);
         else
-            combine_bwd_kernel<12><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, a.w, T, k, L, dyp, dw);
+            combine_bwd_kernel<12><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
+                                                          L, dye, dw);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_combine");
     }
@@ -244,14 +269,13 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     const int max_mt = E * ((cr + 127) / 128);
     int32_t* tile_count = tiles + 2 * max_mt;
     if ((rc = launch_build_tiles(a.expert_count, E, 128, tiles, tile_count, st))) return rc;
-    std::memset(&q, 0, sizeof(q));   // dh = dY Wd_e (rows of dY gathered by the expert lists)
-    q.a_mode = A_GATHER; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
-    q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{nullptr, 0, a.Wd, H, L};
-    q.groups = E; q.rows_per_group = cr; q.b_rows = H;
-    q.b_gstride = static_cast<int64_t>(L) * H;
+    std::memset(&q, 0, sizeof(q));   // dh = dY_e Wd_e (per-expert rows by TMA)
+    q.a_mode = A_GROUPED; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
+    q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{dye, L, a.Wd, H, L};
+    q.groups = E; q.rows_per_group = cr; q.a_gstride = static_cast<int64_t>(cr) * L;
+    q.b_rows = H; q.b_gstride = static_cast<int64_t>(L) * H;
     q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
-    q.gather_src = dyp; q.gather_pitch = L; q.gather_rows = g.pool_rows;
     q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
     if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
     const size_t ghs = static_cast<size_t>(E) * cr * H * 2;
@@ -278,11 +302,10 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
     q.out = dxp; q.ldo = L;
     if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
-    {   // per-expert contiguous, zero-padded copies of X and dY for the weight gradients
+    {   // per-expert contiguous, zero-padded copy of X; h's unwritten rows zeroed
         const int64_t nw = static_cast<int64_t>(E) * cr;
         const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
         gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, L + 8, a.expert_rows, a.expert_count, E, cr, L, xe);
-        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(dyp, L, a.expert_rows, a.expert_count, E, cr, L, dye);
         zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_gather_rows");

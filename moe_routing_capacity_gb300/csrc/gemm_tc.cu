@@ -858,7 +858,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         // backward pass
         case MOE_K(256, A_DENSE, EPI_SWIGLU_BWD, 0): return launch_traced<256, A_DENSE, EPI_SWIGLU_BWD, 0>(p, grid, st, d.name);
         case MOE_K(256, A_GATHER, EPI_SWIGLU_BWD, 0): return launch_traced<256, A_GATHER, EPI_SWIGLU_BWD, 0>(p, grid, st, d.name);
-        case MOE_K(256, A_GATHER, EPI_BF16, 2): return launch_traced<256, A_GATHER, EPI_BF16, 2>(p, grid, st, d.name);
+        case MOE_K(256, A_GROUPED, EPI_BF16, 2): return launch_traced<256, A_GROUPED, EPI_BF16, 2>(p, grid, st, d.name);
         case MOE_K(256, A_GROUPED, EPI_SCATTER, 2): return launch_traced<256, A_GROUPED, EPI_SCATTER, 2>(p, grid, st, d.name);
         case MOE_K(256, A_GROUPED, EPI_F32, 3): return launch_traced<256, A_GROUPED, EPI_F32, 3>(p, grid, st, d.name);
 #undef MOE_K

@@ -133,7 +133,7 @@ int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
 
 // Backward pass: scratch layout (byte offsets) and launch sequence.
 struct BackwardWs {
-    size_t dc, da, dgs, dus, dw, dypool, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles, total;
+    size_t dc, da, dgs, dus, dw, rowinv, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles, total;
 };
 BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int ns);
 int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
