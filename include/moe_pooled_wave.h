@@ -93,7 +93,8 @@ typedef struct moe_plan {
     int32_t c_send;              /* rows per (src, dst, wave) slice                  */
     int32_t c_recv;              /* rows per expert                                  */
     int64_t pool_rows;           /* D * W * S * c_send                               */
-    int64_t pool_row_bytes;      /* 2*L + 16: L bf16 payload + 16-byte tag           */
+    int64_t pool_row_bytes;      /* 2*L + 16 rounded up to a multiple of 128: L bf16 */
+                                 /* payload, 16-byte tag, padding (never written)    */
     int64_t ws_dispatch_bytes;   /* scratch for moe_dispatch_pooled                  */
     int64_t ws_ffn_bytes;        /* scratch for moe_expert_ffn_grouped (incl. h)     */
     int64_t h_offset_bytes;      /* where h [E, c_recv, H] bf16 sits in ws_ffn       */
@@ -176,8 +177,10 @@ int moe_route_project(const moe_config_t* cfg, const uint16_t* x, const uint16_t
  * receiver stage per expert over the sender-kept rows in the same order.
  *   z           [T, L] bf16      idx [T, k] int32 (each row: distinct experts)
  *   ws          scratch, >= plan.ws_dispatch_bytes
- *   pool        [pool_rows, L + 8] uint16: payload z[t] for every
- *               sender-kept assignment, tag (moe_row_tag_t) on every row
+ *   pool        [pool_rows, plan.pool_row_bytes / 2] uint16: payload z[t]
+ *               (elements 0..L-1) for every sender-kept assignment, tag
+ *               (moe_row_tag_t, elements L..L+7) on every row; each row
+ *               starts on a 128-byte boundary
  *   slot_of     [T, k] int32: pool row of a kept assignment, else -1
  *   drop        [T, k] uint8: 0 kept, 1 dropped by the sender cap,
  *               2 dropped by the receiver cap

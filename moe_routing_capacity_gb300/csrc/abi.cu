@@ -128,7 +128,7 @@ static int make_geom(const moe_config_t* c, Geom* out) {
     p.c_send = g.c_send;
     p.c_recv = g.c_recv;
     p.pool_rows = g.pool_rows;
-    p.pool_row_bytes = 2ll * g.L + 16;
+    p.pool_row_bytes = 2 * pool_pitch(g.L);
     p.ws_dispatch_bytes = static_cast<int64_t>(dispatch_ws_layout(g).total);
     const size_t max_mt = static_cast<size_t>(g.E) * ((g.c_recv + 127) / 128);
     const size_t tiles_bytes = align_up(max_mt * 8 + 16, 1024);
@@ -451,7 +451,7 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
     d1.counts = expert_count;
     d1.goff = expert_offsets;
     d1.gather_src = pool;
-    d1.gather_pitch = L + 8;
+    d1.gather_pitch = pool_pitch(L);
     d1.gather_rows = n;
     d1.out = h;
     d1.ldo = H;
@@ -528,7 +528,7 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
     d1.counts = expert_count;
     d1.rowmap_ld = g.c_recv;
     d1.gather_src = pool;
-    d1.gather_pitch = L + 8;
+    d1.gather_pitch = pool_pitch(L);
     d1.gather_rows = g.pool_rows;
     d1.out = h;
     d1.ldo = H;

@@ -288,7 +288,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.b_gstride = static_cast<int64_t>(H) * L;
     q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
-    q.gather_src = a.pool; q.gather_pitch = L + 8; q.gather_rows = g.pool_rows;
+    q.gather_src = a.pool; q.gather_pitch = pool_pitch(L); q.gather_rows = g.pool_rows;
     q.aux = dh; q.out = dg; q.out2 = du; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
     if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
     std::memset(&q, 0, sizeof(q));   // dX = dg Wg_e + du Wu_e, back to the pool rows
@@ -305,7 +305,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     {   // per-expert contiguous, zero-padded copy of X; h's unwritten rows zeroed
         const int64_t nw = static_cast<int64_t>(E) * cr;
         const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
-        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, L + 8, a.expert_rows, a.expert_count, E, cr, L, xe);
+        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, a.expert_count, E, cr, L, xe);
         zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_gather_rows");

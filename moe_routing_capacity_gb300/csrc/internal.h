@@ -102,6 +102,11 @@ int gemm_launch(const GemmDesc& d, cudaStream_t stream);
 int launch_topk(const float* logits, int64_t T, int E, int k, int32_t* idx, float* w,
                 uint8_t* tie, cudaStream_t stream);
 
+// Pool row: L bf16 payload, the 16-byte tag, padding to a multiple of 128
+// bytes, so that every row (and every 64-element K segment of it) starts on a
+// cache-line boundary for the expert GEMM's row gather.  In uint16 elements.
+__host__ __device__ inline int64_t pool_pitch(int L) { return ((2ll * L + 16 + 127) / 128 * 128) / 2; }
+
 struct DispatchGeom {
     int64_t T;
     int k, E, S, D, W, E_l, E_w, L;

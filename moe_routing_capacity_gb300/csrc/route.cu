@@ -159,7 +159,7 @@ __global__ void dispatch_init_kernel(DispatchGeom g, uint16_t* __restrict__ pool
         stats->reserved = 0;
     }
     if (g.ragged) return;   // every row and every list entry gets written
-    const int64_t pitch = g.L + 8;
+    const int64_t pitch = pool_pitch(g.L);
     for (int64_t r = tid; r < g.pool_rows; r += nthr)
         *reinterpret_cast<int4*>(pool + r * pitch + g.L) = make_int4(-1, -1, -1, 0);
     const int64_t ne = static_cast<int64_t>(g.E) * g.c_recv;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= g.T) return;
     const int64_t s = t / g.T_s;
-    const int64_t pitch = g.L + 8;
+    const int64_t pitch = pool_pitch(g.L);
     // lane j < k owns assignment (t, j)
     int64_t row = -1;
     int e = 0;

@@ -40,7 +40,7 @@ class PooledWaveMoE:
         self.tie = e(T, dt=torch.uint8)
         self.z = e(T, L, dt=torch.bfloat16)
         self.ws_dispatch = e(max(1, p.ws_dispatch_bytes), dt=torch.uint8)
-        self.pool = e(p.pool_rows, L + 8, dt=torch.int16)
+        self.pool = e(p.pool_rows, p.pool_row_bytes // 2, dt=torch.int16)
         self.slot_of = e(T, k, dt=torch.int32)
         self.drop = e(T, k, dt=torch.uint8)
         if dropless:    # flat row list with per-expert offsets
@@ -157,7 +157,7 @@ class PooledWaveMoE:
 
     def pool_tags(self):
         L = self.cfg.d_latent
-        return self.pool[:, L:].contiguous().view(torch.int32)
+        return self.pool[:, L:L + 8].contiguous().view(torch.int32)
 
     def drop_stats(self) -> dict:
         return abi.stats_dict(self.stats)

@@ -60,7 +60,8 @@ def test_plan_matches_oracle(cfg):
     assert (p.c_send, p.c_recv, p.pool_rows) == (q.c_send, q.c_recv, q.pool_rows)
     assert p.tokens_per_rank == q.T_s and p.experts_per_rank == q.E_l
     assert p.experts_per_wave == q.E_w
-    assert p.pool_row_bytes == 2 * cfg.d_latent + 16
+    # L bf16 payload + 16-byte tag, padded to whole 128-byte lines
+    assert p.pool_row_bytes == -(-(2 * cfg.d_latent + 16) // 128) * 128
     assert p.h_offset_bytes % 16 == 0
     assert p.ws_ffn_bytes >= p.h_offset_bytes + cfg.n_experts * p.c_recv * cfg.h_expert * 2
 

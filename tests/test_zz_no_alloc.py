@@ -36,7 +36,7 @@ def _outputs(cfg):
     p = abi.plan(cfg)
     dev = "cuda"
     return dict(
-        pool=torch.zeros(p.pool_rows, cfg.d_latent + 8, dtype=torch.int16, device=dev),
+        pool=torch.zeros(p.pool_rows, p.pool_row_bytes // 2, dtype=torch.int16, device=dev),
         slot_of=torch.zeros(cfg.T, cfg.top_k, dtype=torch.int32, device=dev),
         drop=torch.zeros(cfg.T, cfg.top_k, dtype=torch.uint8, device=dev),
         expert_rows=torch.zeros(cfg.n_experts, p.c_recv, dtype=torch.int32, device=dev),
@@ -48,8 +48,8 @@ def _outputs(cfg):
 def _same(a, b, L):
     for key in ("slot_of", "drop", "expert_rows", "expert_count", "stats"):
         assert torch.equal(a[key], b[key]), key
-    tags_a = a["pool"][:, L:]
-    assert torch.equal(tags_a, b["pool"][:, L:])
+    tags_a = a["pool"][:, L:L + 8]
+    assert torch.equal(tags_a, b["pool"][:, L:L + 8])
     filled = tags_a.contiguous().view(torch.int32)[:, 0] >= 0
     assert torch.equal(a["pool"][filled, :L], b["pool"][filled, :L])
 
