@@ -67,10 +67,20 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-def source_hash():
+# Sources a kernel's DRAM traffic depends on: its own translation unit, the
+# shared device helpers and layouts, and the entry points that describe its
+# operands.  A traffic record taken under other sources is not reported.
+KERNEL_SOURCES = {
+    "gemm": ("gemm_tc.cu", "common.cuh", "internal.h", "abi.cu"),
+    "route": ("route.cu", "common.cuh", "internal.h", "abi.cu"),
+}
+
+
+def source_hash(kernel="gemm"):
+    files = KERNEL_SOURCES["gemm" if kernel.startswith("gemm") else "route"]
     h = hashlib.sha256()
     src = os.path.join(ROOT, "moe_routing_capacity_gb300", "csrc")
-    for f in sorted(os.listdir(src)):
+    for f in files:
         h.update(open(os.path.join(src, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -331,12 +341,15 @@ def run_gb300(args, rank, world, local_rank):
         kernels[name] = e
     top = next(iter(kernels))
     twork, tunit, tbound = kernel_work(top, cfg, m.plan, st)
-    traffic = None
+    # DRAM bytes per launch from the committed ncu record, where it was taken
+    # on this workload under the current sources of that kernel
     tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        rec = json.load(open(tp)).get(top)
-        if rec and rec.get("source_hash") == source_hash() and rec.get("workload") == cfg.name:
-            traffic = rec.get("dram_bytes_per_launch")
+    recs = json.load(open(tp)) if os.path.exists(tp) else {}
+    for name, e in kernels.items():
+        rec = recs.get(name)
+        if rec and rec.get("source_hash") == source_hash(name) and rec.get("workload") == cfg.name:
+            e["traffic"] = rec.get("dram_bytes_per_launch")
+    traffic = kernels[top].get("traffic")
     if twork is not None:
         ach = kernels[top]["achieved"]
         peak = pk["bf16_sustained"] if tbound == "tensor" else pk["hbm"]
