@@ -47,15 +47,20 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 #define MOE_GROUPED_B_STAGES 4
 #endif
 
-template <int BN, int AMODE, int EPI>
+// CG2: the tile is computed by a CTA pair (cta_group::2, M = 256); each CTA
+// stages its 128 rows of A and half (BN/2 rows) of the B tile.
+template <int BN, int AMODE, int EPI, bool CG2 = false>
 struct TileCfg {
-    static constexpr int B_STAGE_BYTES = BN * BK * 2;
-    static constexpr int B_STAGES = (BN == 384)              ? 3
+    static constexpr int B_ROWS = CG2 ? BN / 2 : BN;   // B rows staged by this CTA
+    static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
+    static constexpr int B_STAGES = CG2                      ? 6
+                                    : (BN == 384)            ? 3
                                     : (BN != 256)            ? 6
                                     : (AMODE == A_GATHER)    ? MOE_GATHER_B_STAGES
                                     : (AMODE == A_GROUPED)   ? MOE_GROUPED_B_STAGES
                                                              : 4;
-    static constexpr int A_STAGES = (AMODE == A_GATHER)    ? MOE_GATHER_A_STAGES
+    static constexpr int A_STAGES = CG2                    ? 6
+                                    : (AMODE == A_GATHER)  ? MOE_GATHER_A_STAGES
                                     : (AMODE == A_GROUPED) ? MOE_GROUPED_A_STAGES
                                                            : B_STAGES;
     static_assert(AMODE != A_GATHER || A_STAGES >= 3, "the gather needs LAG >= 1");
@@ -133,10 +138,18 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 // MAJ bit 0: A is MN-major (stored [K, M], M contiguous); bit 1: B is
 // MN-major (stored [K, N]).  MN-major tiles arrive as 64 x 64 TMA boxes, one
 // per 64 M/N elements, 8 KB apart.
-template <int BN, int AMODE, int EPI, int MAJ>
+// CG2: launched in clusters of two; the pair computes 256 x BN tiles with
+// tcgen05.mma.cta_group::2 issued by the even CTA.  Both CTAs' TMA loads count
+// on the even CTA's full barriers; the MMA commits arrive on the empty, full
+// and done barriers of both CTAs; both CTAs' epilogues arrive on the even
+// CTA's accumulator-free barriers.
+template <int BN, int AMODE, int EPI, int MAJ, bool CG2>
 __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     gemm_tc_kernel(const __grid_constant__ KParams p) {
-    using C = TileCfg<BN, AMODE, EPI>;
+    using C = TileCfg<BN, AMODE, EPI, CG2>;
+    static_assert(!CG2 || (AMODE == A_DENSE && MAJ == 0 && BN == 256 &&
+                           (EPI == EPI_BF16 || EPI == EPI_SWIGLU || EPI == EPI_SPLIT)),
+                  "CTA pairs: dense K-major tiles with the bf16, SwiGLU or split epilogue");
     constexpr int AST = C::A_STAGES;
     constexpr int BST = C::B_STAGES;
     constexpr bool B3D = (AMODE != A_DENSE);
@@ -163,6 +176,11 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // CTA pairs: rank in the pair; tiles are dealt out per pair
+    const uint32_t crank = CG2 ? cluster_ctarank() : 0u;
+    const bool leader = crank == 0;
+    const int cta0 = CG2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int ncta = CG2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < AST; ++s) {
@@ -175,7 +193,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], CG2 ? 256 : 128);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
@@ -188,12 +206,18 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         }
     }
     if (warp == 2) {
-        tmem_alloc(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (CG2) {
+            tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (CG2) cluster_sync();   // the peer's barriers exist before any remote arrival
     const uint32_t tmem_base = *tmem_slot;
     const int kb_total = p.seg_kb[p.nseg];
 
@@ -204,9 +228,10 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
             uint32_t armedA = 0, parA = 0, armedB = 0, parB = 0;   // for unwinding
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
                 int g, m0, nb;
                 decode_tile<AMODE>(p, tile, g, m0, nb);
+                if (CG2) m0 = 2 * m0 + static_cast<int>(crank) * BM;
                 int seg = 0;
                 for (int kb = 0; kb < kb_total; ++kb) {
                     while (kb >= p.seg_kb[seg + 1]) ++seg;
@@ -217,10 +242,19 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                             break;
                         }
                         const uint32_t a_dst = smem_u32(sA + sa * A_STAGE_BYTES);
-                        mbar_arrive_expect_tx(&fullA[sa], A_STAGE_BYTES);
-                        armedA |= 1u << sa;
-                        parA = (parA & ~(1u << sa)) | (pa << sa);
-                        if (A_MN && AMODE == A_DENSE) {
+                        if constexpr (CG2) {   // both halves count on the even CTA's barrier
+                            if (leader) mbar_arrive_expect_tx(&fullA[sa], 2 * A_STAGE_BYTES);
+                            tma_load_2d_pair(a_dst, &p.mapA[seg],
+                                             mapa_shared(smem_u32(&fullA[sa]), 0), kx, m0);
+                        } else {
+                            mbar_arrive_expect_tx(&fullA[sa], A_STAGE_BYTES);
+                        }
+                        if (!CG2 || leader) {
+                            armedA |= 1u << sa;
+                            parA = (parA & ~(1u << sa)) | (pa << sa);
+                        }
+                        if constexpr (CG2) {
+                        } else if (A_MN && AMODE == A_DENSE) {
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], m0, kx);
                             tma_load_2d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, kx);
                         } else if (A_MN) {
@@ -242,10 +276,29 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         break;
                     }
                     const uint32_t b_dst = smem_u32(sB + sb * C::B_STAGE_BYTES);
-                    mbar_arrive_expect_tx(&fullB[sb], C::B_STAGE_BYTES);
-                    armedB |= 1u << sb;
-                    parB = (parB & ~(1u << sb)) | (pb << sb);
-                    if (B_MN) {
+                    if constexpr (CG2) {
+                        if (leader) mbar_arrive_expect_tx(&fullB[sb], 2 * C::B_STAGE_BYTES);
+                    } else {
+                        mbar_arrive_expect_tx(&fullB[sb], C::B_STAGE_BYTES);
+                    }
+                    if (!CG2 || leader) {
+                        armedB |= 1u << sb;
+                        parB = (parB & ~(1u << sb)) | (pb << sb);
+                    }
+                    if constexpr (CG2) {
+                        // this CTA's half of the B tile: SwiGLU gate rows (even
+                        // CTA) or up rows (odd CTA); otherwise rows crank*BN/2..
+                        const uint32_t fb = mapa_shared(smem_u32(&fullB[sb]), 0);
+                        if (EPI == EPI_SWIGLU)
+                            tma_load_2d_pair(b_dst, crank ? &p.mapBup : &p.mapB[0], fb, kx,
+                                             nb * (BN / 2));
+                        else if (EPI == EPI_SPLIT && nb >= p.nsplit)
+                            tma_load_2d_pair(b_dst, &p.mapBup, fb, kx,
+                                             (nb - p.nsplit) * BN + static_cast<int>(crank) * (BN / 2));
+                        else
+                            tma_load_2d_pair(b_dst, &p.mapB[seg], fb, kx,
+                                             nb * BN + static_cast<int>(crank) * (BN / 2));
+                    } else if (B_MN) {
                         // BN/64 boxes of 64 N x 64 K; SwiGLU: gate then up halves
 #pragma unroll
                         for (int h = 0; h < BN / 64; ++h) {
@@ -304,10 +357,20 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        bool issuer = lane == 0;
+        if constexpr (CG2) {
+            if (!leader && lane == 0) {
+                // the even CTA issues the pair's MMAs; wait until they are all
+                // done (they write this CTA's TMEM and read its shared memory)
+                volatile int no_abort = 0;
+                mbar_wait(done, 0, &no_abort, p.status);
+                issuer = false;
+            }
+        }
+        if (issuer) {
             const int ntiles = num_tiles<AMODE>(p);
             constexpr int N0 = BN <= 256 ? BN : 256;          // first MMA's N
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, N0, A_MN, B_MN);
+            constexpr uint32_t idesc = idesc_bf16_f32(CG2 ? 2 * BM : BM, N0, A_MN, B_MN);
             constexpr uint32_t idesc_hi = idesc_bf16_f32(BM, BN > 256 ? BN - 256 : 16);
             // descriptor step per 16-wide K slice: 32 B along a K-major row,
             // 16 rows of 128 B down an MN-major box
@@ -316,7 +379,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+            for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -333,14 +396,24 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     const uint64_t bd = B_MN ? sdesc_mn_sw128(b_s) : sdesc_k_sw128(b_s);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        mma_bf16(d_tmem, ad + a_step * kk, bd + b_step * kk, idesc,
-                                 (kb | kk) != 0 ? 1u : 0u);
-                        if (BN > 256)   // columns 256.. from B rows 256.. (32 KB further)
+                        if constexpr (CG2) {
+                            mma_bf16_pair(d_tmem, ad + a_step * kk, bd + b_step * kk, idesc,
+                                          (kb | kk) != 0 ? 1u : 0u);
+                        } else {
+                            mma_bf16(d_tmem, ad + a_step * kk, bd + b_step * kk, idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        if constexpr (BN > 256)   // columns 256.. from B rows 256.. (32 KB further)
                             mma_bf16(d_tmem + 256, ad + 2u * kk, bd + (32768u >> 4) + 2u * kk,
                                      idesc_hi, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    mma_commit(&emptyA[sa]);
-                    mma_commit(&emptyB[sb]);
+                    if constexpr (CG2) {   // both CTAs' stages are free once these MMAs finish
+                        mma_commit_pair(&emptyA[sa]);
+                        mma_commit_pair(&emptyB[sb]);
+                    } else {
+                        mma_commit(&emptyA[sa]);
+                        mma_commit(&emptyB[sb]);
+                    }
                     if (++sa == AST) {
                         sa = 0;
                         pa ^= 1u;
@@ -351,14 +424,20 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(&tfull[acc]);
+                if constexpr (CG2)
+                    mma_commit_pair(&tfull[acc]);
+                else
+                    mma_commit(&tfull[acc]);
                 if (++acc == C::NACC) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             // Every MMA this CTA issued must finish before TMEM is released.
-            mma_commit(done);
+            if constexpr (CG2)
+                mma_commit_pair(done);
+            else
+                mma_commit(done);
             volatile int no_abort = 0;
             mbar_wait(done, 0, &no_abort, p.status);
         }
@@ -368,9 +447,12 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         const int r_local = q * 32 + lane;
         const int ntiles = num_tiles<AMODE>(p);
         uint32_t acc = 0, acc_phase = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        // the pair's accumulator-free barrier lives in the even CTA
+        const uint32_t tempty_c0 = CG2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u;
+        for (int tile = cta0; tile < ntiles; tile += ncta) {
             int g, m0, nb;
             decode_tile<AMODE>(p, tile, g, m0, nb);
+            if (CG2) m0 = 2 * m0 + static_cast<int>(crank) * BM;
             if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) break;
             tc_fence_after();
             const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -572,7 +654,10 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            if constexpr (CG2)
+                mbar_arrive_cluster(tempty_c0 + acc * 8u);
+            else
+                mbar_arrive(&tempty[acc]);
             if (++acc == C::NACC) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -610,8 +695,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 nxt_row[i] = m < nxt_cnt ? rl[m] : 0;
             }
         };
-        if (static_cast<int>(blockIdx.x) < ntiles) fetch_rows(blockIdx.x);
-        for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        if (cta0 < ntiles) fetch_rows(cta0);
+        for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
             const uint16_t* src[8];
             uint32_t valid = 0;
 #pragma unroll
@@ -620,7 +705,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 valid |= (v ? 1u : 0u) << i;
                 src[i] = p.gather_src + static_cast<long long>(nxt_row[i]) * p.gather_pitch + c * 8;
             }
-            if (tile + static_cast<int>(gridDim.x) < ntiles) fetch_rows(tile + gridDim.x);
+            if (tile + ncta < ntiles) fetch_rows(tile + ncta);
             for (int kb = 0; kb < kb_total; ++kb) {
                 if (!mbar_wait(&emptyA[sa], pa ^ 1u, abort_flag, p.status)) {
                     ok = false;
@@ -655,7 +740,15 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 2) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    // neither CTA of a pair leaves while the other may still arrive on its
+    // barriers or the pair's MMAs may touch its memory
+    if constexpr (CG2) cluster_sync();
+    if (warp == 2) {
+        if constexpr (CG2)
+            tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
 }
 
 // ==================================================================== host side
@@ -711,21 +804,38 @@ static int map3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
     return make_map(m, base, 3, dims, str, box_rows);
 }
 
-template <int BN, int AMODE, int EPI, int MAJ = 0>
+template <int BN, int AMODE, int EPI, int MAJ = 0, bool CG2 = false>
 static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
-    using C = TileCfg<BN, AMODE, EPI>;
-    auto kern = gemm_tc_kernel<BN, AMODE, EPI, MAJ>;
+    using C = TileCfg<BN, AMODE, EPI, CG2>;
+    auto kern = gemm_tc_kernel<BN, AMODE, EPI, MAJ, CG2>;
     // Attribute setting is per device; cheap and idempotent, done every launch.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
         cudaSuccess)
         return MOE_ECUDA;
-    kern<<<grid, AMODE == A_GATHER ? 384 : 256, C::SMEM_BYTES, st>>>(p);
+    if (CG2) {   // clusters of two CTAs (grid is even)
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
+    } else {
+        kern<<<grid, AMODE == A_GATHER ? 384 : 256, C::SMEM_BYTES, st>>>(p);
+    }
     return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
 
-template <int BN, int AMODE, int EPI, int MAJ = 0>
+template <int BN, int AMODE, int EPI, int MAJ = 0, bool CG2 = false>
 static int launch_traced(const KParams& p, int grid, cudaStream_t st, const char* name) {
-    const int rc = launch_inst<BN, AMODE, EPI, MAJ>(p, grid, st);
+    const int rc = launch_inst<BN, AMODE, EPI, MAJ, CG2>(p, grid, st);
     if (rc == MOE_OK) trace_after(st, name ? name : "gemm");
     return rc;
 }
@@ -740,14 +850,24 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
 
     KParams p;
     std::memset(&p, 0, sizeof(p));
+    // CTA pairs (cta_group::2, 256-row tiles) for the dense K-major products
+    // with the bf16, SwiGLU and split epilogues
+#ifndef MOE_NO_CTA_PAIRS
+    const bool cg2 = d.a_mode == A_DENSE && !d.a_mn && !d.b_mn && d.bn == 256 &&
+                     (d.epi == EPI_BF16 || d.epi == EPI_SWIGLU || d.epi == EPI_SPLIT) && sms >= 2;
+#else
+    const bool cg2 = false;
+#endif
     // gate/up pairs load two 128-row halves, the 384-wide router tile three
-    // 128-row thirds; everything else one box of bn rows (K-major B)
+    // 128-row thirds; everything else one box of bn rows (K-major B); a CTA
+    // of a pair loads one 128-row half of the B tile
     const bool pair = d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD;
-    const uint32_t b_box = (pair || d.bn == 384) ? 128 : d.bn;
+    const uint32_t b_box = (cg2 || pair || d.bn == 384) ? 128 : d.bn;
     {   // every stage must receive exactly the bytes its barrier expects
-        const uint32_t loads = d.b_mn ? d.bn / 64 : pair ? 2 : d.bn == 384 ? 3 : 1;
+        const uint32_t loads = cg2 ? 1 : d.b_mn ? d.bn / 64 : pair ? 2 : d.bn == 384 ? 3 : 1;
         const uint32_t box_rows = d.b_mn ? 64 : b_box;
-        if (loads * box_rows * BK * 2 != static_cast<uint32_t>(d.bn) * BK * 2) return MOE_EINVAL;
+        const uint32_t rows = cg2 ? d.bn / 2 : d.bn;
+        if (loads * box_rows * BK * 2 != rows * BK * 2) return MOE_EINVAL;
     }
     p.nseg = d.nseg;
     p.seg_kb[0] = 0;
@@ -811,7 +931,8 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         p.ldo2 = d.ldo2;
         p.n_tiles_n = d.nsplit + (d.N2 + d.bn - 1) / d.bn;
     }
-    p.m_tiles = static_cast<int>((d.M + BM - 1) / BM);
+    const int bm_tile = cg2 ? 2 * BM : BM;
+    p.m_tiles = static_cast<int>((d.M + bm_tile - 1) / bm_tile);
     p.tile_list = reinterpret_cast<const int2*>(d.tile_list);
     p.tile_count = d.tile_count;
     p.rowmap = d.rowmap;
@@ -833,7 +954,8 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
                 : d.uniform_groups     ? d.uniform_groups * p.m_tiles * p.n_tiles_n
                                        : d.max_tiles * p.n_tiles_n;
     if (tiles <= 0) return MOE_OK;
-    const int grid = tiles < sms ? tiles : sms;
+    int grid = tiles < sms ? tiles : sms;
+    if (cg2) grid = 2 * (tiles < sms / 2 ? tiles : sms / 2);
 
     if ((d.a_mn || d.b_mn) && (d.bn != 256 || d.epi == EPI_SPLIT)) return MOE_EINVAL;
     const int maj = (d.a_mn ? 1 : 0) | (d.b_mn ? 2 : 0);
@@ -842,9 +964,15 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     switch (key) {
         case MOE_K(128, A_DENSE, EPI_F32, 0): return launch_traced<128, A_DENSE, EPI_F32>(p, grid, st, d.name);
         case MOE_K(384, A_DENSE, EPI_F32, 0): return launch_traced<384, A_DENSE, EPI_F32>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_SPLIT, 0): return launch_traced<256, A_DENSE, EPI_SPLIT>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_BF16, 0): return launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_SWIGLU, 0): return launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_SPLIT, 0):
+            return cg2 ? launch_traced<256, A_DENSE, EPI_SPLIT, 0, true>(p, grid, st, d.name)
+                       : launch_traced<256, A_DENSE, EPI_SPLIT>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_BF16, 0):
+            return cg2 ? launch_traced<256, A_DENSE, EPI_BF16, 0, true>(p, grid, st, d.name)
+                       : launch_traced<256, A_DENSE, EPI_BF16>(p, grid, st, d.name);
+        case MOE_K(256, A_DENSE, EPI_SWIGLU, 0):
+            return cg2 ? launch_traced<256, A_DENSE, EPI_SWIGLU, 0, true>(p, grid, st, d.name)
+                       : launch_traced<256, A_DENSE, EPI_SWIGLU>(p, grid, st, d.name);
         case MOE_K(256, A_GATHER, EPI_SWIGLU, 0): return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);
         case MOE_K(256, A_GROUPED, EPI_SCATTER, 0): return launch_traced<256, A_GROUPED, EPI_SCATTER>(p, grid, st, d.name);
         // MN-major operands (general products, the backward pass)
