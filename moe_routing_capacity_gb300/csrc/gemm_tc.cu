@@ -147,9 +147,10 @@ template <int BN, int AMODE, int EPI, int MAJ, bool CG2>
 __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     gemm_tc_kernel(const __grid_constant__ KParams p) {
     using C = TileCfg<BN, AMODE, EPI, CG2>;
-    static_assert(!CG2 || (AMODE == A_DENSE && MAJ == 0 && BN == 256 &&
-                           (EPI == EPI_BF16 || EPI == EPI_SWIGLU || EPI == EPI_SPLIT)),
-                  "CTA pairs: dense K-major tiles with the bf16, SwiGLU or split epilogue");
+    static_assert(!CG2 || (AMODE == A_DENSE && BN == 256 &&
+                           (EPI == EPI_BF16 || EPI == EPI_F32 || (EPI == EPI_SPLIT && MAJ == 0) ||
+                            ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) && !(MAJ & 2)))),
+                  "CTA pairs: dense tiles; bf16, fp32, split, SwiGLU (K-major B) epilogues");
     constexpr int AST = C::A_STAGES;
     constexpr int BST = C::B_STAGES;
     constexpr bool B3D = (AMODE != A_DENSE);
@@ -244,8 +245,13 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         const uint32_t a_dst = smem_u32(sA + sa * A_STAGE_BYTES);
                         if constexpr (CG2) {   // both halves count on the even CTA's barrier
                             if (leader) mbar_arrive_expect_tx(&fullA[sa], 2 * A_STAGE_BYTES);
-                            tma_load_2d_pair(a_dst, &p.mapA[seg],
-                                             mapa_shared(smem_u32(&fullA[sa]), 0), kx, m0);
+                            const uint32_t fa = mapa_shared(smem_u32(&fullA[sa]), 0);
+                            if (A_MN) {   // two 64-row boxes of the MN-major A
+                                tma_load_2d_pair(a_dst, &p.mapA[seg], fa, m0, kx);
+                                tma_load_2d_pair(a_dst + 8192, &p.mapA[seg], fa, m0 + 64, kx);
+                            } else {
+                                tma_load_2d_pair(a_dst, &p.mapA[seg], fa, kx, m0);
+                            }
                         } else {
                             mbar_arrive_expect_tx(&fullA[sa], A_STAGE_BYTES);
                         }
@@ -289,7 +295,11 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         // this CTA's half of the B tile: SwiGLU gate rows (even
                         // CTA) or up rows (odd CTA); otherwise rows crank*BN/2..
                         const uint32_t fb = mapa_shared(smem_u32(&fullB[sb]), 0);
-                        if (EPI == EPI_SWIGLU)
+                        if (B_MN) {   // two 64-column boxes of the MN-major B
+                            const int n = nb * BN + static_cast<int>(crank) * (BN / 2);
+                            tma_load_2d_pair(b_dst, &p.mapB[seg], fb, n, kx);
+                            tma_load_2d_pair(b_dst + 8192, &p.mapB[seg], fb, n + 64, kx);
+                        } else if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD)
                             tma_load_2d_pair(b_dst, crank ? &p.mapBup : &p.mapB[0], fb, kx,
                                              nb * (BN / 2));
                         else if (EPI == EPI_SPLIT && nb >= p.nsplit)
@@ -853,8 +863,9 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     // CTA pairs (cta_group::2, 256-row tiles) for the dense K-major products
     // with the bf16, SwiGLU and split epilogues
 #ifndef MOE_NO_CTA_PAIRS
-    const bool cg2 = d.a_mode == A_DENSE && !d.a_mn && !d.b_mn && d.bn == 256 &&
-                     (d.epi == EPI_BF16 || d.epi == EPI_SWIGLU || d.epi == EPI_SPLIT) && sms >= 2;
+    const bool cg2 = d.a_mode == A_DENSE && d.bn == 256 && sms >= 2 &&
+                     (d.epi == EPI_BF16 || d.epi == EPI_F32 || (d.epi == EPI_SPLIT && !d.b_mn) ||
+                      ((d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD) && !d.b_mn));
 #else
     const bool cg2 = false;
 #endif
@@ -864,7 +875,8 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     const bool pair = d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD;
     const uint32_t b_box = (cg2 || pair || d.bn == 384) ? 128 : d.bn;
     {   // every stage must receive exactly the bytes its barrier expects
-        const uint32_t loads = cg2 ? 1 : d.b_mn ? d.bn / 64 : pair ? 2 : d.bn == 384 ? 3 : 1;
+        const uint32_t loads = cg2 ? (d.b_mn ? 2 : 1)
+                               : d.b_mn ? d.bn / 64 : pair ? 2 : d.bn == 384 ? 3 : 1;
         const uint32_t box_rows = d.b_mn ? 64 : b_box;
         const uint32_t rows = cg2 ? d.bn / 2 : d.bn;
         if (loads * box_rows * BK * 2 != rows * BK * 2) return MOE_EINVAL;
@@ -976,15 +988,20 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         case MOE_K(256, A_GATHER, EPI_SWIGLU, 0): return launch_traced<256, A_GATHER, EPI_SWIGLU>(p, grid, st, d.name);
         case MOE_K(256, A_GROUPED, EPI_SCATTER, 0): return launch_traced<256, A_GROUPED, EPI_SCATTER>(p, grid, st, d.name);
         // MN-major operands (general products, the backward pass)
-        case MOE_K(256, A_DENSE, EPI_BF16, 1): return launch_traced<256, A_DENSE, EPI_BF16, 1>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_BF16, 2): return launch_traced<256, A_DENSE, EPI_BF16, 2>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_BF16, 3): return launch_traced<256, A_DENSE, EPI_BF16, 3>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_F32, 0): return launch_traced<256, A_DENSE, EPI_F32, 0>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_F32, 1): return launch_traced<256, A_DENSE, EPI_F32, 1>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_F32, 2): return launch_traced<256, A_DENSE, EPI_F32, 2>(p, grid, st, d.name);
-        case MOE_K(256, A_DENSE, EPI_F32, 3): return launch_traced<256, A_DENSE, EPI_F32, 3>(p, grid, st, d.name);
+#define MOE_PAIRED(EP_, MJ_)                                                                  \
+    case MOE_K(256, A_DENSE, EP_, MJ_):                                                       \
+        return cg2 ? launch_traced<256, A_DENSE, EP_, MJ_, true>(p, grid, st, d.name)         \
+                   : launch_traced<256, A_DENSE, EP_, MJ_>(p, grid, st, d.name);
+        MOE_PAIRED(EPI_BF16, 1)
+        MOE_PAIRED(EPI_BF16, 2)
+        MOE_PAIRED(EPI_BF16, 3)
+        MOE_PAIRED(EPI_F32, 0)
+        MOE_PAIRED(EPI_F32, 1)
+        MOE_PAIRED(EPI_F32, 2)
+        MOE_PAIRED(EPI_F32, 3)
+        MOE_PAIRED(EPI_SWIGLU_BWD, 0)
+#undef MOE_PAIRED
         // backward pass
-        case MOE_K(256, A_DENSE, EPI_SWIGLU_BWD, 0): return launch_traced<256, A_DENSE, EPI_SWIGLU_BWD, 0>(p, grid, st, d.name);
         case MOE_K(256, A_GATHER, EPI_SWIGLU_BWD, 0): return launch_traced<256, A_GATHER, EPI_SWIGLU_BWD, 0>(p, grid, st, d.name);
         case MOE_K(256, A_GROUPED, EPI_BF16, 2): return launch_traced<256, A_GROUPED, EPI_BF16, 2>(p, grid, st, d.name);
         case MOE_K(256, A_GROUPED, EPI_SCATTER, 2): return launch_traced<256, A_GROUPED, EPI_SCATTER, 2>(p, grid, st, d.name);
