@@ -52,6 +52,8 @@ def parse():
                     help="skip timing the dropless ragged variant")
     ap.add_argument("--no-train", action="store_true",
                     help="skip timing forward + backward (one training step of the layer)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the skewed-routing and long-context lines")
     return ap.parse_args()
 
 
@@ -424,6 +426,38 @@ def run_gb300(args, rank, world, local_rank):
                                                if k2.startswith("gemm_expert")) / nd, 4)}
         del md
 
+    # ---- the skewed-routing and long-context workloads: throughput and drops
+    others = None
+    if not args.no_workloads and args.workload == "full":
+        others = {}
+        for oname in ("skew", "long"):
+            ocfg = wl.CONFIGS[oname]
+            oinp = wl.make_inputs(ocfg, dev)
+            mo = PooledWaveMoE(ocfg, oinp, dev)
+            ox = oinp["x"]
+            for _ in range(3):
+                mo.forward(ox)
+            torch.cuda.synchronize()
+            no = 20
+            o0 = torch.cuda.Event(enable_timing=True)
+            o1 = torch.cuda.Event(enable_timing=True)
+            o0.record(stream)
+            for _ in range(no):
+                mo.forward(ox)
+            o1.record(stream)
+            torch.cuda.synchronize()
+            assert int(mo.status.item()) == 0
+            oms = o0.elapsed_time(o1) / no
+            ost = mo.drop_stats()
+            others[oname] = {
+                "value": world * ocfg.T / (oms / 1e3), "unit": UNIT, "ms_per_step": oms,
+                "steps": no, "T": ocfg.T,
+                "drop_rate": (ost["dropped_send"] + ost["dropped_recv"]) / (ocfg.T * ocfg.top_k),
+                "dropped_send": ost["dropped_send"], "dropped_recv": ost["dropped_recv"],
+                "note": ("Zipf(1.2) prior on the router logits, hot experts on the first ranks"
+                         if oname == "skew" else "one 65536-token AR(1) sequence")}
+            del mo, oinp, ox
+
     # ---- one training step of the layer: forward + backward on the same batch
     train = None
     if not args.no_train:
@@ -489,7 +523,7 @@ def run_gb300(args, rank, world, local_rank):
                       "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
             "gpu_launches": sum(v[1] for v in per.values()),
             "roofline": roof, "kernels": kernels, "clocks": clk, "e2e": e2e,
-            "dropless": dropless, "train_step": train,
+            "dropless": dropless, "train_step": train, "workloads": others,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
