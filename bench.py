@@ -379,7 +379,7 @@ def run_gb300(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        n_e2e = max(4, min(args.steps, 50))
+        n_e2e = max(4, min(args.steps, 100))
         t0 = time.perf_counter()
         for i in range(n_e2e):
             pipe.submit(xh, oh[i % 2], sh[i % 2])
