@@ -379,19 +379,24 @@ def run_gb300(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        n_e2e = max(4, min(args.steps, 100))
-        t0 = time.perf_counter()
-        for i in range(n_e2e):
-            pipe.submit(xh, oh[i % 2], sh[i % 2])
-        pipe.synchronize()
-        torch.cuda.synchronize()
-        el = time.perf_counter() - t0
-        e2e_value, el = replica_throughput(el, cfg.T, n_e2e, dev)
+        # three rounds, the median reported: the host copies share the host's
+        # memory and link with whatever else the machine runs
+        n_e2e = max(4, min(args.steps, 40))
+        rounds = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            for i in range(n_e2e):
+                pipe.submit(xh, oh[i % 2], sh[i % 2])
+            pipe.synchronize()
+            torch.cuda.synchronize()
+            el = time.perf_counter() - t0
+            rounds.append(replica_throughput(el, cfg.T, n_e2e, dev)[0])
         assert int(m.status.item()) == 0
-        e2e = {"value": e2e_value, "unit": UNIT,
+        e2e = {"value": sorted(rounds)[1], "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": oh[0].numel() * oh[0].element_size() + sh[0].numel() * 8,
-               "steps": n_e2e, "timer": "host wall clock around the submitted steps",
+               "steps": 3 * n_e2e, "rounds": [round(r) for r in rounds],
+               "timer": "host wall clock around each round of submitted steps; median of 3",
                "overlap": "H2D / compute / D2H on three streams, double-buffered"}
 
     # ---- the dropless ragged variant on the same batch: the cost of removing drops
