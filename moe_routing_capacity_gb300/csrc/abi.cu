@@ -2,6 +2,7 @@
 // (capacities, pool and scratch sizes), and the launch sequence of each step.
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "internal.h"
@@ -27,6 +28,21 @@ int current_device(int* device, int* num_sms) {
     if (cached_ok[dev] != 1) return MOE_ENODEV;
     *device = dev;
     *num_sms = cached_sms[dev];
+    return MOE_OK;
+}
+
+int ensure_smem_attr(const void* func, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> done;   // (kernel, device) -> limit set
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ECUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    int& have = done[std::make_pair(func, dev)];
+    if (have >= bytes) return MOE_OK;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return MOE_ECUDA;
+    have = bytes;
     return MOE_OK;
 }
 

@@ -818,9 +818,7 @@ template <int BN, int AMODE, int EPI, int MAJ = 0, bool CG2 = false>
 static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
     using C = TileCfg<BN, AMODE, EPI, CG2>;
     auto kern = gemm_tc_kernel<BN, AMODE, EPI, MAJ, CG2>;
-    // Attribute setting is per device; cheap and idempotent, done every launch.
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
+    if (ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES) != MOE_OK)
         return MOE_ECUDA;
     if (CG2) {   // clusters of two CTAs (grid is even)
         cudaLaunchConfig_t cfg;

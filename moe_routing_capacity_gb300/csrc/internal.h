@@ -14,6 +14,11 @@ namespace moe {
 // Checks that the current device is an sm_103 part and returns its SM count.
 int current_device(int* device, int* num_sms);
 
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`, calling the runtime only the first time a larger value is
+// needed (so that launches inside a stream capture make no such call).
+int ensure_smem_attr(const void* func, int bytes);
+
 // Kernel timing trace: after each launch the library calls trace_after(),
 // which records the next trace event on that stream when tracing is on.
 void trace_after(cudaStream_t stream, const char* kernel_name);

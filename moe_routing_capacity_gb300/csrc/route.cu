@@ -442,8 +442,8 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
         static_cast<size_t>(SEND_WARPS + 1) * (g.D * g.W + g.E) * sizeof(int32_t);
     if (shm > 200 * 1024) return MOE_EINVAL;
     if (shm > 48 * 1024 &&
-        cudaFuncSetAttribute(dispatch_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(shm)) != cudaSuccess)
+        ensure_smem_attr(reinterpret_cast<const void*>(dispatch_send_kernel),
+                         static_cast<int>(shm)) != MOE_OK)
         return MOE_ECUDA;
     dispatch_send_kernel<<<g.S, SEND_WARPS * 32, shm, st>>>(g, idx, send_row, rloc, cnt_se,
                                                             demand, stats);
@@ -543,8 +543,8 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
         static_cast<size_t>(SEND_WARPS + 1) * (g.D * g.W + g.E) * sizeof(int32_t);
     if (shm > 200 * 1024) return MOE_EINVAL;
     if (shm > 48 * 1024 &&
-        cudaFuncSetAttribute(dispatch_send_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(shm)) != cudaSuccess)
+        ensure_smem_attr(reinterpret_cast<const void*>(dispatch_send_kernel),
+                         static_cast<int>(shm)) != MOE_OK)
         return MOE_ECUDA;
     dispatch_send_kernel<<<g.S, SEND_WARPS * 32, shm, st>>>(g, idx, send_row, rloc, cnt_se,
                                                             demand, stats);

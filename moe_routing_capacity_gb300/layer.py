@@ -114,6 +114,26 @@ class PooledWaveMoE:
         self.combine(x, out, stream)
         return self.out if out is None else out
 
+    def capture(self, x, out=None):
+        """Record one forward on ``x`` (into ``out`` if given) as a CUDA graph.
+
+        Every step of the layer is a kernel launch or an async memset on the
+        stream, with no host synchronisation and no allocation, so the whole
+        forward replays from the graph: ``g.replay()`` runs it again on
+        whatever ``x`` then holds.  Two eager forwards run first (outside the
+        capture) so that one-time launch attributes are already set."""
+        dev = self.device
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                self.forward(x, out)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.forward(x, out)
+        return g
+
     def backward(self, x, dout, stream=None) -> dict:
         """Gradients of the last forward with respect to x and every weight,
         for the upstream gradient dout [T, d] (capped layout only).  Returns
