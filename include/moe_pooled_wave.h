@@ -305,6 +305,7 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
  *   16-byte aligned; scratch ws of at least layout.total bytes. */
 typedef struct moe_backward_ws {
     int64_t dc, da, dgs, dus, dw, rowinv, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles;
+    int64_t hp, poff;   /* dropless layout only (else 0): padded copy of h, row offsets */
     int64_t total;
 } moe_backward_ws_t;
 
@@ -322,10 +323,25 @@ typedef struct moe_backward_args {
     void* ws;
     size_t ws_bytes;
     int32_t* status;
+    const int32_t* expert_offsets;   /* dropless layout: [E + 1], from moe_dispatch_ragged;
+                                        NULL for the capped layout */
 } moe_backward_args_t;
 
 int moe_backward_plan(const moe_config_t* cfg, moe_backward_ws_t* layout);
 int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* args, void* stream);
+
+/* The backward pass of the dropless ragged layer (the forward of
+ * moe_dispatch_ragged + moe_expert_ffn_ragged + moe_combine): the same
+ * derivative, every assignment kept.  args as for moe_layer_backward, with
+ * expert_rows / expert_offsets / expert_count of the ragged dispatch and h
+ * the flat [T*k, H] of moe_expert_ffn_ragged (left unchanged).  In the
+ * scratch, expert e's rows are padded to a multiple of 64 at poff[e]
+ * (int32 [E+1] at layout.poff) in dye, xe, dh, dg, du and a padded copy of h
+ * (layout.hp), so that each expert's weight gradient contracts over whole
+ * 64-row blocks; rowinv maps pool rows to those positions. */
+int moe_backward_plan_ragged(const moe_config_t* cfg, moe_backward_ws_t* layout);
+int moe_layer_backward_ragged(const moe_config_t* cfg, const moe_backward_args_t* args,
+                              void* stream);
 
 /* Quantile-balancing bias update (devpress.csdn.net, section 四 and appendix
  * A.2): a global histogram H counts how often each expert was selected;

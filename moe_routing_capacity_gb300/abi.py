@@ -23,7 +23,8 @@ EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project"
            "moe_dispatch_pooled",
            "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update",
            "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged",
-           "moe_backward_plan", "moe_layer_backward", "moe_combine", "moe_trace_begin", "moe_trace_mark",
+           "moe_backward_plan", "moe_layer_backward", "moe_backward_plan_ragged",
+           "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
 
 
@@ -60,7 +61,7 @@ class DropStats(ctypes.Structure):
 STATS_WORDS = ctypes.sizeof(DropStats) // 8    # int64 words of a stats record
 
 BWD_WS_FIELDS = ("dc", "da", "dgs", "dus", "dw", "rowinv", "dxpool", "dh", "dg", "du", "xe", "dye",
-                 "dz", "dlogits", "tiles", "total")
+                 "dz", "dlogits", "tiles", "hp", "poff", "total")
 
 
 class BackwardWs(ctypes.Structure):
@@ -75,7 +76,8 @@ BWD_ARG_FIELDS = ("x", "Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Ws
 
 class BackwardArgs(ctypes.Structure):
     _fields_ = ([(f, ctypes.c_void_p) for f in BWD_ARG_FIELDS] +
-                [("ws_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p)])
+                [("ws_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p),
+                 ("expert_offsets", ctypes.c_void_p)])
 
 _lib = None
 
@@ -106,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
         L.moe_backward_plan.argtypes = [pc, ctypes.POINTER(BackwardWs)]
         L.moe_layer_backward.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
+        L.moe_backward_plan_ragged.argtypes = [pc, ctypes.POINTER(BackwardWs)]
+        L.moe_layer_backward_ragged.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
         L.moe_strerror.argtypes = [ctypes.c_int]
         L.moe_strerror.restype = ctypes.c_char_p
         L.moe_abi_version.argtypes = []
@@ -302,10 +306,10 @@ def trace_end() -> list:
 
 # ---------------------------------------------------------------- backward pass
 
-def backward_plan(cfg) -> BackwardWs:
+def backward_plan(cfg, ragged=False) -> BackwardWs:
     w = BackwardWs()
-    _check("moe_backward_plan", lib().moe_backward_plan(ctypes.byref(make_config(cfg)),
-                                                        ctypes.byref(w)))
+    fn = "moe_backward_plan_ragged" if ragged else "moe_backward_plan"
+    _check(fn, getattr(lib(), fn)(ctypes.byref(make_config(cfg)), ctypes.byref(w)))
     return w
 
 
@@ -319,5 +323,8 @@ def layer_backward(cfg, tensors: dict, ws, status, stream=None):
     args.ws = ws.data_ptr()
     args.ws_bytes = ws.numel()
     args.status = status.data_ptr()
-    _check("moe_layer_backward", lib().moe_layer_backward(
-        ctypes.byref(make_config(cfg)), ctypes.byref(args), _stream(stream)))
+    eoff = tensors.get("expert_offsets")
+    args.expert_offsets = None if eoff is None else eoff.data_ptr()
+    fn = "moe_layer_backward" if eoff is None else "moe_layer_backward_ragged"
+    _check(fn, getattr(lib(), fn)(ctypes.byref(make_config(cfg)), ctypes.byref(args),
+                                  _stream(stream)))

@@ -593,24 +593,34 @@ int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* his
                                  static_cast<cudaStream_t>(stream));
 }
 
+static void fill_backward_layout(const BackwardWs& w, moe_backward_ws_t* layout) {
+    layout->dc = w.dc; layout->da = w.da; layout->dgs = w.dgs; layout->dus = w.dus;
+    layout->dw = w.dw; layout->rowinv = w.rowinv; layout->dxpool = w.dxpool; layout->dh = w.dh;
+    layout->dg = w.dg; layout->du = w.du; layout->xe = w.xe; layout->dye = w.dye;
+    layout->dz = w.dz; layout->dlogits = w.dlogits; layout->tiles = w.tiles;
+    layout->hp = w.hp; layout->poff = w.poff;
+    layout->total = w.total;
+}
+
 int moe_backward_plan(const moe_config_t* cfg, moe_backward_ws_t* layout) {
     if (!layout) return MOE_EINVAL;
     Geom G;
     const int rc = make_geom(cfg, &G);
     if (rc) return rc;
-    const BackwardWs w = backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns);
-    layout->dc = w.dc; layout->da = w.da; layout->dgs = w.dgs; layout->dus = w.dus;
-    layout->dw = w.dw; layout->rowinv = w.rowinv; layout->dxpool = w.dxpool; layout->dh = w.dh;
-    layout->dg = w.dg; layout->du = w.du; layout->xe = w.xe; layout->dye = w.dye;
-    layout->dz = w.dz; layout->dlogits = w.dlogits; layout->tiles = w.tiles;
-    layout->total = w.total;
+    fill_backward_layout(backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns), layout);
     return MOE_OK;
 }
 
-int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, void* stream) {
+int moe_backward_plan_ragged(const moe_config_t* cfg, moe_backward_ws_t* layout) {
+    if (!layout) return MOE_EINVAL;
     Geom G;
-    int rc = make_geom(cfg, &G);
+    const int rc = make_geom_ragged(cfg, &G);
     if (rc) return rc;
+    fill_backward_layout(backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns), layout);
+    return MOE_OK;
+}
+
+static int layer_backward(const Geom& G, const moe_backward_args_t* a, void* stream) {
     if (!a) return MOE_EINVAL;
     if (G.g.T == 0) return MOE_OK;
     const void* need[] = {a->x, a->Wr, a->W_ld, a->Wg, a->Wu, a->Wd, a->W_lu, a->idx, a->w,
@@ -621,6 +631,7 @@ int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, vo
         if (!ptr) return MOE_EINVAL;
     if (G.ns > 0 && (!a->Wsg || !a->Wsu || !a->Wsd || !a->a || !a->dWsg || !a->dWsu || !a->dWsd))
         return MOE_EINVAL;
+    if (G.g.ragged ? !a->expert_offsets : a->expert_offsets != nullptr) return MOE_EINVAL;
     const void* al16[] = {a->x, a->Wr, a->W_ld, a->Wg, a->Wu, a->Wd, a->W_lu, a->pool, a->h,
                           a->ypool, a->c, a->dout, a->dx, a->dWr, a->dW_ld, a->dWg, a->dWu,
                           a->dWd, a->dW_lu, a->ws};
@@ -629,9 +640,24 @@ int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, vo
     if (G.g.pool_rows == 0 || G.g.c_recv == 0) return MOE_EINVAL;
     const BackwardWs w = backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns);
     if (a->ws_bytes < w.total) return MOE_ENOSPC;
-    int dev, sms;
+    int dev, sms, rc;
     if ((rc = current_device(&dev, &sms))) return rc;
     return launch_backward(G.g, G.d, G.H, G.Hs, G.ns, *a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, void* stream) {
+    Geom G;
+    const int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    return layer_backward(G, a, stream);
+}
+
+int moe_layer_backward_ragged(const moe_config_t* cfg, const moe_backward_args_t* a,
+                              void* stream) {
+    Geom G;
+    const int rc = make_geom_ragged(cfg, &G);
+    if (rc) return rc;
+    return layer_backward(G, a, stream);
 }
 
 int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* slot_of,

@@ -154,13 +154,107 @@ __global__ void __launch_bounds__(256) zero_pad_rows_kernel(uint16_t* __restrict
     for (int ch = lane; ch < W / 8; ch += 32) d[ch] = make_uint4(0, 0, 0, 0);
 }
 
+// ---- dropless (ragged) layout: expert e's rows padded to a multiple of 64 at
+// poff[e], so that the weight gradients contract over whole 64-row blocks of
+// zero-padded operands.
+
+// poff[e] = sum over e' < e of count[e'] rounded up to 64; poff[E] = total.
+// One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) padded_offsets_kernel(const int32_t* __restrict__ count,
+                                                              int E, int32_t* __restrict__ poff) {
+    __shared__ int warp_sum[32];
+    __shared__ int carry;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const int v = e < E ? (count[e] + 63) & ~63 : 0;
+        int incl = v;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sum[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int ws = warp_sum[lane];
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ws, off);
+                if (lane >= off) ws += y;
+            }
+            warp_sum[lane] = ws;
+        }
+        __syncthreads();
+        const int excl = carry + (wid ? warp_sum[wid - 1] : 0) + incl - v;
+        if (e < E) poff[e] = excl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = excl + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) poff[E] = carry;
+}
+
+// rowinv[rows[eoff[e] + r]] = poff[e] + r for r < count[e].  One CTA per expert.
+__global__ void __launch_bounds__(256) row_inverse_ragged_kernel(
+    const int32_t* __restrict__ rows, const int32_t* __restrict__ eoff,
+    const int32_t* __restrict__ count, const int32_t* __restrict__ poff,
+    int32_t* __restrict__ rowinv) {
+    const int e = blockIdx.x;
+    for (int r = threadIdx.x; r < count[e]; r += blockDim.x) rowinv[rows[eoff[e] + r]] = poff[e] + r;
+}
+
+// Rows poff[e] + count[e] .. poff[e+1] - 1 of a [*, W] buffer set to zero.
+__global__ void __launch_bounds__(256) zero_pad_ragged_kernel(uint16_t* __restrict__ buf,
+                                                              const int32_t* __restrict__ count,
+                                                              const int32_t* __restrict__ poff,
+                                                              int W) {
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int first = poff[e] + count[e];
+    for (int r = first + wid; r < poff[e + 1]; r += blockDim.x >> 5) {
+        uint4* d = reinterpret_cast<uint4*>(buf + static_cast<int64_t>(r) * W);
+        for (int ch = lane; ch < W / 8; ch += 32) d[ch] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// dst[poff[e] + r][0:W] = src[row r of expert e][0:W] for r < count[e], zeros
+// up to poff[e+1]; the source row is rows[eoff[e] + r] (a row map) or, with
+// rows null, eoff[e] + r.  One CTA per expert, a warp per row.
+__global__ void __launch_bounds__(256) gather_ragged_kernel(
+    const uint16_t* __restrict__ src, int64_t pitch, const int32_t* __restrict__ rows,
+    const int32_t* __restrict__ eoff, const int32_t* __restrict__ count,
+    const int32_t* __restrict__ poff, int W, uint16_t* __restrict__ dst) {
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int cnt = count[e], p0 = poff[e], n = poff[e + 1] - p0;
+    for (int r = wid; r < n; r += blockDim.x >> 5) {
+        uint4* d = reinterpret_cast<uint4*>(dst + static_cast<int64_t>(p0 + r) * W);
+        if (r < cnt) {
+            const int64_t sr = rows ? rows[eoff[e] + r] : static_cast<int64_t>(eoff[e]) + r;
+            const uint4* sp = reinterpret_cast<const uint4*>(src + sr * pitch);
+            for (int ch = lane; ch < W / 8; ch += 32) d[ch] = __ldg(sp + ch);
+        } else {
+            for (int ch = lane; ch < W / 8; ch += 32) d[ch] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
 static size_t al(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
+
+// Rows of the per-expert layout: [E, c_recv] (capped) or the padded ragged
+// bound T*k + 64 E.
+static int64_t expert_layout_rows(const DispatchGeom& g) {
+    return g.ragged ? g.T * g.k + 64ll * g.E : static_cast<int64_t>(g.E) * g.c_recv;
+}
 
 BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int ns) {
     BackwardWs w;
+    std::memset(&w, 0, sizeof(w));
     size_t o = 0;
-    const size_t T = static_cast<size_t>(g.T), L = g.L, E = g.E, cr = g.c_recv;
+    const size_t T = static_cast<size_t>(g.T), L = g.L, E = g.E;
     const size_t P = static_cast<size_t>(g.pool_rows), HS = static_cast<size_t>(ns) * Hs;
+    const size_t PE = static_cast<size_t>(expert_layout_rows(g));   // per-expert rows
     w.dc = o;       o = al(o + T * L * 2);
     w.da = o;       o = al(o + T * HS * 2);
     w.dgs = o;      o = al(o + T * HS * 2);
@@ -168,14 +262,19 @@ BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int n
     w.dw = o;       o = al(o + T * g.k * 4);
     w.rowinv = o;   o = al(o + P * 4);
     w.dxpool = o;   o = al(o + P * L * 2);
-    w.dh = o;       o = al(o + E * cr * H * 2);
-    w.dg = o;       o = al(o + E * cr * H * 2);
-    w.du = o;       o = al(o + E * cr * H * 2);
-    w.xe = o;       o = al(o + E * cr * L * 2);
-    w.dye = o;      o = al(o + E * cr * L * 2);
+    w.dh = o;       o = al(o + PE * H * 2);
+    w.dg = o;       o = al(o + PE * H * 2);
+    w.du = o;       o = al(o + PE * H * 2);
+    w.xe = o;       o = al(o + PE * L * 2);
+    w.dye = o;      o = al(o + PE * L * 2);
     w.dz = o;       o = al(o + T * L * 2);
     w.dlogits = o;  o = al(o + T * E * 2);
-    w.tiles = o;    o = al(o + (E * ((cr + 127) / 128)) * 8 + 16);
+    const size_t max_mt = g.ragged ? P / 128 + E : E * ((static_cast<size_t>(g.c_recv) + 127) / 128);
+    w.tiles = o;    o = al(o + max_mt * 8 + 16);
+    if (g.ragged) {   // padded copy of h, padded row offsets
+        w.hp = o;   o = al(o + PE * H * 2);
+        w.poff = o; o = al(o + (E + 1) * 4);
+    }
     w.total = o;
     (void)d;
     return w;
@@ -194,7 +293,14 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     float* dw = reinterpret_cast<float*>(ws + L_.dw);
     int32_t* tiles = reinterpret_cast<int32_t*>(ws + L_.tiles);
     const int64_t T = g.T;
-    const int L = g.L, E = g.E, k = g.k, cr = g.c_recv;
+    const int L = g.L, E = g.E, k = g.k, cr = g.ragged ? 0 : g.c_recv;
+    // ragged layout: expert e's rows at a.expert_offsets[e] in the flat row map
+    // and h; padded to 64-row blocks at poff[e] in the per-expert buffers
+    const bool rag = g.ragged != 0;
+    const int32_t* eoff = a.expert_offsets;
+    int32_t* poff = rag ? reinterpret_cast<int32_t*>(ws + L_.poff) : nullptr;
+    uint16_t* hp = rag ? bf(L_.hp) : nullptr;
+    const int64_t PE = expert_layout_rows(g);
     const int HS = ns * Hs;
     int rc;
     auto mm = [&](GemmDesc& q, const char* name) {
@@ -250,11 +356,18 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     // ---- combine backward (the return path in reverse): dY straight into the
     // per-expert layout, whose rows past each expert's count are zero
     {
-        const int64_t nw = static_cast<int64_t>(E) * cr;
-        const unsigned g_inv = static_cast<unsigned>((nw + 255) / 256);
-        const unsigned g_pad = static_cast<unsigned>((nw + 7) / 8);
-        row_inverse_kernel<<<g_inv, 256, 0, st>>>(a.expert_rows, a.expert_count, E, cr, rowinv);
-        zero_pad_rows_kernel<<<g_pad, 256, 0, st>>>(dye, a.expert_count, E, cr, L);
+        if (rag) {
+            padded_offsets_kernel<<<1, 1024, 0, st>>>(a.expert_count, E, poff);
+            row_inverse_ragged_kernel<<<E, 256, 0, st>>>(a.expert_rows, eoff, a.expert_count, poff,
+                                                         rowinv);
+            zero_pad_ragged_kernel<<<E, 256, 0, st>>>(dye, a.expert_count, poff, L);
+        } else {
+            const int64_t nw = static_cast<int64_t>(E) * cr;
+            const unsigned g_inv = static_cast<unsigned>((nw + 255) / 256);
+            const unsigned g_pad = static_cast<unsigned>((nw + 7) / 8);
+            row_inverse_kernel<<<g_inv, 256, 0, st>>>(a.expert_rows, a.expert_count, E, cr, rowinv);
+            zero_pad_rows_kernel<<<g_pad, 256, 0, st>>>(dye, a.expert_count, E, cr, L);
+        }
         const unsigned grid = static_cast<unsigned>((T + 7) / 8);
         if (L / 8 <= 32 * 4)
             combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
@@ -266,19 +379,21 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         trace_after(st, "bwd_combine");
     }
     // ---- experts
-    const int max_mt = E * ((cr + 127) / 128);
+    const int max_mt = rag ? static_cast<int>(g.pool_rows / 128 + E) : E * ((cr + 127) / 128);
     int32_t* tile_count = tiles + 2 * max_mt;
     if ((rc = launch_build_tiles(a.expert_count, E, 128, tiles, tile_count, st))) return rc;
     std::memset(&q, 0, sizeof(q));   // dh = dY_e Wd_e (per-expert rows by TMA)
     q.a_mode = A_GROUPED; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
     q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{dye, L, a.Wd, H, L};
-    q.groups = E; q.rows_per_group = cr; q.a_gstride = static_cast<int64_t>(cr) * L;
+    q.groups = E; q.rows_per_group = rag ? static_cast<int>(PE) : cr;
+    q.a_gstride = static_cast<int64_t>(cr) * L;
     q.b_rows = H; q.b_gstride = static_cast<int64_t>(L) * H;
     q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+    q.goff = poff;   // ragged: the padded per-expert rows (A and out)
     q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
     if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
-    const size_t ghs = static_cast<size_t>(E) * cr * H * 2;
+    const size_t ghs = static_cast<size_t>(PE) * H * 2;
     if (cudaMemsetAsync(dg, 0, ghs, st) != cudaSuccess || cudaMemsetAsync(du, 0, ghs, st) != cudaSuccess)
         return MOE_ECUDA;
     std::memset(&q, 0, sizeof(q));   // recompute g/u of the received rows, SwiGLU backward
@@ -288,6 +403,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.b_gstride = static_cast<int64_t>(H) * L;
     q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+    q.goff = poff; q.rmoff = eoff;   // ragged: outputs padded, rows from the flat map
     q.gather_src = a.pool; q.gather_pitch = pool_pitch(L); q.gather_rows = g.pool_rows;
     q.aux = dh; q.out = dg; q.out2 = du; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
     if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
@@ -296,13 +412,22 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.N = L; q.nseg = 2;
     q.seg[0] = GemmSeg{dg, H, a.Wg, L, H};
     q.seg[1] = GemmSeg{du, H, a.Wu, L, H};
-    q.groups = E; q.rows_per_group = cr; q.a_gstride = static_cast<int64_t>(cr) * H;
+    q.groups = E; q.rows_per_group = rag ? static_cast<int>(PE) : cr;
+    q.a_gstride = static_cast<int64_t>(cr) * H;
     q.b_rows = L; q.b_gstride = static_cast<int64_t>(H) * L;
     q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+    q.goff = poff; q.rmoff = eoff;
     q.out = dxp; q.ldo = L;
     if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
-    {   // per-expert contiguous, zero-padded copy of X; h's unwritten rows zeroed
+    if (rag) {   // padded per-expert copies of X and of h
+        gather_ragged_kernel<<<E, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, eoff,
+                                                a.expert_count, poff, L, xe);
+        gather_ragged_kernel<<<E, 256, 0, st>>>(a.h, H, nullptr, eoff, a.expert_count, poff, H,
+                                                hp);
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "bwd_gather_rows");
+    } else {   // per-expert contiguous, zero-padded copy of X; h's unwritten rows zeroed
         const int64_t nw = static_cast<int64_t>(E) * cr;
         const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
         gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, a.expert_count, E, cr, L, xe);
@@ -313,14 +438,16 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     auto wgrad = [&](const uint16_t* A, int M, const uint16_t* B, int N, float* out, const char* nm) {
         std::memset(&q, 0, sizeof(q));   // out_e[M, N] = A_e^T B_e over the expert's rows
         q.a_mode = A_GROUPED; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
-        q.M = M; q.N = N; q.nseg = 1; q.seg[0] = GemmSeg{A, M, B, N, cr};
+        q.M = M; q.N = N; q.nseg = 1;
+        q.seg[0] = GemmSeg{A, M, B, N, rag ? static_cast<int>(PE) : cr};
         q.groups = E; q.uniform_groups = E;
         q.a_gstride = static_cast<int64_t>(cr) * M; q.b_rows = N;
         q.b_gstride = static_cast<int64_t>(cr) * N;
+        q.kgoff = poff; q.k_rows = PE;   // ragged: each expert's padded row range
         q.out = out; q.ldo = N; q.out_gstride = static_cast<int64_t>(M) * N;
         return mm(q, nm);
     };
-    if ((rc = wgrad(dye, L, a.h, H, a.dWd, "bwd_gemm_dWd"))) return rc;
+    if ((rc = wgrad(dye, L, rag ? hp : a.h, H, a.dWd, "bwd_gemm_dWd"))) return rc;
     if ((rc = wgrad(dg, H, xe, L, a.dWg, "bwd_gemm_dWg"))) return rc;
     if ((rc = wgrad(du, H, xe, L, a.dWu, "bwd_gemm_dWu"))) return rc;
     // ---- return of the gradients to the tokens, latent projection

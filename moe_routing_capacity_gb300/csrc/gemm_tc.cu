@@ -93,6 +93,8 @@ struct KParams {
     const int* rowmap;
     const int* counts;
     const int* goff;        // optional per-group first row (ragged groups)
+    const int* rmoff;       // optional per-group first row-map entry (else goff)
+    const int* kgoff;       // optional per-group K row range (uniform groups)
     int rowmap_ld;
     const uint16_t* gather_src;
     long long gather_pitch;
@@ -134,6 +136,19 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// First row-map entry of group g.
+__device__ __forceinline__ long long rowmap_base(const KParams& p, int g) {
+    if (p.rmoff) return p.rmoff[g];
+    if (p.goff) return p.goff[g];
+    return static_cast<long long>(g) * p.rowmap_ld;
+}
+
+// K blocks of a tile of group g: the whole contraction, or the group's own
+// row range of flat MN-major operands.
+__device__ __forceinline__ int tile_kblocks(const KParams& p, int g, int kb_total) {
+    return p.kgoff ? (p.kgoff[g + 1] - p.kgoff[g]) / 64 : kb_total;
+}
 
 // MAJ bit 0: A is MN-major (stored [K, M], M contiguous); bit 1: B is
 // MN-major (stored [K, N]).  MN-major tiles arrive as 64 x 64 TMA boxes, one
@@ -233,8 +248,10 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 int g, m0, nb;
                 decode_tile<AMODE>(p, tile, g, m0, nb);
                 if (CG2) m0 = 2 * m0 + static_cast<int>(crank) * BM;
+                const int kbt = tile_kblocks(p, g, kb_total);
+                const int k0 = p.kgoff ? p.kgoff[g] : 0;   // first K row (flat operands)
                 int seg = 0;
-                for (int kb = 0; kb < kb_total; ++kb) {
+                for (int kb = 0; kb < kbt; ++kb) {
                     while (kb >= p.seg_kb[seg + 1]) ++seg;
                     const int kx = (kb - p.seg_kb[seg]) * BK;
                     if (AMODE != A_GATHER) {
@@ -263,6 +280,9 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         } else if (A_MN && AMODE == A_DENSE) {
                             tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], m0, kx);
                             tma_load_2d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, kx);
+                        } else if (A_MN && p.kgoff) {
+                            tma_load_2d(a_dst, &p.mapA[seg], &fullA[sa], m0, k0 + kx);
+                            tma_load_2d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, k0 + kx);
                         } else if (A_MN) {
                             tma_load_3d(a_dst, &p.mapA[seg], &fullA[sa], m0, kx, g);
                             tma_load_3d(a_dst + 8192, &p.mapA[seg], &fullA[sa], m0 + 64, kx, g);
@@ -317,7 +337,9 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                             const int n = PAIR ? nb * (BN / 2) + (h % (BN / 128)) * 64
                                                : nb * BN + h * 64;
                             const CUtensorMap* mp = up ? &p.mapBup : &p.mapB[seg];
-                            if (B3D)
+                            if (B3D && p.kgoff)
+                                tma_load_2d(b_dst + h * 8192, mp, &fullB[sb], n, k0 + kx);
+                            else if (B3D)
                                 tma_load_3d(b_dst + h * 8192, mp, &fullB[sb], n, kx, g);
                             else
                                 tma_load_2d(b_dst + h * 8192, mp, &fullB[sb], n, kx);
@@ -390,10 +412,16 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             uint32_t acc = 0, acc_phase = 0;
             bool ok = true;
             for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
+                int kbt = kb_total;
+                if (p.kgoff) {
+                    int g, m0, nb;
+                    decode_tile<AMODE>(p, tile, g, m0, nb);
+                    kbt = tile_kblocks(p, g, kb_total);
+                }
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < kb_total; ++kb) {
+                for (int kb = 0; kb < kbt; ++kb) {
                     if (!mbar_wait(&fullA[sa], pa, abort_flag, p.status) ||
                         !mbar_wait(&fullB[sb], pb, abort_flag, p.status)) {
                         ok = false;
@@ -475,9 +503,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             } else {
                 row_ok = m < p.counts[g];
                 orow = m;
-                if (EPI == EPI_SCATTER && row_ok)
-                    orow = p.rowmap[(p.goff ? static_cast<long long>(p.goff[g])
-                                            : static_cast<long long>(g) * p.rowmap_ld) + m];
+                if (EPI == EPI_SCATTER && row_ok) orow = p.rowmap[rowmap_base(p, g) + m];
             }
             // element offset of this row in the output (and in aux / out2):
             // dense or scattered rows, or row m of group g
@@ -522,6 +548,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     }
                 }
             } else if (EPI == EPI_F32) {
+                // a group with an empty K range contributes a zero tile
+                const bool zero_tile = p.kgoff && tile_kblocks(p, g, 0) == 0;
                 // Lane i holds row 32q + i.  Each 32-column block goes through
                 // shared memory (16-byte chunks XOR-swizzled by row, so both
                 // the row-wise writes and the column-wise reads are free of
@@ -542,6 +570,10 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tl + c * 32, r);
+                    if (zero_tile) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = 0u;
+                    }
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         stg[lane * 8 + (v ^ (lane & 7))] =
@@ -696,9 +728,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             int g, m0, nb;
             decode_tile<AMODE>(p, tile, g, m0, nb);
             nxt_cnt = p.counts[g] - m0;   // valid rows of the tile, from its first
-            const int* rl = p.rowmap + m0 +
-                            (p.goff ? static_cast<long long>(p.goff[g])
-                                    : static_cast<long long>(g) * p.rowmap_ld);
+            const int* rl = p.rowmap + m0 + rowmap_base(p, g);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int m = rg + 16 * i;
@@ -890,6 +920,8 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         if (d.a_mode == A_DENSE)
             rc = d.a_mn ? map2d(&p.mapA[s], g.A, d.M, g.K, g.lda, 64)
                         : map2d(&p.mapA[s], g.A, g.K, d.M, g.lda, BM);
+        else if (d.a_mode == A_GROUPED && d.kgoff)   // flat [k_rows, M] operand
+            rc = d.a_mn ? map2d(&p.mapA[s], g.A, d.M, d.k_rows, g.lda, 64) : MOE_EINVAL;
         else if (d.a_mode == A_GROUPED && d.goff)
             rc = d.a_mn ? MOE_EINVAL : map2d(&p.mapA[s], g.A, g.K, d.rows_per_group, g.lda, BM);
         else if (d.a_mode == A_GROUPED)
@@ -903,6 +935,8 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
         if (d.a_mode == A_DENSE)
             rc = d.b_mn ? map2d(&p.mapB[s], g.B, d.b_rows, g.K, g.ldb, 64)
                         : map2d(&p.mapB[s], g.B, g.K, d.b_rows, g.ldb, b_box);
+        else if (d.kgoff)   // flat [k_rows, N] operand
+            rc = d.b_mn ? map2d(&p.mapB[s], g.B, d.b_rows, d.k_rows, g.ldb, 64) : MOE_EINVAL;
         else
             rc = d.b_mn ? map3d(&p.mapB[s], g.B, d.b_rows, g.K, d.groups, g.ldb, d.b_gstride, 64)
                         : map3d(&p.mapB[s], g.B, g.K, d.b_rows, d.groups, g.ldb, d.b_gstride,
@@ -948,6 +982,11 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.rowmap = d.rowmap;
     p.counts = d.counts;
     p.goff = d.goff;
+    p.rmoff = d.rmoff;
+    p.kgoff = d.kgoff;
+    if (d.kgoff && (!d.uniform_groups || !d.a_mn || !d.b_mn || d.nseg != 1 || d.epi != EPI_F32 ||
+                    d.k_rows <= 0))
+        return MOE_EINVAL;
     p.rowmap_ld = d.rowmap_ld;
     p.gather_src = d.gather_src;
     p.gather_pitch = d.gather_pitch;

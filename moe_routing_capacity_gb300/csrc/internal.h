@@ -92,6 +92,13 @@ struct GemmDesc {
     const void* aux;        // EPI_SWIGLU_BWD: incoming gradient, addressed like out
     int uniform_groups;     // > 0: grouped tiles over `groups` groups of M rows each
                             // (no tile list), e.g. per-expert weight gradients
+    const int32_t* rmoff;   // optional [groups]: first entry of each group in the row
+                            // map, when it differs from goff (row gather, scatter)
+    const int32_t* kgoff;   // optional [groups + 1] with uniform_groups: group g
+                            // contracts over rows kgoff[g] .. kgoff[g+1] (multiples of
+                            // 64) of MN-major operands stored flat; an empty range
+                            // writes a zero tile
+    int64_t k_rows;         // rows of those flat operands
     // EPI_SPLIT: second output (EPI_SWIGLU_BWD: out2 = du, addressed like out)
     int nsplit;             // column tiles of the first output (N = nsplit * bn)
     int N2;                 // columns of the second output
@@ -143,7 +150,8 @@ int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
 
 // Backward pass: scratch layout (byte offsets) and launch sequence.
 struct BackwardWs {
-    size_t dc, da, dgs, dus, dw, rowinv, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles, total;
+    size_t dc, da, dgs, dus, dw, rowinv, dxpool, dh, dg, du, xe, dye, dz, dlogits, tiles, hp, poff,
+        total;
 };
 BackwardWs backward_ws_layout(const DispatchGeom& g, int d, int H, int Hs, int ns);
 int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,

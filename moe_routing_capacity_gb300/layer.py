@@ -136,15 +136,13 @@ class PooledWaveMoE:
 
     def backward(self, x, dout, stream=None) -> dict:
         """Gradients of the last forward with respect to x and every weight,
-        for the upstream gradient dout [T, d] (capped layout only).  Returns
-        {"x": dx (bf16), "Wr": ..., ...} with fp32 weight gradients."""
-        if self.dropless:
-            raise NotImplementedError("the backward pass covers the capped layout")
+        for the upstream gradient dout [T, d] (capped or dropless layout).
+        Returns {"x": dx (bf16), "Wr": ..., ...} with fp32 weight gradients."""
         cfg, dev = self.cfg, self.device
         T, d, L, E, H = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.h_expert
         ns, Hs = cfg.n_shared, cfg.h_shared
         if not hasattr(self, "bwd_ws"):
-            self.bwd_layout = abi.backward_plan(cfg)
+            self.bwd_layout = abi.backward_plan(cfg, ragged=self.dropless)
             self.bwd_ws = torch.empty(max(1, self.bwd_layout.total), dtype=torch.uint8, device=dev)
             f = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
             self.grads = {"x": torch.empty(T, d, dtype=torch.bfloat16, device=dev),
@@ -152,7 +150,8 @@ class PooledWaveMoE:
                           "Wd": f(E, L, H), "W_lu": f(d, L), "Wsg": f(ns, Hs, d),
                           "Wsu": f(ns, Hs, d), "Wsd": f(ns, d, Hs)}
         hoff = self.plan.h_offset_bytes
-        h = self.ws_ffn[hoff:hoff + E * self.plan.c_recv * H * 2].view(torch.bfloat16)
+        h_rows = self.plan.pool_rows if self.dropless else E * self.plan.c_recv
+        h = self.ws_ffn[hoff:hoff + h_rows * H * 2].view(torch.bfloat16)
         g = self.grads
         tensors = dict(x=x, Wr=self.w["Wr"], W_ld=self.w["W_ld"], Wg=self.w["Wg"], Wu=self.w["Wu"],
                        Wd=self.w["Wd"], W_lu=self.w["W_lu"], Wsg=self.w["Wsg"], Wsu=self.w["Wsu"],
@@ -162,7 +161,8 @@ class PooledWaveMoE:
                        a=self.a if ns else None, dout=dout, dx=g["x"], dWr=g["Wr"],
                        dW_ld=g["W_ld"], dWg=g["Wg"], dWu=g["Wu"], dWd=g["Wd"], dW_lu=g["W_lu"],
                        dWsg=g["Wsg"] if ns else None, dWsu=g["Wsu"] if ns else None,
-                       dWsd=g["Wsd"] if ns else None)
+                       dWsd=g["Wsd"] if ns else None,
+                       expert_offsets=self.expert_offsets if self.dropless else None)
         abi.layer_backward(cfg, tensors, self.bwd_ws, self.status, stream)
         return g
 

@@ -70,3 +70,52 @@ def test_backward_small(kw):
 def test_backward_mid():
     _, _, rep = run(wl.MID)
     print(rep)
+
+
+def run_dropless(cfg, seed_dout=3):
+    """The dropless layer keeps every assignment, so its gradients are those
+    of the capped layer with unbounded factors (the pool layout differs, the
+    derivative does not)."""
+    inp = wl.make_inputs(cfg, "cpu")
+    host = {k: (v.float().numpy() if v is not None else None) for k, v in inp.items()}
+    cfg_ub = cfg.with_(cf_send=float("inf"), cf_recv=float("inf"))
+    fwd = O.layer(cfg_ub, host)
+    assert (fwd["disp"]["drop"] == 0).all()
+    m = PooledWaveMoE(cfg, inp, "cuda", dropless=True)
+    x = inp["x"].cuda()
+    m.forward(x)
+    torch.cuda.synchronize()
+    assert (m.idx.cpu().numpy() == fwd["idx"]).all(), "choose a seed without near-tie flips"
+    g = torch.Generator().manual_seed(seed_dout)
+    dout = torch.randn(cfg.T, cfg.d_model, generator=g).to(torch.bfloat16)
+    grads = m.backward(x, dout.cuda())
+    torch.cuda.synchronize()
+    assert int(m.status.item()) == 0
+    ref = O.layer_backward(cfg_ub, host, fwd, dout.float().numpy())
+    rep = {}
+    check_close("dx", grads["x"].float().cpu().numpy(), ref["x"], rep)
+    for name in ("Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu"):
+        check_grad("d" + name, grads[name].cpu().numpy(), ref[name], rep)
+    if cfg.n_shared:
+        for name in ("Wsg", "Wsu", "Wsd"):
+            check_grad("d" + name, grads[name].cpu().numpy(), ref[name], rep)
+    return m, ref, rep
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(seed=61, T=200, n_ranks=4, d_model=136, d_latent=72, h_expert=136, h_shared=72),
+    dict(seed=62, T=64, n_experts=96, n_ranks=4, top_k=2),     # most experts get no row
+    dict(seed=63, bias_kind="zipf"),                           # a few experts take most rows
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()) or "tiny")
+def test_backward_dropless_small(kw):
+    m, _, rep = run_dropless(wl.TINY.with_(**kw))
+    counts = m.expert_count.cpu()
+    if kw.get("n_experts") == 96:
+        assert (counts == 0).any()      # the empty-group path of the weight gradients ran
+    print(rep)
+
+
+def test_backward_dropless_mid():
+    _, _, rep = run_dropless(wl.MID)
+    print(rep)
