@@ -295,6 +295,9 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert int(m.status.item()) == 0, "device status word set during warm-up"
     st = m.drop_stats()
+    # tokens whose k-th and (k+1)-th (or two adjacent selected) logits are within
+    # the near-tie gap: their routing may legitimately differ from the oracle's
+    near_ties = int((m.tie != 0).sum().item())
 
     # ---- timed region: device-resident inputs
     if world > 1:
@@ -545,7 +548,8 @@ def run_gb300(args, rank, world, local_rank):
                        f"H={cfg.h_expert}, cf {cfg.cf_send}/{cfg.cf_recv}",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (8.1 GB weights per step)"},
-            "drops": {"kept": st["kept"], "dropped_send": st["dropped_send"],
+            "drops": {"near_tie_tokens": near_ties,
+                      "kept": st["kept"], "dropped_send": st["dropped_send"],
                       "dropped_recv": st["dropped_recv"],
                       "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
             "gpu_launches": sum(v[1] for v in per.values()),

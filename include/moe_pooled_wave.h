@@ -358,6 +358,14 @@ int moe_layer_backward_ragged(const moe_config_t* cfg, const moe_backward_args_t
 int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,
                        float* bias, void* stream);
 
+/* Index checks of a checked build (compiled with -DMOE_CHECK=1; the pages
+ * define no such operation): every row, slot, expert and tile index the
+ * kernels compute is checked before use; a failed check skips the access
+ * and records a site code (1001.. by kernel) in a device word.  Returns the
+ * first recorded code since the last call (0: none) and resets it; a normal
+ * build always returns 0.  Synchronous: call after the work has finished. */
+int moe_check_status(void);
+
 /* Kernel timing trace (instrumentation; the pages define no such operation).
  * moe_trace_begin(n) creates n CUDA events (timing enabled) owned by the
  *   library and turns tracing on; from then on every kernel the library

@@ -25,7 +25,8 @@ EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project"
            "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged",
            "moe_backward_plan", "moe_layer_backward", "moe_backward_plan_ragged",
            "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
-           "moe_trace_end", "moe_trace_event", "moe_strerror", "moe_abi_version")
+           "moe_trace_end", "moe_trace_event", "moe_check_status", "moe_strerror",
+           "moe_abi_version")
 
 
 class MoeError(RuntimeError):
@@ -86,43 +87,50 @@ def lib() -> ctypes.CDLL:
     """Load the library once; raise if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "`python -m moe_routing_capacity_gb300.build`")
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
-        pc = ctypes.POINTER(Config)
-        L.moe_plan.argtypes = [pc, ctypes.POINTER(Plan)]
-        L.moe_router_topk.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.moe_latent_proj.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp]
-        L.moe_route_project.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.moe_matmul.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, i64, i32, i32, vp,
-                                 ctypes.c_int, i64, vp, vp]
-        L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
-        L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
-        L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
-        L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
-        L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
-        L.moe_backward_plan.argtypes = [pc, ctypes.POINTER(BackwardWs)]
-        L.moe_layer_backward.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
-        L.moe_backward_plan_ragged.argtypes = [pc, ctypes.POINTER(BackwardWs)]
-        L.moe_layer_backward_ragged.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
-        L.moe_strerror.argtypes = [ctypes.c_int]
-        L.moe_strerror.restype = ctypes.c_char_p
-        L.moe_abi_version.argtypes = []
-        L.moe_trace_begin.argtypes = [ctypes.c_int]
-        L.moe_trace_mark.argtypes = [vp]
-        L.moe_trace_end.argtypes = []
-        L.moe_trace_event.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
-                                      ctypes.POINTER(ctypes.c_float)]
-        for n in EXPORTS:
-            if n != "moe_strerror":
-                getattr(L, n).restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Load one build of the library (e.g. the checked one) with its
+    signatures declared; ``lib()`` serves the package's own build."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m moe_routing_capacity_gb300.build`")
+    L = ctypes.CDLL(path)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    pc = ctypes.POINTER(Config)
+    L.moe_plan.argtypes = [pc, ctypes.POINTER(Plan)]
+    L.moe_router_topk.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_latent_proj.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp]
+    L.moe_route_project.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_matmul.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, i64, i32, i32, vp,
+                             ctypes.c_int, i64, vp, vp]
+    L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
+    L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
+    L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    L.moe_backward_plan.argtypes = [pc, ctypes.POINTER(BackwardWs)]
+    L.moe_layer_backward.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
+    L.moe_backward_plan_ragged.argtypes = [pc, ctypes.POINTER(BackwardWs)]
+    L.moe_layer_backward_ragged.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
+    L.moe_strerror.argtypes = [ctypes.c_int]
+    L.moe_strerror.restype = ctypes.c_char_p
+    L.moe_abi_version.argtypes = []
+    L.moe_check_status.argtypes = []
+    L.moe_trace_begin.argtypes = [ctypes.c_int]
+    L.moe_trace_mark.argtypes = [vp]
+    L.moe_trace_end.argtypes = []
+    L.moe_trace_event.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                  ctypes.POINTER(ctypes.c_float)]
+    for n in EXPORTS:
+        if n != "moe_strerror":
+            getattr(L, n).restype = ctypes.c_int
+    return L
 
 
 def strerror(code: int) -> str:

@@ -16,6 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_pooled_wave.so")
+# the checked build: every kernel index verified before use (-DMOE_CHECK=1)
+CHECK_LIB = os.path.join(HERE, "libmoe_pooled_wave_check.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v"]
@@ -62,5 +64,13 @@ def build(verbose: bool = False, lib_path: str = LIB, extra_flags=()) -> str:
     return lib_path
 
 
+def build_checked(verbose: bool = False) -> str:
+    """The library with the kernels' index checks compiled in."""
+    return build(verbose, CHECK_LIB, ("-DMOE_CHECK=1",))
+
+
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    if "--check" in sys.argv:
+        print(build_checked(verbose="-v" in sys.argv))
+    else:
+        print(build(verbose="-v" in sys.argv))

@@ -5,7 +5,21 @@
 #include <map>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
+
+namespace {
+// One NVTX range per C-ABI compute call (a no-op unless a profiler attaches),
+// so that profiler timelines group each call's kernels under its name.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
+#define MOE_NVTX_RANGE() NvtxRange moe_nvtx_range_(__func__)
 
 namespace moe {
 
@@ -185,6 +199,13 @@ extern "C" {
 
 int moe_abi_version(void) { return 1; }
 
+int moe_check_status(void) {
+    const int v[3] = {check_status_route(), check_status_gemm(), check_status_backward()};
+    for (int x : v)
+        if (x) return x;
+    return 0;
+}
+
 int moe_trace_begin(int capacity) {
     std::lock_guard<std::mutex> lk(trace_mu);
     if (capacity < 0) return MOE_EINVAL;
@@ -253,6 +274,7 @@ int moe_plan(const moe_config_t* cfg, moe_plan_t* plan) {
 int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* Wr,
                     const float* bias, float* logits, int32_t* idx, float* w, uint8_t* tie,
                     int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -284,6 +306,7 @@ int moe_router_topk(const moe_config_t* cfg, const uint16_t* x, const uint16_t* 
 int moe_route_project(const moe_config_t* cfg, const uint16_t* x, const uint16_t* Wr,
                       const float* bias, const uint16_t* W_ld, float* logits, int32_t* idx,
                       float* w, uint8_t* tie, uint16_t* z, int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -322,6 +345,7 @@ int moe_route_project(const moe_config_t* cfg, const uint16_t* x, const uint16_t
 
 int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K, int32_t N,
                     uint16_t* out, int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     if (M < 0 || K <= 0 || N <= 0 || K % 8 || N % 8) return MOE_EINVAL;
     if (M == 0) return MOE_OK;
     if (!in || !W || !out || !status) return MOE_EINVAL;
@@ -346,6 +370,7 @@ int moe_latent_proj(const uint16_t* in, const uint16_t* W, int64_t M, int32_t K,
 int moe_matmul(const uint16_t* A, int a_mn, int64_t lda, const uint16_t* B, int b_mn,
                int64_t ldb, int64_t M, int32_t N, int32_t K, void* out, int out_f32, int64_t ldo,
                int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     if (M < 0 || N <= 0 || K <= 0 || lda <= 0 || ldb <= 0 || ldo < N) return MOE_EINVAL;
     if (lda % 8 || ldb % 8 || (out_f32 ? ldo % 4 : ldo % 8) || (!out_f32 && N % 8))
         return MOE_EINVAL;
@@ -377,6 +402,7 @@ int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_
                         size_t ws_bytes, uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                         int32_t* expert_rows, int32_t* expert_count, moe_drop_stats_t* stats,
                         void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -406,6 +432,7 @@ int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_
                         size_t ws_bytes, uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                         int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
                         moe_drop_stats_t* stats, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom_ragged(cfg, &G);
     if (rc) return rc;
@@ -426,6 +453,7 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
                           const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
                           const uint16_t* Wd, void* ws, size_t ws_bytes, uint16_t* ypool,
                           int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom_ragged(cfg, &G);
     if (rc) return rc;
@@ -497,6 +525,7 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
     d2.ldo = L;
     d2.status = status;
     d2.name = "gemm_expert_down";
+    d2.gather_rows = g.pool_rows;   // the scatter's destination rows
     return gemm_launch(d2, st);
 }
 
@@ -504,6 +533,7 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
                            const int32_t* expert_rows, const int32_t* expert_count,
                            const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, void* ws,
                            size_t ws_bytes, uint16_t* ypool, int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -576,11 +606,13 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
     d2.ldo = L;
     d2.status = status;
     d2.name = "gemm_expert_down";
+    d2.gather_rows = g.pool_rows;   // the scatter's destination rows
     return gemm_launch(d2, st);
 }
 
 int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,
                        float* bias, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -646,6 +678,7 @@ static int layer_backward(const Geom& G, const moe_backward_args_t* a, void* str
 }
 
 int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     const int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -654,6 +687,7 @@ int moe_layer_backward(const moe_config_t* cfg, const moe_backward_args_t* a, vo
 
 int moe_layer_backward_ragged(const moe_config_t* cfg, const moe_backward_args_t* a,
                               void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     const int rc = make_geom_ragged(cfg, &G);
     if (rc) return rc;
@@ -664,6 +698,7 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
                 const float* w, const uint16_t* W_lu, const uint16_t* x, const uint16_t* Wsg,
                 const uint16_t* Wsu, const uint16_t* Wsd, uint16_t* c, uint16_t* a,
                 uint16_t* out, int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
     if (rc) return rc;
@@ -678,7 +713,7 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
                      !aligned16(a)))
         return MOE_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if ((rc = launch_combine(ypool, slot_of, w, g.T, g.k, g.L, c, st))) return rc;
+    if ((rc = launch_combine(ypool, slot_of, w, g.T, g.k, g.L, c, g.pool_rows, st))) return rc;
 
     const int d = G.d, Hs = G.Hs, ns = G.ns;
     const int hs_all = ns * Hs;

@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ rowinv,
                                                           const float* __restrict__ w, int64_t T,
                                                           int k, int L, uint16_t* __restrict__ dy,
-                                                          float* __restrict__ dw) {
+                                                          float* __restrict__ dw, int64_t rows,
+                                                          int64_t dst_rows) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -38,7 +39,9 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __rest
     if (lane < k) {
         my_row = slot_of[t * k + lane];
         my_w = w[t * k + lane];
+        if (my_row >= 0 && !moe_check(my_row < rows, 1007)) my_row = -1;
         if (my_row >= 0) my_dst = rowinv[my_row];
+        if (my_row >= 0 && !moe_check(my_dst >= 0 && my_dst < dst_rows, 1008)) my_row = -1;
     }
     const int nchunk = L / 8;
     float dot_mine = 0.0f;   // lane j keeps dw for assignment j
@@ -242,6 +245,8 @@ __global__ void __launch_bounds__(256) gather_ragged_kernel(
 
 static size_t al(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
+int check_status_backward() { return moe_check_read_reset(); }
+
 // Rows of the per-expert layout: [E, c_recv] (capped) or the padded ragged
 // bound T*k + 64 E.
 static int64_t expert_layout_rows(const DispatchGeom& g) {
@@ -371,10 +376,10 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         const unsigned grid = static_cast<unsigned>((T + 7) / 8);
         if (L / 8 <= 32 * 4)
             combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
-                                                         L, dye, dw);
+                                                         L, dye, dw, g.pool_rows, PE);
         else
             combine_bwd_kernel<12><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
-                                                          L, dye, dw);
+                                                          L, dye, dw, g.pool_rows, PE);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_combine");
     }
@@ -418,7 +423,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
     q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
     q.goff = poff; q.rmoff = eoff;
-    q.out = dxp; q.ldo = L;
+    q.out = dxp; q.ldo = L; q.gather_rows = g.pool_rows;
     if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
     if (rag) {   // padded per-expert copies of X and of h
         gather_ragged_kernel<<<E, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, eoff,
@@ -451,7 +456,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     if ((rc = wgrad(dg, H, xe, L, a.dWg, "bwd_gemm_dWg"))) return rc;
     if ((rc = wgrad(du, H, xe, L, a.dWu, "bwd_gemm_dWu"))) return rc;
     // ---- return of the gradients to the tokens, latent projection
-    if ((rc = launch_combine(dxp, a.slot_of, nullptr, T, k, L, dz, st))) return rc;
+    if ((rc = launch_combine(dxp, a.slot_of, nullptr, T, k, L, dz, g.pool_rows, st))) return rc;
     std::memset(&q, 0, sizeof(q));
     q.a_mode = A_DENSE; q.epi = EPI_F32; q.bn = 256; q.a_mn = 1; q.b_mn = 1;
     q.M = L; q.N = d; q.nseg = 1; q.seg[0] = GemmSeg{dz, L, a.x, d, static_cast<int>(T)};

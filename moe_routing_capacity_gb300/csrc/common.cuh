@@ -31,6 +31,36 @@ __device__ __forceinline__ void report_error(int32_t* status, int code) {
     if (status) atomicCAS(reinterpret_cast<int*>(status), 0, code);
 }
 
+// ------------------------------------------------------------------ checked builds
+// Built with -DMOE_CHECK=1, the kernels check every row, slot, expert and
+// tile index they compute before using it; a failed check records a site
+// code in a device word of its translation unit (the first one wins) and
+// the access is skipped.  Without the flag the checks compile away.
+#ifndef MOE_CHECK
+#define MOE_CHECK 0
+#endif
+
+static __device__ int g_moe_check_error;
+
+__device__ __forceinline__ bool moe_check(bool ok, int site) {
+#if MOE_CHECK
+    if (!ok) atomicCAS(&g_moe_check_error, 0, site);
+    return ok;
+#else
+    (void)site;
+    return true;
+#endif
+}
+
+// Host: this translation unit's recorded site code (0: none); reset to 0.
+static inline int moe_check_read_reset() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_moe_check_error, sizeof(int)) != cudaSuccess) return -1;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_moe_check_error, &zero, sizeof(int)) != cudaSuccess) return -1;
+    return v;
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

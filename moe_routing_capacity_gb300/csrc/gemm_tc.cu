@@ -98,6 +98,7 @@ struct KParams {
     int rowmap_ld;
     const uint16_t* gather_src;
     long long gather_pitch;
+    long long gather_rows;  // rows of the gather source / scatter destination (checks)
     void* out;
     long long ldo;
     long long out_gstride;
@@ -503,7 +504,10 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             } else {
                 row_ok = m < p.counts[g];
                 orow = m;
-                if (EPI == EPI_SCATTER && row_ok) orow = p.rowmap[rowmap_base(p, g) + m];
+                if (EPI == EPI_SCATTER && row_ok) {
+                    orow = p.rowmap[rowmap_base(p, g) + m];
+                    if (!moe_check(orow >= 0 && orow < p.gather_rows, 1006)) row_ok = false;
+                }
             }
             // element offset of this row in the output (and in aux / out2):
             // dense or scattered rows, or row m of group g
@@ -733,6 +737,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             for (int i = 0; i < 8; ++i) {
                 const int m = rg + 16 * i;
                 nxt_row[i] = m < nxt_cnt ? rl[m] : 0;
+                if (!moe_check(nxt_row[i] >= 0 && nxt_row[i] < p.gather_rows, 1004)) nxt_row[i] = 0;
             }
         };
         if (cta0 < ntiles) fetch_rows(cta0);
@@ -878,6 +883,8 @@ static int launch_traced(const KParams& p, int grid, cudaStream_t st, const char
     return rc;
 }
 
+int check_status_gemm() { return moe_check_read_reset(); }
+
 int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
@@ -990,6 +997,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.rowmap_ld = d.rowmap_ld;
     p.gather_src = d.gather_src;
     p.gather_pitch = d.gather_pitch;
+    p.gather_rows = d.gather_rows;
     p.out = d.out;
     p.ldo = d.ldo;
     p.out_gstride = d.out_gstride;

@@ -145,6 +145,12 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
                            moe_drop_stats_t* stats, cudaStream_t stream);
 
 // Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
+// Checked builds: the site code recorded by each translation unit's index
+// checks since the last call (0: none), reset on reading.
+int check_status_route();
+int check_status_gemm();
+int check_status_backward();
+
 int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
                        int32_t* tile_count, cudaStream_t stream);
 
@@ -163,6 +169,6 @@ int launch_balance_update(const int32_t* idx, int64_t n, int E, int64_t* hist, f
 
 // c[t] = bf16(sum over kept j of w[t,j] ypool[slot_of[t,j]]); w == nullptr: weights 1.
 int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
-                   int L, uint16_t* c, cudaStream_t stream);
+                   int L, uint16_t* c, int64_t rows, cudaStream_t stream);
 
 }  // namespace moe

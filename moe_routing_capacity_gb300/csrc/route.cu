@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
         e = idx[a];
         row = send_row[a];
         if (g.ragged && row >= 0) row = blk_off[row >> 32] + (row & 0xffffffffll);
+        if (row >= 0 && !moe_check(row < g.pool_rows, 1001)) row = -1;
         int32_t so = -1;
         uint8_t dr = 1;
         if (row >= 0 && e >= 0 && e < g.E) {
@@ -387,7 +388,10 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
             if (r < g.c_recv) {
                 const int64_t at = g.ragged ? static_cast<int64_t>(eoff[e]) + r
                                             : static_cast<int64_t>(e) * g.c_recv + r;
-                expert_rows[at] = static_cast<int32_t>(row);
+                if (moe_check(at >= 0 && at < (g.ragged ? g.T * g.k
+                                                        : static_cast<int64_t>(g.E) * g.c_recv),
+                              1002))
+                    expert_rows[at] = static_cast<int32_t>(row);
                 so = static_cast<int32_t>(row);
                 dr = 0;
             } else {
@@ -685,7 +689,8 @@ template <int CH>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ ypool,
                                                       const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ w, int64_t T,
-                                                      int k, int L, uint16_t* __restrict__ c) {
+                                                      int k, int L, uint16_t* __restrict__ c,
+                                                      int64_t rows) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -694,6 +699,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     if (lane < k) {
         my_row = slot_of[t * k + lane];
         my_w = w ? w[t * k + lane] : 1.0f;   // no weights: plain sum (gradient return)
+        if (!moe_check(my_row < rows, 1003)) my_row = -1;
     }
     const int nchunk = L / 8;
     uint4* dst = reinterpret_cast<uint4*>(c + t * L);
@@ -734,14 +740,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     }
 }
 
+int check_status_route() { return moe_check_read_reset(); }
+
 int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
-                   int L, uint16_t* c, cudaStream_t st) {
+                   int L, uint16_t* c, int64_t rows, cudaStream_t st) {
     if (T == 0) return MOE_OK;
     const unsigned grid = static_cast<unsigned>((T + 7) / 8);
     if (L / 8 <= 32 * 4)
-        combine_kernel<4><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c);
+        combine_kernel<4><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c, rows);
     else
-        combine_kernel<6><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c);
+        combine_kernel<6><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c, rows);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "combine");
     return MOE_OK;

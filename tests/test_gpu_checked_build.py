@@ -1,0 +1,58 @@
+"""The checked build (-DMOE_CHECK=1: every row, slot, expert and tile index a
+kernel computes is verified before use, failures recorded in a device word
+and the access skipped) on the layer's forward and backward, capped and
+dropless: no check fires, and the results equal the normal build's bit for
+bit.  This stands in for a memory checker, which is not available here."""
+import os
+
+import pytest
+import torch
+
+from moe_routing_capacity_gb300 import abi, build
+from moe_routing_capacity_gb300 import workloads as wl
+from moe_routing_capacity_gb300.layer import PooledWaveMoE
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def checked_lib():
+    if not os.path.exists(build.CHECK_LIB):
+        build.build_checked()
+    return abi.load_library(build.CHECK_LIB)
+
+
+def _run(cfg, dropless, lib=None):
+    saved = abi._lib
+    if lib is not None:
+        abi._lib = lib
+    try:
+        inp = wl.make_inputs(cfg, "cuda")
+        m = PooledWaveMoE(cfg, inp, "cuda", dropless=dropless)
+        x = inp["x"]
+        m.forward(x)
+        g = torch.Generator(device="cuda").manual_seed(5)
+        dout = torch.randn(cfg.T, cfg.d_model, generator=g, device="cuda").to(torch.bfloat16)
+        grads = m.backward(x, dout)
+        torch.cuda.synchronize()
+        code = abi.lib().moe_check_status()
+        assert int(m.status.item()) == 0
+        out = {"out": m.out.clone(), "slot_of": m.slot_of.clone(), "drop": m.drop.clone()}
+        out.update({"d" + k: v.clone() for k, v in grads.items()})
+        return out, code
+    finally:
+        abi._lib = saved
+
+
+@pytest.mark.parametrize("name,dropless", [("tiny", False), ("tiny", True),
+                                           ("mid", False), ("mid", True)])
+def test_checked_build_clean_and_identical(checked_lib, name, dropless):
+    cfg = wl.CONFIGS[name]
+    want, code0 = _run(cfg, dropless)
+    assert code0 == 0                      # the normal build never records anything
+    got, code = _run(cfg, dropless, checked_lib)
+    assert code == 0, f"index check site {code} fired"
+    for key, v in want.items():
+        a = v.contiguous().view(torch.uint8)
+        b = got[key].contiguous().view(torch.uint8)
+        assert torch.equal(a, b), key
