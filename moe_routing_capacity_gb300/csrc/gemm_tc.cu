@@ -69,11 +69,11 @@ struct TileCfg {
     static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
     static constexpr int TMEM_COLS = (BN <= 256) ? 2 * BN : 512;
     static constexpr int BAR_BYTES = 256;
-    // fp32 output: each epilogue warp stages a 32 x 32 block in shared memory
-    // so that the global stores run along rows (full 128-byte lines)
-    static constexpr int STG_BYTES = (EPI == EPI_F32) ? 4 * 32 * 32 * 4 : 0;
+    // fp32 output: each epilogue warp stages 32 x 32 blocks in shared memory
+    // (two, so one can be written while the other is being stored)
+    static constexpr int STG_BYTES = (EPI == EPI_F32) ? 2 * 4 * 32 * 32 * 4 : 0;
     static constexpr int SMEM_BYTES =
-        1024 + A_STAGES * A_STAGE_BYTES + B_STAGES * B_STAGE_BYTES + BAR_BYTES + STG_BYTES;
+        1024 + A_STAGES * A_STAGE_BYTES + B_STAGES * B_STAGE_BYTES + STG_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -81,6 +81,8 @@ struct KParams {
     CUtensorMap mapA[4];
     CUtensorMap mapB[4];
     CUtensorMap mapBup;
+    CUtensorMap omap;       // fp32 output, box 32 x 32, 128-byte swizzle
+    int omap_rank;          // 2 (dense), 3 (per-group), or 0: plain stores
     int nseg;
     int seg_kb[5];          // k-block prefix over segments
     long long M;
@@ -180,7 +182,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     uint8_t* sbase = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sA = sbase;
     uint8_t* sB = sbase + AST * A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + BST * C::B_STAGE_BYTES);
+    uint8_t* sStg = sB + BST * C::B_STAGE_BYTES;   // 1024-aligned fp32 staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + C::STG_BYTES);
     uint64_t* fullA = bars;
     uint64_t* emptyA = fullA + AST;
     uint64_t* fullB = emptyA + AST;
@@ -486,6 +489,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         const int r_local = q * 32 + lane;
         const int ntiles = num_tiles<AMODE>(p);
         uint32_t acc = 0, acc_phase = 0;
+        uint32_t nstore = 0;   // fp32 tile stores this warp committed (lane 0)
         // the pair's accumulator-free barrier lives in the even CTA
         const uint32_t tempty_c0 = CG2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u;
         for (int tile = cta0; tile < ntiles; tile += ncta) {
@@ -554,13 +558,58 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             } else if (EPI == EPI_F32) {
                 // a group with an empty K range contributes a zero tile
                 const bool zero_tile = p.kgoff && tile_kblocks(p, g, 0) == 0;
+                if (p.omap_rank) {
+                    // Lane i holds row 32q + i.  Each 32 x 32 block is written
+                    // to shared memory in the 128-byte-swizzled layout of the
+                    // output map (16-byte chunk v of row i at chunk v ^ (i % 8):
+                    // conflict-free) and stored by one TMA tile store; two
+                    // buffers per warp let the next block be written while
+                    // the previous one is still being read out.
+                    const int row0 = m0 + q * 32;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tl + c * 32, r);
+                        const int col0 = nb * BN + c * 32;
+                        float4* buf = reinterpret_cast<float4*>(sStg) + (q * 2 + (nstore & 1)) * 256;
+                        if (lane == 0 && nstore >= 2) bulk_wait_read1();
+                        __syncwarp();
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 f = make_float4(__uint_as_float(r[4 * v]),
+                                                   __uint_as_float(r[4 * v + 1]),
+                                                   __uint_as_float(r[4 * v + 2]),
+                                                   __uint_as_float(r[4 * v + 3]));
+                            if (zero_tile) f = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (p.bias) {
+                                const int cc = col0 + 4 * v;
+                                if (cc + 0 < p.N) f.x += p.bias[cc + 0];
+                                if (cc + 1 < p.N) f.y += p.bias[cc + 1];
+                                if (cc + 2 < p.N) f.z += p.bias[cc + 2];
+                                if (cc + 3 < p.N) f.w += p.bias[cc + 3];
+                            }
+                            buf[lane * 8 + (v ^ (lane & 7))] = f;
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (col0 < p.N && row0 < p.M) {   // warp-uniform
+                            if (lane == 0) {
+                                if (p.omap_rank == 3)
+                                    tma_store_3d(&p.omap, smem_u32(buf), col0, row0, g);
+                                else
+                                    tma_store_2d(&p.omap, smem_u32(buf), col0, row0);
+                                bulk_commit();
+                            }
+                            ++nstore;   // every lane: the buffer choice stays uniform
+                        }
+                    }
+                } else {
                 // Lane i holds row 32q + i.  Each 32-column block goes through
                 // shared memory (16-byte chunks XOR-swizzled by row, so both
                 // the row-wise writes and the column-wise reads are free of
                 // bank conflicts); then lane l stores columns 4(l%8)..+3 of
                 // rows 4j + l/8: one warp store covers four whole rows.
-                float4* stg = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(bars) +
-                                                        C::BAR_BYTES) + q * 256;
+                float4* stg = reinterpret_cast<float4*>(sStg) + q * 256;
                 float* out = reinterpret_cast<float*>(p.out);
                 const int rsub = lane >> 3, csub = lane & 7;
                 long long rbase[8];
@@ -609,6 +658,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                         }
                     }
                     __syncwarp();
+                }
                 }
             } else if (EPI == EPI_SWIGLU_BWD) {
                 // recomputed g (columns 0..BN/2) and u (BN/2..BN) of hidden units
@@ -709,6 +759,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (EPI == EPI_F32 && lane == 0) bulk_wait_all();   // the last tile stores land
     } else if (AMODE == A_GATHER && warp >= 8) {
         // ------------------------------------------------------------ row gather (A)
         // Thread t copies 16-byte chunk c = t % 8 of tile rows t/8 + 16 i,
@@ -885,6 +936,21 @@ static int launch_traced(const KParams& p, int grid, cudaStream_t st, const char
 
 int check_status_gemm() { return moe_check_read_reset(); }
 
+// fp32 output map, box 32 x 32 with the 128-byte swizzle (rank 2: [rows, cols]
+// with row pitch ld; rank 3: groups of rows, gstride apart).
+static int map_f32(CUtensorMap* m, const void* base, int rank, uint64_t cols, uint64_t rows,
+                   uint64_t groups, uint64_t ld, uint64_t gstride) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return MOE_ECUDA;
+    cuuint64_t gdim[3] = {cols, rows, groups};
+    cuuint64_t gstr[2] = {ld * 4, gstride * 4};
+    cuuint32_t box[3] = {32, 32, 1}, est[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(base), gdim, gstr,
+                     box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
+}
+
 int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
@@ -988,6 +1054,14 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.tile_count = d.tile_count;
     p.rowmap = d.rowmap;
     p.counts = d.counts;
+    // fp32 tile stores by TMA for the dense products (measured: ~3 % faster on
+    // the backward's dense weight gradients); the per-expert weight gradients
+    // (short K, write-bound) stay on the warps' own stores, which measured
+    // ~4 % faster there
+    if (d.epi == EPI_F32 && d.a_mode == A_DENSE && d.ldo % 4 == 0 &&
+        (reinterpret_cast<uintptr_t>(d.out) & 15) == 0) {
+        if (map_f32(&p.omap, d.out, 2, d.N, d.M, 1, d.ldo, 0) == MOE_OK) p.omap_rank = 2;
+    }
     p.goff = d.goff;
     p.rmoff = d.rmoff;
     p.kgoff = d.kgoff;
