@@ -298,6 +298,11 @@ def run_gb300(args, rank, world, local_rank):
     # tokens whose k-th and (k+1)-th (or two adjacent selected) logits are within
     # the near-tie gap: their routing may legitimately differ from the oracle's
     near_ties = int((m.tie != 0).sum().item())
+    # MMA rows the expert GEMMs compute: each expert's rows padded to whole
+    # 128-row tiles (the padding is work the tensor cores do but the
+    # algorithmic flop count leaves out)
+    cnt = m.expert_count.to(torch.int64)
+    tile_rows = int((((cnt + 127) // 128) * 128).sum().item())
 
     # ---- timed region: device-resident inputs
     if world > 1:
@@ -362,6 +367,9 @@ def run_gb300(args, rank, world, local_rank):
                 "unit": "TFLOP/s" if tbound == "tensor" else "GB/s",
                 "frac": round(ach / peak, 4), "traffic": traffic,
                 "peak_source": pk["source"] + (" sustained bf16" if tbound == "tensor" else " HBM copy")}
+        if top.startswith("gemm_expert") and tile_rows:
+            roof["tile_rows"] = tile_rows
+            roof["row_util"] = round(st["kept"] / tile_rows, 4)   # kept rows / MMA rows
     else:
         roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None,
                 "unit": None, "frac": None, "traffic": traffic}
