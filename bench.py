@@ -54,6 +54,12 @@ def parse():
                     help="skip timing forward + backward (one training step of the layer)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the skewed-routing and long-context lines")
+    ap.add_argument("--pipeline", default="shared", choices=["none", "waves", "shared"],
+                    help="how the dispatch's pool fill is scheduled: a kernel of its own "
+                         "(none), wave by wave inside the expert gate/up launch (waves), or "
+                         "inside the shared experts' gate/up launch (shared)")
+    ap.add_argument("--no-pipelines", action="store_true",
+                    help="skip timing the three pool-fill schedules side by side")
     return ap.parse_args()
 
 
@@ -87,8 +93,11 @@ def source_hash(kernel="gemm"):
     return h.hexdigest()[:16]
 
 
-def kernel_work(name, cfg, plan, st):
-    """Algorithmic work of one launch: (amount, unit, bound)."""
+def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None):
+    """Algorithmic work of one launch: (amount, unit, bound).  The pack
+    kernel's bytes depend on where the pool fill runs: all of it (none),
+    wave 0's rows (waves: sent_w0 sender-kept rows), or only the decisions
+    (shared); copies done inside a GEMM launch are not added to its flops."""
     T, d, L, E, k = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.top_k
     H, Hs, ns = cfg.h_expert, cfg.h_shared, cfg.n_shared
     kept = st["kept"]
@@ -108,7 +117,9 @@ def kernel_work(name, cfg, plan, st):
         "router_topk": T * E * 4 + T * k * 8 + T,
         # each token's z row read once, every sender-kept row written with its tag,
         # plus the per-assignment decisions
-        "dispatch_pack": T * L * 2 + sent * (2 * L + 16) + T * k * (4 + 8 + 4 + 4 + 1) + kept * 4,
+        "dispatch_pack": (T * L * 2 + sent * (2 * L + 16) if pipeline == "none" else
+                          T * L * 2 + sent_w0 * (2 * L + 16) if pipeline == "waves" else 0)
+                         + T * k * (4 + 8 + 4 + 4 + 1) + kept * 4,
         "dispatch_init": plan.pool_rows * 16 + E * plan.c_recv * 4,
         # every kept expert row read once, c written once, slots and weights read
         "combine": kept * L * 2 + T * L * 2 + T * k * 8,
@@ -286,7 +297,8 @@ def run_gb300(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     inp = wl.make_inputs(cfg, dev)
-    m = PooledWaveMoE(cfg, inp, dev)
+    pipeline = args.pipeline
+    m = PooledWaveMoE(cfg, inp, dev, pipeline=None if pipeline == "none" else pipeline)
     x = inp["x"]
     stream = torch.cuda.current_stream(dev)
 
@@ -303,6 +315,11 @@ def run_gb300(args, rank, world, local_rank):
     # algorithmic flop count leaves out)
     cnt = m.expert_count.to(torch.int64)
     tile_rows = int((((cnt + 127) // 128) * 128).sum().item())
+    # sender-kept rows of wave 0 (what the pack kernel copies when the later
+    # waves are filled inside the expert gate/up launch)
+    e_w = cfg.n_experts // cfg.n_ranks // cfg.n_waves
+    wave = (m.idx.long() % (cfg.n_experts // cfg.n_ranks)) // e_w
+    sent_w0 = int(((m.drop != 1) & (wave == 0)).sum().item())
 
     # ---- timed region: device-resident inputs
     if world > 1:
@@ -339,7 +356,7 @@ def run_gb300(args, rank, world, local_rank):
     pk = peaks()
     kernels = {}
     for name, (ms, n) in sorted(per.items(), key=lambda kv: -kv[1][0]):
-        work, unit, bound = kernel_work(name, cfg, m.plan, st)
+        work, unit, bound = kernel_work(name, cfg, m.plan, st, pipeline, sent_w0)
         ms_l = ms / n
         e = {"ms_per_launch": round(ms_l, 4), "launches": n,
              "share": round(ms / max(1e-9, sum(v[0] for v in per.values())), 4)}
@@ -350,7 +367,7 @@ def run_gb300(args, rank, world, local_rank):
                       "frac": round(ach / (peak if unit == "TFLOP" else peak), 4)})
         kernels[name] = e
     top = next(iter(kernels))
-    twork, tunit, tbound = kernel_work(top, cfg, m.plan, st)
+    twork, tunit, tbound = kernel_work(top, cfg, m.plan, st, pipeline, sent_w0)
     # DRAM bytes per launch from the committed ncu record, where it was taken
     # on this workload under the current sources of that kernel
     tp = os.path.join(ROOT, "profiles", "traffic.json")
@@ -432,6 +449,45 @@ def run_gb300(args, rank, world, local_rank):
     except RuntimeError as exc:   # report, do not hide: the line says why
         graph = {"unavailable": str(exc).splitlines()[0][:200]}
 
+    # ---- the three pool-fill schedules side by side on the same batch
+    # (rounds in rotated order, median of the rounds per schedule)
+    pipes = None
+    if not args.no_pipelines:
+        arms = {pipeline: m}
+        for pn in ("none", "waves", "shared"):
+            if pn not in arms:
+                arms[pn] = PooledWaveMoE(cfg, inp, dev, pipeline=None if pn == "none" else pn)
+                for _ in range(args.warmup):
+                    arms[pn].forward(x)
+        torch.cuda.synchronize()
+        names = ["none", "waves", "shared"]
+        n_p = max(3, min(args.steps, 30))
+        per_arm = {pn: [] for pn in names}
+        for r in range(7):
+            for j in range(3):
+                pn = names[(r + j) % 3]
+                q0 = torch.cuda.Event(enable_timing=True)
+                q1 = torch.cuda.Event(enable_timing=True)
+                q0.record(stream)
+                for _ in range(n_p):
+                    arms[pn].forward(x)
+                q1.record(stream)
+                torch.cuda.synchronize()
+                per_arm[pn].append(q0.elapsed_time(q1) / n_p)
+        for pn in names:
+            assert int(arms[pn].status.item()) == 0
+        same = all(torch.equal(arms[pn].out.view(torch.int16), m.out.view(torch.int16))
+                   for pn in names)
+        pipes = {pn: {"ms_per_step": round(sorted(v)[3], 4),
+                      "value": world * cfg.T / (sorted(v)[3] / 1e3)} for pn, v in per_arm.items()}
+        pipes["steps_per_round"] = n_p
+        pipes["rounds"] = 7
+        pipes["outputs_bit_identical"] = same
+        for pn in names:
+            if arms[pn] is not m:
+                del arms[pn]
+        torch.cuda.empty_cache()
+
     # ---- the dropless ragged variant on the same batch: the cost of removing drops
     dropless = None
     if not args.no_dropless:
@@ -471,7 +527,7 @@ def run_gb300(args, rank, world, local_rank):
         for oname in ("skew", "long"):
             ocfg = wl.CONFIGS[oname]
             oinp = wl.make_inputs(ocfg, dev)
-            mo = PooledWaveMoE(ocfg, oinp, dev)
+            mo = PooledWaveMoE(ocfg, oinp, dev, pipeline=None if pipeline == "none" else pipeline)
             ox = oinp["x"]
             for _ in range(3):
                 mo.forward(ox)
@@ -555,6 +611,7 @@ def run_gb300(args, rank, world, local_rank):
                        f"top-{cfg.top_k}, {cfg.n_waves} waves, {cfg.n_shared} shared (Hs={cfg.h_shared}), "
                        f"H={cfg.h_expert}, cf {cfg.cf_send}/{cfg.cf_recv}",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "pool_fill": pipeline,
                        "l2": "inputs larger than L2 (8.1 GB weights per step)"},
             "drops": {"near_tie_tokens": near_ties,
                       "kept": st["kept"], "dropped_send": st["dropped_send"],
@@ -562,7 +619,7 @@ def run_gb300(args, rank, world, local_rank):
                       "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
             "gpu_launches": sum(v[1] for v in per.values()),
             "roofline": roof, "kernels": kernels, "clocks": clk, "e2e": e2e,
-            "graph_replay": graph, "dropless": dropless, "train_step": train,
+            "graph_replay": graph, "pipelines": pipes, "dropless": dropless, "train_step": train,
             "workloads": others,
             "cpu_baseline": cpu,
         }

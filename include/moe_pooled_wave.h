@@ -264,6 +264,48 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
                            void* ws, size_t ws_bytes, uint16_t* ypool, int32_t* status,
                            void* stream);
 
+/* Wave-pipelined dispatch and experts (lamjinlab zh-HK section 二: the
+ * waves let the exchange of one wave overlap the computation of another).
+ * Same arguments, outputs and errors as moe_dispatch_pooled(cfg, z, idx, ws,
+ * ws_bytes, pool, slot_of, drop, expert_rows, expert_count, stats, stream)
+ * followed by moe_expert_ffn_grouped(cfg, pool, expert_rows, expert_count,
+ * Wg, Wu, Wd, ffn_ws, ffn_ws_bytes, ypool, status, stream), and the same
+ * results bit for bit.  The dispatch makes every sender and receiver
+ * decision but writes only wave 0's payload rows; the gate/up launch, one
+ * CTA per SM launched cooperatively, copies the rows of waves 1..W-1 into
+ * the pool with four extra warps per CTA while its tensor cores work
+ * through wave 0's experts, and a later wave's expert tiles start once
+ * every CTA has copied that wave (per-wave counters in ws; the wait is
+ * bounded, and on expiry status receives MOE_ETIMEOUT).  With W = 1, no
+ * tokens or c_recv = 0 it is exactly the two calls.  ws must not be shared
+ * with other work in flight. */
+int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                              void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
+                              uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
+                              moe_drop_stats_t* stats, const uint16_t* Wg, const uint16_t* Wu,
+                              const uint16_t* Wd, void* ffn_ws, size_t ffn_ws_bytes,
+                              uint16_t* ypool, int32_t* status, void* stream);
+
+/* Dispatch overlapped with the shared experts.  The shared experts see every
+ * token and do not depend on the routing (lamjinlab zh-HK section 四: a dense
+ * backbone beside the routed experts), so the exchange can proceed while
+ * they compute.  Same arguments, outputs and errors as moe_dispatch_pooled,
+ * plus the shared experts' activations
+ *   a = bf16(silu(x Wsg_s^T) * (x Wsu_s^T)), [T, n_s*Hs] (as moe_combine)
+ *   x [T, d]  Wsg, Wsu [n_s, Hs, d]  status: device status word
+ * and the same results bit for bit as moe_dispatch_pooled followed by
+ * moe_combine's shared step.  The dispatch makes every decision and writes
+ * the empty tags; the payload rows and tags of the kept assignments are
+ * copied by four extra warps per CTA of the shared gate/up launch.  Pass
+ * Wsg = Wsu = NULL to moe_combine afterwards so that it uses this a.  With
+ * n_s = 0 or no tokens it is moe_dispatch_pooled. */
+int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                                void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
+                                uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
+                                moe_drop_stats_t* stats, const uint16_t* x, const uint16_t* Wsg,
+                                const uint16_t* Wsu, uint16_t* a, int32_t* status,
+                                void* stream);
+
 /* Return path, weighted combine, up-projection and shared experts:
  *   c[t]   = bf16(sum over kept j, in j order, of w[t,j] * ypool[slot_of[t,j]])
  *   a      = bf16(silu(x Wsg_s^T) * (x Wsu_s^T)) for each shared expert s,
@@ -273,7 +315,9 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
  * the shared experts see every token (lamjinlab zh-HK sections 二 and 四).
  *   ypool [pool_rows, L]  slot_of [T, k]  w [T, k] fp32  W_lu [d, L]  x [T, d]
  *   Wsg, Wsu [n_s, Hs, d]  Wsd [n_s, d, Hs]
- *   c [T, L] bf16 (out)  a [T, n_s*Hs] bf16 (out)  out [T, d] bf16 (out) */
+ *   c [T, L] bf16 (out)  a [T, n_s*Hs] bf16 (out)  out [T, d] bf16 (out)
+ * Wsg = Wsu = NULL (n_s > 0): a is an input holding the shared activations
+ * (from moe_dispatch_shared_overlap) and x may be NULL. */
 int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* slot_of,
                 const float* w, const uint16_t* W_lu, const uint16_t* x,
                 const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,

@@ -21,7 +21,8 @@ MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2,
 # Every entry point the header declares (checked by the tests).
 EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project", "moe_matmul",
            "moe_dispatch_pooled",
-           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_balance_update",
+           "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_dispatch_expert_waves",
+           "moe_dispatch_shared_overlap", "moe_balance_update",
            "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged",
            "moe_backward_plan", "moe_layer_backward", "moe_backward_plan_ragged",
            "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
@@ -251,6 +252,32 @@ def expert_ffn_grouped(cfg, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ypo
         _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32), _stream(stream)))
 
 
+def dispatch_expert_waves(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
+                          Wg, Wu, Wd, ffn_ws, ypool, status, stream=None):
+    """dispatch_pooled then expert_ffn_grouped, with the later waves' pool rows
+    copied inside the gate/up launch while wave 0's experts compute."""
+    _check("moe_dispatch_expert_waves", lib().moe_dispatch_expert_waves(
+        ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
+        ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
+        _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(stats, torch.int64),
+        _ptr(Wg, bf16), _ptr(Wu, bf16), _ptr(Wd, bf16), _ptr(ffn_ws, u8), ffn_ws.numel(),
+        _ptr(ypool, bf16), _ptr(status, i32), _stream(stream)))
+
+
+def dispatch_shared_overlap(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count,
+                            stats, x, Wsg, Wsu, a, status, stream=None):
+    """dispatch_pooled plus the shared experts' activations a, the pool rows
+    copied while the shared gate/up product computes; then call combine with
+    Wsg = Wsu = None."""
+    _check("moe_dispatch_shared_overlap", lib().moe_dispatch_shared_overlap(
+        ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
+        ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
+        _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(stats, torch.int64),
+        _ptr(x, bf16, allow_none=True), _ptr(Wsg, bf16, allow_none=True),
+        _ptr(Wsu, bf16, allow_none=True), _ptr(a, bf16, allow_none=True), _ptr(status, i32),
+        _stream(stream)))
+
+
 def dispatch_ragged(cfg, z, idx, ws, pool, slot_of, drop, expert_offsets, expert_rows,
                     expert_count, stats, stream=None):
     _check("moe_dispatch_ragged", lib().moe_dispatch_ragged(
@@ -278,7 +305,8 @@ def balance_update(cfg, idx, hist, alpha, bias, stream=None):
 def combine(cfg, ypool, slot_of, w, W_lu, x, Wsg, Wsu, Wsd, c, a, out, status, stream=None):
     _check("moe_combine", lib().moe_combine(
         ctypes.byref(make_config(cfg)), _ptr(ypool, bf16), _ptr(slot_of, i32), _ptr(w, f32),
-        _ptr(W_lu, bf16), _ptr(x, bf16), _ptr(Wsg, bf16), _ptr(Wsu, bf16), _ptr(Wsd, bf16),
+        _ptr(W_lu, bf16), _ptr(x, bf16, allow_none=True), _ptr(Wsg, bf16, allow_none=True),
+        _ptr(Wsu, bf16, allow_none=True), _ptr(Wsd, bf16, allow_none=True),
         _ptr(c, bf16), _ptr(a, bf16, allow_none=True), _ptr(out, bf16), _ptr(status, i32),
         _stream(stream)))
 

@@ -529,29 +529,32 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
     return gemm_launch(d2, st);
 }
 
-int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
-                           const int32_t* expert_rows, const int32_t* expert_count,
-                           const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, void* ws,
-                           size_t ws_bytes, uint16_t* ypool, int32_t* status, void* stream) {
-    MOE_NVTX_RANGE();
-    Geom G;
-    int rc = make_geom(cfg, &G);
-    if (rc) return rc;
-    if (G.g.pool_rows == 0 || G.g.c_recv == 0) return MOE_OK;
-    if (!pool || !expert_rows || !expert_count || !Wg || !Wu || !Wd || !ws || !ypool || !status)
-        return MOE_EINVAL;
-    if (!aligned16(pool) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) ||
-        !aligned16(ypool) || !aligned16(ws))
-        return MOE_EINVAL;
-    if (ws_bytes < static_cast<size_t>(G.plan.ws_ffn_bytes)) return MOE_ENOSPC;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+// The capped layout's expert FFN: gate/up with the rows gathered from the
+// pool, then the down-projection scattered back to the rows.  wp (optional):
+// the wave pipeline's copy of waves 1.. into the pool inside the gate/up launch.
+struct WavePipe {
+    int32_t* ready;
+    const uint16_t* z;
+    const int32_t* idx;
+    const int64_t* send_row;
+};
+
+static int expert_ffn_capped(const Geom& G, uint16_t* pool, const int32_t* expert_rows,
+                             const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                             const uint16_t* Wd, void* ws, uint16_t* ypool, int32_t* status,
+                             cudaStream_t st, const WavePipe* wp) {
+    int rc;
     const DispatchGeom& g = G.g;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     int32_t* tiles = reinterpret_cast<int32_t*>(wsb);
     const int max_mt = g.E * ((g.c_recv + 127) / 128);
     int32_t* tile_count = reinterpret_cast<int32_t*>(wsb + static_cast<size_t>(max_mt) * 8);
     uint16_t* h = reinterpret_cast<uint16_t*>(wsb + G.plan.h_offset_bytes);
-    if ((rc = launch_build_tiles(expert_count, g.E, 128, tiles, tile_count, st))) return rc;
+    // the pipeline takes the tiles wave by wave, so that every CTA works on
+    // wave 0 while the later waves' rows are being copied
+    if ((rc = launch_build_tiles(expert_count, g.E, 128, tiles, tile_count, st, wp ? g.E_l : 0,
+                                 wp ? g.E_w : 0)))
+        return rc;
 
     const int L = g.L, H = G.H;
     GemmDesc d1;
@@ -581,6 +584,22 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
     d1.out_gstride = static_cast<int64_t>(g.c_recv) * H;
     d1.status = status;
     d1.name = "gemm_expert_gateup";
+    if (wp) {
+        d1.wp_ready = wp->ready;
+        d1.wp_pool = pool;
+        d1.wp_z = wp->z;
+        d1.wp_idx = wp->idx;
+        d1.wp_send_row = wp->send_row;
+        d1.wp_T = g.T;
+        d1.wp_k = g.k;
+        d1.wp_E = g.E;
+        d1.wp_El = g.E_l;
+        d1.wp_Ew = g.E_w;
+        d1.wp_W = g.W;
+        d1.wp_L = L;
+        d1.wp_pitch = pool_pitch(L);
+        d1.wp_rows = g.pool_rows;
+    }
     if ((rc = gemm_launch(d1, st))) return rc;
 
     GemmDesc d2;
@@ -608,6 +627,142 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
     d2.name = "gemm_expert_down";
     d2.gather_rows = g.pool_rows;   // the scatter's destination rows
     return gemm_launch(d2, st);
+}
+
+static int check_ffn_args(const Geom& G, const uint16_t* pool, const int32_t* expert_rows,
+                          const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                          const uint16_t* Wd, const void* ws, size_t ws_bytes,
+                          const uint16_t* ypool, const int32_t* status) {
+    if (!pool || !expert_rows || !expert_count || !Wg || !Wu || !Wd || !ws || !ypool || !status)
+        return MOE_EINVAL;
+    if (!aligned16(pool) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) ||
+        !aligned16(ypool) || !aligned16(ws))
+        return MOE_EINVAL;
+    if (ws_bytes < static_cast<size_t>(G.plan.ws_ffn_bytes)) return MOE_ENOSPC;
+    return MOE_OK;
+}
+
+int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
+                           const int32_t* expert_rows, const int32_t* expert_count,
+                           const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, void* ws,
+                           size_t ws_bytes, uint16_t* ypool, int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    if (G.g.pool_rows == 0 || G.g.c_recv == 0) return MOE_OK;
+    if ((rc = check_ffn_args(G, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ws_bytes, ypool,
+                             status)))
+        return rc;
+    return expert_ffn_capped(G, const_cast<uint16_t*>(pool), expert_rows, expert_count, Wg, Wu,
+                             Wd, ws, ypool, status, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                              void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
+                              uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
+                              moe_drop_stats_t* stats, const uint16_t* Wg, const uint16_t* Wu,
+                              const uint16_t* Wd, void* ffn_ws, size_t ffn_ws_bytes,
+                              uint16_t* ypool, int32_t* status, void* stream) {
+    MOE_NVTX_RANGE();
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    const DispatchGeom& g = G.g;
+    if (!stats || !expert_count || (g.T > 0 && (!z || !idx || !slot_of || !drop)) ||
+        (g.pool_rows > 0 && !pool) || (G.plan.c_recv > 0 && !expert_rows) ||
+        (G.plan.ws_dispatch_bytes > 0 && !ws))
+        return MOE_EINVAL;
+    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || (ws && !aligned16(ws)))
+        return MOE_EINVAL;
+    if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
+    const bool ffn = g.pool_rows > 0 && g.c_recv > 0;
+    if (ffn && (rc = check_ffn_args(G, pool, expert_rows, expert_count, Wg, Wu, Wd, ffn_ws,
+                                    ffn_ws_bytes, ypool, status)))
+        return rc;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // with one wave, no rows or no expert rows there is nothing to overlap:
+    // the dispatch fills every wave and the expert FFN runs as usual
+    const bool pipe = ffn && g.T > 0 && g.W > 1;
+    if ((rc = launch_dispatch(g, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
+                              st, pipe ? 0 : -1)))
+        return rc;
+    if (!ffn) return MOE_OK;
+    const DispatchWs L = dispatch_ws_layout(g);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    WavePipe wp{reinterpret_cast<int32_t*>(w + L.wave_ready_off), z, idx,
+                reinterpret_cast<const int64_t*>(w + L.send_row_off)};
+    return expert_ffn_capped(G, pool, expert_rows, expert_count, Wg, Wu, Wd, ffn_ws, ypool,
+                             status, st, pipe ? &wp : nullptr);
+}
+
+int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
+                                void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
+                                uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
+                                moe_drop_stats_t* stats, const uint16_t* x, const uint16_t* Wsg,
+                                const uint16_t* Wsu, uint16_t* a, int32_t* status,
+                                void* stream) {
+    MOE_NVTX_RANGE();
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    const DispatchGeom& g = G.g;
+    if (!stats || !expert_count || !status || (g.T > 0 && (!z || !idx || !slot_of || !drop)) ||
+        (g.pool_rows > 0 && !pool) || (G.plan.c_recv > 0 && !expert_rows) ||
+        (G.plan.ws_dispatch_bytes > 0 && !ws))
+        return MOE_EINVAL;
+    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || (ws && !aligned16(ws)))
+        return MOE_EINVAL;
+    if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
+    const int d = G.d, hs_all = G.ns * G.Hs;
+    if (G.ns > 0 && g.T > 0 &&
+        (!x || !Wsg || !Wsu || !a || !aligned16(x) || !aligned16(Wsg) || !aligned16(Wsu) ||
+         !aligned16(a)))
+        return MOE_EINVAL;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // without shared experts there is nothing to overlap the copies with
+    const bool overlap = G.ns > 0 && g.T > 0 && g.pool_rows > 0;
+    if ((rc = launch_dispatch(g, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
+                              st, overlap ? -2 : -1)))
+        return rc;
+    if (G.ns == 0 || g.T == 0) return MOE_OK;
+    const DispatchWs Lw = dispatch_ws_layout(g);
+    GemmDesc s1;
+    std::memset(&s1, 0, sizeof(s1));
+    s1.a_mode = A_DENSE;
+    s1.epi = EPI_SWIGLU;
+    s1.bn = 256;
+    s1.M = g.T;
+    s1.N = hs_all;
+    s1.nseg = 1;
+    s1.seg[0] = GemmSeg{x, d, Wsg, d, d};
+    s1.B_up = Wsu;
+    s1.b_rows = hs_all;
+    s1.out = a;
+    s1.ldo = hs_all;
+    s1.status = status;
+    s1.name = "gemm_shared_gateup";
+    if (overlap) {
+        s1.wp_pool = pool;
+        s1.wp_z = z;
+        s1.wp_idx = idx;
+        s1.wp_send_row = reinterpret_cast<const int64_t*>(static_cast<uint8_t*>(ws) +
+                                                          Lw.send_row_off);
+        s1.wp_T = g.T;
+        s1.wp_k = g.k;
+        s1.wp_E = g.E;
+        s1.wp_El = g.E_l;
+        s1.wp_Ew = g.E_w;
+        s1.wp_W = g.W;
+        s1.wp_L = g.L;
+        s1.wp_pitch = pool_pitch(g.L);
+        s1.wp_rows = g.pool_rows;
+    }
+    return gemm_launch(s1, st);
 }
 
 int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,
@@ -706,18 +861,21 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
     if (g.T == 0) return MOE_OK;
     if (!slot_of || !w || !W_lu || !c || !out || !status || (g.pool_rows > 0 && !ypool))
         return MOE_EINVAL;
-    if (G.ns > 0 && (!x || !Wsg || !Wsu || !Wsd || !a)) return MOE_EINVAL;
+    // Wsg = Wsu = NULL: a already holds the shared activations (computed
+    // beside the dispatch by moe_dispatch_shared_overlap)
+    const bool a_ready = G.ns > 0 && !Wsg && !Wsu;
+    if (G.ns > 0 && (!Wsd || !a || (!a_ready && (!x || !Wsg || !Wsu)))) return MOE_EINVAL;
     if ((ypool && !aligned16(ypool)) || !aligned16(W_lu) || !aligned16(c) || !aligned16(out))
         return MOE_EINVAL;
-    if (G.ns > 0 && (!aligned16(x) || !aligned16(Wsg) || !aligned16(Wsu) || !aligned16(Wsd) ||
-                     !aligned16(a)))
+    if (G.ns > 0 && (!aligned16(Wsd) || !aligned16(a) ||
+                     (!a_ready && (!aligned16(x) || !aligned16(Wsg) || !aligned16(Wsu)))))
         return MOE_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = launch_combine(ypool, slot_of, w, g.T, g.k, g.L, c, g.pool_rows, st))) return rc;
 
     const int d = G.d, Hs = G.Hs, ns = G.ns;
     const int hs_all = ns * Hs;
-    if (ns > 0) {
+    if (ns > 0 && !a_ready) {
         GemmDesc s1;
         std::memset(&s1, 0, sizeof(s1));
         s1.a_mode = A_DENSE;

@@ -114,6 +114,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// ------------------------------------------------------------------ grid counters
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *ctr >= target (another CTA's release: fence + atomic add),
+// with the same limits as mbar_wait.  Only for counters that CTAs of the
+// same cooperative launch advance: they are all resident, so the wait ends.
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, volatile int* abort_flag,
+                                           int32_t* status, uint64_t limit_ns = kWaitTimeoutNs) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(200);
+        if (ld_acquire_gpu(ctr) >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            report_error(status, MOE_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Barrier over `count` threads (whole warps) of the CTA, id 1..15.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

@@ -17,7 +17,10 @@
 // warps 8-11 copy the tile's 128 rows (indices from the expert's row list)
 // with cp.async, eight threads per 128-byte row segment so every global
 // access is a full, coalesced line.  Two TMEM accumulators let the epilogue
-// of tile i overlap the main loop of tile i+1.
+// of tile i overlap the main loop of tile i+1.  In the wave-pipelined
+// dispatch, warps 12-15 of the gathered-A kernel copy the payload rows of
+// waves 1.. into the pool while the tiles of wave 0 compute; the row gather
+// of a later wave's tile first waits for every CTA's copies of that wave.
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -112,7 +115,94 @@ struct KParams {
     long long ldo2;
     const uint16_t* aux;
     int uniform_groups;
+    // wave pipeline (gathered A): warps 12-15 fill the pool rows of waves
+    // 1..wp_W-1 while the tiles of earlier waves compute
+    int* wp_ready;
+    uint16_t* wp_pool;
+    const uint16_t* wp_z;
+    const int32_t* wp_idx;
+    const long long* wp_send_row;
+    long long wp_T;
+    int wp_k, wp_E, wp_El, wp_Ew, wp_W;
+    int wp_L;               // latent width: payload values of a pool row
+    long long wp_pitch;     // elements between pool rows
+    long long wp_rows;      // pool rows (checks)
 };
+
+// The pool fill of the dispatch run by extra warps of a GEMM launch: the
+// latent rows of the sender-kept assignments of wave w (every wave if w < 0)
+// copied into their pool rows, plus each row's tag.  One warp a token,
+// tokens dealt out over the grid's copy warps (cw of ncw in this CTA): lane
+// j holds assignment (t, j); the token's latent row is read once in 16-byte
+// chunks and written to each of its kept rows.
+// pace (optional): token i of this warp's n is copied once the CTA has
+// started i * tiles / (n + 1) of its tiles (pace[0]: tiles started, pace[1]:
+// this CTA's tile count), spreading the copy over the product.
+__device__ __forceinline__ void copy_pool_rows(const KParams& p, int w, int cw, int ncw, int lane,
+                                               const volatile int* pace = nullptr,
+                                               const volatile int* abort_flag = nullptr) {
+    const long long nwarps = static_cast<long long>(ncw) * gridDim.x;
+    const int L = p.wp_L;
+    const int nchunk = L / 8;
+    const long long pitch = p.wp_pitch;
+    const long long first = static_cast<long long>(ncw) * blockIdx.x + cw;
+    const long long ntok = first < p.wp_T ? (p.wp_T - first + nwarps - 1) / nwarps : 0;
+    long long i = 0;
+    for (long long t = first; t < p.wp_T; t += nwarps, ++i) {
+#ifndef MOE_COPY_NOPACE
+        if (pace) {
+            const long long need = i * pace[1] / (ntok + 1);
+            if (pace[0] <= need) {
+                const uint64_t t0 = globaltimer_ns();
+                while (pace[0] <= need && !*abort_flag &&
+                       globaltimer_ns() - t0 < kWaitTimeoutNs)
+                    __nanosleep(1000);
+            }
+        }
+#endif
+        long long row = -1;
+        int e = -1;
+        if (lane < p.wp_k) {
+            const long long a = t * p.wp_k + lane;
+            e = p.wp_idx[a];
+            row = p.wp_send_row[a];
+            if (row >= 0 && !(e >= 0 && e < p.wp_E && (w < 0 || (e % p.wp_El) / p.wp_Ew == w)))
+                row = -1;
+            if (row >= 0 && !moe_check(row < p.wp_rows, 1001)) row = -1;
+        }
+        if (!__any_sync(0xffffffffu, row >= 0)) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(p.wp_z + t * L);
+        for (int cb = 0; cb < nchunk; cb += 32 * 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int ch = cb + lane + 32 * c;
+#ifndef MOE_COPY_NOHINT
+                if (ch < nchunk) v[c] = __ldcs(src + ch);   // streaming: keep the product's
+#else                                                       // tiles in L2
+                if (ch < nchunk) v[c] = __ldg(src + ch);
+#endif
+            }
+            for (int j = 0; j < p.wp_k; ++j) {
+                const long long rj = __shfl_sync(0xffffffffu, row, j);
+                if (rj < 0) continue;
+                uint4* dst = reinterpret_cast<uint4*>(p.wp_pool + rj * pitch);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int ch = cb + lane + 32 * c;
+#ifndef MOE_COPY_NOHINT
+                    if (ch < nchunk) __stcs(dst + ch, v[c]);
+#else
+                    if (ch < nchunk) dst[ch] = v[c];
+#endif
+                }
+            }
+        }
+        if (lane < p.wp_k && row >= 0)
+            *reinterpret_cast<int4*>(p.wp_pool + row * pitch + L) =
+                make_int4(e, static_cast<int>(t), lane, 0);
+    }
+}
 
 template <int AMODE>
 __device__ __forceinline__ int num_tiles(const KParams& p) {
@@ -162,7 +252,7 @@ __device__ __forceinline__ int tile_kblocks(const KParams& p, int g, int kb_tota
 // and done barriers of both CTAs; both CTAs' epilogues arrive on the even
 // CTA's accumulator-free barriers.
 template <int BN, int AMODE, int EPI, int MAJ, bool CG2>
-__global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
+__global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
     gemm_tc_kernel(const __grid_constant__ KParams p) {
     using C = TileCfg<BN, AMODE, EPI, CG2>;
     static_assert(!CG2 || (AMODE == A_DENSE && BN == 256 &&
@@ -193,6 +283,12 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
     uint64_t* done = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // wave pipeline: the wave of the tiles this CTA's row gather has reached
+    // (W once it has no more), which paces the copies of the later waves
+    volatile int* gather_wave = abort_flag + 1;
+    // dense products carrying the pool fill: tiles this CTA's producer has
+    // started, and this CTA's tile count (the copy's pace)
+    volatile int* tiles_pace = gather_wave + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -217,6 +313,12 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         }
         mbar_init(done, 1);
         *abort_flag = 0;
+        *gather_wave = 0;
+        tiles_pace[0] = 0;
+        {
+            const int nt = num_tiles<AMODE>(p);
+            tiles_pace[1] = nt > cta0 ? (nt - cta0 + ncta - 1) / ncta : 0;
+        }
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -248,7 +350,9 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
             uint32_t armedA = 0, parA = 0, armedB = 0, parB = 0;   // for unwinding
             bool ok = true;
+            int started = 0;
             for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
+                tiles_pace[0] = ++started;
                 int g, m0, nb;
                 decode_tile<AMODE>(p, tile, g, m0, nb);
                 if (CG2) m0 = 2 * m0 + static_cast<int>(crank) * BM;
@@ -380,6 +484,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                     }
                 }
             }
+            tiles_pace[0] = 1 << 30;   // no more tiles: the copy may finish
             if (!ok || *abort_flag) {
                 // Unwinding: let every armed TMA load land before the CTA exits.
                 volatile int no_abort = 0;
@@ -760,7 +865,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
             }
         }
         if (EPI == EPI_F32 && lane == 0) bulk_wait_all();   // the last tile stores land
-    } else if (AMODE == A_GATHER && warp >= 8) {
+    } else if (AMODE == A_GATHER && warp >= 8 && warp < 12) {
         // ------------------------------------------------------------ row gather (A)
         // Thread t copies 16-byte chunk c = t % 8 of tile rows t/8 + 16 i,
         // i = 0..7: a warp instruction moves four whole 128-byte row segments.
@@ -778,10 +883,12 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         int it = 0;
         bool ok = true;
         int nxt_row[8];
-        int nxt_cnt = 0;
+        int nxt_cnt = 0, nxt_g = 0;
+        uint32_t waves_seen = 1u;   // wave 0's rows were written before this launch
         auto fetch_rows = [&](int tile) {
             int g, m0, nb;
             decode_tile<AMODE>(p, tile, g, m0, nb);
+            nxt_g = g;
             nxt_cnt = p.counts[g] - m0;   // valid rows of the tile, from its first
             const int* rl = p.rowmap + m0 + rowmap_base(p, g);
 #pragma unroll
@@ -793,6 +900,18 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
         };
         if (cta0 < ntiles) fetch_rows(cta0);
         for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
+            if (p.wp_ready) {   // the tile's wave: its pool rows filled by every CTA
+                const int wv = (nxt_g % p.wp_El) / p.wp_Ew;
+                if (!(waves_seen >> wv & 1u)) {
+                    if (t == 0) *gather_wave = wv;   // lets this CTA copy wave wv + 1
+                    if (!wait_count(p.wp_ready + wv, static_cast<int>(gridDim.x), abort_flag,
+                                    p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    waves_seen |= 1u << wv;
+                }
+            }
             const uint16_t* src[8];
             uint32_t valid = 0;
 #pragma unroll
@@ -828,9 +947,43 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 384 : 256, 1)
                 }
             }
         }
+        if (t == 0) *gather_wave = 1 << 30;   // no more tiles: copy what is left
         cp_async_wait<0>();
         fence_proxy_async_smem();
         for (int i = (it > LAG ? it - LAG : 0); i < it; ++i) mbar_arrive(&fullA[i % AST]);
+    } else if (AMODE == A_GATHER && warp >= 12 && p.wp_ready) {
+        // ------------------------------------------------------------ pool fill, waves 1..
+        // Wave by wave; after wave w the CTA's four copy warps meet and one
+        // thread releases the CTA's count in wp_ready[w].  Wave w >= 2 is
+        // copied once this CTA's row gather has reached wave w-1, so that
+        // the extra memory traffic spreads over the compute of the earlier
+        // waves instead of piling onto wave 0's (a bounded wait: on expiry
+        // the copy goes ahead).
+        const int cw = warp - 12;
+        for (int w = 1; w < p.wp_W; ++w) {
+            if (w >= 2 && *gather_wave < w - 1) {
+                const uint64_t t0 = globaltimer_ns();
+                while (*gather_wave < w - 1 && !*abort_flag) {
+                    __nanosleep(500);
+                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                        report_error(p.status, MOE_ETIMEOUT);
+                        break;
+                    }
+                }
+            }
+            copy_pool_rows(p, w, cw, 4, lane);
+            named_bar_sync(1, 128);
+            if (cw == 0 && lane == 0) {
+                __threadfence();
+                atomicAdd(p.wp_ready + w, 1);
+            }
+        }
+    } else if (AMODE != A_GATHER && warp >= 8 && p.wp_pool) {
+        // ------------------------------------------------------------ pool fill, every wave
+        // The dispatch's copies overlapped with this product (the shared
+        // experts' gate/up, which does not depend on the routing); nothing
+        // in this launch reads the pool, the next launch on the stream does.
+        copy_pool_rows(p, -1, warp - 8, 4, lane, tiles_pace, abort_flag);
     }
 
     tc_fence_before();
@@ -910,7 +1063,7 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(256, 1, 1);
+        cfg.blockDim = dim3(p.wp_pool ? 384 : 256, 1, 1);   // + 4 copy warps
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -921,8 +1074,22 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
+    } else if (AMODE == A_GATHER && p.wp_ready) {
+        // the copy warps' counters are waited on by every CTA: all resident
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(512, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
     } else {
-        kern<<<grid, AMODE == A_GATHER ? 384 : 256, C::SMEM_BYTES, st>>>(p);
+        kern<<<grid, AMODE == A_GATHER ? 512 : (p.wp_pool ? 384 : 256), C::SMEM_BYTES, st>>>(p);
     }
     return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
@@ -1080,6 +1247,34 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.aux = static_cast<const uint16_t*>(d.aux);
     p.uniform_groups = d.uniform_groups;
     if (d.epi == EPI_SWIGLU_BWD) p.out2 = d.out2;
+    if (d.wp_pool) {   // the dispatch's pool fill rides along (waves pipeline or dense overlap)
+        if (!d.wp_z || !d.wp_idx || !d.wp_send_row || d.wp_k < 1 || d.wp_k > 32 ||
+            d.wp_W < 1 || d.wp_W > 32 || d.wp_Ew < 1 || d.wp_El != d.wp_Ew * d.wp_W ||
+            d.wp_E % d.wp_El || d.wp_L < 8 || d.wp_L % 8 || d.wp_pitch < d.wp_L + 8 ||
+            d.wp_pitch % 8 || (reinterpret_cast<uintptr_t>(d.wp_z) & 15) ||
+            (reinterpret_cast<uintptr_t>(d.wp_pool) & 15))
+            return MOE_EINVAL;
+        if (d.wp_ready && (d.a_mode != A_GATHER || d.nseg != 1 || d.wp_pool != d.gather_src ||
+                           d.wp_L != d.seg[0].K || d.wp_pitch != d.gather_pitch))
+            return MOE_EINVAL;
+        if (!d.wp_ready && d.a_mode == A_GATHER) return MOE_EINVAL;
+        p.wp_ready = d.wp_ready;
+        p.wp_pool = d.wp_pool;
+        p.wp_z = d.wp_z;
+        p.wp_idx = d.wp_idx;
+        p.wp_send_row = reinterpret_cast<const long long*>(d.wp_send_row);
+        p.wp_T = d.wp_T;
+        p.wp_k = d.wp_k;
+        p.wp_E = d.wp_E;
+        p.wp_El = d.wp_El;
+        p.wp_Ew = d.wp_Ew;
+        p.wp_W = d.wp_W;
+        p.wp_L = d.wp_L;
+        p.wp_pitch = d.wp_pitch;
+        p.wp_rows = d.wp_rows;
+    } else if (d.wp_ready) {
+        return MOE_EINVAL;
+    }
 
     int tiles = (d.a_mode == A_DENSE) ? p.m_tiles * p.n_tiles_n
                 : d.uniform_groups     ? d.uniform_groups * p.m_tiles * p.n_tiles_n
@@ -1087,6 +1282,7 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     if (tiles <= 0) return MOE_OK;
     int grid = tiles < sms ? tiles : sms;
     if (cg2) grid = 2 * (tiles < sms / 2 ? tiles : sms / 2);
+    if (p.wp_ready) grid = sms;   // every SM copies its share of the later waves
 
     if ((d.a_mn || d.b_mn) && (d.bn != 256 || d.epi == EPI_SPLIT)) return MOE_EINVAL;
     const int maj = (d.a_mn ? 1 : 0) | (d.b_mn ? 2 : 0);

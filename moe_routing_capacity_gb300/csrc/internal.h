@@ -105,6 +105,23 @@ struct GemmDesc {
     void* out2;
     int64_t ldo2;
     int b2_rows;            // rows of the second B (B_up)
+    // pool fill riding along a GEMM launch.  Wave pipeline (gathered A): the
+    // launch also copies the payload rows and tags of waves 1..wp_W-1 into
+    // the pool (gather_src) while it computes;
+    // the row gather of a wave-w tile waits until every CTA has counted wave
+    // w in wp_ready[w] (a cooperative launch of one CTA per SM)
+    int32_t* wp_ready;      // [W] counters, zero at launch; null: no pipeline
+    uint16_t* wp_pool;      // the pool (same memory as gather_src)
+    const uint16_t* wp_z;   // [T, L] latent rows
+    const int32_t* wp_idx;  // [T, k] expert ids
+    const int64_t* wp_send_row;   // [T, k] pool row of each sender-kept assignment, else -1
+    int64_t wp_T;
+    int wp_k, wp_E, wp_El, wp_Ew, wp_W;
+    int wp_L;               // latent width (payload values of a pool row)
+    int64_t wp_pitch;       // elements between pool rows
+    int64_t wp_rows;        // pool rows
+    // (wp_pool without wp_ready, dense products only: every wave's rows are
+    // copied by extra warps of the launch, which nothing in it waits for)
 };
 
 int gemm_launch(const GemmDesc& d, cudaStream_t stream);
@@ -131,13 +148,18 @@ struct DispatchGeom {
 // Scratch layout of moe_dispatch_pooled (and of the ragged dispatch, which
 // adds the block offsets).
 struct DispatchWs {
-    size_t send_row_off, rloc_off, cnt_se_off, base_se_off, demand_off, blk_off_off, total;
+    size_t send_row_off, rloc_off, cnt_se_off, base_se_off, demand_off, blk_off_off,
+        wave_ready_off, total;
 };
 DispatchWs dispatch_ws_layout(const DispatchGeom& g);
 
+// copy_wave >= 0: every decision is made, but only the payload rows (and
+// tags) of that wave are written; copy_wave < -1: none are (the overlapped
+// paths fill them from a GEMM launch); -1: all.
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
-                    int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream);
+                    int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream,
+                    int copy_wave = -1);
 
 int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                            uint16_t* pool, int32_t* slot_of, uint8_t* drop,
@@ -151,8 +173,11 @@ int check_status_route();
 int check_status_gemm();
 int check_status_backward();
 
+// wave_El > 0: wave-major entry order (wave_El local experts a destination,
+// wave_Ew a wave); else expert order.
 int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
-                       int32_t* tile_count, cudaStream_t stream);
+                       int32_t* tile_count, cudaStream_t stream, int wave_El = 0,
+                       int wave_Ew = 0);
 
 // Backward pass: scratch layout (byte offsets) and launch sequence.
 struct BackwardWs {

@@ -137,17 +137,20 @@ DispatchWs dispatch_ws_layout(const DispatchGeom& g) {
     w.demand_off = o;    o = align256(o + static_cast<size_t>(g.S) * g.D * g.W * sizeof(int32_t));
     w.blk_off_off = o;
     if (g.ragged) o = align256(o + (static_cast<size_t>(g.S) * g.D * g.W + 1) * sizeof(int32_t));
+    w.wave_ready_off = o; o = align256(o + static_cast<size_t>(g.W) * sizeof(int32_t));
     w.total = o;
     return w;
 }
 
-// Reset the stats, write the empty tag into every pool row and -1 into the
-// expert row lists.
+// Reset the stats and the per-wave copy counters, write the empty tag into
+// every pool row and -1 into the expert row lists.
 __global__ void dispatch_init_kernel(DispatchGeom g, uint16_t* __restrict__ pool,
                                      int32_t* __restrict__ expert_rows,
-                                     moe_drop_stats_t* __restrict__ stats) {
+                                     moe_drop_stats_t* __restrict__ stats,
+                                     int32_t* __restrict__ wave_ready) {
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (tid < g.W) wave_ready[tid] = 0;
     if (tid == 0) {
         stats->assignments = g.T * g.k;
         stats->kept = 0;
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
     const int64_t* __restrict__ send_row, const int32_t* __restrict__ rloc,
     const int32_t* __restrict__ base_se, uint16_t* __restrict__ pool,
     int32_t* __restrict__ slot_of, uint8_t* __restrict__ drop, int32_t* __restrict__ expert_rows,
-    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ eoff) {
+    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ eoff, int copy_wave) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= g.T) return;
@@ -400,6 +403,10 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
         }
         slot_of[a] = so;
         drop[a] = dr;
+        // overlapped dispatch: only this wave's rows (copy_wave >= 0) or none
+        // (copy_wave < -1) are filled here, the rest by warps of a GEMM launch
+        if (copy_wave < -1 || (copy_wave >= 0 && row >= 0 && (e % g.E_l) / g.E_w != copy_wave))
+            row = -1;
     }
     const int nchunk = g.L / 8;
     const uint4* src = reinterpret_cast<const uint4*>(z + t * g.L);
@@ -428,7 +435,8 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
 
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
-                    int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t st) {
+                    int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t st,
+                    int copy_wave) {
     const DispatchWs L = dispatch_ws_layout(g);
     uint8_t* w = static_cast<uint8_t*>(ws);
     int64_t* send_row = reinterpret_cast<int64_t*>(w + L.send_row_off);
@@ -436,8 +444,9 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
     int32_t* cnt_se = reinterpret_cast<int32_t*>(w + L.cnt_se_off);
     int32_t* base_se = reinterpret_cast<int32_t*>(w + L.base_se_off);
     int32_t* demand = reinterpret_cast<int32_t*>(w + L.demand_off);
+    int32_t* wave_ready = reinterpret_cast<int32_t*>(w + L.wave_ready_off);
 
-    dispatch_init_kernel<<<1024, 256, 0, st>>>(g, pool, expert_rows, stats);
+    dispatch_init_kernel<<<1024, 256, 0, st>>>(g, pool, expert_rows, stats, wave_ready);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_init");
     // per-warp counters plus running totals: (SEND_WARPS + 1) x (D*W + E) ints;
@@ -463,11 +472,11 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
     if (nchunk <= 32 * 4)
         dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                        slot_of, drop, expert_rows, nullptr,
-                                                       nullptr);
+                                                       nullptr, copy_wave);
     else
         dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                         slot_of, drop, expert_rows, nullptr,
-                                                        nullptr);
+                                                        nullptr, copy_wave);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_pack");
     return MOE_OK;
@@ -539,8 +548,9 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
     int32_t* base_se = reinterpret_cast<int32_t*>(w + L.base_se_off);
     int32_t* demand = reinterpret_cast<int32_t*>(w + L.demand_off);
     int32_t* blk_off = reinterpret_cast<int32_t*>(w + L.blk_off_off);
+    int32_t* wave_ready = reinterpret_cast<int32_t*>(w + L.wave_ready_off);
 
-    dispatch_init_kernel<<<1, 32, 0, st>>>(g, pool, expert_rows, stats);
+    dispatch_init_kernel<<<1, 32, 0, st>>>(g, pool, expert_rows, stats, wave_ready);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_init");
     const size_t shm =
@@ -566,11 +576,11 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
     if (g.L / 8 <= 32 * 4)
         dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                        slot_of, drop, expert_rows, blk_off,
-                                                       expert_offsets);
+                                                       expert_offsets, -1);
     else
         dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                         slot_of, drop, expert_rows, blk_off,
-                                                        expert_offsets);
+                                                        expert_offsets, -1);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_pack");
     return MOE_OK;
@@ -580,17 +590,26 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
 
 // One CTA: per expert ceil(count/bm) row tiles, exclusive prefix over
 // experts, entries {e, m0} in expert order.
+// wave_El > 0: entries in wave-major order, i.e. the experts of wave 0 on
+// every destination (destination by destination), then those of wave 1, ...
+// (wave_El local experts a destination, wave_Ew of them a wave).
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ counts,
                                                            int E, int bm,
                                                            int2* __restrict__ tiles,
-                                                           int32_t* __restrict__ tile_count) {
+                                                           int32_t* __restrict__ tile_count,
+                                                           int wave_El, int wave_Ew) {
     __shared__ int warp_sum[32];
     __shared__ int carry;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int per_wave = wave_El > 0 ? (E / wave_El) * wave_Ew : E;   // experts a wave
     for (int e0 = 0; e0 < E; e0 += blockDim.x) {
-        const int e = e0 + threadIdx.x;
+        int e = e0 + threadIdx.x;   // position in the list order
+        if (wave_El > 0 && e < E) {
+            const int wv = e / per_wave, rem = e - wv * per_wave;
+            e = (rem / wave_Ew) * wave_El + wv * wave_Ew + rem % wave_Ew;
+        }
         const int mt = e < E ? (counts[e] + bm - 1) / bm : 0;
         int incl = mt;
         for (int off = 1; off < 32; off <<= 1) {
@@ -618,9 +637,10 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
 }
 
 int launch_build_tiles(const int32_t* counts, int E, int bm, int32_t* tile_list,
-                       int32_t* tile_count, cudaStream_t st) {
+                       int32_t* tile_count, cudaStream_t st, int wave_El, int wave_Ew) {
+    if (wave_El > 0 && (wave_Ew <= 0 || wave_El % wave_Ew || E % wave_El)) return MOE_EINVAL;
     build_tiles_kernel<<<1, 1024, 0, st>>>(counts, E, bm, reinterpret_cast<int2*>(tile_list),
-                                           tile_count);
+                                           tile_count, wave_El, wave_Ew);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "build_tiles");
     return MOE_OK;

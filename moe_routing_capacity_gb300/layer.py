@@ -6,6 +6,12 @@ once through PyTorch's caching allocator) and runs the layer as
     moe_route_project (= moe_router_topk + moe_latent_proj in one pass over x)
         -> moe_dispatch_pooled -> moe_expert_ffn_grouped -> moe_combine
 
+(``pipeline="waves"``: the middle two are the single wave-pipelined call
+moe_dispatch_expert_waves; ``pipeline="shared"``: moe_dispatch_shared_overlap
+copies the pool rows while the shared experts' gate/up runs, then
+moe_expert_ffn_grouped and moe_combine with the shared activations given;
+same results either way)
+
 on one CUDA stream, with no host synchronisation, so the whole forward can be
 captured in a CUDA graph.  Intermediates stay readable as attributes.
 """
@@ -20,12 +26,23 @@ class PooledWaveMoE:
     """``balance_alpha``: if set, after each batch's routing the
     quantile-balancing bias is recomputed from the running selection
     histogram (``self.hist``) into the router bias, so it applies from the
-    next batch on."""
+    next batch on.  ``pipeline``: None (the calls one after another),
+    "waves" (dispatch and experts as one wave-pipelined call: the later
+    waves' pool rows copied while wave 0's experts run) or "shared" (the
+    pool rows copied while the shared experts' gate/up runs); the capped
+    layout only."""
+
+    PIPELINES = (None, "waves", "shared")
 
     def __init__(self, cfg, weights: dict, device="cuda", balance_alpha=None,
-                 dropless=False):
+                 dropless=False, pipeline=None):
         self.cfg = cfg
         self.dropless = dropless
+        if pipeline not in self.PIPELINES:
+            raise ValueError(f"pipeline must be one of {self.PIPELINES}")
+        if pipeline and dropless:
+            raise ValueError("the overlapped dispatch is built for the capped layout")
+        self.pipeline = pipeline
         self.plan = abi.plan_ragged(cfg) if dropless else abi.plan(cfg)
         self.device = torch.device(device)
         dev = self.device
@@ -109,9 +126,25 @@ class PooledWaveMoE:
         if self.balance_alpha is not None:
             abi.balance_update(self.cfg, self.idx, self.hist, self.balance_alpha,
                                self.w["bias"], stream)
-        self.dispatch(stream)
-        self.experts(stream)
-        self.combine(x, out, stream)
+        if self.pipeline == "waves":
+            abi.dispatch_expert_waves(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
+                                      self.slot_of, self.drop, self.expert_rows,
+                                      self.expert_count, self.stats, self.w["Wg"], self.w["Wu"],
+                                      self.w["Wd"], self.ws_ffn, self.ypool, self.status, stream)
+            self.combine(x, out, stream)
+        elif self.pipeline == "shared" and self.cfg.n_shared:
+            abi.dispatch_shared_overlap(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
+                                        self.slot_of, self.drop, self.expert_rows,
+                                        self.expert_count, self.stats, x, self.w["Wsg"],
+                                        self.w["Wsu"], self.a, self.status, stream)
+            self.experts(stream)
+            abi.combine(self.cfg, self.ypool, self.slot_of, self.gate_w, self.w["W_lu"], None,
+                        None, None, self.w["Wsd"], self.c, self.a,
+                        self.out if out is None else out, self.status, stream)
+        else:
+            self.dispatch(stream)
+            self.experts(stream)
+            self.combine(x, out, stream)
         return self.out if out is None else out
 
     def capture(self, x, out=None):

@@ -29,8 +29,8 @@ def _host_inputs(inp):
     return {k: (v.float().cpu().numpy() if v is not None else None) for k, v in inp.items()}
 
 
-def run_gpu(cfg, inp):
-    m = PooledWaveMoE(cfg, inp, "cuda")
+def run_gpu(cfg, inp, **layer_kw):
+    m = PooledWaveMoE(cfg, inp, "cuda", **layer_kw)
     x = inp["x"].cuda()
     m.forward(x)
     torch.cuda.synchronize()
@@ -40,12 +40,12 @@ def run_gpu(cfg, inp):
     return m
 
 
-def compare_full(cfg, inp, report=None):
+def compare_full(cfg, inp, report=None, **layer_kw):
     """Element-by-element comparison of every stage (sizes the oracle
-    finishes in seconds)."""
+    finishes in seconds); layer_kw selects a variant of the GPU layer."""
     report = {} if report is None else report
     ref = O.layer(cfg, _host_inputs(inp))
-    m = run_gpu(cfg, inp)
+    m = run_gpu(cfg, inp, **layer_kw)
     p = ref["plan"]
     # router
     lg = _np(m.logits)
