@@ -369,12 +369,14 @@ def run_gb300(args, rank, world, local_rank):
     top = next(iter(kernels))
     twork, tunit, tbound = kernel_work(top, cfg, m.plan, st, pipeline, sent_w0)
     # DRAM bytes per launch from the committed ncu record, where it was taken
-    # on this workload under the current sources of that kernel
+    # on this workload and pool-fill schedule under the current sources of
+    # that kernel
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     recs = json.load(open(tp)) if os.path.exists(tp) else {}
     for name, e in kernels.items():
         rec = recs.get(name)
-        if rec and rec.get("source_hash") == source_hash(name) and rec.get("workload") == cfg.name:
+        if (rec and rec.get("source_hash") == source_hash(name) and rec.get("workload") == cfg.name
+                and rec.get("pool_fill", "none") == pipeline):
             e["traffic"] = rec.get("dram_bytes_per_launch")
     traffic = kernels[top].get("traffic")
     if twork is not None:

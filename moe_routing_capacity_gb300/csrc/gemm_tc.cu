@@ -125,6 +125,7 @@ struct KParams {
     long long wp_T;
     int wp_k, wp_E, wp_El, wp_Ew, wp_W;
     int wp_L;               // latent width: payload values of a pool row
+    int raster_gn;          // dense tiles: column blocks a band (0: row tile by row tile)
     long long wp_pitch;     // elements between pool rows
     long long wp_rows;      // pool rows (checks)
 };
@@ -217,7 +218,27 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
     nb = tile - entry * p.n_tiles_n;
     if (AMODE == A_DENSE) {
         g = 0;
-        m0 = entry * BM;
+        int m = entry;
+        if (p.raster_gn > 0) {
+            // bands of raster_gn column blocks: every row tile crosses one band
+            // before the next band starts, so the band's B stays in L2 while
+            // A streams (A is read once a band instead of B once a row tile)
+            const int gn = p.raster_gn;
+            const int full = (p.n_tiles_n / gn) * gn * p.m_tiles;   // tiles in whole bands
+            int band, r, width;
+            if (tile < full) {
+                band = tile / (gn * p.m_tiles);
+                r = tile - band * gn * p.m_tiles;
+                width = gn;
+            } else {
+                band = p.n_tiles_n / gn;
+                r = tile - full;
+                width = p.n_tiles_n - band * gn;
+            }
+            m = r / width;
+            nb = band * gn + (r - m * width);
+        }
+        m0 = m * BM;
     } else if (p.uniform_groups) {
         g = entry / p.m_tiles;
         m0 = (entry - g * p.m_tiles) * BM;
@@ -1217,6 +1238,22 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     }
     const int bm_tile = cg2 ? 2 * BM : BM;
     p.m_tiles = static_cast<int>((d.M + bm_tile - 1) / bm_tile);
+#ifndef MOE_RASTER_MB
+#define MOE_RASTER_MB 48
+#endif
+    // dense products whose whole B does not fit comfortably in L2 walk the
+    // tiles in bands of column blocks whose B spans about MOE_RASTER_MB
+    if (d.a_mode == A_DENSE && MOE_RASTER_MB > 0 && p.n_tiles_n > 1) {
+        long long ktot = 0;
+        for (int s = 0; s < d.nseg; ++s) ktot += d.seg[s].K;
+        const long long bblk = static_cast<long long>(d.bn) * ktot * 2;   // B bytes a column block
+        long long gn = (static_cast<long long>(MOE_RASTER_MB) << 20) / (bblk > 0 ? bblk : 1);
+        if (gn < 1) gn = 1;
+        if (gn < p.n_tiles_n) {
+            const long long nb_ = (p.n_tiles_n + gn - 1) / gn;   // bands, then even widths
+            p.raster_gn = static_cast<int>((p.n_tiles_n + nb_ - 1) / nb_);
+        }
+    }
     p.tile_list = reinterpret_cast<const int2*>(d.tile_list);
     p.tile_count = d.tile_count;
     p.rowmap = d.rowmap;
