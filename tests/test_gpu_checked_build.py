@@ -1,8 +1,10 @@
 """The checked build (-DMOE_CHECK=1: every row, slot, expert and tile index a
 kernel computes is verified before use, failures recorded in a device word
 and the access skipped) on the layer's forward and backward, capped and
-dropless: no check fires, and the results equal the normal build's bit for
-bit.  This stands in for a memory checker, which is not available here."""
+dropless, and on the overlapped pool fills (copy warps inside the shared
+or the expert gate/up launch): no check fires, and the results equal the
+normal build's bit for bit.  This stands in for a memory checker, which is
+not available here."""
 import os
 
 import pytest
@@ -22,13 +24,13 @@ def checked_lib():
     return abi.load_library(build.CHECK_LIB)
 
 
-def _run(cfg, dropless, lib=None):
+def _run(cfg, dropless, lib=None, pipeline=None):
     saved = abi._lib
     if lib is not None:
         abi._lib = lib
     try:
         inp = wl.make_inputs(cfg, "cuda")
-        m = PooledWaveMoE(cfg, inp, "cuda", dropless=dropless)
+        m = PooledWaveMoE(cfg, inp, "cuda", dropless=dropless, pipeline=pipeline)
         x = inp["x"]
         m.forward(x)
         g = torch.Generator(device="cuda").manual_seed(5)
@@ -37,7 +39,8 @@ def _run(cfg, dropless, lib=None):
         torch.cuda.synchronize()
         code = abi.lib().moe_check_status()
         assert int(m.status.item()) == 0
-        out = {"out": m.out.clone(), "slot_of": m.slot_of.clone(), "drop": m.drop.clone()}
+        out = {"out": m.out.clone(), "slot_of": m.slot_of.clone(), "drop": m.drop.clone(),
+               "tags": m.pool_tags().clone()}
         out.update({"d" + k: v.clone() for k, v in grads.items()})
         return out, code
     finally:
@@ -56,3 +59,15 @@ def test_checked_build_clean_and_identical(checked_lib, name, dropless):
         a = v.contiguous().view(torch.uint8)
         b = got[key].contiguous().view(torch.uint8)
         assert torch.equal(a, b), key
+
+
+@pytest.mark.parametrize("pipeline", ["waves", "shared"])
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_checked_build_overlapped_fill(checked_lib, name, pipeline):
+    cfg = wl.CONFIGS[name]
+    want, code0 = _run(cfg, False, pipeline=pipeline)
+    assert code0 == 0
+    got, code = _run(cfg, False, checked_lib, pipeline=pipeline)
+    assert code == 0, f"index check site {code} fired"
+    for key, v in want.items():
+        assert torch.equal(v.contiguous().view(torch.uint8), got[key].contiguous().view(torch.uint8)), key
