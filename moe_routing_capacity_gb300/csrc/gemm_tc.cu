@@ -852,6 +852,17 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
                                                pk[4 * v + 3]);
                     }
+#ifndef MOE_NO_ZERO_PAD
+                    else if (AMODE == A_GATHER && !p.goff && m < p.out_gstride / p.ldo) {
+                        // a padding row of the expert's last tile (inside its
+                        // slab of h): zeros, so the down-projection's padded
+                        // MMAs multiply zeros instead of a stale row
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (col0 + 8 * v < p.N)
+                                *reinterpret_cast<uint4*>(out + col0 + 8 * v) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+#endif
                 }
             } else {   // EPI_BF16 / EPI_SCATTER
                 uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + obase;
