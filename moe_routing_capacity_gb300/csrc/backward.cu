@@ -449,6 +449,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         q.a_gstride = static_cast<int64_t>(cr) * M; q.b_rows = N;
         q.b_gstride = static_cast<int64_t>(cr) * N;
         q.kgoff = poff; q.k_rows = PE;   // ragged: each expert's padded row range
+        if (!rag) q.kcount = a.expert_count;   // capped: only the blocks holding its rows
         q.out = out; q.ldo = N; q.out_gstride = static_cast<int64_t>(M) * N;
         return mm(q, nm);
     };

@@ -100,6 +100,8 @@ struct KParams {
     const int* goff;        // optional per-group first row (ragged groups)
     const int* rmoff;       // optional per-group first row-map entry (else goff)
     const int* kgoff;       // optional per-group K row range (uniform groups)
+    const int* kcount;      // optional per-group rows contracted (uniform groups, 3-D
+                            // operands whose rows past the count are zero)
     int rowmap_ld;
     const uint16_t* gather_src;
     long long gather_pitch;
@@ -261,7 +263,12 @@ __device__ __forceinline__ long long rowmap_base(const KParams& p, int g) {
 // K blocks of a tile of group g: the whole contraction, or the group's own
 // row range of flat MN-major operands.
 __device__ __forceinline__ int tile_kblocks(const KParams& p, int g, int kb_total) {
-    return p.kgoff ? (p.kgoff[g + 1] - p.kgoff[g]) / 64 : kb_total;
+    if (p.kgoff) return (p.kgoff[g + 1] - p.kgoff[g]) / 64;
+    if (p.kcount) {
+        const int kb = (p.kcount[g] + BK - 1) / BK;
+        return kb < kb_total ? kb : kb_total;
+    }
+    return kb_total;
 }
 
 // MAJ bit 0: A is MN-major (stored [K, M], M contiguous); bit 1: B is
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
             bool ok = true;
             for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
                 int kbt = kb_total;
-                if (p.kgoff) {
+                if (p.kgoff || p.kcount) {
                     int g, m0, nb;
                     decode_tile<AMODE>(p, tile, g, m0, nb);
                     kbt = tile_kblocks(p, g, kb_total);
@@ -683,7 +690,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                 }
             } else if (EPI == EPI_F32) {
                 // a group with an empty K range contributes a zero tile
-                const bool zero_tile = p.kgoff && tile_kblocks(p, g, 0) == 0;
+                const bool zero_tile = (p.kgoff || p.kcount) && tile_kblocks(p, g, kb_total) == 0;
                 if (p.omap_rank) {
                     // Lane i holds row 32q + i.  Each 32 x 32 block is written
                     // to shared memory in the 128-byte-swizzled layout of the
@@ -1283,6 +1290,8 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     if (d.kgoff && (!d.uniform_groups || !d.a_mn || !d.b_mn || d.nseg != 1 || d.epi != EPI_F32 ||
                     d.k_rows <= 0))
         return MOE_EINVAL;
+    p.kcount = d.kcount;
+    if (d.kcount && (!d.uniform_groups || d.kgoff || d.a_mode != A_GROUPED)) return MOE_EINVAL;
     p.rowmap_ld = d.rowmap_ld;
     p.gather_src = d.gather_src;
     p.gather_pitch = d.gather_pitch;

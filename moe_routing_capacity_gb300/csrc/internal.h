@@ -99,6 +99,9 @@ struct GemmDesc {
                             // 64) of MN-major operands stored flat; an empty range
                             // writes a zero tile
     int64_t k_rows;         // rows of those flat operands
+    const int32_t* kcount;  // optional [groups] with uniform_groups (3-D grouped operands whose
+                            // rows past each group's count are zero): group g contracts over
+                            // its first ceil(kcount[g] / 64) blocks of 64 rows only
     // EPI_SPLIT: second output (EPI_SWIGLU_BWD: out2 = du, addressed like out)
     int nsplit;             // column tiles of the first output (N = nsplit * bn)
     int N2;                 // columns of the second output
