@@ -19,12 +19,40 @@ namespace moe {
 
 constexpr float kTieEps = 1e-4f;
 
+// Routing order: the larger logit first, the lower expert id on equal logits.
+__device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb) {
+    return va > vb || (va == vb && ea < eb);
+}
+
+// Bitonic sort of one (logit, id) pair per lane across the warp, in routing
+// order (lane 0 first); empty slots are (-inf, INT_MAX) and sort last.
+__device__ __forceinline__ void warp_sort_routing(float& v, int& e, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+            const int oe = __shfl_xor_sync(0xffffffffu, e, stride);
+            // the lower lane of a pair keeps the earlier entry in the blocks
+            // sorted first-to-last (lane & size == 0), the later one otherwise
+            const bool keep_earlier = ((lane & size) == 0) == ((lane & stride) == 0);
+            if (keep_earlier ? ranks_before(ov, oe, v, e) : ranks_before(v, e, ov, oe)) {
+                v = ov;
+                e = oe;
+            }
+        }
+    }
+}
+
 template <int PER>   // logits per lane: E <= 32 * PER
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int64_t T,
                                                    int E, int k, int32_t* __restrict__ idx,
                                                    float* __restrict__ w,
                                                    uint8_t* __restrict__ tie) {
+    __shared__ float cand_v[8][32];
+    __shared__ int cand_e[8][32];
     const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float* row = logits + t * E;
@@ -34,16 +62,68 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
         const int e = lane + 32 * i;
         v[i] = e < E ? __ldg(row + e) : 0.0f;
     }
+
+    float my_v = 0.0f;   // lane j holds the j-th entry in routing order
+    int my_e = 0;
+    float next_v = 0.0f; // the (k+1)-th largest logit
+    const int rounds = k < E ? k + 1 : k;   // entries to rank
+    bool ranked = false;
+    if (rounds <= 32) {
+        // Candidates: the n = rounds largest lane maxima are n distinct
+        // entries, so every entry of the top n ranks at or before the n-th
+        // of them, (tv, te).  Usually few entries do; gathered one per lane
+        // and sorted, they give the top n directly.
+        float lm = -INFINITY;
+        int le = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if (lane + 32 * i < E && (le == INT_MAX || v[i] > lm)) {
+                lm = v[i];
+                le = lane + 32 * i;
+            }
+        warp_sort_routing(lm, le, lane);
+        const float tv = __shfl_sync(0xffffffffu, lm, rounds - 1);
+        const int te = __shfl_sync(0xffffffffu, le, rounds - 1);
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && (v[i] > tv || (v[i] == tv && e <= te))) ++cnt;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total <= 32) {   // warp-uniform
+            int pos = incl - cnt;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && (v[i] > tv || (v[i] == tv && e <= te))) {
+                    cand_v[wib][pos] = v[i];
+                    cand_e[wib][pos] = e;
+                    ++pos;
+                }
+            }
+            __syncwarp();
+            float cv = lane < total ? cand_v[wib][lane] : -INFINITY;
+            int ce = lane < total ? cand_e[wib][lane] : INT_MAX;
+            warp_sort_routing(cv, ce, lane);
+            my_v = cv;
+            my_e = ce;
+            next_v = __shfl_sync(0xffffffffu, cv, k < 31 ? k : 31);
+            ranked = true;
+        }
+    }
+    // otherwise rounds of warp arg-max over the entries still in play
     uint32_t live = 0;   // bit i: entry i still a candidate
 #pragma unroll
     for (int i = 0; i < PER; ++i)
         if (lane + 32 * i < E) live |= 1u << i;
-
-    float my_v = 0.0f;   // lane j keeps round j's winner
-    int my_e = 0;
-    float next_v = 0.0f; // the (k+1)-th largest logit
-    const int rounds = k < E ? k + 1 : k;
-    for (int rd = 0; rd < rounds; ++rd) {
+    for (int rd = 0; !ranked && rd < rounds; ++rd) {
         // best live entry of this lane: largest value, lowest expert id on ties
         float bv = -INFINITY;
         int be = INT_MAX;
