@@ -95,9 +95,11 @@ def source_hash(kernel="gemm"):
 
 def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None):
     """Algorithmic work of one launch: (amount, unit, bound).  The pack
-    kernel's bytes depend on where the pool fill runs: all of it (none),
-    wave 0's rows (waves: sent_w0 sender-kept rows), or only the decisions
-    (shared); copies done inside a GEMM launch are not added to its flops."""
+    kernel's bytes depend on where the pool fill runs: all of it (none) or
+    wave 0's rows (waves: sent_w0 sender-kept rows); with the shared
+    schedule the whole pack runs inside the shared gate/up launch and the
+    pack kernel is not launched.  Pack work done inside a GEMM launch is not
+    added to its flops."""
     T, d, L, E, k = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.top_k
     H, Hs, ns = cfg.h_expert, cfg.h_shared, cfg.n_shared
     kept = st["kept"]

@@ -294,9 +294,10 @@ int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const 
  *   a = bf16(silu(x Wsg_s^T) * (x Wsu_s^T)), [T, n_s*Hs] (as moe_combine)
  *   x [T, d]  Wsg, Wsu [n_s, Hs, d]  status: device status word
  * and the same results bit for bit as moe_dispatch_pooled followed by
- * moe_combine's shared step.  The dispatch makes every decision and writes
- * the empty tags; the payload rows and tags of the kept assignments are
- * copied by four extra warps per CTA of the shared gate/up launch.  Pass
+ * moe_combine's shared step.  The sender stage and the receiver counts run
+ * as kernels of their own; the final decisions (slot_of, drop codes, the
+ * expert row lists) and the pool's payload rows and tags are written by
+ * four extra warps per CTA of the shared gate/up launch.  Pass
  * Wsg = Wsu = NULL to moe_combine afterwards so that it uses this a.  With
  * n_s = 0 or no tokens it is moe_dispatch_pooled. */
 int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,

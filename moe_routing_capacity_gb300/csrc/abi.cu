@@ -534,9 +534,7 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
 // the wave pipeline's copy of waves 1.. into the pool inside the gate/up launch.
 struct WavePipe {
     int32_t* ready;
-    const uint16_t* z;
-    const int32_t* idx;
-    const int64_t* send_row;
+    PackArgs a;
 };
 
 static int expert_ffn_capped(const Geom& G, uint16_t* pool, const int32_t* expert_rows,
@@ -586,19 +584,8 @@ static int expert_ffn_capped(const Geom& G, uint16_t* pool, const int32_t* exper
     d1.name = "gemm_expert_gateup";
     if (wp) {
         d1.wp_ready = wp->ready;
-        d1.wp_pool = pool;
-        d1.wp_z = wp->z;
-        d1.wp_idx = wp->idx;
-        d1.wp_send_row = wp->send_row;
-        d1.wp_T = g.T;
-        d1.wp_k = g.k;
-        d1.wp_E = g.E;
-        d1.wp_El = g.E_l;
-        d1.wp_Ew = g.E_w;
-        d1.wp_W = g.W;
-        d1.wp_L = L;
-        d1.wp_pitch = pool_pitch(L);
-        d1.wp_rows = g.pool_rows;
+        d1.wp_g = g;
+        d1.wp_a = wp->a;
     }
     if ((rc = gemm_launch(d1, st))) return rc;
 
@@ -692,8 +679,13 @@ int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const 
     if (!ffn) return MOE_OK;
     const DispatchWs L = dispatch_ws_layout(g);
     uint8_t* w = static_cast<uint8_t*>(ws);
-    WavePipe wp{reinterpret_cast<int32_t*>(w + L.wave_ready_off), z, idx,
-                reinterpret_cast<const int64_t*>(w + L.send_row_off)};
+    WavePipe wp;
+    std::memset(&wp, 0, sizeof(wp));
+    wp.ready = reinterpret_cast<int32_t*>(w + L.wave_ready_off);
+    wp.a.z = z;
+    wp.a.idx = idx;
+    wp.a.send_row = reinterpret_cast<const int64_t*>(w + L.send_row_off);
+    wp.a.pool = pool;
     return expert_ffn_capped(G, pool, expert_rows, expert_count, Wg, Wu, Wd, ffn_ws, ypool,
                              status, st, pipe ? &wp : nullptr);
 }
@@ -724,10 +716,10 @@ int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, cons
     int dev, sms;
     if ((rc = current_device(&dev, &sms))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // without shared experts there is nothing to overlap the copies with
+    // without shared experts there is nothing to overlap the pack with
     const bool overlap = G.ns > 0 && g.T > 0 && g.pool_rows > 0;
     if ((rc = launch_dispatch(g, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
-                              st, overlap ? -2 : -1)))
+                              st, -1, !overlap)))
         return rc;
     if (G.ns == 0 || g.T == 0) return MOE_OK;
     const DispatchWs Lw = dispatch_ws_layout(g);
@@ -746,21 +738,18 @@ int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, cons
     s1.ldo = hs_all;
     s1.status = status;
     s1.name = "gemm_shared_gateup";
-    if (overlap) {
-        s1.wp_pool = pool;
-        s1.wp_z = z;
-        s1.wp_idx = idx;
-        s1.wp_send_row = reinterpret_cast<const int64_t*>(static_cast<uint8_t*>(ws) +
-                                                          Lw.send_row_off);
-        s1.wp_T = g.T;
-        s1.wp_k = g.k;
-        s1.wp_E = g.E;
-        s1.wp_El = g.E_l;
-        s1.wp_Ew = g.E_w;
-        s1.wp_W = g.W;
-        s1.wp_L = g.L;
-        s1.wp_pitch = pool_pitch(g.L);
-        s1.wp_rows = g.pool_rows;
+    if (overlap) {   // the whole pack: final decisions, row lists, copies, tags
+        uint8_t* w = static_cast<uint8_t*>(ws);
+        s1.wp_g = g;
+        s1.wp_a.z = z;
+        s1.wp_a.idx = idx;
+        s1.wp_a.send_row = reinterpret_cast<const int64_t*>(w + Lw.send_row_off);
+        s1.wp_a.rloc = reinterpret_cast<const int32_t*>(w + Lw.rloc_off);
+        s1.wp_a.base_se = reinterpret_cast<const int32_t*>(w + Lw.base_se_off);
+        s1.wp_a.pool = pool;
+        s1.wp_a.slot_of = slot_of;
+        s1.wp_a.drop = drop;
+        s1.wp_a.expert_rows = expert_rows;
     }
     return gemm_launch(s1, st);
 }

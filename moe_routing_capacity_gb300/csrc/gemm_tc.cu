@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pack.cuh"
 
 namespace moe {
 
@@ -117,93 +118,39 @@ struct KParams {
     long long ldo2;
     const uint16_t* aux;
     int uniform_groups;
-    // wave pipeline (gathered A): warps 12-15 fill the pool rows of waves
-    // 1..wp_W-1 while the tiles of earlier waves compute
+    // pool fill riding along (wp_a.pool non-null): wave pipeline (gathered
+    // A, wp_ready non-null: warps 12-15 copy waves 1..W-1 while the tiles of
+    // earlier waves compute) or the whole pack in a dense product (warps 8-11)
     int* wp_ready;
-    uint16_t* wp_pool;
-    const uint16_t* wp_z;
-    const int32_t* wp_idx;
-    const long long* wp_send_row;
-    long long wp_T;
-    int wp_k, wp_E, wp_El, wp_Ew, wp_W;
-    int wp_L;               // latent width: payload values of a pool row
+    DispatchGeom wp_g;
+    PackArgs wp_a;
     int raster_gn;          // dense tiles: column blocks a band (0: row tile by row tile)
-    long long wp_pitch;     // elements between pool rows
-    long long wp_rows;      // pool rows (checks)
 };
 
-// The pool fill of the dispatch run by extra warps of a GEMM launch: the
-// latent rows of the sender-kept assignments of wave w (every wave if w < 0)
-// copied into their pool rows, plus each row's tag.  One warp a token,
-// tokens dealt out over the grid's copy warps (cw of ncw in this CTA): lane
-// j holds assignment (t, j); the token's latent row is read once in 16-byte
-// chunks and written to each of its kept rows.
-// pace (optional): token i of this warp's n is copied once the CTA has
-// started i * tiles / (n + 1) of its tiles (pace[0]: tiles started, pace[1]:
-// this CTA's tile count), spreading the copy over the product.
-__device__ __forceinline__ void copy_pool_rows(const KParams& p, int w, int cw, int ncw, int lane,
-                                               const volatile int* pace = nullptr,
-                                               const volatile int* abort_flag = nullptr) {
+// The pack run by extra warps of a GEMM launch (pack_token), tokens dealt
+// out over the grid's copy warps (cw of ncw in this CTA): the receiver
+// decisions (decide) and the copies of wave w (every wave if w < 0), with
+// streaming loads and stores so the product's tiles keep their L2 lines.
+// pace (optional): token i of this warp's n goes once the CTA has started
+// i * tiles / (n + 1) of its tiles (pace[0]: tiles started, pace[1]: this
+// CTA's tile count), spreading the copy over the product.
+__device__ __forceinline__ void pack_tokens(const KParams& p, bool decide, int w, int cw, int ncw,
+                                            int lane, const volatile int* pace = nullptr,
+                                            const volatile int* abort_flag = nullptr) {
     const long long nwarps = static_cast<long long>(ncw) * gridDim.x;
-    const int L = p.wp_L;
-    const int nchunk = L / 8;
-    const long long pitch = p.wp_pitch;
     const long long first = static_cast<long long>(ncw) * blockIdx.x + cw;
-    const long long ntok = first < p.wp_T ? (p.wp_T - first + nwarps - 1) / nwarps : 0;
+    const long long ntok = first < p.wp_g.T ? (p.wp_g.T - first + nwarps - 1) / nwarps : 0;
     long long i = 0;
-    for (long long t = first; t < p.wp_T; t += nwarps, ++i) {
-#ifndef MOE_COPY_NOPACE
+    for (long long t = first; t < p.wp_g.T; t += nwarps, ++i) {
         if (pace) {
             const long long need = i * pace[1] / (ntok + 1);
             if (pace[0] <= need) {
                 const uint64_t t0 = globaltimer_ns();
-                while (pace[0] <= need && !*abort_flag &&
-                       globaltimer_ns() - t0 < kWaitTimeoutNs)
+                while (pace[0] <= need && !*abort_flag && globaltimer_ns() - t0 < kWaitTimeoutNs)
                     __nanosleep(1000);
             }
         }
-#endif
-        long long row = -1;
-        int e = -1;
-        if (lane < p.wp_k) {
-            const long long a = t * p.wp_k + lane;
-            e = p.wp_idx[a];
-            row = p.wp_send_row[a];
-            if (row >= 0 && !(e >= 0 && e < p.wp_E && (w < 0 || (e % p.wp_El) / p.wp_Ew == w)))
-                row = -1;
-            if (row >= 0 && !moe_check(row < p.wp_rows, 1001)) row = -1;
-        }
-        if (!__any_sync(0xffffffffu, row >= 0)) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(p.wp_z + t * L);
-        for (int cb = 0; cb < nchunk; cb += 32 * 4) {
-            uint4 v[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int ch = cb + lane + 32 * c;
-#ifndef MOE_COPY_NOHINT
-                if (ch < nchunk) v[c] = __ldcs(src + ch);   // streaming: keep the product's
-#else                                                       // tiles in L2
-                if (ch < nchunk) v[c] = __ldg(src + ch);
-#endif
-            }
-            for (int j = 0; j < p.wp_k; ++j) {
-                const long long rj = __shfl_sync(0xffffffffu, row, j);
-                if (rj < 0) continue;
-                uint4* dst = reinterpret_cast<uint4*>(p.wp_pool + rj * pitch);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int ch = cb + lane + 32 * c;
-#ifndef MOE_COPY_NOHINT
-                    if (ch < nchunk) __stcs(dst + ch, v[c]);
-#else
-                    if (ch < nchunk) dst[ch] = v[c];
-#endif
-                }
-            }
-        }
-        if (lane < p.wp_k && row >= 0)
-            *reinterpret_cast<int4*>(p.wp_pool + row * pitch + L) =
-                make_int4(e, static_cast<int>(t), lane, 0);
+        pack_token<4, true>(p.wp_g, p.wp_a, t, lane, decide, w);
     }
 }
 
@@ -940,7 +887,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
         if (cta0 < ntiles) fetch_rows(cta0);
         for (int tile = cta0; ok && tile < ntiles; tile += ncta) {
             if (p.wp_ready) {   // the tile's wave: its pool rows filled by every CTA
-                const int wv = (nxt_g % p.wp_El) / p.wp_Ew;
+                const int wv = (nxt_g % p.wp_g.E_l) / p.wp_g.E_w;
                 if (!(waves_seen >> wv & 1u)) {
                     if (t == 0) *gather_wave = wv;   // lets this CTA copy wave wv + 1
                     if (!wait_count(p.wp_ready + wv, static_cast<int>(gridDim.x), abort_flag,
@@ -999,7 +946,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
         // waves instead of piling onto wave 0's (a bounded wait: on expiry
         // the copy goes ahead).
         const int cw = warp - 12;
-        for (int w = 1; w < p.wp_W; ++w) {
+        for (int w = 1; w < p.wp_g.W; ++w) {
             if (w >= 2 && *gather_wave < w - 1) {
                 const uint64_t t0 = globaltimer_ns();
                 while (*gather_wave < w - 1 && !*abort_flag) {
@@ -1010,19 +957,20 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                     }
                 }
             }
-            copy_pool_rows(p, w, cw, 4, lane);
+            pack_tokens(p, false, w, cw, 4, lane);
             named_bar_sync(1, 128);
             if (cw == 0 && lane == 0) {
                 __threadfence();
                 atomicAdd(p.wp_ready + w, 1);
             }
         }
-    } else if (AMODE != A_GATHER && warp >= 8 && p.wp_pool) {
-        // ------------------------------------------------------------ pool fill, every wave
-        // The dispatch's copies overlapped with this product (the shared
-        // experts' gate/up, which does not depend on the routing); nothing
-        // in this launch reads the pool, the next launch on the stream does.
-        copy_pool_rows(p, -1, warp - 8, 4, lane, tiles_pace, abort_flag);
+    } else if (AMODE != A_GATHER && warp >= 8 && p.wp_a.pool) {
+        // ------------------------------------------------------------ the pack
+        // The dispatch's final decisions and every copy, overlapped with this
+        // product (the shared experts' gate/up, which does not depend on the
+        // routing); nothing in this launch reads what they write, the next
+        // launch on the stream does.
+        pack_tokens(p, true, -1, warp - 8, 4, lane, tiles_pace, abort_flag);
     }
 
     tc_fence_before();
@@ -1102,7 +1050,7 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof(cfg));
         cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(p.wp_pool ? 384 : 256, 1, 1);   // + 4 copy warps
+        cfg.blockDim = dim3(p.wp_a.pool ? 384 : 256, 1, 1);   // + 4 copy warps
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -1128,7 +1076,7 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
     } else {
-        kern<<<grid, AMODE == A_GATHER ? 512 : (p.wp_pool ? 384 : 256), C::SMEM_BYTES, st>>>(p);
+        kern<<<grid, AMODE == A_GATHER ? 512 : (p.wp_a.pool ? 384 : 256), C::SMEM_BYTES, st>>>(p);
     }
     return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
@@ -1304,31 +1252,22 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     p.aux = static_cast<const uint16_t*>(d.aux);
     p.uniform_groups = d.uniform_groups;
     if (d.epi == EPI_SWIGLU_BWD) p.out2 = d.out2;
-    if (d.wp_pool) {   // the dispatch's pool fill rides along (waves pipeline or dense overlap)
-        if (!d.wp_z || !d.wp_idx || !d.wp_send_row || d.wp_k < 1 || d.wp_k > 32 ||
-            d.wp_W < 1 || d.wp_W > 32 || d.wp_Ew < 1 || d.wp_El != d.wp_Ew * d.wp_W ||
-            d.wp_E % d.wp_El || d.wp_L < 8 || d.wp_L % 8 || d.wp_pitch < d.wp_L + 8 ||
-            d.wp_pitch % 8 || (reinterpret_cast<uintptr_t>(d.wp_z) & 15) ||
-            (reinterpret_cast<uintptr_t>(d.wp_pool) & 15))
+    if (d.wp_a.pool) {   // the dispatch's pack rides along (waves pipeline or dense overlap)
+        const DispatchGeom& g = d.wp_g;
+        if (!d.wp_a.z || !d.wp_a.idx || !d.wp_a.send_row || g.ragged || g.k < 1 || g.k > 32 ||
+            g.W < 1 || g.W > 32 || g.E_w < 1 || g.E_l != g.E_w * g.W || g.E % g.E_l || g.L < 8 ||
+            g.L % 8 || (reinterpret_cast<uintptr_t>(d.wp_a.z) & 15) ||
+            (reinterpret_cast<uintptr_t>(d.wp_a.pool) & 15))
             return MOE_EINVAL;
-        if (d.wp_ready && (d.a_mode != A_GATHER || d.nseg != 1 || d.wp_pool != d.gather_src ||
-                           d.wp_L != d.seg[0].K || d.wp_pitch != d.gather_pitch))
+        if (d.wp_ready && (d.a_mode != A_GATHER || d.nseg != 1 || d.wp_a.pool != d.gather_src ||
+                           g.L != d.seg[0].K || pool_pitch(g.L) != d.gather_pitch))
             return MOE_EINVAL;
-        if (!d.wp_ready && d.a_mode == A_GATHER) return MOE_EINVAL;
+        if (!d.wp_ready && (d.a_mode == A_GATHER || !d.wp_a.rloc || !d.wp_a.base_se ||
+                            !d.wp_a.slot_of || !d.wp_a.drop || !d.wp_a.expert_rows))
+            return MOE_EINVAL;
         p.wp_ready = d.wp_ready;
-        p.wp_pool = d.wp_pool;
-        p.wp_z = d.wp_z;
-        p.wp_idx = d.wp_idx;
-        p.wp_send_row = reinterpret_cast<const long long*>(d.wp_send_row);
-        p.wp_T = d.wp_T;
-        p.wp_k = d.wp_k;
-        p.wp_E = d.wp_E;
-        p.wp_El = d.wp_El;
-        p.wp_Ew = d.wp_Ew;
-        p.wp_W = d.wp_W;
-        p.wp_L = d.wp_L;
-        p.wp_pitch = d.wp_pitch;
-        p.wp_rows = d.wp_rows;
+        p.wp_g = g;
+        p.wp_a = d.wp_a;
     } else if (d.wp_ready) {
         return MOE_EINVAL;
     }

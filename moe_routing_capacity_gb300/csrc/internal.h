@@ -50,6 +50,30 @@ struct GemmSeg {        // one K segment of the contraction: A_s [M, K_s] . B_s 
     int K;
 };
 
+struct DispatchGeom {
+    int64_t T;
+    int k, E, S, D, W, E_l, E_w, L;
+    int64_t T_s;
+    int c_send, c_recv;
+    int64_t pool_rows;
+    int ragged;   // 1: dropless ragged layout (no caps, pool of T*k rows)
+};
+
+// Pointers of one dispatch's pack: what pack_token (pack.cuh) reads and writes.
+struct PackArgs {
+    const uint16_t* z;          // [T, L] latent rows
+    const int32_t* idx;         // [T, k] expert ids
+    const int64_t* send_row;    // [T, k] sender-kept pool row (ragged: block | offset), else -1
+    const int32_t* rloc;        // [T, k] rank among the source's kept rows of its expert
+    const int32_t* base_se;     // [S, E] first receiver rank of each source's rows
+    uint16_t* pool;             // [pool_rows, pitch]
+    int32_t* slot_of;           // [T, k]
+    uint8_t* drop;              // [T, k]
+    int32_t* expert_rows;       // [E, c_recv] (ragged: flat, eoff)
+    const int32_t* blk_off;     // ragged: first row of each (source, destination, wave) block
+    const int32_t* eoff;        // ragged: first row-list entry of each expert
+};
+
 // out = sum_s A_s B_s^T with one of the epilogues above.  For EPI_SWIGLU the
 // B operand of segment 0 is the gate weight and B_up the up weight (same
 // shape); N then counts hidden units.  Grouped modes take the tile list
@@ -108,23 +132,16 @@ struct GemmDesc {
     void* out2;
     int64_t ldo2;
     int b2_rows;            // rows of the second B (B_up)
-    // pool fill riding along a GEMM launch.  Wave pipeline (gathered A): the
-    // launch also copies the payload rows and tags of waves 1..wp_W-1 into
-    // the pool (gather_src) while it computes;
-    // the row gather of a wave-w tile waits until every CTA has counted wave
-    // w in wp_ready[w] (a cooperative launch of one CTA per SM)
-    int32_t* wp_ready;      // [W] counters, zero at launch; null: no pipeline
-    uint16_t* wp_pool;      // the pool (same memory as gather_src)
-    const uint16_t* wp_z;   // [T, L] latent rows
-    const int32_t* wp_idx;  // [T, k] expert ids
-    const int64_t* wp_send_row;   // [T, k] pool row of each sender-kept assignment, else -1
-    int64_t wp_T;
-    int wp_k, wp_E, wp_El, wp_Ew, wp_W;
-    int wp_L;               // latent width (payload values of a pool row)
-    int64_t wp_pitch;       // elements between pool rows
-    int64_t wp_rows;        // pool rows
-    // (wp_pool without wp_ready, dense products only: every wave's rows are
-    // copied by extra warps of the launch, which nothing in it waits for)
+    // pool fill riding along a GEMM launch (the pack's PackArgs non-null).
+    // Wave pipeline (gathered A, wp_ready non-null): extra warps copy the
+    // payload rows and tags of waves 1..W-1 into the pool (gather_src) while
+    // the launch computes; the row gather of a wave-w tile waits until every
+    // CTA has counted wave w in wp_ready[w] (a cooperative launch of one CTA
+    // per SM).  Dense products (wp_ready null): extra warps run the whole
+    // pack (decisions and every copy), which nothing in the launch waits for.
+    int32_t* wp_ready;      // [W] counters, zero at launch
+    DispatchGeom wp_g;
+    PackArgs wp_a;
 };
 
 int gemm_launch(const GemmDesc& d, cudaStream_t stream);
@@ -139,15 +156,6 @@ int launch_topk(const float* logits, int64_t T, int E, int k, int32_t* idx, floa
 // cache-line boundary for the expert GEMM's row gather.  In uint16 elements.
 __host__ __device__ inline int64_t pool_pitch(int L) { return ((2ll * L + 16 + 127) / 128 * 128) / 2; }
 
-struct DispatchGeom {
-    int64_t T;
-    int k, E, S, D, W, E_l, E_w, L;
-    int64_t T_s;
-    int c_send, c_recv;
-    int64_t pool_rows;
-    int ragged;   // 1: dropless ragged layout (no caps, pool of T*k rows)
-};
-
 // Scratch layout of moe_dispatch_pooled (and of the ragged dispatch, which
 // adds the block offsets).
 struct DispatchWs {
@@ -157,12 +165,13 @@ struct DispatchWs {
 DispatchWs dispatch_ws_layout(const DispatchGeom& g);
 
 // copy_wave >= 0: every decision is made, but only the payload rows (and
-// tags) of that wave are written; copy_wave < -1: none are (the overlapped
-// paths fill them from a GEMM launch); -1: all.
+// tags) of that wave are written; -1: all.  run_pack false: the sender and
+// receiver counts only, the pack (decisions and copies) left to a GEMM
+// launch that carries it.
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
                     int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream,
-                    int copy_wave = -1);
+                    int copy_wave = -1, bool run_pack = true);
 
 int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                            uint16_t* pool, int32_t* slot_of, uint8_t* drop,

@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pack.cuh"
 
 namespace moe {
 
@@ -440,9 +441,10 @@ __global__ void dispatch_recv_scan_kernel(DispatchGeom g, const int32_t* __restr
     }
 }
 
-// Final decisions and the pack, one warp per token: the token's latent row
-// is read once into registers (16-byte loads) and written with 16-byte
-// stores to each of its sender-kept pool rows, followed by the row's tag.
+// Final decisions and the pack, one warp per token (pack_token): the
+// token's latent row is read once into registers (16-byte loads) and written
+// with 16-byte stores to each of its sender-kept pool rows (all of them, one
+// wave's, or none: copy_wave), followed by the row's tag.
 template <int CH>   // 16-byte chunks per lane per column block
 __global__ void __launch_bounds__(256) dispatch_pack_kernel(
     DispatchGeom g, const uint16_t* __restrict__ z, const int32_t* __restrict__ idx,
@@ -453,70 +455,14 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= g.T) return;
-    const int64_t s = t / g.T_s;
-    const int64_t pitch = pool_pitch(g.L);
-    // lane j < k owns assignment (t, j)
-    int64_t row = -1;
-    int e = 0;
-    if (lane < g.k) {
-        const int64_t a = t * g.k + lane;
-        e = idx[a];
-        row = send_row[a];
-        if (g.ragged && row >= 0) row = blk_off[row >> 32] + (row & 0xffffffffll);
-        if (row >= 0 && !moe_check(row < g.pool_rows, 1001)) row = -1;
-        int32_t so = -1;
-        uint8_t dr = 1;
-        if (row >= 0 && e >= 0 && e < g.E) {
-            const int r = base_se[s * g.E + e] + rloc[a];
-            if (r < g.c_recv) {
-                const int64_t at = g.ragged ? static_cast<int64_t>(eoff[e]) + r
-                                            : static_cast<int64_t>(e) * g.c_recv + r;
-                if (moe_check(at >= 0 && at < (g.ragged ? g.T * g.k
-                                                        : static_cast<int64_t>(g.E) * g.c_recv),
-                              1002))
-                    expert_rows[at] = static_cast<int32_t>(row);
-                so = static_cast<int32_t>(row);
-                dr = 0;
-            } else {
-                dr = 2;
-            }
-        }
-        slot_of[a] = so;
-        drop[a] = dr;
-        // overlapped dispatch: only this wave's rows (copy_wave >= 0) or none
-        // (copy_wave < -1) are filled here, the rest by warps of a GEMM launch
-        if (copy_wave < -1 || (copy_wave >= 0 && row >= 0 && (e % g.E_l) / g.E_w != copy_wave))
-            row = -1;
-    }
-    const int nchunk = g.L / 8;
-    const uint4* src = reinterpret_cast<const uint4*>(z + t * g.L);
-    for (int cb = 0; cb < nchunk; cb += 32 * CH) {
-        uint4 v[CH];
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int ch = cb + lane + 32 * c;
-            if (ch < nchunk) v[c] = __ldg(src + ch);
-        }
-        for (int j = 0; j < g.k; ++j) {
-            const int64_t rj = __shfl_sync(0xffffffffu, row, j);
-            if (rj < 0) continue;
-            uint4* dst = reinterpret_cast<uint4*>(pool + rj * pitch);
-#pragma unroll
-            for (int c = 0; c < CH; ++c) {
-                const int ch = cb + lane + 32 * c;
-                if (ch < nchunk) dst[ch] = v[c];
-            }
-        }
-    }
-    if (lane < g.k && row >= 0)
-        *reinterpret_cast<int4*>(pool + row * pitch + g.L) =
-            make_int4(e, static_cast<int>(t), lane, 0);
+    const PackArgs P{z, idx, send_row, rloc, base_se, pool, slot_of, drop, expert_rows, blk_off, eoff};
+    pack_token<CH, false>(g, P, t, lane, true, copy_wave);
 }
 
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
                     int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t st,
-                    int copy_wave) {
+                    int copy_wave, bool run_pack) {
     const DispatchWs L = dispatch_ws_layout(g);
     uint8_t* w = static_cast<uint8_t*>(ws);
     int64_t* send_row = reinterpret_cast<int64_t*>(w + L.send_row_off);
@@ -546,7 +492,7 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
                                                                   stats);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_recv_scan");
-    if (g.T == 0) return MOE_OK;
+    if (g.T == 0 || !run_pack) return MOE_OK;
     const unsigned grid = static_cast<unsigned>((g.T + 7) / 8);
     const int nchunk = g.L / 8;
     if (nchunk <= 32 * 4)
