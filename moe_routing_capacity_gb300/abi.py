@@ -111,6 +111,10 @@ def load_library(path: str) -> ctypes.CDLL:
     L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_expert_waves.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, vp, sz, vp, vp, vp]
+    L.moe_dispatch_shared_overlap.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, vp, vp]
     L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
     L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
     L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]

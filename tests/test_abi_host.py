@@ -40,6 +40,20 @@ def test_library_exports_every_declared_symbol():
     assert L.moe_abi_version() == 1
 
 
+def test_every_export_declares_its_signature():
+    """ctypes passes undeclared integer arguments as 32-bit ints, which is
+    wrong for sizes and pointers: every entry point gets its argtypes, and
+    their count matches the header's parameter list."""
+    L = abi.lib()
+    src = open(HEADER).read()
+    for name in abi.EXPORTS:
+        fn = getattr(L, name)
+        assert fn.argtypes is not None, name
+        m = re.search(r"^\s*(?:const\s+)?\w+\s*\*?\s*" + name + r"\s*\(([^)]*)\)", src, re.M)
+        params = [a for a in m.group(1).split(",") if a.strip() and a.strip() != "void"]
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
+
+
 def test_struct_sizes():
     assert ctypes.sizeof(abi.Config) == 64
     assert ctypes.sizeof(abi.Plan) == 64
@@ -122,6 +136,25 @@ def test_entry_points_validate_before_touching_the_gpu():
     assert L.moe_expert_ffn_grouped(cp, fake, fake, fake, fake, fake, fake, fake,
                                     p.ws_ffn_bytes - 1, fake, fake, n) == abi.MOE_ENOSPC
     assert L.moe_combine(cp, n, n, n, n, n, n, n, n, n, n, n, n, n) == abi.MOE_EINVAL
+    # shared activations given (Wsg = Wsu = NULL) but no a: refused
+    assert L.moe_combine(cp, fake, fake, fake, fake, n, n, n, fake, fake, n, fake, fake,
+                         n) == abi.MOE_EINVAL
+    # the overlapped paths: null pointers, then short scratch of either kind
+    # (sizes passed as size_t: past the sixth argument they travel on the stack)
+    sz = ctypes.c_size_t
+    assert L.moe_dispatch_expert_waves(cp, *([n] * 3), sz(0), *([n] * 10), sz(0), n, n,
+                                       n) == abi.MOE_EINVAL
+    assert L.moe_dispatch_expert_waves(cp, fake, fake, fake, sz(p.ws_dispatch_bytes - 1),
+                                       *([fake] * 9), fake, sz(p.ws_ffn_bytes), fake, fake,
+                                       n) == abi.MOE_ENOSPC
+    assert L.moe_dispatch_expert_waves(cp, fake, fake, fake, sz(p.ws_dispatch_bytes),
+                                       *([fake] * 9), fake, sz(p.ws_ffn_bytes - 1), fake, fake,
+                                       n) == abi.MOE_ENOSPC
+    assert L.moe_dispatch_shared_overlap(cp, *([n] * 3), sz(0), *([n] * 12)) == abi.MOE_EINVAL
+    assert L.moe_dispatch_shared_overlap(cp, fake, fake, fake, sz(p.ws_dispatch_bytes - 1),
+                                         *([fake] * 10), fake, n) == abi.MOE_ENOSPC
+    assert L.moe_dispatch_shared_overlap(cp, fake, fake, fake, sz(p.ws_dispatch_bytes),
+                                         *([fake] * 9), n, fake, n) == abi.MOE_EINVAL   # no a
     bad = abi.make_config(_small(T=63))
     assert L.moe_plan(ctypes.byref(bad), ctypes.byref(abi.Plan())) == abi.MOE_EINVAL
 
