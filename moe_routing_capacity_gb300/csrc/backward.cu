@@ -398,10 +398,8 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.goff = poff;   // ragged: the padded per-expert rows (A and out)
     q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
     if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
-    const size_t ghs = static_cast<size_t>(PE) * H * 2;
-    if (cudaMemsetAsync(dg, 0, ghs, st) != cudaSuccess || cudaMemsetAsync(du, 0, ghs, st) != cudaSuccess)
-        return MOE_ECUDA;
     std::memset(&q, 0, sizeof(q));   // recompute g/u of the received rows, SwiGLU backward
+    // (its epilogue also zeroes each expert's padding rows of dg and du)
     q.a_mode = A_GATHER; q.epi = EPI_SWIGLU_BWD; q.bn = 256;
     q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{nullptr, 0, a.Wg, L, L};
     q.B_up = a.Wu; q.groups = E; q.rows_per_group = cr; q.b_rows = H;

@@ -779,6 +779,17 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                             *reinterpret_cast<uint4*>(dgo + col) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
                             *reinterpret_cast<uint4*>(duo + col) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
                         }
+                    } else if (AMODE == A_GATHER &&
+                               m < (p.goff ? p.goff[g + 1] - p.goff[g] : p.out_gstride / p.ldo)) {
+                        // a padding row inside the group's slab: zeros, which
+                        // the weight gradients contract over
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = col0 + 8 * v;
+                            if (col >= p.N) continue;
+                            *reinterpret_cast<uint4*>(dgo + col) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(duo + col) = make_uint4(0u, 0u, 0u, 0u);
+                        }
                     }
                 }
             } else if (EPI == EPI_SWIGLU) {
