@@ -128,7 +128,7 @@ def test_overlap_mid_matches_oracle(pipeline):
 
 
 @pytest.mark.parametrize("pipeline", PIPES)
-@pytest.mark.parametrize("name", ["mid", "full"])
+@pytest.mark.parametrize("name", ["mid", "full", "long", "skew"])
 def test_overlap_equals_separate_calls_large(name, pipeline):
     """At the bench's size, repeated steps (counters reset each step)."""
     cfg = wl.CONFIGS[name]
