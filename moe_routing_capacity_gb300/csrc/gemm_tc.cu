@@ -1087,7 +1087,10 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
     } else {
-        kern<<<grid, AMODE == A_GATHER ? 512 : (p.wp_a.pool ? 384 : 256), C::SMEM_BYTES, st>>>(p);
+        // gathered A: warps 8-11 gather (12-15 copy only in the wave pipeline,
+        // launched cooperatively above); dense products carrying the pack: 8-11
+        const int threads = (AMODE == A_GATHER || p.wp_a.pool) ? 384 : 256;
+        kern<<<grid, threads, C::SMEM_BYTES, st>>>(p);
     }
     return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
