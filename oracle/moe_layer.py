@@ -42,6 +42,7 @@ __all__ = [
     "bf16_round", "silu", "Plan", "make_plan", "router_logits", "router_topk",
     "latent_down", "placement", "dispatch", "pack_pool", "expert_ffn",
     "experts_forward", "combine", "shared_act", "output", "layer", "balance_update",
+    "balance_update_window",
     "dispatch_ragged", "layer_ragged", "layer_backward", "silu_grad", "exact",
     "TIE_EPS", "EMPTY_TAG", "DROP_KEPT", "DROP_SEND", "DROP_RECV",
 ]
@@ -582,6 +583,27 @@ def balance_update(idx, hist, alpha: float, n_experts: int):
         return h, np.zeros(n_experts)
     f = h / total
     return h, -alpha * (f - 1.0 / n_experts)
+
+
+def balance_update_window(idx, hist, ring, step: int, alpha: float, n_experts: int):
+    """The same bias over the past N batches exactly ([CSDN] appendix A.2:
+    H counts each expert's selections "in the past N batches").
+
+    ring [N, E] holds batch b's counts in row b % N; this batch (number
+    `step`, counted from 0) replaces the row of batch step - N, which leaves
+    the window, so H = sum of the last N batches' counts.  [CSDN] sec. 四
+    calls the histogram "10,000 bins"; read here as the window length N,
+    the caller's choice.  Returns (hist, ring, step + 1, bias).
+    """
+    ring = np.array(ring, dtype=np.int64, copy=True)
+    counts = np.bincount(np.asarray(idx, dtype=np.int64).reshape(-1), minlength=n_experts)
+    slot = step % ring.shape[0]
+    h = np.asarray(hist, dtype=np.int64) - ring[slot] + counts
+    ring[slot] = counts
+    total = int(h.sum())
+    if total == 0:
+        return h, ring, step + 1, np.zeros(n_experts)
+    return h, ring, step + 1, -alpha * (h / total - 1.0 / n_experts)
 
 
 # ---------------------------------------------------------------- layer

@@ -449,6 +449,38 @@ def test_balance_update_invariants():
     assert (bz == 0).all()
 
 
+def test_balance_window_closed_form():
+    # window of 2 batches over 3 batches that select expert 0, then 1, then 2
+    # (three assignments each): after batch 3, H holds batches 2 and 3 only
+    E, alpha = 4, 0.5
+    h = np.zeros(E, dtype=np.int64)
+    ring = np.zeros((2, E), dtype=np.int64)
+    step = 0
+    for e in (0, 1, 2):
+        h, ring, step, b = O.balance_update_window(np.full((3, 1), e), h, ring, step, alpha, E)
+    assert step == 3
+    assert h.tolist() == [0, 3, 3, 0]
+    np.testing.assert_allclose(b, [alpha / 4, -alpha / 4, -alpha / 4, alpha / 4], rtol=1e-15)
+    # window of one batch: H is the last batch's counts
+    h1, r1, _, _ = O.balance_update_window(np.array([[1, 3], [3, 3]]), np.array([5, 0, 0, 0]),
+                                           np.array([[5, 0, 0, 0]]), 7, alpha, E)
+    assert h1.tolist() == [0, 1, 0, 3] and r1.tolist() == [[0, 1, 0, 3]]
+
+
+def test_balance_window_longer_than_history_is_plain_accumulation():
+    rng = np.random.default_rng(4)
+    E = 12
+    h_w = h_a = np.zeros(E, dtype=np.int64)
+    ring = np.zeros((10, E), dtype=np.int64)
+    step = 0
+    for _ in range(6):
+        idx = _random_routing(rng, 40, E, 3)
+        h_w, ring, step, b_w = O.balance_update_window(idx, h_w, ring, step, 0.1, E)
+        h_a, b_a = O.balance_update(idx, h_a, 0.1, E)
+        assert (h_w == h_a).all()
+        np.testing.assert_array_equal(b_w, b_a)
+
+
 # ------------------------------------------------------------------ dropless ragged dispatch
 
 @pytest.mark.parametrize("seed", range(6))
