@@ -399,9 +399,25 @@ int moe_layer_backward_ragged(const moe_config_t* cfg, const moe_backward_args_t
  *   bias  [E] fp32 (out): the new bias; 0 everywhere while H is empty.  It
  *         may be the buffer moe_router_topk reads: calls on the same stream
  *         then route the next batch with it.
- * The second reading on the pages (a "10,000-bin" histogram) is not built. */
+ * For an exact window of the past N batches see moe_balance_update_window. */
 int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,
                        float* bias, void* stream);
+
+/* The same bias with H over exactly the past `window` batches (appendix
+ * A.2: "the past N batches"; section 四's "10,000 bins" read as that window
+ * length, the caller's choice).  Each call counts this batch's selections,
+ * takes the counts of the batch leaving the window out of H and puts this
+ * batch's in, then writes the bias as moe_balance_update does.
+ *   hist   [E] int64 (in/out): H, zero before the first call
+ *   ring   [window, E] int64 (in/out): per-batch counts, batch b in row
+ *          b % window; zero before the first call
+ *   step   [1] int64 (in/out, device): batches seen so far, zero before the
+ *          first call (kept on the device: the update needs no host state
+ *          and can be captured in a CUDA graph)
+ *   window >= 1, else MOE_EINVAL. */
+int moe_balance_update_window(const moe_config_t* cfg, const int32_t* idx, int64_t* hist,
+                              int64_t* ring, int32_t window, int64_t* step, float alpha,
+                              float* bias, void* stream);
 
 /* Index checks of a checked build (compiled with -DMOE_CHECK=1; the pages
  * define no such operation): every row, slot, expert and tile index the

@@ -22,7 +22,7 @@ MOE_OK, MOE_EINVAL, MOE_ENOSPC, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENODEV = 0, -1, -2,
 EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project", "moe_matmul",
            "moe_dispatch_pooled",
            "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_dispatch_expert_waves",
-           "moe_dispatch_shared_overlap", "moe_balance_update",
+           "moe_dispatch_shared_overlap", "moe_balance_update", "moe_balance_update_window",
            "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged",
            "moe_backward_plan", "moe_layer_backward", "moe_backward_plan_ragged",
            "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
@@ -116,6 +116,7 @@ def load_library(path: str) -> ctypes.CDLL:
     L.moe_dispatch_shared_overlap.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp,
                                               vp, vp, vp, vp]
     L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
+    L.moe_balance_update_window.argtypes = [pc, vp, vp, vp, i32, vp, ctypes.c_float, vp, vp]
     L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
     L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
@@ -304,6 +305,15 @@ def balance_update(cfg, idx, hist, alpha, bias, stream=None):
     _check("moe_balance_update", lib().moe_balance_update(
         ctypes.byref(make_config(cfg)), _ptr(idx, i32), _ptr(hist, torch.int64),
         float(alpha), _ptr(bias, f32), _stream(stream)))
+
+
+def balance_update_window(cfg, idx, hist, ring, step, alpha, bias, stream=None):
+    """moe_balance_update over exactly the past ring.shape[0] batches (ring
+    [N, E] int64 and step [1] int64 live on the device, zero at the start)."""
+    _check("moe_balance_update_window", lib().moe_balance_update_window(
+        ctypes.byref(make_config(cfg)), _ptr(idx, i32), _ptr(hist, torch.int64),
+        _ptr(ring, torch.int64), int(ring.shape[0]), _ptr(step, torch.int64), float(alpha),
+        _ptr(bias, f32), _stream(stream)))
 
 
 def combine(cfg, ypool, slot_of, w, W_lu, x, Wsg, Wsu, Wsd, c, a, out, status, stream=None):

@@ -769,6 +769,24 @@ int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* his
                                  static_cast<cudaStream_t>(stream));
 }
 
+int moe_balance_update_window(const moe_config_t* cfg, const int32_t* idx, int64_t* hist,
+                              int64_t* ring, int32_t window, int64_t* step, float alpha,
+                              float* bias, void* stream) {
+    MOE_NVTX_RANGE();
+    Geom G;
+    int rc = make_geom(cfg, &G);
+    if (rc) return rc;
+    if (!hist || !ring || !step || !bias || window < 1 || (G.g.T > 0 && !idx) || !(alpha == alpha))
+        return MOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(hist) & 7u) || (reinterpret_cast<uintptr_t>(ring) & 7u) ||
+        (reinterpret_cast<uintptr_t>(step) & 7u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+        return MOE_EINVAL;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    return launch_balance_window(idx, G.g.T * G.g.k, G.g.E, hist, ring, window, step, alpha, bias,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 static void fill_backward_layout(const BackwardWs& w, moe_backward_ws_t* layout) {
     layout->dc = w.dc; layout->da = w.da; layout->dgs = w.dgs; layout->dus = w.dus;
     layout->dw = w.dw; layout->rowinv = w.rowinv; layout->dxpool = w.dxpool; layout->dh = w.dh;

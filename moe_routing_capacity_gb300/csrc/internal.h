@@ -203,6 +203,8 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
 // Quantile-balancing bias update: hist += counts of idx; bias from hist.
 int launch_balance_update(const int32_t* idx, int64_t n, int E, int64_t* hist, float alpha,
                           float* bias, cudaStream_t stream);
+int launch_balance_window(const int32_t* idx, int64_t n, int E, int64_t* hist, int64_t* ring,
+                          int window, int64_t* step, float alpha, float* bias, cudaStream_t st);
 
 // c[t] = bf16(sum over kept j of w[t,j] ypool[slot_of[t,j]]); w == nullptr: weights 1.
 int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,

@@ -727,6 +727,54 @@ int launch_balance_update(const int32_t* idx, int64_t n, int E, int64_t* hist, f
     return MOE_OK;
 }
 
+// The bias over the past `window` batches, one CTA: this batch's counts
+// (shared-memory histogram), the ring row of the batch leaving the window
+// swapped for them in H, then the bias as above; the step counter lives on
+// the device so that the update needs no host state.
+__global__ void __launch_bounds__(1024) balance_window_kernel(
+    const int32_t* __restrict__ idx, int64_t n, int E, int64_t* __restrict__ hist,
+    int64_t* __restrict__ ring, int window, int64_t* __restrict__ step, float alpha,
+    float* __restrict__ bias) {
+    extern __shared__ unsigned int cnt[];
+    __shared__ long long part[32];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int e = idx[i];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1u);
+    }
+    __syncthreads();
+    const int64_t s = *step;
+    int64_t* slot = ring + (s % window) * E;
+    long long sum = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const long long h = hist[e] - slot[e] + cnt[e];
+        hist[e] = h;
+        slot[e] = cnt[e];
+        sum += h;
+    }
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += part[w];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const double f = total > 0 ? static_cast<double>(hist[e]) / static_cast<double>(total)
+                                   : 1.0 / E;
+        bias[e] = static_cast<float>(-static_cast<double>(alpha) * (f - 1.0 / E));
+    }
+    if (threadIdx.x == 0) *step = s + 1;   // every thread read it before the barrier above
+}
+
+int launch_balance_window(const int32_t* idx, int64_t n, int E, int64_t* hist, int64_t* ring,
+                          int window, int64_t* step, float alpha, float* bias, cudaStream_t st) {
+    balance_window_kernel<<<1, 1024, E * sizeof(unsigned int), st>>>(idx, n, E, hist, ring, window,
+                                                                    step, alpha, bias);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "balance_window");
+    return MOE_OK;
+}
+
 // ==================================================================== combine
 
 // The return path, one warp per token: c[t] = bf16(sum_j w[t,j] Y[slot_of[t,j]])

@@ -26,7 +26,8 @@ class PooledWaveMoE:
     """``balance_alpha``: if set, after each batch's routing the
     quantile-balancing bias is recomputed from the running selection
     histogram (``self.hist``) into the router bias, so it applies from the
-    next batch on.  ``pipeline``: None (the calls one after another),
+    next batch on; with ``balance_window`` = N the histogram spans exactly
+    the past N batches.  ``pipeline``: None (the calls one after another),
     "waves" (dispatch and experts as one wave-pipelined call: the later
     waves' pool rows copied while wave 0's experts run) or "shared" (the
     pool rows copied while the shared experts' gate/up runs); the capped
@@ -35,7 +36,7 @@ class PooledWaveMoE:
     PIPELINES = (None, "waves", "shared")
 
     def __init__(self, cfg, weights: dict, device="cuda", balance_alpha=None,
-                 dropless=False, pipeline=None):
+                 dropless=False, pipeline=None, balance_window=None):
         self.cfg = cfg
         self.dropless = dropless
         if pipeline not in self.PIPELINES:
@@ -74,10 +75,14 @@ class PooledWaveMoE:
         self.out = e(T, d, dt=torch.bfloat16)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.balance_alpha = balance_alpha
+        self.balance_window = balance_window
         if balance_alpha is not None:
             if self.w.get("bias") is None:
                 self.w["bias"] = torch.zeros(E, dtype=torch.float32, device=dev)
             self.hist = torch.zeros(E, dtype=torch.int64, device=dev)
+            if balance_window:   # exact window of the past N batches
+                self.ring = torch.zeros(balance_window, E, dtype=torch.int64, device=dev)
+                self.bstep = torch.zeros(1, dtype=torch.int64, device=dev)
 
     # -- the five steps -------------------------------------------------
     def route(self, x, stream=None):
@@ -123,7 +128,10 @@ class PooledWaveMoE:
         """Enqueue the whole layer on ``stream``; returns the output tensor
         (``out`` if given, else the layer's own output buffer)."""
         self.route_and_latent(x, stream)
-        if self.balance_alpha is not None:
+        if self.balance_alpha is not None and self.balance_window:
+            abi.balance_update_window(self.cfg, self.idx, self.hist, self.ring, self.bstep,
+                                      self.balance_alpha, self.w["bias"], stream)
+        elif self.balance_alpha is not None:
             abi.balance_update(self.cfg, self.idx, self.hist, self.balance_alpha,
                                self.w["bias"], stream)
         if self.pipeline == "waves":

@@ -155,6 +155,8 @@ def test_entry_points_validate_before_touching_the_gpu():
                                          *([fake] * 10), fake, n) == abi.MOE_ENOSPC
     assert L.moe_dispatch_shared_overlap(cp, fake, fake, fake, sz(p.ws_dispatch_bytes),
                                          *([fake] * 9), n, fake, n) == abi.MOE_EINVAL   # no a
+    assert L.moe_balance_update_window(cp, fake, fake, fake, 0, fake, ctypes.c_float(1.0), fake,
+                                       n) == abi.MOE_EINVAL   # window < 1
     bad = abi.make_config(_small(T=63))
     assert L.moe_plan(ctypes.byref(bad), ctypes.byref(abi.Plan())) == abi.MOE_EINVAL
 
