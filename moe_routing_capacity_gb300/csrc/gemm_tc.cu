@@ -817,7 +817,6 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
                                                pk[4 * v + 3]);
                     }
-#ifndef MOE_NO_ZERO_PAD
                     else if (AMODE == A_GATHER && !p.goff && m < p.out_gstride / p.ldo) {
                         // a padding row of the expert's last tile (inside its
                         // slab of h): zeros, so the down-projection's padded
@@ -827,7 +826,6 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                             if (col0 + 8 * v < p.N)
                                 *reinterpret_cast<uint4*>(out + col0 + 8 * v) = make_uint4(0u, 0u, 0u, 0u);
                     }
-#endif
                 }
             } else {   // EPI_BF16 / EPI_SCATTER
                 uint16_t* out = reinterpret_cast<uint16_t*>(p.out) + obase;
@@ -1131,13 +1129,9 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     std::memset(&p, 0, sizeof(p));
     // CTA pairs (cta_group::2, 256-row tiles) for the dense K-major products
     // with the bf16, SwiGLU and split epilogues
-#ifndef MOE_NO_CTA_PAIRS
     const bool cg2 = d.a_mode == A_DENSE && d.bn == 256 && sms >= 2 &&
                      (d.epi == EPI_BF16 || d.epi == EPI_F32 || (d.epi == EPI_SPLIT && !d.b_mn) ||
                       ((d.epi == EPI_SWIGLU || d.epi == EPI_SWIGLU_BWD) && !d.b_mn));
-#else
-    const bool cg2 = false;
-#endif
     // gate/up pairs load two 128-row halves, the 384-wide router tile three
     // 128-row thirds; everything else one box of bn rows (K-major B); a CTA
     // of a pair loads one 128-row half of the B tile
