@@ -816,8 +816,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                                 *reinterpret_cast<uint4*>(out + col0 + 8 * v) =
                                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
                                                pk[4 * v + 3]);
-                    }
-                    else if (AMODE == A_GATHER && !p.goff && m < p.out_gstride / p.ldo) {
+                    } else if (AMODE == A_GATHER && !p.goff && m < p.out_gstride / p.ldo) {
                         // a padding row of the expert's last tile (inside its
                         // slab of h): zeros, so the down-projection's padded
                         // MMAs multiply zeros instead of a stale row
