@@ -95,7 +95,8 @@ typedef struct moe_plan {
     int64_t pool_rows;           /* D * W * S * c_send                               */
     int64_t pool_row_bytes;      /* 2*L + 16 rounded up to a multiple of 128: L bf16 */
                                  /* payload, 16-byte tag, padding (never written)    */
-    int64_t ws_dispatch_bytes;   /* scratch for moe_dispatch_pooled                  */
+    int64_t ws_dispatch_bytes;   /* scratch for moe_dispatch_pooled (and the         */
+                                 /* overlapped dispatch calls)                       */
     int64_t ws_ffn_bytes;        /* scratch for moe_expert_ffn_grouped (incl. h)     */
     int64_t h_offset_bytes;      /* where h [E, c_recv, H] bf16 sits in ws_ffn       */
 } moe_plan_t;
