@@ -209,6 +209,13 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                  : "memory");
 }
 
+// Arrive on the mbarrier once all of this thread's earlier cp.async copies
+// have landed (the arrival does not raise the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -218,8 +225,10 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Make this thread's generic-proxy shared-memory writes (cp.async lands in the
-// generic proxy) visible to the async proxy that tcgen05.mma reads through.
+// Order generic-proxy shared-memory writes (cp.async lands in the generic
+// proxy) before the async-proxy reads of tcgen05.mma and TMA stores: issued
+// by the writing thread after its writes, or by the reading thread after it
+// has observed their completion through an mbarrier.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

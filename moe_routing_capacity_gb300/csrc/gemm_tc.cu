@@ -67,7 +67,7 @@ struct TileCfg {
                                     : (AMODE == A_GATHER)  ? MOE_GATHER_A_STAGES
                                     : (AMODE == A_GROUPED) ? MOE_GROUPED_A_STAGES
                                                            : B_STAGES;
-    static_assert(AMODE != A_GATHER || A_STAGES >= 3, "the gather needs LAG >= 1");
+    static_assert(AMODE != A_GATHER || A_STAGES >= 2, "the row gather needs two stages");
     // two accumulators (double buffering) when they fit in the 512 TMEM
     // columns; the 384-wide router tile gets one
     static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
@@ -511,6 +511,9 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                         ok = false;
                         break;
                     }
+                    // gathered rows came through cp.async (generic proxy): make
+                    // them visible to the tensor core's reads
+                    if constexpr (AMODE == A_GATHER) fence_proxy_async_smem();
                     tc_fence_after();
                     const uint32_t a_s = smem_u32(sA + sa * A_STAGE_BYTES);
                     const uint32_t b_s = smem_u32(sB + sb * C::B_STAGE_BYTES);
@@ -863,18 +866,17 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
         // ------------------------------------------------------------ row gather (A)
         // Thread t copies 16-byte chunk c = t % 8 of tile rows t/8 + 16 i,
         // i = 0..7: a warp instruction moves four whole 128-byte row segments.
-        // Each thread keeps LAG k-blocks of copies in flight, then waits for
-        // the oldest, fences them into the async proxy and signals its stage.
-        // LAG = A_STAGES - 2 leaves the MMA one stage of slack, so a stage is
-        // never signalled behind a wait for the slot two blocks ahead.  The
-        // next tile's row indices are fetched while this tile streams.
-        constexpr int LAG = AST - 2;
+        // Each thread's copies of a stage arrive on the stage's full barrier by
+        // themselves once they land (cp.async.mbarrier.arrive.noinc, 128
+        // arrivals a phase), so the thread moves on to the next free stage
+        // at once; the MMA thread fences them into the async proxy after its
+        // wait.  The next tile's row indices are fetched while this tile
+        // streams.
         const int t = threadIdx.x - 256;
         const int c = t & 7;
         const int rg = t >> 3;
         const int ntiles = num_tiles<AMODE>(p);
         uint32_t sa = 0, pa = 0;
-        int it = 0;
         bool ok = true;
         int nxt_row[8];
         int nxt_cnt = 0, nxt_g = 0;
@@ -928,13 +930,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                     const uint32_t nbytes = ((valid >> i & 1u) && kin) ? 16u : 0u;
                     cp_async_16(dst + (rg + 16 * i) * 128, src[i] + (nbytes ? kc : 0), nbytes);
                 }
-                cp_async_commit();
-                if (it >= LAG) {
-                    cp_async_wait<LAG>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&fullA[(it - LAG) % AST]);
-                }
-                ++it;
+                cp_async_arrive_noinc(&fullA[sa]);   // arrives when these copies land
                 if (++sa == AST) {
                     sa = 0;
                     pa ^= 1u;
@@ -942,9 +938,8 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
             }
         }
         if (t == 0) *gather_wave = 1 << 30;   // no more tiles: copy what is left
+        cp_async_commit();    // every copy (none were grouped) lands before the CTA may exit
         cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (int i = (it > LAG ? it - LAG : 0); i < it; ++i) mbar_arrive(&fullA[i % AST]);
     } else if (AMODE == A_GATHER && warp >= 12 && p.wp_ready) {
         // ------------------------------------------------------------ pool fill, waves 1..
         // Wave by wave; after wave w the CTA's four copy warps meet and one
