@@ -617,6 +617,7 @@ def run_gb300(args, rank, world, local_rank):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "pool_fill": pipeline,
                        "l2": "inputs larger than L2 (8.1 GB weights per step)"},
+            "assignments_per_s": value * cfg.top_k,
             "drops": {"near_tie_tokens": near_ties,
                       "kept": st["kept"], "dropped_send": st["dropped_send"],
                       "dropped_recv": st["dropped_recv"],
