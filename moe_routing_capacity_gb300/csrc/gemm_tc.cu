@@ -38,6 +38,10 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KB
 // Shared-memory rings: A stages (128 x 64 bf16, 16 KB) and B stages (BN x 64
 // bf16) have their own depths.  Gathered A (cp.async, latency-bound) gets a
 // deeper ring than the TMA-fed B.
+// ring depth of the CTA-pair products without fp32 staging (32 KB a stage)
+#ifndef MOE_PAIR_STAGES
+#define MOE_PAIR_STAGES 7
+#endif
 #ifndef MOE_GATHER_A_STAGES
 #define MOE_GATHER_A_STAGES 6
 #endif
@@ -57,13 +61,13 @@ template <int BN, int AMODE, int EPI, bool CG2 = false>
 struct TileCfg {
     static constexpr int B_ROWS = CG2 ? BN / 2 : BN;   // B rows staged by this CTA
     static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
-    static constexpr int B_STAGES = CG2                      ? 6
+    static constexpr int B_STAGES = CG2                      ? (EPI == EPI_F32 ? 6 : MOE_PAIR_STAGES)
                                     : (BN == 384)            ? 3
                                     : (BN != 256)            ? 6
                                     : (AMODE == A_GATHER)    ? MOE_GATHER_B_STAGES
                                     : (AMODE == A_GROUPED)   ? MOE_GROUPED_B_STAGES
                                                              : 4;
-    static constexpr int A_STAGES = CG2                    ? 6
+    static constexpr int A_STAGES = CG2                    ? (EPI == EPI_F32 ? 6 : MOE_PAIR_STAGES)
                                     : (AMODE == A_GATHER)  ? MOE_GATHER_A_STAGES
                                     : (AMODE == A_GROUPED) ? MOE_GROUPED_A_STAGES
                                                            : B_STAGES;
@@ -72,7 +76,10 @@ struct TileCfg {
     // columns; the 384-wide router tile gets one
     static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
     static constexpr int TMEM_COLS = (BN <= 256) ? 2 * BN : 512;
-    static constexpr int BAR_BYTES = 256;
+    // barriers (full/empty per stage, two accumulator pairs, done) and the
+    // words after them (TMEM slot, abort flag, gather wave, two pace words),
+    // rounded up to 64 bytes
+    static constexpr int BAR_BYTES = ((2 * (A_STAGES + B_STAGES) + 5) * 8 + 5 * 4 + 63) / 64 * 64;
     // fp32 output: each epilogue warp stages 32 x 32 blocks in shared memory
     // (two, so one can be written while the other is being stored)
     static constexpr int STG_BYTES = (EPI == EPI_F32) ? 2 * 4 * 32 * 32 * 4 : 0;
