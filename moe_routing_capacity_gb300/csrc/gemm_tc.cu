@@ -65,11 +65,11 @@ struct TileCfg {
                                     : (BN == 384)            ? 3
                                     : (BN != 256)            ? 6
                                     : (AMODE == A_GATHER)    ? MOE_GATHER_B_STAGES
-                                    : (AMODE == A_GROUPED)   ? MOE_GROUPED_B_STAGES
+                                    : (AMODE == A_GROUPED)   ? (EPI == EPI_F32 ? 4 : MOE_GROUPED_B_STAGES)
                                                              : 4;
     static constexpr int A_STAGES = CG2                    ? (EPI == EPI_F32 ? 6 : MOE_PAIR_STAGES)
                                     : (AMODE == A_GATHER)  ? MOE_GATHER_A_STAGES
-                                    : (AMODE == A_GROUPED) ? MOE_GROUPED_A_STAGES
+                                    : (AMODE == A_GROUPED) ? (EPI == EPI_F32 ? 4 : MOE_GROUPED_A_STAGES)
                                                            : B_STAGES;
     static_assert(AMODE != A_GATHER || A_STAGES >= 2, "the row gather needs two stages");
     // two accumulators (double buffering) when they fit in the 512 TMEM
