@@ -60,7 +60,11 @@ def parse():
                          "inside the shared experts' gate/up launch (shared)")
     ap.add_argument("--no-pipelines", action="store_true",
                     help="skip timing the three pool-fill schedules side by side")
-    return ap.parse_args()
+    args = ap.parse_args()
+    # at least three untimed warm-up steps whatever is asked; the line
+    # reports the number run
+    args.warmup = max(args.warmup, 3)
+    return args
 
 
 # ------------------------------------------------------------------ helpers
