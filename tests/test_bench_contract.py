@@ -1,0 +1,47 @@
+"""bench.py's output contract, checked on CPU: the reference arm (the oracle
+timed on the host cores) prints one JSON line with the keys the driver
+reads, and the GB300 arm refuses to run without a GPU instead of falling
+back to anything on the CPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(args, timeout=300):
+    return subprocess.run([sys.executable, "bench.py", *args], cwd=ROOT, capture_output=True,
+                          text=True, timeout=timeout)
+
+
+def test_reference_arm_line():
+    r = _run(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "0"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == "routed tokens/sec per MoE layer on 1 GB300"
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 2
+    assert d["warmup"] >= 3                      # at least three untimed steps whatever is asked
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["data"] == "synthetic" and d["vs_baseline"] is None
+    assert d["config"]["workload"].startswith("tiny")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == d["unit"]
+    assert cb["cores"] >= 1 and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
+def test_gb300_arm_fails_without_gpu():
+    r = _run(["--steps", "1", "--warmup", "1", "--no-cpu-baseline"])
+    assert r.returncode != 0
+    assert not r.stdout.strip(), "no result line without a GPU"
