@@ -777,8 +777,12 @@ int launch_balance_window(const int32_t* idx, int64_t n, int E, int64_t* hist, i
 
 // ==================================================================== combine
 
-// The return path, one warp per token: c[t] = bf16(sum_j w[t,j] Y[slot_of[t,j]])
-// over kept j in j order, fp32 accumulation, 16-byte loads of the rows.
+// The return path: c[t] = bf16(sum_j w[t,j] Y[slot_of[t,j]]) over kept j in j
+// order, fp32 accumulation, 16-byte loads of the rows.  A warp's unit of
+// work is one pass of 32*CH 16-byte chunks of one token's row; the grid
+// holds only the blocks that are resident at once and each warp strides over
+// the units, so that the last round of work is not left half empty.  Two
+// rows' loads are in flight before their products are accumulated.
 template <int CH>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ ypool,
                                                       const int32_t* __restrict__ slot_of,
@@ -786,42 +790,57 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       int k, int L, uint16_t* __restrict__ c,
                                                       int64_t rows) {
     const int lane = threadIdx.x & 31;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    int32_t my_row = -1;
-    float my_w = 0.0f;
-    if (lane < k) {
-        my_row = slot_of[t * k + lane];
-        my_w = w ? w[t * k + lane] : 1.0f;   // no weights: plain sum (gradient return)
-        if (!moe_check(my_row < rows, 1003)) my_row = -1;
-    }
     const int nchunk = L / 8;
-    uint4* dst = reinterpret_cast<uint4*>(c + t * L);
-    for (int cb = 0; cb < nchunk; cb += 32 * CH) {
+    const int npass = (nchunk + 32 * CH - 1) / (32 * CH);
+    const int64_t units = T * npass;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         u < units; u += nwarps) {
+        const int64_t t = u / npass;
+        const int cb = static_cast<int>(u - t * npass) * 32 * CH;
+        int32_t my_row = -1;
+        float my_w = 0.0f;
+        if (lane < k) {
+            my_row = slot_of[t * k + lane];
+            my_w = w ? w[t * k + lane] : 1.0f;   // no weights: plain sum (gradient return)
+            if (!moe_check(my_row < rows, 1003)) my_row = -1;
+        }
         float acc[CH][8];
 #pragma unroll
         for (int q = 0; q < CH; ++q)
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[q][i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
-            const float wj = __shfl_sync(0xffffffffu, my_w, j);
-            if (r < 0) continue;
+        auto add = [&](const uint4 (&v)[CH], float wj) {
+#pragma unroll
+            for (int q = 0; q < CH; ++q) {
+                const uint32_t u4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    acc[q][2 * h] = fmaf(wj, bf16_lo(u4[h]), acc[q][2 * h]);
+                    acc[q][2 * h + 1] = fmaf(wj, bf16_hi(u4[h]), acc[q][2 * h + 1]);
+                }
+            }
+        };
+        auto load = [&](uint4 (&v)[CH], int32_t r) {
             const uint4* src = reinterpret_cast<const uint4*>(ypool + static_cast<int64_t>(r) * L);
 #pragma unroll
             for (int q = 0; q < CH; ++q) {
                 const int ch = cb + lane + 32 * q;
-                if (ch < nchunk) {
-                    const uint4 v = __ldg(src + ch);
-                    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        acc[q][2 * h] = fmaf(wj, bf16_lo(u[h]), acc[q][2 * h]);
-                        acc[q][2 * h + 1] = fmaf(wj, bf16_hi(u[h]), acc[q][2 * h + 1]);
-                    }
-                }
+                v[q] = ch < nchunk ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
             }
+        };
+        for (int j = 0; j < k; j += 2) {
+            const int32_t r0 = __shfl_sync(0xffffffffu, my_row, j);
+            const float w0 = __shfl_sync(0xffffffffu, my_w, j);
+            const int32_t r1 = j + 1 < k ? __shfl_sync(0xffffffffu, my_row, j + 1) : -1;
+            const float w1 = j + 1 < k ? __shfl_sync(0xffffffffu, my_w, j + 1) : 0.0f;
+            uint4 v0[CH], v1[CH];
+            if (r0 >= 0) load(v0, r0);
+            if (r1 >= 0) load(v1, r1);
+            if (r0 >= 0) add(v0, w0);   // dropped assignments add nothing
+            if (r1 >= 0) add(v1, w1);
         }
+        uint4* dst = reinterpret_cast<uint4*>(c + t * L);
 #pragma unroll
         for (int q = 0; q < CH; ++q) {
             const int ch = cb + lane + 32 * q;
@@ -839,11 +858,29 @@ int check_status_route() { return moe_check_read_reset(); }
 int launch_combine(const uint16_t* ypool, const int32_t* slot_of, const float* w, int64_t T, int k,
                    int L, uint16_t* c, int64_t rows, cudaStream_t st) {
     if (T == 0) return MOE_OK;
-    const unsigned grid = static_cast<unsigned>((T + 7) / 8);
-    if (L / 8 <= 32 * 4)
-        combine_kernel<4><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c, rows);
-    else
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    // resident blocks of each instance (queried once; no runtime call inside
+    // a stream capture after the first launch)
+    static int per_sm[2] = {0, 0};
+    const bool wide = L / 8 > 32 * 4;
+    if (!per_sm[wide]) {
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &nb, wide ? combine_kernel<6> : combine_kernel<4>, 256, 0) != cudaSuccess)
+            return MOE_ECUDA;
+        per_sm[wide] = nb > 0 ? nb : 1;
+    }
+    const int ch = wide ? 6 : 4;
+    const int64_t units = T * ((L / 8 + 32 * ch - 1) / (32 * ch));
+    const int64_t need = (units + 7) / 8;   // blocks of 8 warps, one unit each
+    const int64_t most = static_cast<int64_t>(sms) * per_sm[wide];
+    const unsigned grid = static_cast<unsigned>(need < most ? need : most);
+    if (wide)
         combine_kernel<6><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c, rows);
+    else
+        combine_kernel<4><<<grid, 256, 0, st>>>(ypool, slot_of, w, T, k, L, c, rows);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "combine");
     return MOE_OK;
