@@ -21,7 +21,10 @@ namespace moe {
 
 // dY = bf16(w_tj dc_t) for kept (t, j), written to the assignment's row in
 // the per-expert layout (rowinv of its pool slot); dw_tj = <dc_t, Y[slot]>
-// (fp32).  One warp per token.
+// (fp32).  One warp per token, each lane's 16-byte chunks ch = lane + 32 i
+// taken in passes of CH, both rows' chunks of a pass loaded before any is
+// used.  The grid holds only the blocks resident at once; each warp strides
+// over the tokens.
 template <int CH>
 __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ dc,
                                                           const uint16_t* __restrict__ ypool,
@@ -32,48 +35,64 @@ __global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __rest
                                                           float* __restrict__ dw, int64_t rows,
                                                           int64_t dst_rows) {
     const int lane = threadIdx.x & 31;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    int32_t my_row = -1, my_dst = 0;
-    float my_w = 0.0f;
-    if (lane < k) {
-        my_row = slot_of[t * k + lane];
-        my_w = w[t * k + lane];
-        if (my_row >= 0 && !moe_check(my_row < rows, 1007)) my_row = -1;
-        if (my_row >= 0) my_dst = rowinv[my_row];
-        if (my_row >= 0 && !moe_check(my_dst >= 0 && my_dst < dst_rows, 1008)) my_row = -1;
-    }
     const int nchunk = L / 8;
-    float dot_mine = 0.0f;   // lane j keeps dw for assignment j
-    for (int j = 0; j < k; ++j) {
-        const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
-        const int32_t rd = __shfl_sync(0xffffffffu, my_dst, j);
-        const float wj = __shfl_sync(0xffffffffu, my_w, j);
-        float dot = 0.0f;
-        if (r >= 0) {
-            const uint4* yrow = reinterpret_cast<const uint4*>(ypool + static_cast<int64_t>(r) * L);
-            uint4* drow = reinterpret_cast<uint4*>(dy + static_cast<int64_t>(rd) * L);
-            const uint4* crow = reinterpret_cast<const uint4*>(dc + t * L);
-            for (int ch = lane; ch < nchunk; ch += 32) {
-                const uint4 cv = __ldg(crow + ch);
-                const uint4 yv = __ldg(yrow + ch);
-                const uint32_t cu[4] = {cv.x, cv.y, cv.z, cv.w};
-                const uint32_t yu[4] = {yv.x, yv.y, yv.z, yv.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float c0 = bf16_lo(cu[h]), c1 = bf16_hi(cu[h]);
-                    dot = fmaf(c0, bf16_lo(yu[h]), dot);
-                    dot = fmaf(c1, bf16_hi(yu[h]), dot);
-                    o[h] = pack_bf16x2(wj * c0, wj * c1);
-                }
-                drow[ch] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         t < T; t += nwarps) {
+        int32_t my_row = -1, my_dst = 0;
+        float my_w = 0.0f;
+        if (lane < k) {
+            my_row = slot_of[t * k + lane];
+            my_w = w[t * k + lane];
+            if (my_row >= 0 && !moe_check(my_row < rows, 1007)) my_row = -1;
+            if (my_row >= 0) my_dst = rowinv[my_row];
+            if (my_row >= 0 && !moe_check(my_dst >= 0 && my_dst < dst_rows, 1008)) my_row = -1;
         }
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        if (lane == j) dot_mine = r >= 0 ? dot : 0.0f;
+        const uint4* crow = reinterpret_cast<const uint4*>(dc + t * L);
+        float dot_mine = 0.0f;   // lane j keeps dw for assignment j
+        for (int j = 0; j < k; ++j) {
+            const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+            const int32_t rd = __shfl_sync(0xffffffffu, my_dst, j);
+            const float wj = __shfl_sync(0xffffffffu, my_w, j);
+            float dot = 0.0f;
+            if (r >= 0) {
+                const uint4* yrow =
+                    reinterpret_cast<const uint4*>(ypool + static_cast<int64_t>(r) * L);
+                uint4* drow = reinterpret_cast<uint4*>(dy + static_cast<int64_t>(rd) * L);
+                for (int cb = 0; cb < nchunk; cb += 32 * CH) {
+                    uint4 cv[CH], yv[CH];
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) {
+                        const int ch = cb + lane + 32 * q;
+                        if (ch < nchunk) {
+                            cv[q] = __ldg(crow + ch);
+                            yv[q] = __ldg(yrow + ch);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < CH; ++q) {
+                        const int ch = cb + lane + 32 * q;
+                        if (ch < nchunk) {
+                            const uint32_t cu[4] = {cv[q].x, cv[q].y, cv[q].z, cv[q].w};
+                            const uint32_t yu[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const float c0 = bf16_lo(cu[h]), c1 = bf16_hi(cu[h]);
+                                dot = fmaf(c0, bf16_lo(yu[h]), dot);
+                                dot = fmaf(c1, bf16_hi(yu[h]), dot);
+                                o[h] = pack_bf16x2(wj * c0, wj * c1);
+                            }
+                            drow[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+            }
+            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+            if (lane == j) dot_mine = r >= 0 ? dot : 0.0f;
+        }
+        if (lane < k) dw[t * k + lane] = dot_mine;
     }
-    if (lane < k) dw[t * k + lane] = dot_mine;
 }
 
 // dlogits[t, e] = bf16(w_j (dw_j - sum_i w_i dw_i)) for e = idx[t, j], else 0.
@@ -373,13 +392,28 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
             row_inverse_kernel<<<g_inv, 256, 0, st>>>(a.expert_rows, a.expert_count, E, cr, rowinv);
             zero_pad_rows_kernel<<<g_pad, 256, 0, st>>>(dye, a.expert_count, E, cr, L);
         }
-        const unsigned grid = static_cast<unsigned>((T + 7) / 8);
-        if (L / 8 <= 32 * 4)
-            combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
-                                                         L, dye, dw, g.pool_rows, PE);
-        else
+        // resident blocks of each instance, queried once (no runtime call
+        // inside a stream capture after the first launch)
+        static int per_sm[2] = {0, 0};
+        const bool wide = L / 8 > 32 * 4;
+        if (!per_sm[wide]) {
+            int nb = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &nb, wide ? combine_bwd_kernel<12> : combine_bwd_kernel<4>, 256, 0) !=
+                cudaSuccess)
+                return MOE_ECUDA;
+            per_sm[wide] = nb > 0 ? nb : 1;
+        }
+        int dev, sms;
+        if ((rc = current_device(&dev, &sms))) return rc;
+        const int64_t need = (T + 7) / 8, most = static_cast<int64_t>(sms) * per_sm[wide];
+        const unsigned grid = static_cast<unsigned>(need < most ? need : most);
+        if (wide)
             combine_bwd_kernel<12><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
                                                           L, dye, dw, g.pool_rows, PE);
+        else
+            combine_bwd_kernel<4><<<grid, 256, 0, st>>>(dc, a.ypool, a.slot_of, rowinv, a.w, T, k,
+                                                         L, dye, dw, g.pool_rows, PE);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_combine");
     }
