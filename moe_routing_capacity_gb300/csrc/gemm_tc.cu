@@ -1057,8 +1057,7 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
     if (ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES) != MOE_OK)
         return MOE_ECUDA;
     if (CG2) {   // clusters of two CTAs (grid is even)
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof(cfg));
+        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid, 1, 1);
         cfg.blockDim = dim3(p.wp_a.pool ? 384 : 256, 1, 1);   // + 4 copy warps
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -1073,8 +1072,7 @@ static int launch_inst(const KParams& p, int grid, cudaStream_t st) {
         if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
     } else if (AMODE == A_GATHER && p.wp_ready) {
         // the copy warps' counters are waited on by every CTA: all resident
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof(cfg));
+        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid, 1, 1);
         cfg.blockDim = dim3(512, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
