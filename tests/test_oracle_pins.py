@@ -320,14 +320,17 @@ def _tiny_inputs(cfg):
             for k, v in wl.make_inputs(cfg, "cpu").items()}
 
 
-def test_worked_example_by_hand():
-    g = json.load(open(os.path.join(GOLD, "worked_example.json")))
+def _golden_layer(name):
+    g = json.load(open(os.path.join(GOLD, name)))
     cfg = _cfg(**g["config"])
     t = {k: np.array(g[k], dtype=np.float64) for k in
          ("x", "Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Wsd")}
     t["bias"] = None
-    r = O.layer(cfg, t)
-    ex = g["expect"]
+    return O.layer(cfg, t), g["expect"]
+
+
+def test_worked_example_by_hand():
+    r, ex = _golden_layer("worked_example.json")
     np.testing.assert_array_equal(r["logits"], ex["logits"])
     assert r["idx"].tolist() == ex["idx"]
     np.testing.assert_array_equal(r["w"], ex["w"])
@@ -337,6 +340,50 @@ def test_worked_example_by_hand():
     assert r["disp"]["slot_of"].tolist() == ex["slot_of"]
     np.testing.assert_array_equal(r["Y"][0], ex["Y_row0"])
     np.testing.assert_array_equal(r["Y"][1], ex["Y_row1"])
+    np.testing.assert_array_equal(r["c"], ex["c"])
+    np.testing.assert_array_equal(r["a"], ex["a"])
+    np.testing.assert_array_equal(r["out"], ex["out"])
+
+
+def test_partial_drop_by_hand():
+    """A token whose second assignment overflows the receiver's one-row cap
+    keeps its first expert's output at the unchanged gate weight (no
+    renormalisation), and its shared term; the dropped row is counted."""
+    r, ex = _golden_layer("partial_drop.json")
+    np.testing.assert_array_equal(r["logits"], ex["logits"])
+    assert r["idx"].tolist() == ex["idx"]
+    np.testing.assert_allclose(r["w"], ex["w"], rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(r["z"], ex["z"])
+    assert (r["plan"].c_send, r["plan"].c_recv, r["plan"].pool_rows) == \
+        (ex["c_send"], ex["c_recv"], ex["pool_rows"])
+    d = r["disp"]
+    assert d["slot_of"].tolist() == ex["slot_of"]
+    assert d["drop"].tolist() == ex["drop"]
+    assert d["expert_rows"].tolist() == ex["expert_rows"]
+    assert d["count"].tolist() == ex["count"]
+    assert d["stats"] == ex["stats"]
+    assert r["tags"].tolist() == ex["tags"]
+    assert sorted(r["Y"]) == sorted(int(k) for k in ex["Y"])
+    for row, y in ex["Y"].items():
+        np.testing.assert_array_equal(r["Y"][int(row)], y)
+    np.testing.assert_array_equal(r["c"], ex["c"])
+    for wrong in ("c_if_renormalised", "c_if_wrong_rank_dropped"):
+        assert not np.array_equal(r["c"], ex[wrong])
+    np.testing.assert_array_equal(r["a"], ex["a"])
+    np.testing.assert_array_equal(r["out"], ex["out"])
+
+
+def test_two_shared_experts_by_hand():
+    """Two shared experts with distinct weights: each one's activations sit
+    in its own slice of a, and out carries the sum of both down-projections."""
+    r, ex = _golden_layer("two_shared.json")
+    np.testing.assert_array_equal(r["logits"], ex["logits"])
+    assert r["idx"].tolist() == ex["idx"]
+    np.testing.assert_array_equal(r["w"], ex["w"])
+    np.testing.assert_array_equal(r["z"], ex["z"])
+    assert (r["plan"].c_send, r["plan"].c_recv, r["plan"].pool_rows) == \
+        (ex["c_send"], ex["c_recv"], ex["pool_rows"])
+    assert r["disp"]["slot_of"].tolist() == ex["slot_of"]
     np.testing.assert_array_equal(r["c"], ex["c"])
     np.testing.assert_array_equal(r["a"], ex["a"])
     np.testing.assert_array_equal(r["out"], ex["out"])
