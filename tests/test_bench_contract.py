@@ -45,3 +45,17 @@ def test_gb300_arm_fails_without_gpu():
     r = _run(["--steps", "1", "--warmup", "1", "--no-cpu-baseline"])
     assert r.returncode != 0
     assert not r.stdout.strip(), "no result line without a GPU"
+
+
+def test_tensor_peak_follows_the_clock_of_the_timed_region():
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = dict(hbm=6786.6, bf16=1910.8, bf16_sustained=1715.2, source="measured")
+    at_max = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    capped = {"sm_mhz": 1650.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert bench.tensor_peak_for(pk, 0.09, at_max) == ("burst", 1910.8, 1715.2)
+    assert bench.tensor_peak_for(pk, 0.09, None) == ("burst", 1910.8, 1715.2)
+    assert bench.tensor_peak_for(pk, 1.4, at_max) == ("sustained", 1715.2, 1910.8)
+    assert bench.tensor_peak_for(pk, 0.5, capped) == ("sustained", 1715.2, 1910.8)
+    low = {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.tensor_peak_for(pk, 0.5, low)[0] == "sustained"
