@@ -211,7 +211,10 @@ int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_
  *    T*k up to about 678,000 assignments at E=384, 64 ranks, 3 waves).
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress, with that device current) and caches
- *    it; make that first call before any stream capture.
+ *    it together with the id of the device's CUDA context; make that first
+ *    call before any stream capture.  After cudaDeviceReset the device's
+ *    next context has another id, so the next call looks the address up
+ *    again (and should also come before any capture).
  *  - Sharing: every call on a device uses the same array, which keeps the
  *    last call's contents.  Nothing in it needs to start at zero (each call
  *    writes every word before reading it), but calls whose work overlaps on
@@ -427,6 +430,18 @@ int moe_balance_update_window(const moe_config_t* cfg, const int32_t* idx, int64
  * first recorded code since the last call (0: none) and resets it; a normal
  * build always returns 0.  Synchronous: call after the work has finished. */
 int moe_check_status(void);
+
+/* Checked builds only (libmoe_pooled_wave_check.so; a normal build does not
+ * export it; the pages define no such operation): sets the limit, in ns of
+ * the GPU's global timer, of the wave pipeline's wait for every CTA's count
+ * of a wave (moe_dispatch_expert_waves; default 4e9 = 4 s).  A test sets it
+ * near 0 so that the wait runs out on legitimate work: the waiting threads
+ * record MOE_ETIMEOUT in the status word, raise their CTA's abort flag and
+ * the CTA unwinds (armed copies land, issued MMAs finish, TMEM is freed)
+ * and returns.  The waits that drain copies and MMAs keep their own limits.
+ * Affects launches enqueued after it returns, on the current device.
+ * Returns MOE_OK, or MOE_ECUDA if the device symbol cannot be written. */
+int moe_check_set_wave_wait_limit_ns(unsigned long long ns);
 
 /* Kernel timing trace (instrumentation; the pages define no such operation).
  * moe_trace_begin(n) creates n CUDA events (timing enabled) owned by the

@@ -28,6 +28,8 @@ EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project"
            "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_check_status", "moe_strerror",
            "moe_abi_version")
+# Declared in the header too, but exported by the checked build only.
+CHECKED_ONLY = ("moe_check_set_wave_wait_limit_ns",)
 
 
 class MoeError(RuntimeError):
@@ -136,6 +138,9 @@ def load_library(path: str) -> ctypes.CDLL:
     for n in EXPORTS:
         if n != "moe_strerror":
             getattr(L, n).restype = ctypes.c_int
+    if hasattr(L, "moe_check_set_wave_wait_limit_ns"):
+        L.moe_check_set_wave_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        L.moe_check_set_wave_wait_limit_ns.restype = ctypes.c_int
     return L
 
 
@@ -236,6 +241,8 @@ def dispatch_pooled(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_co
         _stream(stream)))
 
 
+# MOE_DISPATCH_NOALLOC_SCRATCH_BYTES of the header (a host test checks that
+# the two agree)
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 

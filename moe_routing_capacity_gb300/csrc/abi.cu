@@ -206,6 +206,13 @@ int moe_check_status(void) {
     return 0;
 }
 
+#if MOE_CHECK
+int moe_check_set_wave_wait_limit_ns(unsigned long long ns) {
+    const int rc = moe::set_wave_wait_limit(ns);
+    return rc;
+}
+#endif
+
 int moe_trace_begin(int capacity) {
     std::lock_guard<std::mutex> lk(trace_mu);
     if (capacity < 0) return MOE_EINVAL;

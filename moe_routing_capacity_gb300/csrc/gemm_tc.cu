@@ -134,6 +134,27 @@ struct KParams {
     int raster_gn;          // dense tiles: column blocks a band (0: row tile by row tile)
 };
 
+// Limit of the wave pipeline's wait for every CTA's count of a wave.  In
+// checked builds a test can shorten it from the host, so that the wait runs
+// out on legitimate work and the unwinding path is exercised; only this wait
+// reads it (the waits that drain copies and MMAs keep their own limits).
+#if MOE_CHECK
+static __device__ unsigned long long g_wave_wait_limit_ns = kWaitTimeoutNs;
+__device__ __forceinline__ uint64_t wave_wait_limit() { return g_wave_wait_limit_ns; }
+#else
+__device__ __forceinline__ uint64_t wave_wait_limit() { return kWaitTimeoutNs; }
+#endif
+
+int set_wave_wait_limit(unsigned long long ns) {
+#if MOE_CHECK
+    return cudaMemcpyToSymbol(g_wave_wait_limit_ns, &ns, sizeof(ns)) == cudaSuccess ? MOE_OK
+                                                                                    : MOE_ECUDA;
+#else
+    (void)ns;
+    return MOE_EINVAL;
+#endif
+}
+
 // The pack run by extra warps of a GEMM launch (pack_token), tokens dealt
 // out over the grid's copy warps (cw of ncw in this CTA): the receiver
 // decisions (decide) and the copies of wave w (every wave if w < 0), with
@@ -908,7 +929,7 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                 if (!(waves_seen >> wv & 1u)) {
                     if (t == 0) *gather_wave = wv;   // lets this CTA copy wave wv + 1
                     if (!wait_count(p.wp_ready + wv, static_cast<int>(gridDim.x), abort_flag,
-                                    p.status)) {
+                                    p.status, wave_wait_limit())) {
                         ok = false;
                         break;
                     }
@@ -953,19 +974,15 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
         // thread releases the CTA's count in wp_ready[w].  Wave w >= 2 is
         // copied once this CTA's row gather has reached wave w-1, so that
         // the extra memory traffic spreads over the compute of the earlier
-        // waves instead of piling onto wave 0's (a bounded wait: on expiry
-        // the copy goes ahead).
+        // waves instead of piling onto wave 0's.  This wait only paces the
+        // copy: on expiry the copy goes ahead and nothing is reported, since
+        // the results do not depend on it.
         const int cw = warp - 12;
         for (int w = 1; w < p.wp_g.W; ++w) {
             if (w >= 2 && *gather_wave < w - 1) {
                 const uint64_t t0 = globaltimer_ns();
-                while (*gather_wave < w - 1 && !*abort_flag) {
+                while (*gather_wave < w - 1 && !*abort_flag && globaltimer_ns() - t0 < kWaitTimeoutNs)
                     __nanosleep(500);
-                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-                        report_error(p.status, MOE_ETIMEOUT);
-                        break;
-                    }
-                }
             }
             pack_tokens(p, false, w, cw, 4, lane);
             named_bar_sync(1, 128);

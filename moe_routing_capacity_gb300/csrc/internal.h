@@ -183,6 +183,8 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
 // checks since the last call (0: none), reset on reading.
 int check_status_route();
 int check_status_gemm();
+// Checked builds: the limit of the wave pipeline's cross-CTA wait (MOE_EINVAL otherwise).
+int set_wave_wait_limit(unsigned long long ns);
 int check_status_backward();
 
 // wave_El > 0: wave-major entry order (wave_El local experts a destination,

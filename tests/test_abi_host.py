@@ -24,13 +24,32 @@ def built_library():
     return abi.lib()
 
 
-def _declared():
+def _declared_all():
     src = open(HEADER).read()
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, re.M)))
 
 
+def _declared():
+    """Entry points every build exports (the checked build's test hooks aside)."""
+    return [n for n in _declared_all() if n not in abi.CHECKED_ONLY]
+
+
 def test_header_and_binding_agree():
     assert sorted(abi.EXPORTS) == _declared()
+    assert set(abi.CHECKED_ONLY) <= set(_declared_all())
+
+
+def test_checked_only_hooks_absent_from_the_normal_build():
+    L = abi.lib()
+    for name in abi.CHECKED_ONLY:
+        assert not hasattr(L, name), name
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+MOE_DISPATCH_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "MOE_DISPATCH_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert abi.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
 
 
 def test_library_exports_every_declared_symbol():
