@@ -11,6 +11,8 @@
 // as long as the library is loaded, and forwards to moe_dispatch_pooled.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "internal.h"
 
 // The fixed scratch.  Every GPU that loads the library holds these bytes
@@ -24,18 +26,50 @@ namespace {
 constexpr size_t kScratchBytes = MOE_DISPATCH_NOALLOC_SCRATCH_BYTES;
 
 std::mutex g_mu;
-void* g_scratch_ptr[128];   // device address of g_dispatch_scratch, per device
+void* g_scratch_ptr[128];                 // device address of g_dispatch_scratch, per device
+unsigned long long g_scratch_ctx[128];    // id of the context that address belongs to
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(f);
+}
+
+// Id of this thread's current CUDA context (unique within the process and
+// never reused, so a context made after cudaDeviceReset gets a new one);
+// 0 when there is no current context or the id cannot be read.
+unsigned long long current_context_id() {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of the scratch on the current device.  Looked up with that
+// device current the first time a context of the device calls here, and
+// cached with the context's id; a later context of the same device (after a
+// device reset) looks it up again.  Without a readable context id nothing is
+// cached.
 int scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return MOE_ECUDA;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ECUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return MOE_OK;
