@@ -98,13 +98,14 @@ def source_hash(kernel="gemm"):
     return h.hexdigest()[:16]
 
 
-def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None):
+def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None, bank=False):
     """Algorithmic work of one launch: (amount, unit, bound).  The pack
     kernel's bytes depend on where the pool fill runs: all of it (none) or
     wave 0's rows (waves: sent_w0 sender-kept rows); with the shared
     schedule the whole pack runs inside the shared gate/up launch and the
-    pack kernel is not launched.  Pack work done inside a GEMM launch is not
-    added to its flops."""
+    pack kernel is not launched.  With the per-expert bank the pack also
+    writes every receiver-kept row a second time.  Pack work done inside a
+    GEMM launch is not added to its flops."""
     T, d, L, E, k = cfg.T, cfg.d_model, cfg.d_latent, cfg.n_experts, cfg.top_k
     H, Hs, ns = cfg.h_expert, cfg.h_shared, cfg.n_shared
     kept = st["kept"]
@@ -126,7 +127,8 @@ def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None):
         # plus the per-assignment decisions
         "dispatch_pack": (T * L * 2 + sent * (2 * L + 16) if pipeline == "none" else
                           T * L * 2 + sent_w0 * (2 * L + 16) if pipeline == "waves" else 0)
-                         + T * k * (4 + 8 + 4 + 4 + 1) + kept * 4,
+                         + T * k * (4 + 8 + 4 + 4 + 1) + kept * 4
+                         + (kept * L * 2 if bank and pipeline == "none" else 0),
         "dispatch_init": plan.pool_rows * 16 + E * plan.c_recv * 4,
         # every kept expert row read once, c written once, slots and weights read
         "combine": kept * L * 2 + T * L * 2 + T * k * 8,
@@ -134,6 +136,27 @@ def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None):
     if name in B:
         return B[name] / 1e9, "GB", "hbm"
     return None, None, "latency"
+
+
+def expert_mma_rows(counts, c_recv, bank_path):
+    """Rows the expert products multiply per weight row.  Gathered path: each
+    expert's rows padded to whole 128-row tiles.  Bank path (CTA pairs, rows
+    on the MMA's N axis): an expert's n rows in ceil(n / 256) chunks of even
+    size rounded up to 32, each chunk's width rounded up to 32."""
+    total = 0
+    for n in counts:
+        n = max(0, min(int(n), c_recv))
+        if not bank_path:
+            total += (n + 127) // 128 * 128
+            continue
+        nch = (n + 255) // 256
+        if nch == 0:
+            continue
+        per = ((n + nch - 1) // nch + 31) // 32 * 32
+        for i in range(nch):
+            rows = min(per, n - i * per)
+            total += (rows + 31) // 32 * 32
+    return total
 
 
 def tensor_peak_for(pk, elapsed_s, clk):
@@ -338,11 +361,11 @@ def run_gb300(args, rank, world, local_rank):
     # tokens whose k-th and (k+1)-th (or two adjacent selected) logits are within
     # the near-tie gap: their routing may legitimately differ from the oracle's
     near_ties = int((m.tie != 0).sum().item())
-    # MMA rows the expert GEMMs compute: each expert's rows padded to whole
-    # 128-row tiles (the padding is work the tensor cores do but the
-    # algorithmic flop count leaves out)
-    cnt = m.expert_count.to(torch.int64)
-    tile_rows = int((((cnt + 127) // 128) * 128).sum().item())
+    # MMA rows the expert GEMMs compute (the padding is work the tensor cores
+    # do but the algorithmic flop count leaves out)
+    tile_rows = expert_mma_rows(m.expert_count.tolist(), m.plan.c_recv,
+                                m.bank is not None and cfg.d_latent % 256 == 0
+                                and cfg.h_expert % 128 == 0)
     # sender-kept rows of wave 0 (what the pack kernel copies when the later
     # waves are filled inside the expert gate/up launch)
     e_w = cfg.n_experts // cfg.n_ranks // cfg.n_waves
@@ -541,7 +564,8 @@ def run_gb300(args, rank, world, local_rank):
         # bandwidth against the HBM copy peak, beside the main arm's kernels
         pk_ms = pipes["none"]["kernel_ms"].get("dispatch_pack")
         if pk_ms:
-            pw, pu, _ = kernel_work("dispatch_pack", cfg, m.plan, st, "none")
+            pw, pu, _ = kernel_work("dispatch_pack", cfg, m.plan, st, "none",
+                                    bank=arms["none"].bank is not None)
             ach = pw / (pk_ms / 1e3)
             kernels["dispatch_pack"] = {
                 "ms_per_launch": pk_ms, "launches": 7 * n_p, "work_per_launch": pw,
@@ -552,7 +576,8 @@ def run_gb300(args, rank, world, local_rank):
         sg_with = pipes["shared"]["kernel_ms"].get("gemm_shared_gateup")
         sg_without = pipes["none"]["kernel_ms"].get("gemm_shared_gateup")
         if sg_with and sg_without:
-            pw, _, _ = kernel_work("dispatch_pack", cfg, m.plan, st, "none")
+            pw, _, _ = kernel_work("dispatch_pack", cfg, m.plan, st, "none",
+                                   bank=arms["shared"].bank is not None)
             marg = sg_with - sg_without
             pipes["pack_in_shared_gateup"] = {
                 "with_pack_ms": sg_with, "without_pack_ms": sg_without,
@@ -689,6 +714,9 @@ def run_gb300(args, rank, world, local_rank):
                        f"H={cfg.h_expert}, cf {cfg.cf_send}/{cfg.cf_recv}",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "pool_fill": pipeline,
+                       "expert_path": ("CTA pairs, expert rows on the MMA's N axis from the "
+                                       "per-expert bank" if m.bank is not None
+                                       else "rows gathered from the pool"),
                        "l2": "inputs larger than L2 (8.1 GB weights per step)"},
             "assignments_per_s": value * cfg.top_k,
             "drops": {"near_tie_tokens": near_ties,

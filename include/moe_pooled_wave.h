@@ -188,12 +188,19 @@ int moe_route_project(const moe_config_t* cfg, const uint16_t* x, const uint16_t
  *   expert_rows [E, c_recv] int32: pool rows of expert e in arrival order,
  *               -1 after expert_count[e]
  *   expert_count[E] int32        stats: moe_drop_stats_t (device)
+ *   bank        optional (NULL: not written) [E, c_recv, L] bf16, 16-byte
+ *               aligned: the receiver's rows grouped by local expert, i.e.
+ *               bank[e][r] = z[t] for the assignment in expert_rows[e][r];
+ *               rows r >= expert_count[e] are left as they were.  On one GPU
+ *               the receiver side of the exchange lives in the same memory,
+ *               so the pack writes this arrangement directly; it lets
+ *               moe_expert_ffn_grouped load each expert's rows as whole tiles.
  * Out-of-range expert ids in idx give MOE_EINVAL in stats->status and leave
  * the outputs undefined. */
 int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
                         void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
                         uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
-                        moe_drop_stats_t* stats, void* stream);
+                        moe_drop_stats_t* stats, uint16_t* bank, void* stream);
 
 /* moe_dispatch_pooled for callers that cannot allocate device memory.  The
  * paper has no counterpart: it is a way of calling the dispatch above.
@@ -259,10 +266,17 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
  * and Y is written to ypool at that same pool row (the return path keeps the
  * slot).  Rows of ypool that no expert computes are left untouched.
  *   Wg, Wu [E, H, L] bf16     Wd [E, L, H] bf16     ypool [pool_rows, L] bf16
- *   ws     scratch, >= plan.ws_ffn_bytes (holds h at plan.h_offset_bytes)
+ *   ws     scratch, >= plan.ws_ffn_bytes (holds h [E, c_recv, H] at
+ *          plan.h_offset_bytes; rows r < expert_count[e] written)
+ *   bank   optional: the per-expert rows written by the dispatch (see
+ *          moe_dispatch_pooled); NULL: the rows are gathered from the pool.
+ *          With a bank, L a multiple of 256 and H of 128, the products run
+ *          on CTA pairs with each expert's rows on the MMA's N axis, in
+ *          chunks of at most 256 rows (less padding than 128-row tiles);
+ *          otherwise as without it.
  * The pages give each receiver its local experts (section 二) but no
  * activation; the SwiGLU form and the hidden size are the workload's. */
-int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
+int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool, const uint16_t* bank,
                            const int32_t* expert_rows, const int32_t* expert_count,
                            const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                            void* ws, size_t ws_bytes, uint16_t* ypool, int32_t* status,
@@ -271,9 +285,9 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
 /* Wave-pipelined dispatch and experts (lamjinlab zh-HK section 二: the
  * waves let the exchange of one wave overlap the computation of another).
  * Same arguments, outputs and errors as moe_dispatch_pooled(cfg, z, idx, ws,
- * ws_bytes, pool, slot_of, drop, expert_rows, expert_count, stats, stream)
- * followed by moe_expert_ffn_grouped(cfg, pool, expert_rows, expert_count,
- * Wg, Wu, Wd, ffn_ws, ffn_ws_bytes, ypool, status, stream), and the same
+ * ws_bytes, pool, slot_of, drop, expert_rows, expert_count, stats, NULL,
+ * stream) followed by moe_expert_ffn_grouped(cfg, pool, NULL, expert_rows,
+ * expert_count, Wg, Wu, Wd, ffn_ws, ffn_ws_bytes, ypool, status, stream), and the same
  * results bit for bit.  The dispatch makes every sender and receiver
  * decision but writes only wave 0's payload rows; the gate/up launch, one
  * CTA per SM launched cooperatively, copies the rows of waves 1..W-1 into
@@ -293,23 +307,24 @@ int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const 
 /* Dispatch overlapped with the shared experts.  The shared experts see every
  * token and do not depend on the routing (lamjinlab zh-HK section 四: a dense
  * backbone beside the routed experts), so the exchange can proceed while
- * they compute.  Same arguments, outputs and errors as moe_dispatch_pooled,
- * plus the shared experts' activations
+ * they compute.  Same arguments, outputs and errors as moe_dispatch_pooled
+ * (the optional bank included), plus the shared experts' activations
  *   a = bf16(silu(x Wsg_s^T) * (x Wsu_s^T)), [T, n_s*Hs] (as moe_combine)
  *   x [T, d]  Wsg, Wsu [n_s, Hs, d]  status: device status word
  * and the same results bit for bit as moe_dispatch_pooled followed by
  * moe_combine's shared step.  The sender stage and the receiver counts run
  * as kernels of their own; the final decisions (slot_of, drop codes, the
- * expert row lists) and the pool's payload rows and tags are written by
- * four extra warps per CTA of the shared gate/up launch.  Pass
+ * expert row lists) and the pool's payload rows and tags (and the bank's
+ * rows) are written by four extra warps per CTA of the shared gate/up
+ * launch.  Pass
  * Wsg = Wsu = NULL to moe_combine afterwards so that it uses this a.  With
  * n_s = 0 or no tokens it is moe_dispatch_pooled. */
 int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
                                 void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
                                 uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
-                                moe_drop_stats_t* stats, const uint16_t* x, const uint16_t* Wsg,
-                                const uint16_t* Wsu, uint16_t* a, int32_t* status,
-                                void* stream);
+                                moe_drop_stats_t* stats, uint16_t* bank, const uint16_t* x,
+                                const uint16_t* Wsg, const uint16_t* Wsu, uint16_t* a,
+                                int32_t* status, void* stream);
 
 /* Return path, weighted combine, up-projection and shared experts:
  *   c[t]   = bf16(sum over kept j, in j order, of w[t,j] * ypool[slot_of[t,j]])
@@ -462,7 +477,8 @@ int moe_trace_event(int i, const char** name, float* ms_since_prev);
 /* Human-readable name of a MOE_* code (static string). */
 const char* moe_strerror(int code);
 
-/* ABI version: 1. */
+/* ABI version: 2 (the optional per-expert bank of the dispatch and the
+ * expert FFN). */
 int moe_abi_version(void);
 
 #ifdef __cplusplus

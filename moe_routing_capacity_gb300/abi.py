@@ -109,14 +109,14 @@ def load_library(path: str) -> ctypes.CDLL:
     L.moe_route_project.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_matmul.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, i64, i32, i32, vp,
                              ctypes.c_int, i64, vp, vp]
-    L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_pooled.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_dispatch_pooled_noalloc.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-    L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    L.moe_expert_ffn_grouped.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.moe_combine.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_dispatch_expert_waves.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp,
                                             vp, vp, sz, vp, vp, vp]
     L.moe_dispatch_shared_overlap.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp,
-                                              vp, vp, vp, vp]
+                                              vp, vp, vp, vp, vp]
     L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
     L.moe_balance_update_window.argtypes = [pc, vp, vp, vp, i32, vp, ctypes.c_float, vp, vp]
     L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
@@ -233,12 +233,14 @@ def route_project(cfg, x, Wr, bias, W_ld, logits, idx, w, tie, z, status, stream
 
 
 def dispatch_pooled(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
-                    stream=None):
+                    stream=None, bank=None):
+    """bank (optional, [E, c_recv, L] bf16): also receives each receiver-kept
+    row at its expert's receiver rank."""
     _check("moe_dispatch_pooled", lib().moe_dispatch_pooled(
         ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
         ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
         _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(stats, torch.int64),
-        _stream(stream)))
+        _ptr(bank, bf16, allow_none=True), _stream(stream)))
 
 
 # MOE_DISPATCH_NOALLOC_SCRATCH_BYTES of the header (a host test checks that
@@ -257,9 +259,12 @@ def dispatch_pooled_noalloc(cfg, z, idx, pool, slot_of, drop, expert_rows, exper
 
 
 def expert_ffn_grouped(cfg, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ypool, status,
-                       stream=None):
+                       stream=None, bank=None):
+    """bank (optional): the per-expert rows the dispatch wrote; None gathers
+    the rows from the pool."""
     _check("moe_expert_ffn_grouped", lib().moe_expert_ffn_grouped(
-        ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16), _ptr(expert_rows, i32),
+        ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16),
+        _ptr(bank, bf16, allow_none=True), _ptr(expert_rows, i32),
         _ptr(expert_count, i32), _ptr(Wg, bf16), _ptr(Wu, bf16), _ptr(Wd, bf16),
         _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32), _stream(stream)))
 
@@ -277,7 +282,7 @@ def dispatch_expert_waves(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, exp
 
 
 def dispatch_shared_overlap(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count,
-                            stats, x, Wsg, Wsu, a, status, stream=None):
+                            stats, x, Wsg, Wsu, a, status, stream=None, bank=None):
     """dispatch_pooled plus the shared experts' activations a, the pool rows
     copied while the shared gate/up product computes; then call combine with
     Wsg = Wsu = None."""
@@ -285,6 +290,7 @@ def dispatch_shared_overlap(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, e
         ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
         ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
         _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(stats, torch.int64),
+        _ptr(bank, bf16, allow_none=True),
         _ptr(x, bf16, allow_none=True), _ptr(Wsg, bf16, allow_none=True),
         _ptr(Wsu, bf16, allow_none=True), _ptr(a, bf16, allow_none=True), _ptr(status, i32),
         _stream(stream)))

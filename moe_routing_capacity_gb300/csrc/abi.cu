@@ -161,7 +161,9 @@ static int make_geom(const moe_config_t* c, Geom* out) {
     p.pool_row_bytes = 2 * pool_pitch(g.L);
     p.ws_dispatch_bytes = static_cast<int64_t>(dispatch_ws_layout(g).total);
     const size_t max_mt = static_cast<size_t>(g.E) * ((g.c_recv + 127) / 128);
-    const size_t tiles_bytes = align_up(max_mt * 8 + 16, 1024);
+    // the tile list of the gathered path or the chunk list of the bank path
+    const size_t tiles_bytes =
+        align_up(std::max(max_mt * 8 + 16, expert_pair_chunks_bytes(g.E, g.c_recv)), 1024);
     p.h_offset_bytes = static_cast<int64_t>(tiles_bytes);
     p.ws_ffn_bytes = static_cast<int64_t>(tiles_bytes + static_cast<size_t>(g.E) * g.c_recv * out->H * 2);
     return MOE_OK;
@@ -197,10 +199,11 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 1; }
+int moe_abi_version(void) { return 2; }
 
 int moe_check_status(void) {
-    const int v[3] = {check_status_route(), check_status_gemm(), check_status_backward()};
+    const int v[4] = {check_status_route(), check_status_gemm(), check_status_backward(),
+                      check_status_expert_pair()};
     for (int x : v)
         if (x) return x;
     return 0;
@@ -408,7 +411,7 @@ int moe_matmul(const uint16_t* A, int a_mn, int64_t lda, const uint16_t* B, int 
 int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx, void* ws,
                         size_t ws_bytes, uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                         int32_t* expert_rows, int32_t* expert_count, moe_drop_stats_t* stats,
-                        void* stream) {
+                        uint16_t* bank, void* stream) {
     MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom(cfg, &G);
@@ -417,13 +420,14 @@ int moe_dispatch_pooled(const moe_config_t* cfg, const uint16_t* z, const int32_
         (G.g.pool_rows > 0 && !pool) || (G.plan.c_recv > 0 && !expert_rows) ||
         (G.plan.ws_dispatch_bytes > 0 && !ws))
         return MOE_EINVAL;
-    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || (ws && !aligned16(ws)))
+    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || (ws && !aligned16(ws)) ||
+        (bank && (!aligned16(bank) || G.g.L % 8)))
         return MOE_EINVAL;
     if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
     int dev, sms;
     if ((rc = current_device(&dev, &sms))) return rc;
     return launch_dispatch(G.g, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
-                           static_cast<cudaStream_t>(stream));
+                           static_cast<cudaStream_t>(stream), -1, true, bank);
 }
 
 int moe_plan_ragged(const moe_config_t* cfg, moe_plan_t* plan) {
@@ -544,13 +548,21 @@ struct WavePipe {
     PackArgs a;
 };
 
+// The per-expert bank path (CTA pairs, rows on the MMA's N axis) takes
+// widths that are whole 256-column output blocks and 128-unit hidden blocks.
+static bool pair_path_fits(const Geom& G) { return G.g.L % 256 == 0 && G.H % 128 == 0; }
+
 static int expert_ffn_capped(const Geom& G, uint16_t* pool, const int32_t* expert_rows,
                              const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
                              const uint16_t* Wd, void* ws, uint16_t* ypool, int32_t* status,
-                             cudaStream_t st, const WavePipe* wp) {
+                             cudaStream_t st, const WavePipe* wp, const uint16_t* bank = nullptr) {
     int rc;
     const DispatchGeom& g = G.g;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
+    if (bank && !wp && pair_path_fits(G))
+        return expert_ffn_pair(g.E, g.c_recv, g.L, G.H, bank, expert_rows, expert_count, Wg, Wu,
+                               Wd, ws, reinterpret_cast<uint16_t*>(wsb + G.plan.h_offset_bytes),
+                               ypool, g.pool_rows, status, st);
     int32_t* tiles = reinterpret_cast<int32_t*>(wsb);
     const int max_mt = g.E * ((g.c_recv + 127) / 128);
     int32_t* tile_count = reinterpret_cast<int32_t*>(wsb + static_cast<size_t>(max_mt) * 8);
@@ -636,7 +648,7 @@ static int check_ffn_args(const Geom& G, const uint16_t* pool, const int32_t* ex
     return MOE_OK;
 }
 
-int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
+int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool, const uint16_t* bank,
                            const int32_t* expert_rows, const int32_t* expert_count,
                            const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, void* ws,
                            size_t ws_bytes, uint16_t* ypool, int32_t* status, void* stream) {
@@ -648,8 +660,10 @@ int moe_expert_ffn_grouped(const moe_config_t* cfg, const uint16_t* pool,
     if ((rc = check_ffn_args(G, pool, expert_rows, expert_count, Wg, Wu, Wd, ws, ws_bytes, ypool,
                              status)))
         return rc;
+    if (bank && !aligned16(bank)) return MOE_EINVAL;
     return expert_ffn_capped(G, const_cast<uint16_t*>(pool), expert_rows, expert_count, Wg, Wu,
-                             Wd, ws, ypool, status, static_cast<cudaStream_t>(stream), nullptr);
+                             Wd, ws, ypool, status, static_cast<cudaStream_t>(stream), nullptr,
+                             bank);
 }
 
 int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
@@ -700,7 +714,8 @@ int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const 
 int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
                                 void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
                                 uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
-                                moe_drop_stats_t* stats, const uint16_t* x, const uint16_t* Wsg,
+                                moe_drop_stats_t* stats, uint16_t* bank, const uint16_t* x,
+                                const uint16_t* Wsg,
                                 const uint16_t* Wsu, uint16_t* a, int32_t* status,
                                 void* stream) {
     MOE_NVTX_RANGE();
@@ -726,7 +741,7 @@ int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, cons
     // without shared experts there is nothing to overlap the pack with
     const bool overlap = G.ns > 0 && g.T > 0 && g.pool_rows > 0;
     if ((rc = launch_dispatch(g, z, idx, ws, pool, slot_of, drop, expert_rows, expert_count, stats,
-                              st, -1, !overlap)))
+                              st, -1, !overlap, bank)))
         return rc;
     if (G.ns == 0 || g.T == 0) return MOE_OK;
     const DispatchWs Lw = dispatch_ws_layout(g);
@@ -757,6 +772,7 @@ int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, cons
         s1.wp_a.slot_of = slot_of;
         s1.wp_a.drop = drop;
         s1.wp_a.expert_rows = expert_rows;
+        s1.wp_a.bank = bank;
     }
     return gemm_launch(s1, st);
 }

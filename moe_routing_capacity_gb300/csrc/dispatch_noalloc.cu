@@ -92,5 +92,5 @@ extern "C" int moe_dispatch_pooled_noalloc(const moe_config_t* cfg, const uint16
     // Nothing in the scratch has to start at zero: within one call every word
     // the kernels read was written earlier in the same call.
     return moe_dispatch_pooled(cfg, z, idx, ws, moe::kScratchBytes, pool, slot_of, drop,
-                               expert_rows, expert_count, stats, stream);
+                               expert_rows, expert_count, stats, nullptr, stream);
 }

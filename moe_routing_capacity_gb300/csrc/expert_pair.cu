@@ -1,0 +1,555 @@
+// expert_pair.cu -- the routed experts' two products on CTA pairs, with an
+// expert's received rows on the MMA's N axis.
+//
+//   gate/up:  [Wg_e ; Wu_e] . X_e^T  ->  h_e = bf16(silu(g) * u)
+//   down:     Wd_e . h_e^T           ->  Y = bf16(.), each row scattered to its pool row
+//
+// The weight rows sit on M: a pair tile is 256 weight rows, 128 staged by each
+// CTA of a two-CTA cluster (tcgen05.mma.cta_group::2, issued by the even
+// CTA).  For gate/up a CTA's 128 rows are the gate and the up rows of the
+// same 64 hidden units, so its SwiGLU epilogue needs only its own TMEM.  The
+// expert's rows sit on N, in chunks of at most 256 rows sized evenly over
+// the expert's count and rounded up to 32 (each CTA stages half of them):
+// an M x N x 16 MMA costs N/2 cycles for N >= 128 (measured on this part),
+// so an expert with 316 rows computes two chunks of 160 (320 MMA rows)
+// instead of three 128-row tiles (384).  Both operands arrive by TMA: the
+// weights from their [E, rows, K] tensors, the expert's rows from a
+// per-expert bank [E, c_recv, K] (the received rows grouped by local expert,
+// written by the dispatch's pack; for the down product, h itself).  Bank
+// rows past an expert's count hold stale values: each one reaches only its
+// own column of the accumulator, which the epilogue never stores.
+//
+// Warp roles per CTA: 0 TMA producer, 1 MMA issuer (even CTA) or the wait
+// for the pair's last MMA (odd CTA), 2 TMEM allocation, 4-7 epilogue.  The
+// epilogue moves each 32-column block of its accumulator through shared
+// memory (column-major, 132 floats a column, so both the writes and the
+// row-wise reads are free of bank conflicts), then each thread writes
+// whole 32- or 64-byte pieces of one output row.
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int XBK = 64;                              // K block: one 128-byte swizzle row
+constexpr int XA_BYTES = 128 * XBK * 2;              // this CTA's weight rows: 16 KB
+constexpr int XB_ROWS = 128;                         // this CTA's half of at most 256 rows
+constexpr int XB_BYTES = XB_ROWS * XBK * 2;          // 16 KB
+constexpr int XSTAGE = XA_BYTES + XB_BYTES;          // 32 KB a ring stage
+#ifndef MOE_XPAIR_STAGES
+#define MOE_XPAIR_STAGES 6
+#endif
+constexpr int XST = MOE_XPAIR_STAGES;
+constexpr int XSTG_LD = 132;                         // gate/up: floats a staged column
+constexpr int XSTG_WLD = 36;                         // down: floats a staged row (per warp)
+constexpr int XSTG_BYTES = (32 * XSTG_LD > 4 * 32 * XSTG_WLD ? 32 * XSTG_LD : 4 * 32 * XSTG_WLD) * 4;
+constexpr int XBAR_BYTES = ((2 * XST + 5) * 8 + 2 * 4 + 63) / 64 * 64;
+constexpr int XSMEM = 1024 + XST * XSTAGE + XSTG_BYTES + XBAR_BYTES;
+static_assert(XSMEM <= 232448, "shared memory budget");
+constexpr int XCHUNK = 256;                          // most rows a chunk (the MMA's N)
+constexpr int XGRAN = 32;                            // chunk N: a multiple of 32 (16-row boxes a CTA)
+// A CTA loads its half of a chunk (16 .. 128 rows, a multiple of 16) with
+// one box of exactly that height: one tensor map per height.  Every extra
+// box a stage costs the TMA unit time, every row loaded but not used costs
+// shared-memory bandwidth.
+constexpr int XNMAP = XB_ROWS / 16;
+
+struct XParams {
+    CUtensorMap mapW0;     // gate/up: Wg [E, H, L], box {64, 64} (or, wpair, both: see below);
+                           // down: Wd [E, L, H], box {64, 128}
+    CUtensorMap mapW1;     // gate/up: Wu [E, H, L], box {64, 64}
+    CUtensorMap mapX[XNMAP];   // the rows: bank [E, c_recv, L] or h [E, c_recv, H], box {64, 16 (i+1)}
+    const int4* chunks;    // {expert, first row, rows, N}
+    const int* nchunks;
+    int n_mb;              // 256-row weight blocks a chunk (gate/up: H / 128; down: L / 256)
+    int wpair;             // gate/up: mapW0 is [2][E*H/64][64][L] over the lower-addressed of
+                           // Wg, Wu and the other, one box {64, 64, 1, 2} fetching both halves
+    int gate_hi;           // gate/up: the gate rows are the second half (Wu below Wg)
+    int hblk;              // gate/up: H / 64
+    int kb;                // K blocks
+    int c_recv;
+    uint16_t* out;         // h [E, c_recv, H] (gate/up) or ypool [pool_rows, L] (down)
+    long long ldo;         // H or L
+    const int* rowmap;     // down: expert_rows [E, c_recv]
+    long long out_rows;    // down: pool rows (checked builds)
+    int* status;
+};
+
+__device__ __forceinline__ float silu_x(float g) { return g / (1.0f + expf(-g)); }
+
+template <int EPI>
+__global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_constant__ XParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sbase = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sStage = sbase;                                        // XST x (A 16 KB | B 16 KB)
+    float* stg = reinterpret_cast<float*>(sbase + XST * XSTAGE);    // epilogue staging
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + XST * XSTAGE + XSTG_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = full + XST;
+    uint64_t* tfull = empty + XST;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_ctarank();
+    const bool leader = crank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int npairs = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < XST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 256);   // both CTAs' 128 epilogue threads
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.mapW0);
+        if (EPI == EPI_SWIGLU && !p.wpair) tma_prefetch_map(&p.mapW1);
+        for (int i = 0; i < XNMAP; ++i) tma_prefetch_map(&p.mapX[i]);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();   // the peer's barriers exist before any remote arrival
+    const uint32_t tmem_base = *tmem_slot;
+    const int ntiles = *reinterpret_cast<const volatile int*>(p.nchunks) * p.n_mb;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            uint32_t armed = 0, par = 0;   // stages armed by the even CTA (for unwinding)
+            bool ok = true;
+            for (int tile = pair; ok && tile < ntiles; tile += npairs) {
+                const int ci = tile / p.n_mb;
+                const int mb = tile - ci * p.n_mb;
+                const int4 ch = p.chunks[ci];
+                const int e = ch.x, half = ch.w >> 1;
+                const int xrow = ch.y + static_cast<int>(crank) * half;   // this CTA's first row
+                const CUtensorMap* xmap = &p.mapX[half / 16 - 1];
+                const uint32_t bytes = XA_BYTES + static_cast<uint32_t>(half) * XBK * 2;
+                for (int kb = 0; kb < p.kb; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        mbar_arrive_expect_tx(&full[s], 2u * bytes);
+                        armed |= 1u << s;
+                        par = (par & ~(1u << s)) | (ph << s);
+                    }
+                    const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+                    const uint32_t a_dst = smem_u32(sStage + s * XSTAGE);
+                    const uint32_t b_dst = a_dst + XA_BYTES;
+                    const int kx = kb * XBK;
+                    if (EPI == EPI_SWIGLU) {   // gate then up rows of 64 hidden units
+                        const int u = mb * 128 + static_cast<int>(crank) * 64;
+                        if (p.wpair) {
+                            tma_load_4d_pair(a_dst, &p.mapW0, fb, kx, 0, e * p.hblk + u / 64, 0);
+                        } else {
+                            tma_load_3d_pair(a_dst, &p.mapW0, fb, kx, u, e);
+                            tma_load_3d_pair(a_dst + XA_BYTES / 2, &p.mapW1, fb, kx, u, e);
+                        }
+                    } else {                   // 128 output features
+                        tma_load_3d_pair(a_dst, &p.mapW0, fb, kx,
+                                         mb * 256 + static_cast<int>(crank) * 128, e);
+                    }
+                    tma_load_3d_pair(b_dst, xmap, fb, kx, xrow, e);
+                    if (++s == XST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok || *abort_flag) {
+                // Unwinding: every armed stage's loads (both CTAs') land before
+                // the pair may exit.
+                volatile int no_abort = 0;
+                for (int i = 0; i < XST; ++i)
+                    if (armed >> i & 1u)
+                        mbar_wait(&full[i], (par >> i) & 1u, &no_abort, nullptr, 20000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && !leader) {
+            // the even CTA issues the pair's MMAs, which read this CTA's shared
+            // memory and write its TMEM: wait until the last one is done
+            volatile int no_abort = 0;
+            mbar_wait(done, 0, &no_abort, p.status);
+        } else if (lane == 0) {
+            uint32_t s = 0, ph = 0, acc = 0, acc_ph = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < ntiles; tile += npairs) {
+                const int4 ch = p.chunks[tile / p.n_mb];
+                const uint32_t idesc = idesc_bf16_f32(256, ch.w);
+                if (!mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * 256;
+                for (int kb = 0; kb < p.kb; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_s = smem_u32(sStage + s * XSTAGE);
+                    const uint64_t ad = sdesc_k_sw128(a_s);
+                    const uint64_t bd = sdesc_k_sw128(a_s + XA_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < XBK / 16; ++kk)
+                        mma_bf16_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit_pair(&empty[s]);   // the stage is free in both CTAs
+                    if (++s == XST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair(&tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_ph ^= 1u;
+                }
+            }
+            // every MMA issued must finish before either CTA releases TMEM
+            mma_commit_pair(done);
+            volatile int no_abort = 0;
+            mbar_wait(done, 0, &no_abort, p.status);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp - 4;
+        const int t = threadIdx.x - 128;          // 0..127
+        const uint32_t tempty_c0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        uint32_t acc = 0, acc_ph = 0;
+        for (int tile = pair; tile < ntiles; tile += npairs) {
+            const int ci = tile / p.n_mb;
+            const int mb = tile - ci * p.n_mb;
+            const int4 ch = p.chunks[ci];
+            const int e = ch.x, row0 = ch.y, nrows = ch.z, N = ch.w;
+            if (EPI == EPI_SWIGLU) {
+                if (!mbar_wait(&tfull[acc], acc_ph, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
+                // gate rows at lanes go .. go+63, up rows at uo .. uo+63
+                const int go = p.gate_hi ? 64 : 0, uo = 64 - go;
+#pragma unroll 1
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + c0, r);
+                    // column j of this block, TMEM lane 32q + lane
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) stg[j * XSTG_LD + q * 32 + lane] = __uint_as_float(r[j]);
+                    named_bar_sync(1, 128);
+                    // thread t: row j = t % 32 of the block, units 16 (t / 32) .. +15
+                    const int j = t & 31, grp = t >> 5;
+                    const int rr = c0 + j;            // row within the chunk
+                    if (rr < nrows) {
+                        const float* col = stg + j * XSTG_LD;
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 g4 = *reinterpret_cast<const float4*>(col + go + 16 * grp + 4 * v);
+                            const float4 u4 = *reinterpret_cast<const float4*>(col + uo + 16 * grp + 4 * v);
+                            pk[2 * v] = pack_bf16x2(silu_x(g4.x) * u4.x, silu_x(g4.y) * u4.y);
+                            pk[2 * v + 1] = pack_bf16x2(silu_x(g4.z) * u4.z, silu_x(g4.w) * u4.w);
+                        }
+                        const long long hrow = static_cast<long long>(e) * p.c_recv + row0 + rr;
+                        uint16_t* dst = p.out + hrow * p.ldo + mb * 128 +
+                                        static_cast<int>(crank) * 64 + 16 * grp;
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4*>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                    named_bar_sync(1, 128);   // the staging is rewritten by the next block
+                }
+            } else {
+                // The pool row of each of the tile's rows, loaded before the
+                // accumulator is ready: lane j holds rows j, 32 + j, ...
+                long long prow[XCHUNK / 32];
+#pragma unroll
+                for (int c = 0; c < XCHUNK / 32; ++c) {
+                    const int rr = 32 * c + lane;
+                    prow[c] = -1;
+                    if (rr < nrows) {
+                        const long long v =
+                            p.rowmap[static_cast<long long>(e) * p.c_recv + row0 + rr];
+                        if (moe_check(v >= 0 && v < p.out_rows, 1101)) prow[c] = v;
+                    }
+                }
+                if (!mbar_wait(&tfull[acc], acc_ph, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
+                // each warp transposes its own 32 features x 32 rows through
+                // its part of the staging (row-major, 36 floats a row)
+                float* w = stg + q * 32 * XSTG_WLD;
+                uint16_t* obase = p.out + mb * 256 + static_cast<int>(crank) * 128 + 32 * q;
+#pragma unroll
+                for (int c = 0; c < XCHUNK / 32; ++c) {
+                    if (32 * c < N) {                 // warp-uniform
+                        uint32_t r[32];
+                        tmem_ld32(tl + 32 * c, r);    // feature 32q + lane, rows 32c ..
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) w[j * XSTG_WLD + lane] = __uint_as_float(r[j]);
+                        __syncwarp();
+                        // four lanes a row, 16 bytes (8 features) each: one
+                        // store instruction writes 8 rows x 64 contiguous bytes
+                        const int sub = lane & 3;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int j = 8 * i + (lane >> 2);     // row 32c + j
+                            const long long pr = __shfl_sync(0xffffffffu, prow[c], j);
+                            const float* row = w + j * XSTG_WLD + 8 * sub;
+                            const float4 y0 = *reinterpret_cast<const float4*>(row);
+                            const float4 y1 = *reinterpret_cast<const float4*>(row + 4);
+                            if (pr >= 0)
+                                *reinterpret_cast<uint4*>(obase + pr * p.ldo + 8 * sub) =
+                                    make_uint4(pack_bf16x2(y0.x, y0.y), pack_bf16x2(y0.z, y0.w),
+                                               pack_bf16x2(y1.x, y1.y), pack_bf16x2(y1.z, y1.w));
+                        }
+                        __syncwarp();                 // before the next block overwrites w
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(tempty_c0 + acc * 8u);
+            if (++acc == 2) {
+                acc = 0;
+                acc_ph ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // neither CTA leaves while the other may still arrive on its barriers or
+    // the pair's MMAs may touch its memory
+    cluster_sync();
+    if (warp == 2) tmem_dealloc_pair(tmem_base, 512);
+}
+
+// Chunks {expert, first row, rows, N} of every expert with rows: an expert's
+// n rows split into ceil(n / 256) chunks of even size rounded up to 32 (the
+// last one takes the rest), N = the chunk's rows rounded up to 32.  One CTA;
+// a block-wide exclusive prefix over the experts' chunk counts.
+__global__ void __launch_bounds__(1024) chunk_list_kernel(const int32_t* __restrict__ counts,
+                                                          int E, int c_recv, int4* __restrict__ chunks,
+                                                          int32_t* __restrict__ nchunks) {
+    __shared__ int warp_sum[32];
+    __shared__ int carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        int n = e < E ? counts[e] : 0;
+        n = n < 0 ? 0 : (n > c_recv ? c_recv : n);
+        const int nch = (n + XCHUNK - 1) / XCHUNK;
+        int incl = nch;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_sum[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ws, off);
+                if (lane >= off) ws += y;
+            }
+            warp_sum[lane] = ws;
+        }
+        __syncthreads();
+        const int excl = carry + (wid ? warp_sum[wid - 1] : 0) + incl - nch;
+        if (nch > 0) {
+            const int per = ((n + nch - 1) / nch + XGRAN - 1) / XGRAN * XGRAN;
+            for (int i = 0; i < nch; ++i) {
+                const int r0 = i * per;
+                const int rows = (n - r0 < per) ? n - r0 : per;
+                chunks[excl + i] = make_int4(e, r0, rows, (rows + XGRAN - 1) / XGRAN * XGRAN);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = excl + nch;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *nchunks = carry;
+}
+
+typedef CUresult (*EncodeTiledFnX)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFnX encode_x() {
+    static EncodeTiledFnX fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFnX>(f);
+    }();
+    return fn;
+}
+
+// bf16 [groups, rows, cols] (row pitch ld, group stride gs elements), box
+// {64, box_rows, 1}, 128-byte swizzle; reads past the rows give zeros.
+int map3(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t groups,
+         uint64_t ld, uint64_t gs, uint32_t box_rows) {
+    EncodeTiledFnX enc = encode_x();
+    if (!enc) return MOE_ECUDA;
+    const cuuint64_t gdim[3] = {cols, rows, groups};
+    const cuuint64_t gstr[2] = {ld * 2, gs * 2};
+    const cuuint32_t box[3] = {XBK, box_rows, 1}, est[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstr,
+                     box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
+}
+
+// One map over both gate/up weight tensors, so that one box brings a CTA's
+// 64 gate rows and the 64 up rows of the same units: dims {L, 64, E*H/64,
+// 2}, the outermost one stepping from the lower-addressed tensor to the
+// other (strides grow outward only when the two do not overlap), box
+// {64, 64, 1, 2}: rows 0-63 of the box from the lower tensor, 64-127 from
+// the other.  MOE_EINVAL when the tensors' distance does not allow it.
+int map_gateup(CUtensorMap* m, const void* Wg, const void* Wu, int E, int H, int L,
+               int* gate_hi) {
+    EncodeTiledFnX enc = encode_x();
+    if (!enc) return MOE_ECUDA;
+    const uintptr_t g = reinterpret_cast<uintptr_t>(Wg), u = reinterpret_cast<uintptr_t>(Wu);
+    const uintptr_t lo = g < u ? g : u, hi = g < u ? u : g;
+    const uint64_t span = static_cast<uint64_t>(E) * H * L * 2;   // bytes of one tensor
+    const uint64_t dist = hi - lo;
+    if (dist < span || (dist & 15) || dist >= (1ull << 40) || H % 64) return MOE_EINVAL;
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(L), 64,
+                                static_cast<cuuint64_t>(E) * (H / 64), 2};
+    const cuuint64_t gstr[3] = {static_cast<cuuint64_t>(L) * 2, 64ull * L * 2, dist};
+    const cuuint32_t box[4] = {XBK, 64, 1, 2}, est[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, reinterpret_cast<void*>(lo), gdim, gstr,
+                     box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MOE_EINVAL;
+    *gate_hi = g > u ? 1 : 0;
+    return MOE_OK;
+}
+
+template <int EPI>
+int launch_pair(const XParams& p, int sms, cudaStream_t st, const char* name) {
+    auto kern = expert_pair_kernel<EPI>;
+    if (ensure_smem_attr(reinterpret_cast<const void*>(kern), XSMEM) != MOE_OK) return MOE_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = XSMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, name);
+    return MOE_OK;
+}
+
+}  // namespace
+
+int check_status_expert_pair() { return moe_check_read_reset(); }
+
+size_t expert_pair_chunks_bytes(int E, int c_recv) {
+    const size_t per = static_cast<size_t>((c_recv + XCHUNK - 1) / XCHUNK);
+    return static_cast<size_t>(E) * (per > 0 ? per : 1) * sizeof(int4) + 16;
+}
+
+int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
+                    const int32_t* expert_rows, const int32_t* expert_count, const uint16_t* Wg,
+                    const uint16_t* Wu, const uint16_t* Wd, void* chunk_ws, uint16_t* h,
+                    uint16_t* ypool, int64_t pool_rows, int32_t* status, cudaStream_t st) {
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    if (sms < 2 || E <= 0 || c_recv <= 0 || L % 256 || H % 128 || L < 64 || H < 64) return MOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(chunk_ws) & 15) || (reinterpret_cast<uintptr_t>(bank) & 15) ||
+        (reinterpret_cast<uintptr_t>(h) & 15))
+        return MOE_EINVAL;
+    int4* chunks = static_cast<int4*>(chunk_ws);
+    int32_t* nchunks = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(chunk_ws) +
+                                                  expert_pair_chunks_bytes(E, c_recv) - 16);
+    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, c_recv, chunks, nchunks);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "build_chunks");
+
+    XParams a;
+    std::memset(&a, 0, sizeof(a));
+#ifndef MOE_XPAIR_ONE_WLOAD
+#define MOE_XPAIR_ONE_WLOAD 1
+#endif
+    if (MOE_XPAIR_ONE_WLOAD && map_gateup(&a.mapW0, Wg, Wu, E, H, L, &a.gate_hi) == MOE_OK) {
+        a.wpair = 1;
+    } else {   // two boxes a stage: the gate rows, then the up rows
+        if ((rc = map3(&a.mapW0, Wg, L, H, E, L, static_cast<uint64_t>(H) * L, 64))) return rc;
+        if ((rc = map3(&a.mapW1, Wu, L, H, E, L, static_cast<uint64_t>(H) * L, 64))) return rc;
+        a.wpair = 0;
+        a.gate_hi = 0;
+    }
+    a.hblk = H / 64;
+    for (int i = 0; i < XNMAP; ++i)
+        if ((rc = map3(&a.mapX[i], bank, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
+                       16 * (i + 1))))
+            return rc;
+    a.chunks = chunks;
+    a.nchunks = nchunks;
+    a.n_mb = H / 128;
+    a.kb = (L + XBK - 1) / XBK;
+    a.c_recv = c_recv;
+    a.out = h;
+    a.ldo = H;
+    a.status = status;
+    if ((rc = launch_pair<EPI_SWIGLU>(a, sms, st, "gemm_expert_gateup"))) return rc;
+
+    XParams b;
+    std::memset(&b, 0, sizeof(b));
+    if ((rc = map3(&b.mapW0, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
+    for (int i = 0; i < XNMAP; ++i)
+        if ((rc = map3(&b.mapX[i], h, H, c_recv, E, H, static_cast<uint64_t>(c_recv) * H,
+                       16 * (i + 1))))
+            return rc;
+    b.chunks = chunks;
+    b.nchunks = nchunks;
+    b.n_mb = L / 256;
+    b.kb = (H + XBK - 1) / XBK;
+    b.c_recv = c_recv;
+    b.out = ypool;
+    b.ldo = L;
+    b.rowmap = expert_rows;
+    b.out_rows = pool_rows;
+    b.status = status;
+    return launch_pair<EPI_SCATTER>(b, sms, st, "gemm_expert_down");
+}
+
+}  // namespace moe

@@ -72,6 +72,7 @@ struct PackArgs {
     int32_t* expert_rows;       // [E, c_recv] (ragged: flat, eoff)
     const int32_t* blk_off;     // ragged: first row of each (source, destination, wave) block
     const int32_t* eoff;        // ragged: first row-list entry of each expert
+    uint16_t* bank;             // optional [E, c_recv, L]: receiver-kept rows grouped by expert
 };
 
 // out = sum_s A_s B_s^T with one of the epilogues above.  For EPI_SWIGLU the
@@ -168,15 +169,28 @@ DispatchWs dispatch_ws_layout(const DispatchGeom& g);
 // tags) of that wave are written; -1: all.  run_pack false: the sender and
 // receiver counts only, the pack (decisions and copies) left to a GEMM
 // launch that carries it.
+// bank (optional, [E, c_recv, L]): the pack also writes each receiver-kept
+// row there, at its expert's receiver rank.
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
                     int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream,
-                    int copy_wave = -1, bool run_pack = true);
+                    int copy_wave = -1, bool run_pack = true, uint16_t* bank = nullptr);
 
 int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                            uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                            int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
                            moe_drop_stats_t* stats, cudaStream_t stream);
+
+// The capped layout's expert FFN on CTA pairs with the expert's rows on the
+// MMA's N axis (expert_pair.cu): chunk list, gate/up from the per-expert
+// bank into h [E, c_recv, H], down from h scattered to the pool rows of
+// ypool.  chunk_ws: expert_pair_chunks_bytes(E, c_recv), 16-byte aligned.
+size_t expert_pair_chunks_bytes(int E, int c_recv);
+int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
+                    const int32_t* expert_rows, const int32_t* expert_count, const uint16_t* Wg,
+                    const uint16_t* Wu, const uint16_t* Wd, void* chunk_ws, uint16_t* h,
+                    uint16_t* ypool, int64_t pool_rows, int32_t* status, cudaStream_t stream);
+int check_status_expert_pair();
 
 // Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
 // Checked builds: the site code recorded by each translation unit's index

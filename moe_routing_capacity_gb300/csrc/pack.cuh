@@ -13,8 +13,10 @@ namespace moe {
 // receiver decisions -- expert row list entry, slot_of, drop code (0 kept,
 // 1 dropped by the sender, 2 by the receiver).  copy_wave: copy the latent
 // row and write the tag into the pool rows of every sender-kept assignment
-// (-1), of those of one wave (>= 0), or of none (< -1).  The latent row is
-// read once, CH 16-byte chunks a lane at a time, and written to each row.
+// (-1), of those of one wave (>= 0), or of none (< -1); with a bank and
+// decide, each receiver-kept row copied is also written to the bank row of
+// its expert and receiver rank.  The latent row is read once, CH 16-byte
+// chunks a lane at a time, and written to each row.
 // STREAM: streaming (evict-first) loads and stores, for a copy that runs
 // beside a product whose tiles should stay in L2.
 template <int CH, bool STREAM>
@@ -23,6 +25,7 @@ __device__ __forceinline__ void pack_token(const DispatchGeom& g, const PackArgs
     const int64_t s = t / g.T_s;
     const int64_t pitch = pool_pitch(g.L);
     int64_t row = -1;
+    int64_t brow = -1;   // bank row (expert e, receiver rank r) of a receiver-kept row
     int e = 0;
     if (lane < g.k) {
         const int64_t a = t * g.k + lane;
@@ -44,6 +47,7 @@ __device__ __forceinline__ void pack_token(const DispatchGeom& g, const PackArgs
                         P.expert_rows[at] = static_cast<int32_t>(row);
                     so = static_cast<int32_t>(row);
                     dr = 0;
+                    if (P.bank && !g.ragged) brow = static_cast<int64_t>(e) * g.c_recv + r;
                 } else {
                     dr = 2;
                 }
@@ -53,7 +57,7 @@ __device__ __forceinline__ void pack_token(const DispatchGeom& g, const PackArgs
         }
         if (copy_wave < -1 ||
             (copy_wave >= 0 && row >= 0 && !(e >= 0 && e < g.E && (e % g.E_l) / g.E_w == copy_wave)))
-            row = -1;
+            row = brow = -1;
     }
     if (!__any_sync(0xffffffffu, row >= 0)) return;
     const int nchunk = g.L / 8;
@@ -77,6 +81,19 @@ __device__ __forceinline__ void pack_token(const DispatchGeom& g, const PackArgs
                         __stcs(dst + ch, v[c]);
                     else
                         dst[ch] = v[c];
+                }
+            }
+            const int64_t bj = __shfl_sync(0xffffffffu, brow, j);
+            if (bj < 0) continue;
+            uint4* bdst = reinterpret_cast<uint4*>(P.bank + bj * g.L);
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int ch = cb + lane + 32 * c;
+                if (ch < nchunk) {
+                    if (STREAM)
+                        __stcs(bdst + ch, v[c]);
+                    else
+                        bdst[ch] = v[c];
                 }
             }
         }

@@ -451,18 +451,20 @@ __global__ void __launch_bounds__(256) dispatch_pack_kernel(
     const int64_t* __restrict__ send_row, const int32_t* __restrict__ rloc,
     const int32_t* __restrict__ base_se, uint16_t* __restrict__ pool,
     int32_t* __restrict__ slot_of, uint8_t* __restrict__ drop, int32_t* __restrict__ expert_rows,
-    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ eoff, int copy_wave) {
+    const int32_t* __restrict__ blk_off, const int32_t* __restrict__ eoff, int copy_wave,
+    uint16_t* __restrict__ bank) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= g.T) return;
-    const PackArgs P{z, idx, send_row, rloc, base_se, pool, slot_of, drop, expert_rows, blk_off, eoff};
+    const PackArgs P{z, idx, send_row, rloc, base_se, pool, slot_of, drop, expert_rows, blk_off, eoff,
+                     bank};
     pack_token<CH, false>(g, P, t, lane, true, copy_wave);
 }
 
 int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                     uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
                     int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t st,
-                    int copy_wave, bool run_pack) {
+                    int copy_wave, bool run_pack, uint16_t* bank) {
     const DispatchWs L = dispatch_ws_layout(g);
     uint8_t* w = static_cast<uint8_t*>(ws);
     int64_t* send_row = reinterpret_cast<int64_t*>(w + L.send_row_off);
@@ -498,11 +500,11 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
     if (nchunk <= 32 * 4)
         dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                        slot_of, drop, expert_rows, nullptr,
-                                                       nullptr, copy_wave);
+                                                       nullptr, copy_wave, bank);
     else
         dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                         slot_of, drop, expert_rows, nullptr,
-                                                        nullptr, copy_wave);
+                                                        nullptr, copy_wave, bank);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_pack");
     return MOE_OK;
@@ -602,11 +604,11 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
     if (g.L / 8 <= 32 * 4)
         dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                        slot_of, drop, expert_rows, blk_off,
-                                                       expert_offsets, -1);
+                                                       expert_offsets, -1, nullptr);
     else
         dispatch_pack_kernel<12><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,
                                                         slot_of, drop, expert_rows, blk_off,
-                                                        expert_offsets, -1);
+                                                        expert_offsets, -1, nullptr);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "dispatch_pack");
     return MOE_OK;

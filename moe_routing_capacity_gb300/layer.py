@@ -31,12 +31,15 @@ class PooledWaveMoE:
     "waves" (dispatch and experts as one wave-pipelined call: the later
     waves' pool rows copied while wave 0's experts run) or "shared" (the
     pool rows copied while the shared experts' gate/up runs); the capped
-    layout only."""
+    layout only.  ``expert_bank``: the dispatch also writes the received
+    rows grouped by expert (``self.bank``), from which the expert products
+    load whole tiles (capped layout, calls one after another or "shared");
+    False gathers each expert's rows from the pool instead."""
 
     PIPELINES = (None, "waves", "shared")
 
     def __init__(self, cfg, weights: dict, device="cuda", balance_alpha=None,
-                 dropless=False, pipeline=None, balance_window=None):
+                 dropless=False, pipeline=None, balance_window=None, expert_bank=True):
         self.cfg = cfg
         self.dropless = dropless
         if pipeline not in self.PIPELINES:
@@ -69,6 +72,9 @@ class PooledWaveMoE:
         self.expert_count = e(E, dt=torch.int32)
         self.stats = torch.zeros(abi.STATS_WORDS, dtype=torch.int64, device=dev)
         self.ws_ffn = e(max(1, p.ws_ffn_bytes), dt=torch.uint8)
+        # the received rows grouped by local expert (written by the pack)
+        self.bank = (e(E, max(1, p.c_recv), L, dt=torch.bfloat16)
+                     if expert_bank and not dropless and pipeline != "waves" else None)
         self.ypool = e(p.pool_rows, L, dt=torch.bfloat16)
         self.c = e(T, L, dt=torch.bfloat16)
         self.a = e(T, max(1, cfg.n_shared * cfg.h_shared), dt=torch.bfloat16)
@@ -100,7 +106,7 @@ class PooledWaveMoE:
         else:
             abi.dispatch_pooled(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
                                 self.slot_of, self.drop, self.expert_rows, self.expert_count,
-                                self.stats, stream)
+                                self.stats, stream, bank=self.bank)
 
     def experts(self, stream=None):
         if self.dropless:
@@ -110,7 +116,7 @@ class PooledWaveMoE:
         else:
             abi.expert_ffn_grouped(self.cfg, self.pool, self.expert_rows, self.expert_count,
                                    self.w["Wg"], self.w["Wu"], self.w["Wd"], self.ws_ffn,
-                                   self.ypool, self.status, stream)
+                                   self.ypool, self.status, stream, bank=self.bank)
 
     def combine(self, x, out=None, stream=None):
         abi.combine(self.cfg, self.ypool, self.slot_of, self.gate_w, self.w["W_lu"], x,
@@ -144,7 +150,8 @@ class PooledWaveMoE:
             abi.dispatch_shared_overlap(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
                                         self.slot_of, self.drop, self.expert_rows,
                                         self.expert_count, self.stats, x, self.w["Wsg"],
-                                        self.w["Wsu"], self.a, self.status, stream)
+                                        self.w["Wsu"], self.a, self.status, stream,
+                                        bank=self.bank)
             self.experts(stream)
             abi.combine(self.cfg, self.ypool, self.slot_of, self.gate_w, self.w["W_lu"], None,
                         None, None, self.w["Wsd"], self.c, self.a,

@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     L = abi.lib()
     for name in _declared():
         assert hasattr(L, name), name
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
 
 
 def test_every_export_declares_its_signature():
@@ -147,12 +147,16 @@ def test_entry_points_validate_before_touching_the_gpu():
     assert L.moe_latent_proj(n, n, 4, 8, 8, n, n, n) == abi.MOE_EINVAL
     assert L.moe_latent_proj(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 12, 8,
                              ctypes.c_void_p(16), ctypes.c_void_p(16), n) == abi.MOE_EINVAL
-    assert L.moe_dispatch_pooled(cp, n, n, n, 0, n, n, n, n, n, n, n) == abi.MOE_EINVAL
+    assert L.moe_dispatch_pooled(cp, n, n, n, 0, n, n, n, n, n, n, n, n) == abi.MOE_EINVAL
     p = abi.plan(_small())
     fake = ctypes.c_void_p(1 << 20)
     assert L.moe_dispatch_pooled(cp, fake, fake, fake, p.ws_dispatch_bytes - 1, fake, fake, fake,
-                                 fake, fake, fake, n) == abi.MOE_ENOSPC
-    assert L.moe_expert_ffn_grouped(cp, fake, fake, fake, fake, fake, fake, fake,
+                                 fake, fake, fake, n, n) == abi.MOE_ENOSPC
+    # a bank that is not 16-byte aligned is refused
+    assert L.moe_dispatch_pooled(cp, fake, fake, fake, p.ws_dispatch_bytes, fake, fake, fake,
+                                 fake, fake, fake, ctypes.c_void_p((1 << 20) + 8),
+                                 n) == abi.MOE_EINVAL
+    assert L.moe_expert_ffn_grouped(cp, fake, n, fake, fake, fake, fake, fake, fake,
                                     p.ws_ffn_bytes - 1, fake, fake, n) == abi.MOE_ENOSPC
     assert L.moe_combine(cp, n, n, n, n, n, n, n, n, n, n, n, n, n) == abi.MOE_EINVAL
     # shared activations given (Wsg = Wsu = NULL) but no a: refused
@@ -169,11 +173,12 @@ def test_entry_points_validate_before_touching_the_gpu():
     assert L.moe_dispatch_expert_waves(cp, fake, fake, fake, sz(p.ws_dispatch_bytes),
                                        *([fake] * 9), fake, sz(p.ws_ffn_bytes - 1), fake, fake,
                                        n) == abi.MOE_ENOSPC
-    assert L.moe_dispatch_shared_overlap(cp, *([n] * 3), sz(0), *([n] * 12)) == abi.MOE_EINVAL
+    assert L.moe_dispatch_shared_overlap(cp, *([n] * 3), sz(0), *([n] * 13)) == abi.MOE_EINVAL
     assert L.moe_dispatch_shared_overlap(cp, fake, fake, fake, sz(p.ws_dispatch_bytes - 1),
-                                         *([fake] * 10), fake, n) == abi.MOE_ENOSPC
+                                         *([fake] * 6), n, *([fake] * 5), n) == abi.MOE_ENOSPC
     assert L.moe_dispatch_shared_overlap(cp, fake, fake, fake, sz(p.ws_dispatch_bytes),
-                                         *([fake] * 9), n, fake, n) == abi.MOE_EINVAL   # no a
+                                         *([fake] * 6), n, *([fake] * 3), n, fake,
+                                         n) == abi.MOE_EINVAL   # no a
     assert L.moe_balance_update_window(cp, fake, fake, fake, 0, fake, ctypes.c_float(1.0), fake,
                                        n) == abi.MOE_EINVAL   # window < 1
     bad = abi.make_config(_small(T=63))

@@ -59,3 +59,17 @@ def test_tensor_peak_follows_the_clock_of_the_timed_region():
     assert bench.tensor_peak_for(pk, 0.5, capped) == ("sustained", 1715.2, 1910.8)
     low = {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []}
     assert bench.tensor_peak_for(pk, 0.5, low)[0] == "sustained"
+
+
+def test_expert_mma_rows():
+    sys.path.insert(0, ROOT)
+    import bench
+    # gathered path: 128-row tiles
+    assert bench.expert_mma_rows([0, 1, 128, 129, 316], 393, False) == 0 + 128 + 128 + 256 + 384
+    # bank path: 316 -> two chunks of 160 (158 rows each, rounded to 32);
+    # 393 -> 224 + 169 (-> 192); 250 -> 256; 33 -> 64; 0 -> nothing
+    assert bench.expert_mma_rows([316], 393, True) == 320
+    assert bench.expert_mma_rows([393], 393, True) == 224 + 192
+    assert bench.expert_mma_rows([250, 33, 0], 393, True) == 256 + 64
+    # counts past c_recv are clamped
+    assert bench.expert_mma_rows([500], 393, True) == 224 + 192

@@ -1,0 +1,91 @@
+"""The expert products on CTA pairs with each expert's rows on the MMA's N
+axis, fed from the per-expert bank that the dispatch's pack writes.
+
+Checked against the oracle element by element on a 4096-token layer whose
+widths take that path (L = 256, H = 128): uniform routing (experts of
+281-393 rows, each split into two chunks), and a Zipf prior with some
+experts ruled out (experts at the receiver cap, experts with a handful of
+rows, experts with none).  The bank itself is compared with the pool rows
+it groups, and the whole layer with the path that gathers each expert's
+rows from the pool, for each pool-fill schedule.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_routing_capacity_gb300 import workloads as wl
+
+from test_gpu_parity import compare_full, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+# widths whose expert products take the bank path; ~341 rows an expert before drops
+PAIRS = wl.LayerConfig("pairs", T=4096, d_model=256, d_latent=256, n_experts=24, n_ranks=4,
+                       top_k=2, n_waves=3, n_shared=1, h_expert=128, h_shared=128, seed=5)
+
+
+def _inputs(kind):
+    cfg = PAIRS
+    inp = wl.make_inputs(cfg, "cpu")
+    if kind == "skew":
+        b = wl.zipf_bias(cfg.n_experts, 1.2)
+        b[[3, 10, 17]] = -1.0e4          # three experts that receive nothing
+        inp["bias"] = b
+    return cfg, inp
+
+
+def _bank_matches_pool(m, cfg):
+    """bank[e][r] is the payload of pool row expert_rows[e][r], r < count."""
+    L = cfg.d_latent
+    rows = m.expert_rows.long()
+    cnt = m.expert_count.long()
+    r_idx = torch.arange(rows.shape[1], device=rows.device)[None, :]
+    valid = r_idx < cnt[:, None]
+    pool_payload = m.pool[:, :L]
+    got = m.bank.view(torch.int16)[valid]
+    want = pool_payload[rows[valid]]
+    assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("kind", ["uniform", "skew"])
+def test_bank_path_matches_oracle(kind):
+    cfg, inp = _inputs(kind)
+    m, ref, rep = compare_full(cfg, inp, expert_bank=True)
+    assert m.bank is not None
+    cnt = m.expert_count.cpu().numpy()
+    if kind == "uniform":
+        assert (cnt > 256).sum() >= cfg.n_experts // 2, cnt   # most experts in two chunks
+    else:
+        p = ref["plan"]
+        # experts at the receiver cap, with no rows, and with fewer than 128
+        # (chunks narrower than the full-rate MMA width)
+        assert (cnt == p.c_recv).any() and (cnt == 0).sum() == 3 and (cnt[cnt > 0] < 128).any(), cnt
+    _bank_matches_pool(m, cfg)
+    print(kind, rep)
+
+
+@pytest.mark.parametrize("pipeline", [None, "shared"])
+@pytest.mark.parametrize("kind", ["uniform", "skew"])
+def test_bank_path_equals_gathered_rows(kind, pipeline):
+    cfg, inp = _inputs(kind)
+    a = run_gpu(cfg, inp, expert_bank=True, pipeline=pipeline)
+    b = run_gpu(cfg, inp, expert_bank=False, pipeline=pipeline)
+    assert a.bank is not None and b.bank is None
+    _bank_matches_pool(a, cfg)
+    kept = a.slot_of[a.slot_of >= 0].long()
+    for name in ("slot_of", "drop", "expert_rows", "expert_count"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert torch.equal(a.ypool[kept].view(torch.int16), b.ypool[kept].view(torch.int16))
+    for name in ("c", "out"):
+        assert torch.equal(getattr(a, name).view(torch.int16), getattr(b, name).view(torch.int16)), name
+
+
+def test_mid_bank_path_equals_gathered_rows():
+    cfg = wl.MID
+    inp = wl.make_inputs(cfg, "cpu")
+    a = run_gpu(cfg, inp, expert_bank=True)
+    b = run_gpu(cfg, inp, expert_bank=False)
+    _bank_matches_pool(a, cfg)
+    kept = a.slot_of[a.slot_of >= 0].long()
+    assert torch.equal(a.ypool[kept].view(torch.int16), b.ypool[kept].view(torch.int16))
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
