@@ -85,12 +85,19 @@ def peaks():
 # operands.  A traffic record taken under other sources is not reported.
 KERNEL_SOURCES = {
     "gemm": ("gemm_tc.cu", "common.cuh", "internal.h", "abi.cu"),
+    "expert": ("expert_pair.cu", "common.cuh", "internal.h", "abi.cu"),
     "route": ("route.cu", "common.cuh", "internal.h", "abi.cu"),
 }
 
 
-def source_hash(kernel="gemm"):
-    files = KERNEL_SOURCES["gemm" if kernel.startswith("gemm") else "route"]
+def source_group(kernel: str, bank_path: bool = True) -> str:
+    if kernel.startswith("gemm_expert") and bank_path:
+        return "expert"
+    return "gemm" if kernel.startswith("gemm") else "route"
+
+
+def source_hash(kernel="gemm", bank_path=True):
+    files = KERNEL_SOURCES[source_group(kernel, bank_path)]
     h = hashlib.sha256()
     src = os.path.join(ROOT, "moe_routing_capacity_gb300", "csrc")
     for f in files:
@@ -425,11 +432,15 @@ def run_gb300(args, rank, world, local_rank):
     # that kernel
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     recs = json.load(open(tp)) if os.path.exists(tp) else {}
+    bank_path = m.bank is not None
     for name, e in kernels.items():
         rec = recs.get(name)
-        if (rec and rec.get("source_hash") == source_hash(name) and rec.get("workload") == cfg.name
-                and rec.get("pool_fill", "none") == pipeline):
+        if (rec and rec.get("source_hash") == source_hash(name, bank_path)
+                and rec.get("workload") == cfg.name and rec.get("pool_fill", "none") == pipeline
+                and rec.get("bank", bank_path) == bank_path):
             e["traffic"] = rec.get("dram_bytes_per_launch")
+            if rec.get("measured_on"):
+                e["traffic_from"] = rec["measured_on"]
     traffic = kernels[top].get("traffic")
     if twork is not None:
         ach = kernels[top]["achieved"]
