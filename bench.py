@@ -149,7 +149,7 @@ def expert_mma_rows(counts, c_recv, bank_path):
     """Rows the expert products multiply per weight row.  Gathered path: each
     expert's rows padded to whole 128-row tiles.  Bank path (CTA pairs, rows
     on the MMA's N axis): an expert's n rows in ceil(n / 256) chunks of even
-    size rounded up to 32, each chunk's width rounded up to 32."""
+    size rounded up to 16, each chunk's width rounded up to 16."""
     total = 0
     for n in counts:
         n = max(0, min(int(n), c_recv))
@@ -159,10 +159,10 @@ def expert_mma_rows(counts, c_recv, bank_path):
         nch = (n + 255) // 256
         if nch == 0:
             continue
-        per = ((n + nch - 1) // nch + 31) // 32 * 32
+        per = ((n + nch - 1) // nch + 15) // 16 * 16
         for i in range(nch):
             rows = min(per, n - i * per)
-            total += (rows + 31) // 32 * 32
+            total += (rows + 15) // 16 * 16
     return total
 
 

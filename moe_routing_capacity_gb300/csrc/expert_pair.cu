@@ -9,7 +9,7 @@
 // CTA).  For gate/up a CTA's 128 rows are the gate and the up rows of the
 // same 64 hidden units, so its SwiGLU epilogue needs only its own TMEM.  The
 // expert's rows sit on N, in chunks of at most 256 rows sized evenly over
-// the expert's count and rounded up to 32 (each CTA stages half of them):
+// the expert's count and rounded up to 16 (each CTA stages half of them):
 // an M x N x 16 MMA costs N/2 cycles for N >= 128 (measured on this part),
 // so an expert with 316 rows computes two chunks of 160 (320 MMA rows)
 // instead of three 128-row tiles (384).  Both operands arrive by TMA: the
@@ -49,18 +49,23 @@ constexpr int XBAR_BYTES = ((2 * XST + 5) * 8 + 2 * 4 + 63) / 64 * 64;
 constexpr int XSMEM = 1024 + XST * XSTAGE + XSTG_BYTES + XBAR_BYTES;
 static_assert(XSMEM <= 232448, "shared memory budget");
 constexpr int XCHUNK = 256;                          // most rows a chunk (the MMA's N)
-constexpr int XGRAN = 32;                            // chunk N: a multiple of 32 (16-row boxes a CTA)
-// A CTA loads its half of a chunk (16 .. 128 rows, a multiple of 16) with
-// one box of exactly that height: one tensor map per height.  Every extra
-// box a stage costs the TMA unit time, every row loaded but not used costs
-// shared-memory bandwidth.
-constexpr int XNMAP = XB_ROWS / 16;
+#ifndef MOE_XPAIR_GRAN
+#define MOE_XPAIR_GRAN 16
+#endif
+constexpr int XGRAN = MOE_XPAIR_GRAN;                // chunk N: a multiple of this (N/2 rows a CTA)
+static_assert(XGRAN == 16 || XGRAN == 32, "chunk granularity");
+// A CTA loads its half of a chunk (XGRAN/2 .. 128 rows, a multiple of
+// XGRAN/2, whole 8-row swizzle atoms) with one box of exactly that height:
+// one tensor map per height.  Every extra box a stage costs the TMA unit
+// time, every row loaded but not used costs shared-memory bandwidth.
+constexpr int XHSTEP = XGRAN / 2;
+constexpr int XNMAP = XB_ROWS / XHSTEP;
 
 struct XParams {
     CUtensorMap mapW0;     // gate/up: Wg [E, H, L], box {64, 64} (or, wpair, both: see below);
                            // down: Wd [E, L, H], box {64, 128}
     CUtensorMap mapW1;     // gate/up: Wu [E, H, L], box {64, 64}
-    CUtensorMap mapX[XNMAP];   // the rows: bank [E, c_recv, L] or h [E, c_recv, H], box {64, 16 (i+1)}
+    CUtensorMap mapX[XNMAP];   // the rows: bank [E, c_recv, L] or h [E, c_recv, H], box {64, XHSTEP (i+1)}
     const int4* chunks;    // {expert, first row, rows, N}
     const int* nchunks;
     int n_mb;              // 256-row weight blocks a chunk (gate/up: H / 128; down: L / 256)
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
                 const int4 ch = p.chunks[ci];
                 const int e = ch.x, half = ch.w >> 1;
                 const int xrow = ch.y + static_cast<int>(crank) * half;   // this CTA's first row
-                const CUtensorMap* xmap = &p.mapX[half / 16 - 1];
+                const CUtensorMap* xmap = &p.mapX[half / XHSTEP - 1];
                 const uint32_t bytes = XA_BYTES + static_cast<uint32_t>(half) * XBK * 2;
                 for (int kb = 0; kb < p.kb; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) {
@@ -347,8 +352,8 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
 }
 
 // Chunks {expert, first row, rows, N} of every expert with rows: an expert's
-// n rows split into ceil(n / 256) chunks of even size rounded up to 32 (the
-// last one takes the rest), N = the chunk's rows rounded up to 32.  One CTA;
+// n rows split into ceil(n / 256) chunks of even size rounded up to XGRAN (the
+// last one takes the rest), N = the chunk's rows rounded up to XGRAN.  One CTA;
 // a block-wide exclusive prefix over the experts' chunk counts.
 __global__ void __launch_bounds__(1024) chunk_list_kernel(const int32_t* __restrict__ counts,
                                                           int E, int c_recv, int4* __restrict__ chunks,
@@ -520,7 +525,7 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
     a.hblk = H / 64;
     for (int i = 0; i < XNMAP; ++i)
         if ((rc = map3(&a.mapX[i], bank, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
-                       16 * (i + 1))))
+                       XHSTEP * (i + 1))))
             return rc;
     a.chunks = chunks;
     a.nchunks = nchunks;
@@ -537,7 +542,7 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
     if ((rc = map3(&b.mapW0, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
     for (int i = 0; i < XNMAP; ++i)
         if ((rc = map3(&b.mapX[i], h, H, c_recv, E, H, static_cast<uint64_t>(c_recv) * H,
-                       16 * (i + 1))))
+                       XHSTEP * (i + 1))))
             return rc;
     b.chunks = chunks;
     b.nchunks = nchunks;
