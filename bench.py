@@ -463,9 +463,10 @@ def run_gb300(args, rank, world, local_rank):
         roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None,
                 "unit": None, "frac": None, "traffic": traffic}
 
-    # ---- end to end through the public API with host buffers: every step
-    # copies its x from pinned host memory and its output + drop stats back;
-    # HostPipeline overlaps those copies with the previous step's compute.
+    # ---- end to end through the C ABI with host buffers: every step copies
+    # its x from pinned host memory and its output + drop stats back, inside
+    # the library (moe_host_pipe_submit, the copies overlapped with the
+    # neighbouring steps' compute).
     e2e = None
     if not args.no_e2e:
         from moe_routing_capacity_gb300.layer import HostPipeline
@@ -497,7 +498,8 @@ def run_gb300(args, rank, world, local_rank):
                "d2h_bytes_per_step": oh[0].numel() * oh[0].element_size() + sh[0].numel() * 8,
                "steps": 5 * n_e2e, "rounds": [round(r) for r in rounds],
                "timer": "host wall clock around each round of submitted steps; median of 5",
-               "overlap": "H2D / compute / D2H on three streams, double-buffered"}
+               "path": "moe_host_pipe_submit (C ABI) with pinned host buffers: the whole "
+                       "forward per call, H2D / compute / D2H on three streams, double-buffered"}
 
     # ---- the same step replayed from a CUDA graph (no host launch work)
     graph = None

@@ -343,6 +343,86 @@ int moe_combine(const moe_config_t* cfg, const uint16_t* ypool, const int32_t* s
                 const uint16_t* Wsg, const uint16_t* Wsu, const uint16_t* Wsd,
                 uint16_t* c, uint16_t* a, uint16_t* out, int32_t* status, void* stream);
 
+/* The whole layer forward in one call, and a pipeline that feeds it from
+ * host memory.  These compose the calls above; the pages describe the layer
+ * (lamjinlab zh-HK section 二), not this packaging of it.
+ *
+ * moe_layer_buffers_t: every device buffer of one layer instance (caller-
+ * owned; sizes as for the individual calls: logits [T, E] fp32, idx, w
+ * [T, k], tie [T], z [T, L], ws_dispatch >= plan.ws_dispatch_bytes, pool,
+ * slot_of, drop, expert_rows, expert_count, stats, bank (optional, NULL:
+ * no bank), ws_ffn >= plan.ws_ffn_bytes, ypool [pool_rows, L], c [T, L],
+ * a [T, n_s*Hs] (NULL when n_s = 0), status), plus the weights (bias
+ * optional).
+ *
+ * moe_layer_forward: out = layer(x) for device x [T, d] and out [T, d]
+ * bf16, enqueued on `stream`: moe_route_project; with shared experts
+ * moe_dispatch_shared_overlap (the pool fill inside their gate/up launch),
+ * else moe_dispatch_pooled; moe_expert_ffn_grouped; moe_combine.  Results as
+ * those calls in that order; errors as theirs (the first one returned). */
+typedef struct moe_layer_buffers {
+    const uint16_t* Wr;
+    const float* bias;
+    const uint16_t* W_ld;
+    const uint16_t* Wg;
+    const uint16_t* Wu;
+    const uint16_t* Wd;
+    const uint16_t* W_lu;
+    const uint16_t* Wsg;
+    const uint16_t* Wsu;
+    const uint16_t* Wsd;
+    float* logits;
+    int32_t* idx;
+    float* w;
+    uint8_t* tie;
+    uint16_t* z;
+    void* ws_dispatch;
+    size_t ws_dispatch_bytes;
+    uint16_t* pool;
+    int32_t* slot_of;
+    uint8_t* drop;
+    int32_t* expert_rows;
+    int32_t* expert_count;
+    moe_drop_stats_t* stats;
+    uint16_t* bank;
+    void* ws_ffn;
+    size_t ws_ffn_bytes;
+    uint16_t* ypool;
+    uint16_t* c;
+    uint16_t* a;
+    int32_t* status;
+} moe_layer_buffers_t;
+
+int moe_layer_forward(const moe_config_t* cfg, const moe_layer_buffers_t* buffers,
+                      const uint16_t* x, uint16_t* out, void* stream);
+
+/* Host-memory pipeline over moe_layer_forward, as a serving loop runs it:
+ * batch i's x is copied host -> device on the pipeline's own stream while
+ * batch i-1 computes on the caller's stream and batch i-2's output (and
+ * drop statistics) copy back on a second stream of its own; events order
+ * the three over a ring of `depth` device staging buffers.
+ *   create:  x_dev[depth], out_dev[depth] [T, d] bf16 and stats_dev[depth]
+ *            (device, caller-owned, 16- and 8-byte aligned) form the ring;
+ *            the pipeline creates its two streams and 3*depth events on the
+ *            current device (no device memory).  MOE_EINVAL on bad
+ *            arguments, MOE_ECUDA if a stream or event cannot be created.
+ *   submit:  enqueue one batch: x_host [T, d] -> the layer (buffers, on
+ *            `stream`) -> out_host [T, d] and, if not NULL, stats_host.  All
+ *            asynchronous; host buffers should be pinned for the copies to
+ *            overlap.  Call with the pipeline's device current.  After an
+ *            error the pipeline's state is undefined: destroy it.
+ *   sync:    wait until every submitted batch's copies back have landed.
+ *   destroy: sync, then release the streams and events. */
+typedef struct moe_host_pipe moe_host_pipe_t;
+int moe_host_pipe_create(const moe_config_t* cfg, int depth, uint16_t* const* x_dev,
+                         uint16_t* const* out_dev, moe_drop_stats_t* const* stats_dev,
+                         moe_host_pipe_t** pipe);
+int moe_host_pipe_submit(moe_host_pipe_t* pipe, const moe_layer_buffers_t* buffers,
+                         const uint16_t* x_host, uint16_t* out_host,
+                         moe_drop_stats_t* stats_host, void* stream);
+int moe_host_pipe_sync(moe_host_pipe_t* pipe);
+int moe_host_pipe_destroy(moe_host_pipe_t* pipe);
+
 /* Backward pass of the layer (capped layout).  The pages give the forward
  * only; the throughput they quote is a training step, so this is the
  * forward's derivative, step by step in reverse: output layer, shared
@@ -477,8 +557,8 @@ int moe_trace_event(int i, const char** name, float* ms_since_prev);
 /* Human-readable name of a MOE_* code (static string). */
 const char* moe_strerror(int code);
 
-/* ABI version: 2 (the optional per-expert bank of the dispatch and the
- * expert FFN). */
+/* ABI version: 3 (2: the optional per-expert bank of the dispatch and the
+ * expert FFN; 3: the whole-layer forward and the host-memory pipeline). */
 int moe_abi_version(void);
 
 #ifdef __cplusplus

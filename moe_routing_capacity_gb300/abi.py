@@ -27,7 +27,8 @@ EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project"
            "moe_backward_plan", "moe_layer_backward", "moe_backward_plan_ragged",
            "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_check_status", "moe_strerror",
-           "moe_abi_version")
+           "moe_abi_version", "moe_layer_forward", "moe_host_pipe_create", "moe_host_pipe_submit",
+           "moe_host_pipe_sync", "moe_host_pipe_destroy")
 # Declared in the header too, but exported by the checked build only.
 CHECKED_ONLY = ("moe_check_set_wave_wait_limit_ns",)
 
@@ -82,6 +83,16 @@ class BackwardArgs(ctypes.Structure):
     _fields_ = ([(f, ctypes.c_void_p) for f in BWD_ARG_FIELDS] +
                 [("ws_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p),
                  ("expert_offsets", ctypes.c_void_p)])
+
+LAYER_BUFFER_FIELDS = ("Wr", "bias", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Wsd",
+                       "logits", "idx", "w", "tie", "z", "ws_dispatch", "ws_dispatch_bytes",
+                       "pool", "slot_of", "drop", "expert_rows", "expert_count", "stats", "bank",
+                       "ws_ffn", "ws_ffn_bytes", "ypool", "c", "a", "status")
+
+
+class LayerBuffers(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_size_t if f.endswith("_bytes") else ctypes.c_void_p)
+                for f in LAYER_BUFFER_FIELDS]
 
 _lib = None
 
@@ -138,6 +149,13 @@ def load_library(path: str) -> ctypes.CDLL:
     for n in EXPORTS:
         if n != "moe_strerror":
             getattr(L, n).restype = ctypes.c_int
+    pb = ctypes.POINTER(LayerBuffers)
+    L.moe_layer_forward.argtypes = [pc, pb, vp, vp, vp]
+    L.moe_host_pipe_create.argtypes = [pc, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                       ctypes.POINTER(vp), ctypes.POINTER(vp)]
+    L.moe_host_pipe_submit.argtypes = [vp, pb, vp, vp, vp, vp]
+    L.moe_host_pipe_sync.argtypes = [vp]
+    L.moe_host_pipe_destroy.argtypes = [vp]
     if hasattr(L, "moe_check_set_wave_wait_limit_ns"):
         L.moe_check_set_wave_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         L.moe_check_set_wave_wait_limit_ns.restype = ctypes.c_int
@@ -343,6 +361,72 @@ def stats_dict(stats_tensor) -> dict:
     raw = bytes(stats_tensor.detach().cpu().numpy().tobytes())
     s = DropStats.from_buffer_copy(raw)
     return {f: getattr(s, f) for f, _ in DropStats._fields_}
+
+
+# ---------------------------------------------------------------- whole layer
+
+def layer_buffers(tensors: dict) -> LayerBuffers:
+    """moe_layer_buffers_t from tensors named as its fields (None: NULL); the
+    two sizes are taken from the scratch tensors."""
+    b = LayerBuffers()
+    for f in LAYER_BUFFER_FIELDS:
+        if f.endswith("_bytes"):
+            t = tensors.get(f[: -len("_bytes")])
+            setattr(b, f, t.numel() * t.element_size() if t is not None else 0)
+            continue
+        t = tensors.get(f)
+        if t is not None:
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{f}: contiguous device tensor required")
+            setattr(b, f, t.data_ptr())
+    return b
+
+
+def layer_forward(cfg, buffers: LayerBuffers, x, out, stream=None):
+    _check("moe_layer_forward", lib().moe_layer_forward(
+        ctypes.byref(make_config(cfg)), ctypes.byref(buffers), _ptr(x, bf16), _ptr(out, bf16),
+        _stream(stream)))
+
+
+class HostPipe:
+    """moe_host_pipe_*: batches from host memory through moe_layer_forward,
+    the copies on the pipeline's own streams.  x_dev, out_dev, stats_dev:
+    lists of device staging tensors (the ring)."""
+
+    def __init__(self, cfg, x_dev, out_dev, stats_dev):
+        self.cfg = make_config(cfg)
+        n = len(x_dev)
+        arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+        self._keep = (x_dev, out_dev, stats_dev)
+        self.h = ctypes.c_void_p()
+        _check("moe_host_pipe_create", lib().moe_host_pipe_create(
+            ctypes.byref(self.cfg), n, arr(x_dev), arr(out_dev), arr(stats_dev),
+            ctypes.byref(self.h)))
+
+    def submit(self, buffers: LayerBuffers, x_host, out_host, stats_host=None, stream=None):
+        for t in (x_host, out_host) + ((stats_host,) if stats_host is not None else ()):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("host tensors required (pinned for overlap)")
+        _check("moe_host_pipe_submit", lib().moe_host_pipe_submit(
+            self.h, ctypes.byref(buffers), ctypes.c_void_p(x_host.data_ptr()),
+            ctypes.c_void_p(out_host.data_ptr()),
+            ctypes.c_void_p(stats_host.data_ptr()) if stats_host is not None else None,
+            _stream(stream)))
+
+    def synchronize(self):
+        _check("moe_host_pipe_sync", lib().moe_host_pipe_sync(self.h))
+
+    def close(self):
+        if self.h:
+            rc = lib().moe_host_pipe_destroy(self.h)
+            self.h = ctypes.c_void_p()
+            _check("moe_host_pipe_destroy", rc)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ---------------------------------------------------------------- timing trace

@@ -199,7 +199,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 2; }
+int moe_abi_version(void) { return 3; }
 
 int moe_check_status(void) {
     const int v[4] = {check_status_route(), check_status_gemm(), check_status_backward(),

@@ -220,6 +220,26 @@ class PooledWaveMoE:
         return self.bwd_ws[off:]
 
     # -- views ------------------------------------------------------------
+    def buffers(self):
+        """The layer's weights and buffers as moe_layer_buffers_t (capped layout)."""
+        if self.dropless:
+            raise ValueError("moe_layer_forward runs the capped layout")
+        t = {k: v for k, v in self.w.items() if v is not None and v.numel() > 0}
+        t.update(logits=self.logits, idx=self.idx, w=self.gate_w, tie=self.tie, z=self.z,
+                 ws_dispatch=self.ws_dispatch, pool=self.pool, slot_of=self.slot_of,
+                 drop=self.drop, expert_rows=self.expert_rows, expert_count=self.expert_count,
+                 stats=self.stats, bank=self.bank, ws_ffn=self.ws_ffn, ypool=self.ypool,
+                 c=self.c, a=self.a if self.cfg.n_shared else None, status=self.status)
+        return abi.layer_buffers(t)
+
+    def forward_native(self, x, out=None, stream=None):
+        """The whole forward as one library call (moe_layer_forward: the pool
+        fill inside the shared experts' gate/up launch); same results as
+        forward() with pipeline="shared"."""
+        out = self.out if out is None else out
+        abi.layer_forward(self.cfg, self.buffers(), x, out, stream)
+        return out
+
     def pool_payload(self):
         return self.pool[:, : self.cfg.d_latent].view(torch.bfloat16)
 
@@ -232,15 +252,20 @@ class PooledWaveMoE:
 
 
 class HostPipeline:
-    """Runs host-resident batches through a layer with the copies overlapped.
-
-    Batch i's host->device copy runs on its own stream while batch i-1
-    computes and batch i-2's output (and drop statistics) copy back on a third
-    stream; ``depth`` device buffers per direction keep the three in flight.
-    Host tensors should be pinned for the copies to be asynchronous.
+    """Runs host-resident batches through a layer with the copies overlapped,
+    in the library (moe_host_pipe_*, over moe_layer_forward: the pool fill
+    inside the shared experts' gate/up launch, the layer's bank if it has
+    one).  Batch i's host->device copy runs on the library's own stream while
+    batch i-1 computes on the caller's stream and batch i-2's output (and
+    drop statistics) copy back on a second stream of the library's;
+    ``depth`` device staging buffers per direction keep the three in flight.
+    Host tensors should be pinned for the copies to be asynchronous.  The
+    layer's balancing-bias update is not applied on this path.
     """
 
     def __init__(self, layer: "PooledWaveMoE", depth: int = 2):
+        if layer.dropless:
+            raise ValueError("the host pipeline runs the capped layout")
         self.m = layer
         self.depth = depth
         cfg, dev = layer.cfg, layer.device
@@ -249,37 +274,15 @@ class HostPipeline:
         self.od = [torch.empty(cfg.T, cfg.d_model, dtype=torch.bfloat16, device=dev)
                    for _ in range(depth)]
         self.sd = [torch.empty_like(layer.stats) for _ in range(depth)]
-        self.h2d = torch.cuda.Stream(dev)
-        self.d2h = torch.cuda.Stream(dev)
-        self.comp = torch.cuda.current_stream(dev)
-        self.ev_in = [torch.cuda.Event() for _ in range(depth)]     # x[b] landed
-        self.ev_done = [torch.cuda.Event() for _ in range(depth)]   # layer read x[b], wrote out[b]
-        self.ev_out = [torch.cuda.Event() for _ in range(depth)]    # out[b] copied back
-        self.i = 0
+        self.buffers = layer.buffers()
+        self.pipe = abi.HostPipe(cfg, self.xd, self.od, self.sd)
 
-    def submit(self, x_host, out_host, stats_host=None):
+    def submit(self, x_host, out_host, stats_host=None, stream=None):
         """Enqueue one batch: x_host -> layer -> out_host (all asynchronous)."""
-        b = self.i % self.depth
-        m = self.m
-        if self.i >= self.depth:
-            self.h2d.wait_event(self.ev_done[b])      # x[b] no longer read
-        with torch.cuda.stream(self.h2d):
-            self.xd[b].copy_(x_host, non_blocking=True)
-            self.ev_in[b].record(self.h2d)
-        self.comp.wait_event(self.ev_in[b])
-        if self.i >= self.depth:
-            self.comp.wait_event(self.ev_out[b])     # out[b] copied back
-        m.forward(self.xd[b], out=self.od[b], stream=self.comp)
-        self.sd[b].copy_(m.stats, non_blocking=True)
-        self.ev_done[b].record(self.comp)
-        self.d2h.wait_event(self.ev_done[b])
-        with torch.cuda.stream(self.d2h):
-            out_host.copy_(self.od[b], non_blocking=True)
-            if stats_host is not None:
-                stats_host.copy_(self.sd[b], non_blocking=True)
-            self.ev_out[b].record(self.d2h)
-        self.i += 1
+        self.pipe.submit(self.buffers, x_host, out_host, stats_host, stream)
 
     def synchronize(self):
-        for ev in self.ev_out:
-            ev.synchronize()
+        self.pipe.synchronize()
+
+    def close(self):
+        self.pipe.close()

@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     L = abi.lib()
     for name in _declared():
         assert hasattr(L, name), name
-    assert L.moe_abi_version() == 2
+    assert L.moe_abi_version() == 3
 
 
 def test_every_export_declares_its_signature():
@@ -191,3 +191,19 @@ def test_capacity_uses_decimal_factor():
     p = abi.plan(cfg)
     assert (p.c_send, p.c_recv) == (55, 55)
     assert not math.isclose(1.1 * 50, 55.0, rel_tol=0, abs_tol=0)
+
+
+def test_layer_forward_and_host_pipe_refuse_bad_arguments():
+    """Refused on the host before any device call."""
+    L = abi.lib()
+    c = abi.make_config(_small())
+    cp = ctypes.byref(c)
+    arr0 = (ctypes.c_void_p * 1)()
+    h = ctypes.c_void_p()
+    assert L.moe_host_pipe_create(cp, 0, arr0, arr0, arr0, ctypes.byref(h)) == abi.MOE_EINVAL
+    assert L.moe_host_pipe_create(cp, 1, arr0, arr0, arr0, ctypes.byref(h)) == abi.MOE_EINVAL
+    assert not h.value
+    assert L.moe_layer_forward(cp, None, None, None, None) == abi.MOE_EINVAL
+    assert L.moe_host_pipe_submit(None, None, None, None, None, None) == abi.MOE_EINVAL
+    assert L.moe_host_pipe_sync(None) == abi.MOE_EINVAL
+    assert L.moe_host_pipe_destroy(None) == abi.MOE_OK
