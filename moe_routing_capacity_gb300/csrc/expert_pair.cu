@@ -22,9 +22,9 @@
 // Warp roles per CTA: 0 TMA producer, 1 MMA issuer (even CTA) or the wait
 // for the pair's last MMA (odd CTA), 2 TMEM allocation, 4-7 epilogue.  The
 // epilogue moves each 32-column block of its accumulator through shared
-// memory (column-major, 132 floats a column, so both the writes and the
-// row-wise reads are free of bank conflicts), then each thread writes
-// whole 32- or 64-byte pieces of one output row.
+// memory (gate/up: fp32 across the four warps, 132 floats a column; down:
+// bf16 within each warp, 64 bytes a row; both free of bank conflicts), then
+// each thread writes whole 16- or 32-byte pieces of one output row.
 #include <cstring>
 
 #include "common.cuh"
@@ -43,8 +43,7 @@ constexpr int XSTAGE = XA_BYTES + XB_BYTES;          // 32 KB a ring stage
 #endif
 constexpr int XST = MOE_XPAIR_STAGES;
 constexpr int XSTG_LD = 132;                         // gate/up: floats a staged column
-constexpr int XSTG_WLD = 36;                         // down: floats a staged row (per warp)
-constexpr int XSTG_BYTES = (32 * XSTG_LD > 4 * 32 * XSTG_WLD ? 32 * XSTG_LD : 4 * 32 * XSTG_WLD) * 4;
+constexpr int XSTG_BYTES = 32 * XSTG_LD * 4;           // (down: 4 warps x 32 x 32 bf16, less)
 constexpr int XBAR_BYTES = ((2 * XST + 5) * 8 + 2 * 4 + 63) / 64 * 64;
 constexpr int XSMEM = 1024 + XST * XSTAGE + XSTG_BYTES + XBAR_BYTES;
 static_assert(XSMEM <= 232448, "shared memory budget");
@@ -303,8 +302,9 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
                 tc_fence_after();
                 const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
                 // each warp transposes its own 32 features x 32 rows through
-                // its part of the staging (row-major, 36 floats a row)
-                float* w = stg + q * 32 * XSTG_WLD;
+                // its part of the staging, already rounded to bf16 (the
+                // output's rounding): row-major, 64 bytes a row
+                uint16_t* w = reinterpret_cast<uint16_t*>(stg) + q * 32 * 32;
                 uint16_t* obase = p.out + mb * 256 + static_cast<int>(crank) * 128 + 32 * q;
 #pragma unroll
                 for (int c = 0; c < XCHUNK / 32; ++c) {
@@ -312,7 +312,9 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
                         uint32_t r[32];
                         tmem_ld32(tl + 32 * c, r);    // feature 32q + lane, rows 32c ..
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) w[j * XSTG_WLD + lane] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32; ++j)
+                            w[j * 32 + lane] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[j])));
                         __syncwarp();
                         // four lanes a row, 16 bytes (8 features) each: one
                         // store instruction writes 8 rows x 64 contiguous bytes
@@ -321,13 +323,8 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
                         for (int i = 0; i < 4; ++i) {
                             const int j = 8 * i + (lane >> 2);     // row 32c + j
                             const long long pr = __shfl_sync(0xffffffffu, prow[c], j);
-                            const float* row = w + j * XSTG_WLD + 8 * sub;
-                            const float4 y0 = *reinterpret_cast<const float4*>(row);
-                            const float4 y1 = *reinterpret_cast<const float4*>(row + 4);
-                            if (pr >= 0)
-                                *reinterpret_cast<uint4*>(obase + pr * p.ldo + 8 * sub) =
-                                    make_uint4(pack_bf16x2(y0.x, y0.y), pack_bf16x2(y0.z, y0.w),
-                                               pack_bf16x2(y1.x, y1.y), pack_bf16x2(y1.z, y1.w));
+                            const uint4 y = *reinterpret_cast<const uint4*>(w + j * 32 + 8 * sub);
+                            if (pr >= 0) *reinterpret_cast<uint4*>(obase + pr * p.ldo + 8 * sub) = y;
                         }
                         __syncwarp();                 // before the next block overwrites w
                     }
