@@ -335,6 +335,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane; waits for the load.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // ------------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs on two SMs runs one M = 256 tcgen05.mma
 // (cta_group::2): each CTA holds 128 rows of A and half of B's N rows in its
@@ -432,6 +445,15 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
         "h"(static_cast<uint16_t>(3))
         : "memory");
 }
+
+// ------------------------------------------------------------------ activations
+
+// silu(g) = g / (1 + e^-g) with the fast exponential and divide (__expf,
+// __fdividef): within a few fp32 ulp, far below the bf16 rounding of the
+// product it feeds; g -> -inf gives -0 (the divisor overflows to inf), g ->
+// +inf gives g.  Every forward SwiGLU epilogue uses it, so the expert paths
+// agree bit for bit.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // ------------------------------------------------------------------ bf16 packing
 

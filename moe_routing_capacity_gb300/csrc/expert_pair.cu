@@ -8,23 +8,30 @@
 // CTA of a two-CTA cluster (tcgen05.mma.cta_group::2, issued by the even
 // CTA).  For gate/up a CTA's 128 rows are the gate and the up rows of the
 // same 64 hidden units, so its SwiGLU epilogue needs only its own TMEM.  The
-// expert's rows sit on N, in chunks of at most 256 rows sized evenly over
-// the expert's count and rounded up to 16 (each CTA stages half of them):
-// an M x N x 16 MMA costs N/2 cycles for N >= 128 (measured on this part),
-// so an expert with 316 rows computes two chunks of 160 (320 MMA rows)
-// instead of three 128-row tiles (384).  Both operands arrive by TMA: the
-// weights from their [E, rows, K] tensors, the expert's rows from a
-// per-expert bank [E, c_recv, K] (the received rows grouped by local expert,
-// written by the dispatch's pack; for the down product, h itself).  Bank
-// rows past an expert's count hold stale values: each one reaches only its
-// own column of the accumulator, which the epilogue never stores.
+// expert's rows sit on N in chunks of at most 256 rows (an M x N x 16 MMA
+// costs N/2 cycles for N >= 128, measured on this part), sized evenly over
+// the expert's count and rounded up to 16, each CTA staging half of them.
+// Both operands arrive by TMA: the weights from their [E, rows, K] tensors,
+// the expert's rows from a per-expert bank [E, c_recv, K] (the received rows
+// grouped by local expert, written by the dispatch's pack; for the down
+// product, h itself).  Bank rows past an expert's count hold stale values:
+// each one reaches only its own column of the accumulator, which the
+// epilogue never stores.
 //
+// Two kernels:
+//  * expert_gateup_kernel (gate/up): a tile is a group of up to 416 of an
+//    expert's rows in one or two chunks that share each weight block staged
+//    in shared memory; see its section below.
+//  * expert_pair_kernel: a tile is one chunk, two accumulators of 256
+//    columns in turn.  The down product; also gate/up when the two weight
+//    tensors cannot share one tensor map.
 // Warp roles per CTA: 0 TMA producer, 1 MMA issuer (even CTA) or the wait
-// for the pair's last MMA (odd CTA), 2 TMEM allocation, 4-7 epilogue.  The
-// epilogue moves each 32-column block of its accumulator through shared
-// memory (gate/up: fp32 across the four warps, 132 floats a column; down:
-// bf16 within each warp, 64 bytes a row; both free of bank conflicts), then
-// each thread writes whole 16- or 32-byte pieces of one output row.
+// for the pair's last MMA (odd CTA), 2 TMEM allocation, 4 and up epilogue.
+// expert_pair_kernel's epilogue moves each 32-column block of its
+// accumulator through shared memory (gate/up: fp32 across the four warps,
+// 132 floats a column; down: bf16 within each warp, 64 bytes a row; both free
+// of bank conflicts), then each thread writes whole 16- or 32-byte pieces of
+// one output row.
 #include <cstring>
 
 #include "common.cuh"
@@ -59,6 +66,11 @@ static_assert(XGRAN == 16 || XGRAN == 32, "chunk granularity");
 // time, every row loaded but not used costs shared-memory bandwidth.
 constexpr int XHSTEP = XGRAN / 2;
 constexpr int XNMAP = XB_ROWS / XHSTEP;
+// gate/up over row groups (expert_gateup_kernel); 0: the chunk-tile kernel
+#ifndef MOE_XPAIR_TM
+#define MOE_XPAIR_TM 1
+#endif
+static_assert(!MOE_XPAIR_TM || XGRAN == 16, "gate/up groups split into halves of 16-row multiples");
 
 struct XParams {
     CUtensorMap mapW0;     // gate/up: Wg [E, H, L], box {64, 64} (or, wpair, both: see below);
@@ -80,8 +92,6 @@ struct XParams {
     long long out_rows;    // down: pool rows (checked builds)
     int* status;
 };
-
-__device__ __forceinline__ float silu_x(float g) { return g / (1.0f + expf(-g)); }
 
 template <int EPI>
 __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_constant__ XParams p) {
@@ -273,8 +283,8 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
                         for (int v = 0; v < 4; ++v) {
                             const float4 g4 = *reinterpret_cast<const float4*>(col + go + 16 * grp + 4 * v);
                             const float4 u4 = *reinterpret_cast<const float4*>(col + uo + 16 * grp + 4 * v);
-                            pk[2 * v] = pack_bf16x2(silu_x(g4.x) * u4.x, silu_x(g4.y) * u4.y);
-                            pk[2 * v + 1] = pack_bf16x2(silu_x(g4.z) * u4.z, silu_x(g4.w) * u4.w);
+                            pk[2 * v] = pack_bf16x2(silu_fast(g4.x) * u4.x, silu_fast(g4.y) * u4.y);
+                            pk[2 * v + 1] = pack_bf16x2(silu_fast(g4.z) * u4.z, silu_fast(g4.w) * u4.w);
                         }
                         const long long hrow = static_cast<long long>(e) * p.c_recv + row0 + rr;
                         uint16_t* dst = p.out + hrow * p.ldo + mb * 128 +
@@ -348,53 +358,427 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
     if (warp == 2) tmem_dealloc_pair(tmem_base, 512);
 }
 
-// Chunks {expert, first row, rows, N} of every expert with rows: an expert's
-// n rows split into ceil(n / 256) chunks of even size rounded up to XGRAN (the
-// last one takes the rest), N = the chunk's rows rounded up to XGRAN.  One CTA;
-// a block-wide exclusive prefix over the experts' chunk counts.
+// ---------------------------------------------------------------- gate/up over row groups
+//
+// With one tile a chunk, an expert's second chunk streams the same 48 weight
+// blocks through shared memory again: at N = 160 a CTA's shared memory moves
+// 52 KB a K block (TMA writes and MMA reads of 16 KB of weights and 10 KB of
+// rows) for 320 MMA cycles, more than it sustains.  Here a tile is a group of
+// up to 416 of an expert's rows in one or two chunks (an MMA's N is at most
+// 256): each weight block is loaded once and read by both chunks' MMAs, 36 KB
+// written and 52 KB read a K block for 640 MMA cycles.
+//
+// A group's accumulator takes S = N0 + N1 TMEM columns.  Consecutive tiles of
+// a CTA pair sit at the two ends of the 512 columns (even tiles from column
+// 0, odd tiles ending at column 511, every start a multiple of 32), so the
+// next tile's MMAs start while the previous tile drains unless the two
+// overlap; then the epilogue drains the overlapping columns first (both
+// warp groups, from the end facing the other tile) and releases them before
+// the rest.  The MMA issuer waits for the overlap of the tile before and for
+// the whole of the tile two before (the same end).
+//
+// A CTA's 128 weight rows arrive by one TMA box that interleaves the two
+// tensors by 16 rows: lanes 32q .. 32q+15 hold 16 hidden units of the lower-
+// addressed tensor, lanes 32q+16 .. 32q+31 the same units of the other, so a
+// lane's SwiGLU partner is lane ^ 16 of its own warp (one shuffle, no shared-
+// memory exchange).  Eight epilogue warps, two a lane quarter, take
+// alternate 32-column blocks.
+constexpr int GACC = 416;                      // most rows (accumulator columns) a group
+constexpr int GB_BYTES = GACC / 2 * XBK * 2;   // this CTA's rows a stage: at most 208
+constexpr int GSTAGE = XA_BYTES + GB_BYTES;    // 42 KB
+#ifndef MOE_XGATE_STAGES
+#define MOE_XGATE_STAGES 5
+#endif
+constexpr int GST = MOE_XGATE_STAGES;
+constexpr int GBAR_BYTES = ((2 * GST + 7) * 8 + 2 * 4 + 63) / 64 * 64;
+constexpr int GSMEM = 1024 + GST * GSTAGE + GBAR_BYTES;
+static_assert(GSMEM <= 232448, "shared memory budget");
+constexpr int GEPI_WARPS = 8;
+constexpr int GTHREADS = 128 + 32 * GEPI_WARPS;
+
+struct GParams {
+    CUtensorMap mapW;          // [Wg ; Wu] as dims {L, 16, 2, E*H/16}: box {64, 16, 2, 4}
+    CUtensorMap mapX[XNMAP];   // bank [E, c_recv, L], box {64, XHSTEP (i+1)}
+    const int4* groups;        // {expert, first row, rows, N0 | N1 << 16}
+    const int* ngroups;
+    int n_mb;                  // H / 128: weight blocks a group
+    int zpe;                   // H / 16: 16-unit blocks an expert
+    int gate_hi;               // the gate tensor is the higher-addressed one
+    int kb;                    // K blocks (L / 64)
+    int c_recv;
+    int H;
+    uint16_t* h;               // [E, c_recv, H]
+    int* status;
+};
+
+struct GTile {
+    int e, row0, rows, n0, n1, mb;
+};
+
+__device__ __forceinline__ GTile gate_tile(const GParams& p, int tile) {
+    const int gi = tile / p.n_mb;
+    const int4 g = p.groups[gi];
+    GTile t;
+    t.e = g.x;
+    t.row0 = g.y;
+    t.rows = g.z;
+    t.n0 = g.w & 0xffff;
+    t.n1 = static_cast<int>(static_cast<uint32_t>(g.w) >> 16);
+    t.mb = tile - gi * p.n_mb;
+    return t;
+}
+
+// First TMEM column of the k-th tile of a pair whose accumulator has S columns.
+__device__ __forceinline__ int gate_base(int k, int S) { return (k & 1) ? (512 - S) & ~31 : 0; }
+
+__device__ __forceinline__ int gate_cols(const GParams& p, int tile) {
+    const int w = p.groups[tile / p.n_mb].w;
+    return (w & 0xffff) + static_cast<int>(static_cast<uint32_t>(w) >> 16);
+}
+
+__global__ void __launch_bounds__(GTHREADS, 1) expert_gateup_kernel(const __grid_constant__ GParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sbase = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sStage = sbase;                                   // GST x (W 16 KB | rows 26 KB)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + GST * GSTAGE);
+    uint64_t* full = bars;
+    uint64_t* empty = full + GST;
+    uint64_t* tfull = empty + GST;   // [2]: a tile at that end is accumulated
+    uint64_t* ovl = tfull + 2;       // [2]: its columns the next tile needs are drained
+    uint64_t* fdone = ovl + 2;       // [2]: all its columns are drained
+    uint64_t* done = fdone + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_ctarank();
+    const bool leader = crank == 0;
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int npairs = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&ovl[a], 2 * GEPI_WARPS);     // one arrival a warp, both CTAs
+            mbar_init(&fdone[a], 2 * GEPI_WARPS);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.mapW);
+        for (int i = 0; i < XNMAP; ++i) tma_prefetch_map(&p.mapX[i]);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    const int ntiles = *reinterpret_cast<const volatile int*>(p.ngroups) * p.n_mb;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            uint32_t armed = 0, par = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < ntiles; tile += npairs) {
+                const GTile t = gate_tile(p, tile);
+                const int h0 = t.n0 >> 1, h1 = t.n1 >> 1;      // this CTA's rows of each chunk
+                const int xrow0 = t.row0 + static_cast<int>(crank) * h0;
+                const int xrow1 = t.row0 + t.n0 + static_cast<int>(crank) * h1;
+                const uint32_t bytes = XA_BYTES + static_cast<uint32_t>(h0 + h1) * XBK * 2;
+                const int z = t.e * p.zpe + t.mb * 8 + static_cast<int>(crank) * 4;
+                for (int kb = 0; kb < p.kb; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        mbar_arrive_expect_tx(&full[s], 2u * bytes);
+                        armed |= 1u << s;
+                        par = (par & ~(1u << s)) | (ph << s);
+                    }
+                    const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+                    const uint32_t a_dst = smem_u32(sStage + s * GSTAGE);
+                    const uint32_t b_dst = a_dst + XA_BYTES;
+                    const int kx = kb * XBK;
+                    tma_load_4d_pair(a_dst, &p.mapW, fb, kx, 0, 0, z);
+                    tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, xrow0, t.e);
+                    if (h1)
+                        tma_load_3d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kx,
+                                         xrow1, t.e);
+                    if (++s == GST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok || *abort_flag) {
+                volatile int no_abort = 0;
+                for (int i = 0; i < GST; ++i)
+                    if (armed >> i & 1u)
+                        mbar_wait(&full[i], (par >> i) & 1u, &no_abort, nullptr, 20000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && !leader) {
+            volatile int no_abort = 0;
+            mbar_wait(done, 0, &no_abort, p.status);
+        } else if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            bool ok = true;
+            int k = 0;   // this pair's tiles so far
+            for (int tile = pair; ok && tile < ntiles; tile += npairs, ++k) {
+                const GTile t = gate_tile(p, tile);
+                const uint32_t end = static_cast<uint32_t>(k & 1);
+                // the tile two before (same end) fully drained, the tile
+                // before drained where this one's columns lie
+                if (k >= 2)
+                    ok = mbar_wait(&fdone[end], static_cast<uint32_t>((k - 2) >> 1) & 1u, abort_flag,
+                                   p.status);
+                if (ok && k >= 1)
+                    ok = mbar_wait(&ovl[end ^ 1u], static_cast<uint32_t>((k - 1) >> 1) & 1u,
+                                   abort_flag, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + static_cast<uint32_t>(gate_base(k, t.n0 + t.n1));
+                const uint32_t d1 = d0 + static_cast<uint32_t>(t.n0);
+                const uint32_t id0 = idesc_bf16_f32(256, t.n0);
+                const uint32_t id1 = idesc_bf16_f32(256, t.n1 ? t.n1 : 16);
+                const uint32_t boff1 = static_cast<uint32_t>(t.n0 >> 1) * XBK * 2;
+                for (int kb = 0; kb < p.kb; ++kb) {
+                    if (!mbar_wait(&full[s], ph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_s = smem_u32(sStage + s * GSTAGE);
+                    const uint64_t ad = sdesc_k_sw128(a_s);
+                    const uint64_t bd0 = sdesc_k_sw128(a_s + XA_BYTES);
+                    const uint64_t bd1 = sdesc_k_sw128(a_s + XA_BYTES + boff1);
+#pragma unroll
+                    for (int kk = 0; kk < XBK / 16; ++kk) {
+                        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+                        mma_bf16_pair(d0, ad + 2u * kk, bd0 + 2u * kk, id0, acc);
+                        if (t.n1) mma_bf16_pair(d1, ad + 2u * kk, bd1 + 2u * kk, id1, acc);
+                    }
+                    mma_commit_pair(&empty[s]);
+                    if (++s == GST) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair(&tfull[end]);
+            }
+            mma_commit_pair(done);
+            volatile int no_abort = 0;
+            mbar_wait(done, 0, &no_abort, p.status);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 4;
+        const int q = ew & 3;                     // TMEM lane quarter (= warp % 4)
+        const int grp = ew >> 2;                  // order positions grp, grp + 2, ...
+        const bool hi = lane >= 16;               // lanes of the higher-addressed tensor
+        const int y = lane & 15;
+        const bool odd = (y & 1) != 0;
+        const uint32_t bar_c0 = mapa_shared(smem_u32(&ovl[0]), 0);
+        const uint32_t fdone_c0 = mapa_shared(smem_u32(&fdone[0]), 0);
+        int k = 0;
+        for (int tile = pair; tile < ntiles; tile += npairs, ++k) {
+            const GTile t = gate_tile(p, tile);
+            const uint32_t end = static_cast<uint32_t>(k & 1);
+            const int S = t.n0 + t.n1;
+            const int base = gate_base(k, S);
+            const int nblk = (S + 31) >> 5;
+            // columns the next tile (other end) needs: blocks met first in
+            // this tile's drain order (from the end facing it)
+            int n_ov = 0;
+            if (tile + npairs < ntiles) {
+                const int S2 = gate_cols(p, tile + npairs);
+                const int b2 = gate_base(k + 1, S2);
+                const int lo = base > b2 ? base : b2;
+                const int hi_c = base + S < b2 + S2 ? base + S : b2 + S2;
+                if (lo < hi_c)
+                    n_ov = end ? (hi_c - base + 31) >> 5                 // ascending: blocks below hi_c
+                               : nblk - ((lo - base) >> 5);              // descending: blocks from lo up
+            }
+            const int my_ov = n_ov > grp ? (n_ov - grp + 1) >> 1 : 0;
+            if (my_ov == 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
+            }
+            if (!mbar_wait(&tfull[end], static_cast<uint32_t>(k >> 1) & 1u, abort_flag, p.status))
+                break;
+            tc_fence_after();
+            const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(base);
+            // column c of the tile is the group's row row0 + c (chunk 0 is full)
+            const int unit = t.mb * 128 + static_cast<int>(crank) * 64 + q * 16 + (y & ~1);
+            uint16_t* hb = p.h + (static_cast<long long>(t.e) * p.c_recv + t.row0) * p.H + unit;
+            int drained = 0;
+#pragma unroll 1
+            for (int pos = grp; pos < nblk; pos += 2) {
+                const int b = end ? pos : nblk - 1 - pos;
+                uint32_t r[32];
+                if (S - 32 * b >= 32) {
+                    tmem_ld32(tl + 32 * b, r);
+                } else {
+                    uint32_t r16[16];
+                    tmem_ld16(tl + 32 * b, r16);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        r[j] = r16[j];
+                        r[16 + j] = 0u;
+                    }
+                }
+                if (++drained == my_ov) {   // this warp's share of the overlap is out of TMEM
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
+                }
+                // lanes < 16 finish rows 0-15 of the block, lanes >= 16 rows 16-31
+                float hv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t mine = hi ? r[16 + j] : r[j];
+                    const uint32_t give = hi ? r[j] : r[16 + j];
+                    const float oth = __uint_as_float(__shfl_xor_sync(0xffffffffu, give, 16));
+                    const float own = __uint_as_float(mine);
+                    const float lo_t = hi ? oth : own, hi_t = hi ? own : oth;
+                    const float g = p.gate_hi ? hi_t : lo_t, u = p.gate_hi ? lo_t : hi_t;
+                    hv[j] = silu_fast(g) * u;
+                }
+                // pairs of units to 32-bit stores: even lanes rows 0-7, odd lanes 8-15
+                const int rb = 32 * b + (hi ? 16 : 0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float other = __shfl_xor_sync(0xffffffffu, odd ? hv[j] : hv[8 + j], 1);
+                    const int row = rb + (odd ? 8 + j : j);
+                    const uint32_t word = odd ? pack_bf16x2(other, hv[8 + j]) : pack_bf16x2(hv[j], other);
+                    if (row < t.rows)
+                        *reinterpret_cast<uint32_t*>(hb + static_cast<long long>(row) * p.H) = word;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(fdone_c0 + end * 8u);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();
+    if (warp == 2) tmem_dealloc_pair(tmem_base, 512);
+}
+
+// Block-wide exclusive prefix of v over the CTA's threads, plus the running
+// total carried across calls (all threads call it; blockDim a multiple of 32).
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sum, int* carry) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = v;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ws, off);
+            if (lane >= off) ws += y;
+        }
+        warp_sum[lane] = ws;
+    }
+    __syncthreads();
+    const int excl = *carry + (wid ? warp_sum[wid - 1] : 0) + incl - v;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) *carry = excl + v;
+    __syncthreads();
+    return excl;
+}
+
+__device__ __forceinline__ int round_gran(int n) { return (n + XGRAN - 1) / XGRAN * XGRAN; }
+
+// Pieces of at most `cap` rows covering n rows, sized evenly and rounded up to
+// XGRAN (the last one takes the rest): the piece size, and their number.
+__device__ __forceinline__ int piece_rows(int n, int cap, int* count) {
+    if (n <= 0) {
+        *count = 0;
+        return 0;
+    }
+    const int per = round_gran((n + (n + cap - 1) / cap - 1) / ((n + cap - 1) / cap));
+    *count = (n + per - 1) / per;
+    return per;
+}
+
+// For every expert with rows:
+//  chunks {expert, first row, rows, N}: pieces of at most 256 rows, N = the
+//    rows rounded up to XGRAN (the down product's tiles);
+//  groups {expert, first row, rows, N0 | N1 << 16}: pieces of at most 416 rows
+//    (the gate/up product's tiles), each one chunk (N0 = rows rounded up,
+//    N1 = 0) up to 256 rows, else two: N0 = half the rows rounded up to 32
+//    (chunk 0 exactly full), N1 = the rest rounded up to XGRAN; N0 + N1 is at
+//    most the rows rounded up to XGRAN, so at most 416.
+// One CTA; block-wide exclusive prefixes over the experts' counts.
 __global__ void __launch_bounds__(1024) chunk_list_kernel(const int32_t* __restrict__ counts,
                                                           int E, int c_recv, int4* __restrict__ chunks,
-                                                          int32_t* __restrict__ nchunks) {
+                                                          int32_t* __restrict__ nchunks,
+                                                          int4* __restrict__ groups,
+                                                          int32_t* __restrict__ ngroups) {
     __shared__ int warp_sum[32];
-    __shared__ int carry;
-    if (threadIdx.x == 0) carry = 0;
+    __shared__ int carry_c, carry_g;
+    if (threadIdx.x == 0) carry_c = carry_g = 0;
     __syncthreads();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int e0 = 0; e0 < E; e0 += blockDim.x) {
         const int e = e0 + threadIdx.x;
         int n = e < E ? counts[e] : 0;
         n = n < 0 ? 0 : (n > c_recv ? c_recv : n);
-        const int nch = (n + XCHUNK - 1) / XCHUNK;
-        int incl = nch;
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
+        int nch, ngr;
+        const int per = piece_rows(n, XCHUNK, &nch);
+        const int pg = piece_rows(n, GACC, &ngr);
+        const int exc = block_excl_scan(nch, warp_sum, &carry_c);
+        const int exg = block_excl_scan(ngr, warp_sum, &carry_g);
+        for (int i = 0; i < nch; ++i) {
+            const int r0 = i * per;
+            const int rows = (n - r0 < per) ? n - r0 : per;
+            chunks[exc + i] = make_int4(e, r0, rows, round_gran(rows));
         }
-        if (lane == 31) warp_sum[wid] = incl;
-        __syncthreads();
-        if (wid == 0) {
-            int ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, ws, off);
-                if (lane >= off) ws += y;
+        for (int i = 0; i < ngr; ++i) {
+            const int r0 = i * pg;
+            const int rows = (n - r0 < pg) ? n - r0 : pg;
+            int n0, n1;
+            if (rows <= XCHUNK) {
+                n0 = round_gran(rows);
+                n1 = 0;
+            } else {   // chunk 0: half the rows rounded up to 32 (at most 224)
+                n0 = ((rows + 1) / 2 + 31) / 32 * 32;
+                n1 = round_gran(rows - n0);
             }
-            warp_sum[lane] = ws;
+            groups[exg + i] = make_int4(e, r0, rows, n0 | (n1 << 16));
         }
-        __syncthreads();
-        const int excl = carry + (wid ? warp_sum[wid - 1] : 0) + incl - nch;
-        if (nch > 0) {
-            const int per = ((n + nch - 1) / nch + XGRAN - 1) / XGRAN * XGRAN;
-            for (int i = 0; i < nch; ++i) {
-                const int r0 = i * per;
-                const int rows = (n - r0 < per) ? n - r0 : per;
-                chunks[excl + i] = make_int4(e, r0, rows, (rows + XGRAN - 1) / XGRAN * XGRAN);
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == blockDim.x - 1) carry = excl + nch;
-        __syncthreads();
     }
-    if (threadIdx.x == 0) *nchunks = carry;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        *nchunks = carry_c;
+        *ngroups = carry_g;
+    }
 }
 
 typedef CUresult (*EncodeTiledFnX)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -479,13 +863,94 @@ int launch_pair(const XParams& p, int sms, cudaStream_t st, const char* name) {
     return MOE_OK;
 }
 
+// [Wg ; Wu] for the TMEM-held gate/up product: dims {L, 16, 2, E*H/16} with
+// strides {row, distance from the lower-addressed tensor to the other, 16
+// rows}, box {64, 16, 2, 4}: a box of 128 rows holds, for each of 4 blocks of
+// 16 hidden units, the 16 rows of the lower tensor then the 16 of the other.
+// MOE_EINVAL when the two tensors' distance cannot be a stride.
+int map_gateup_il(CUtensorMap* m, const void* Wg, const void* Wu, int E, int H, int L,
+                  int* gate_hi) {
+    EncodeTiledFnX enc = encode_x();
+    if (!enc) return MOE_ECUDA;
+    const uintptr_t g = reinterpret_cast<uintptr_t>(Wg), u = reinterpret_cast<uintptr_t>(Wu);
+    const uintptr_t lo = g < u ? g : u, hi = g < u ? u : g;
+    const uint64_t dist = hi - lo;
+    if (dist == 0 || (dist & 15) || dist >= (1ull << 40) || H % 64 || (lo & 15)) return MOE_EINVAL;
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(L), 16, 2,
+                                static_cast<cuuint64_t>(E) * (H / 16)};
+    const cuuint64_t gstr[3] = {static_cast<cuuint64_t>(L) * 2, dist, 16ull * L * 2};
+    const cuuint32_t box[4] = {XBK, 16, 2, 4}, est[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, reinterpret_cast<void*>(lo), gdim, gstr,
+                     box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return MOE_EINVAL;
+    *gate_hi = g > u ? 1 : 0;
+    return MOE_OK;
+}
+
+int launch_gateup(const GParams& p, int sms, cudaStream_t st, const char* name) {
+    auto kern = expert_gateup_kernel;
+    if (ensure_smem_attr(reinterpret_cast<const void*>(kern), GSMEM) != MOE_OK) return MOE_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(GTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = GSMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ECUDA;
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, name);
+    return MOE_OK;
+}
+
+// The down product over the chunk list.
+int launch_down(int E, int c_recv, int L, int H, const uint16_t* Wd, const int4* chunks,
+                const int32_t* nchunks, uint16_t* h, const int32_t* expert_rows, uint16_t* ypool,
+                int64_t pool_rows, int32_t* status, int sms, cudaStream_t st) {
+    int rc;
+    XParams b;
+    std::memset(&b, 0, sizeof(b));
+    if ((rc = map3(&b.mapW0, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
+    for (int i = 0; i < XNMAP; ++i)
+        if ((rc = map3(&b.mapX[i], h, H, c_recv, E, H, static_cast<uint64_t>(c_recv) * H,
+                       XHSTEP * (i + 1))))
+            return rc;
+    b.chunks = chunks;
+    b.nchunks = nchunks;
+    b.n_mb = L / 256;
+    b.kb = (H + XBK - 1) / XBK;
+    b.c_recv = c_recv;
+    b.out = ypool;
+    b.ldo = L;
+    b.rowmap = expert_rows;
+    b.out_rows = pool_rows;
+    b.status = status;
+    return launch_pair<EPI_SCATTER>(b, sms, st, "gemm_expert_down");
+}
+
 }  // namespace
 
 int check_status_expert_pair() { return moe_check_read_reset(); }
 
-size_t expert_pair_chunks_bytes(int E, int c_recv) {
+// Chunk list, group list, then the two counts (16 bytes).
+static size_t chunk_list_bytes(int E, int c_recv) {
     const size_t per = static_cast<size_t>((c_recv + XCHUNK - 1) / XCHUNK);
-    return static_cast<size_t>(E) * (per > 0 ? per : 1) * sizeof(int4) + 16;
+    return static_cast<size_t>(E) * (per > 0 ? per : 1) * sizeof(int4);
+}
+
+static size_t group_list_bytes(int E, int c_recv) {
+    const size_t per = static_cast<size_t>((c_recv + GACC - 1) / GACC);
+    return static_cast<size_t>(E) * (per > 0 ? per : 1) * sizeof(int4);
+}
+
+size_t expert_pair_chunks_bytes(int E, int c_recv) {
+    return chunk_list_bytes(E, c_recv) + group_list_bytes(E, c_recv) + 16;
 }
 
 int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
@@ -499,13 +964,38 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
     if ((reinterpret_cast<uintptr_t>(chunk_ws) & 15) || (reinterpret_cast<uintptr_t>(bank) & 15) ||
         (reinterpret_cast<uintptr_t>(h) & 15))
         return MOE_EINVAL;
-    int4* chunks = static_cast<int4*>(chunk_ws);
-    int32_t* nchunks = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(chunk_ws) +
-                                                  expert_pair_chunks_bytes(E, c_recv) - 16);
-    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, c_recv, chunks, nchunks);
+    uint8_t* ws = static_cast<uint8_t*>(chunk_ws);
+    int4* chunks = reinterpret_cast<int4*>(ws);
+    int4* groups = reinterpret_cast<int4*>(ws + chunk_list_bytes(E, c_recv));
+    int32_t* nchunks = reinterpret_cast<int32_t*>(ws + expert_pair_chunks_bytes(E, c_recv) - 16);
+    int32_t* ngroups = nchunks + 1;
+    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, c_recv, chunks, nchunks, groups,
+                                          ngroups);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "build_chunks");
 
+    if (MOE_XPAIR_TM) {
+        GParams g;
+        std::memset(&g, 0, sizeof(g));
+        if (map_gateup_il(&g.mapW, Wg, Wu, E, H, L, &g.gate_hi) == MOE_OK) {
+            for (int i = 0; i < XNMAP; ++i)
+                if ((rc = map3(&g.mapX[i], bank, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
+                               XHSTEP * (i + 1))))
+                    return rc;
+            g.groups = groups;
+            g.ngroups = ngroups;
+            g.n_mb = H / 128;
+            g.zpe = H / 16;
+            g.kb = L / XBK;
+            g.c_recv = c_recv;
+            g.H = H;
+            g.h = h;
+            g.status = status;
+            if ((rc = launch_gateup(g, sms, st, "gemm_expert_gateup"))) return rc;
+            return launch_down(E, c_recv, L, H, Wd, chunks, nchunks, h, expert_rows, ypool, pool_rows,
+                               status, sms, st);
+        }
+    }
     XParams a;
     std::memset(&a, 0, sizeof(a));
 #ifndef MOE_XPAIR_ONE_WLOAD
@@ -533,25 +1023,8 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
     a.ldo = H;
     a.status = status;
     if ((rc = launch_pair<EPI_SWIGLU>(a, sms, st, "gemm_expert_gateup"))) return rc;
-
-    XParams b;
-    std::memset(&b, 0, sizeof(b));
-    if ((rc = map3(&b.mapW0, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
-    for (int i = 0; i < XNMAP; ++i)
-        if ((rc = map3(&b.mapX[i], h, H, c_recv, E, H, static_cast<uint64_t>(c_recv) * H,
-                       XHSTEP * (i + 1))))
-            return rc;
-    b.chunks = chunks;
-    b.nchunks = nchunks;
-    b.n_mb = L / 256;
-    b.kb = (H + XBK - 1) / XBK;
-    b.c_recv = c_recv;
-    b.out = ypool;
-    b.ldo = L;
-    b.rowmap = expert_rows;
-    b.out_rows = pool_rows;
-    b.status = status;
-    return launch_pair<EPI_SCATTER>(b, sms, st, "gemm_expert_down");
+    return launch_down(E, c_recv, L, H, Wd, chunks, nchunks, h, expert_rows, ypool, pool_rows, status,
+                       sms, st);
 }
 
 }  // namespace moe

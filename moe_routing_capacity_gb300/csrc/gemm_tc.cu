@@ -226,7 +226,7 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
     }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return silu_fast(g); }
 
 // First row-map entry of group g.
 __device__ __forceinline__ long long rowmap_base(const KParams& p, int g) {
