@@ -19,12 +19,13 @@
 // epilogue never stores.
 //
 // Two kernels:
-//  * expert_gateup_kernel (gate/up): a tile is a group of up to 416 of an
-//    expert's rows in one or two chunks that share each weight block staged
-//    in shared memory; see its section below.
+//  * expert_group_kernel (both products): a tile is a group of up to 416 of
+//    an expert's rows in one or two chunks that share each weight block
+//    staged in shared memory; see its section below.
 //  * expert_pair_kernel: a tile is one chunk, two accumulators of 256
-//    columns in turn.  The down product; also gate/up when the two weight
-//    tensors cannot share one tensor map.
+//    columns in turn; gate/up when the two weight tensors cannot share one
+//    tensor map, and either product when built with MOE_XPAIR_TM=0 or
+//    MOE_XPAIR_DGROUP=0.
 // Warp roles per CTA: 0 TMA producer, 1 MMA issuer (even CTA) or the wait
 // for the pair's last MMA (odd CTA), 2 TMEM allocation, 4 and up epilogue.
 // expert_pair_kernel's epilogue moves each 32-column block of its
@@ -66,7 +67,7 @@ static_assert(XGRAN == 16 || XGRAN == 32, "chunk granularity");
 // time, every row loaded but not used costs shared-memory bandwidth.
 constexpr int XHSTEP = XGRAN / 2;
 constexpr int XNMAP = XB_ROWS / XHSTEP;
-// gate/up over row groups (expert_gateup_kernel); 0: the chunk-tile kernel
+// gate/up over row groups (expert_group_kernel); 0: the chunk-tile kernel
 #ifndef MOE_XPAIR_TM
 #define MOE_XPAIR_TM 1
 #endif
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
     if (warp == 2) tmem_dealloc_pair(tmem_base, 512);
 }
 
-// ---------------------------------------------------------------- gate/up over row groups
+// ---------------------------------------------------------------- both products over row groups
 //
 // With one tile a chunk, an expert's second chunk streams the same 48 weight
 // blocks through shared memory again: at N = 160 a CTA's shared memory moves
@@ -377,12 +378,14 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
 // the rest.  The MMA issuer waits for the overlap of the tile before and for
 // the whole of the tile two before (the same end).
 //
-// A CTA's 128 weight rows arrive by one TMA box that interleaves the two
-// tensors by 16 rows: lanes 32q .. 32q+15 hold 16 hidden units of the lower-
-// addressed tensor, lanes 32q+16 .. 32q+31 the same units of the other, so a
-// lane's SwiGLU partner is lane ^ 16 of its own warp (one shuffle, no shared-
-// memory exchange).  Eight epilogue warps, two a lane quarter, take
-// alternate 32-column blocks.
+// Gate/up: a CTA's 128 weight rows arrive by one TMA box that interleaves the
+// two tensors by 16 rows: lanes 32q .. 32q+15 hold 16 hidden units of the
+// lower-addressed tensor, lanes 32q+16 .. 32q+31 the same units of the other,
+// so a lane's SwiGLU partner is lane ^ 16 of its own warp (one shuffle, no
+// shared-memory exchange).  Down: a CTA's 128 rows of Wd are 128 output
+// features; lanes pair adjacent features by a shuffle into 32-bit stores
+// scattered to the rows' pool rows.  Eight epilogue warps, two a lane
+// quarter, take alternate 32-column blocks.
 constexpr int GACC = 416;                      // most rows (accumulator columns) a group
 constexpr int GB_BYTES = GACC / 2 * XBK * 2;   // this CTA's rows a stage: at most 208
 constexpr int GSTAGE = XA_BYTES + GB_BYTES;    // 42 KB
@@ -394,20 +397,24 @@ constexpr int GBAR_BYTES = ((2 * GST + 7) * 8 + 2 * 4 + 63) / 64 * 64;
 constexpr int GSMEM = 1024 + GST * GSTAGE + GBAR_BYTES;
 static_assert(GSMEM <= 232448, "shared memory budget");
 constexpr int GEPI_WARPS = 8;
+constexpr int GMAXB = (GACC / 32 + 2) / 2;      // most 32-column blocks a warp drains a tile
 constexpr int GTHREADS = 128 + 32 * GEPI_WARPS;
 
 struct GParams {
-    CUtensorMap mapW;          // [Wg ; Wu] as dims {L, 16, 2, E*H/16}: box {64, 16, 2, 4}
-    CUtensorMap mapX[XNMAP];   // bank [E, c_recv, L], box {64, XHSTEP (i+1)}
+    CUtensorMap mapW;          // gate/up: [Wg ; Wu] as dims {L, 16, 2, E*H/16}, box {64, 16, 2, 4};
+                               // down: Wd [E, L, H], box {64, 128}
+    CUtensorMap mapX[XNMAP];   // the rows: bank [E, c_recv, L] or h [E, c_recv, H], box {64, XHSTEP (i+1)}
     const int4* groups;        // {expert, first row, rows, N0 | N1 << 16}
     const int* ngroups;
-    int n_mb;                  // H / 128: weight blocks a group
-    int zpe;                   // H / 16: 16-unit blocks an expert
-    int gate_hi;               // the gate tensor is the higher-addressed one
-    int kb;                    // K blocks (L / 64)
+    int n_mb;                  // 256-row weight blocks a group (gate/up: H / 128; down: L / 256)
+    int zpe;                   // gate/up: H / 16, 16-unit blocks an expert
+    int gate_hi;               // gate/up: the gate tensor is the higher-addressed one
+    int kb;                    // K blocks
     int c_recv;
-    int H;
-    uint16_t* h;               // [E, c_recv, H]
+    uint16_t* out;             // h [E, c_recv, H] (gate/up) or ypool [pool_rows, L] (down)
+    long long ldo;             // H or L
+    const int* rowmap;         // down: expert_rows [E, c_recv]
+    long long out_rows;        // down: pool rows (checked builds)
     int* status;
 };
 
@@ -436,7 +443,8 @@ __device__ __forceinline__ int gate_cols(const GParams& p, int tile) {
     return (w & 0xffff) + static_cast<int>(static_cast<uint32_t>(w) >> 16);
 }
 
-__global__ void __launch_bounds__(GTHREADS, 1) expert_gateup_kernel(const __grid_constant__ GParams p) {
+template <int EPI>
+__global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_constant__ GParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sbase = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -514,7 +522,11 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_gateup_kernel(const __grid
                     const uint32_t a_dst = smem_u32(sStage + s * GSTAGE);
                     const uint32_t b_dst = a_dst + XA_BYTES;
                     const int kx = kb * XBK;
-                    tma_load_4d_pair(a_dst, &p.mapW, fb, kx, 0, 0, z);
+                    if (EPI == EPI_SWIGLU)
+                        tma_load_4d_pair(a_dst, &p.mapW, fb, kx, 0, 0, z);
+                    else
+                        tma_load_3d_pair(a_dst, &p.mapW, fb, kx,
+                                         t.mb * 256 + static_cast<int>(crank) * 128, t.e);
                     tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, xrow0, t.e);
                     if (h1)
                         tma_load_3d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kx,
@@ -622,14 +634,78 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_gateup_kernel(const __grid
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
             }
+            const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                static_cast<uint32_t>(base);
+            if (EPI == EPI_SCATTER) {
+                // The pool row of each row of this warp's blocks, loaded before
+                // the accumulator is ready: lane j holds row 32 b + j of its
+                // i-th block b.
+                int prow[GMAXB];
+#pragma unroll
+                for (int i = 0; i < GMAXB; ++i) {
+                    const int pos = grp + 2 * i;
+                    const int b = end ? pos : nblk - 1 - pos;
+                    const int rr = 32 * b + lane;
+                    prow[i] = -1;
+                    if (pos < nblk && rr < t.rows) {
+                        const int v = p.rowmap[static_cast<long long>(t.e) * p.c_recv + t.row0 + rr];
+                        if (moe_check(v >= 0 && v < p.out_rows, 1102)) prow[i] = v;
+                    }
+                }
+                if (!mbar_wait(&tfull[end], static_cast<uint32_t>(k >> 1) & 1u, abort_flag, p.status))
+                    break;
+                tc_fence_after();
+                // lane f: output feature 32 q + f of this CTA's 128
+                uint16_t* ob = p.out + t.mb * 256 + static_cast<int>(crank) * 128 + 32 * q + (lane & ~1);
+                const bool fodd = (lane & 1) != 0;
+#pragma unroll
+                for (int i = 0; i < GMAXB; ++i) {
+                    const int pos = grp + 2 * i;
+                    if (pos >= nblk) break;   // warp-uniform
+                    const int b = end ? pos : nblk - 1 - pos;
+                    uint32_t r[32];
+                    if (S - 32 * b >= 32) {
+                        tmem_ld32(tl + 32 * b, r);
+                    } else {
+                        uint32_t r16[16];
+                        tmem_ld16(tl + 32 * b, r16);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            r[j] = r16[j];
+                            r[16 + j] = 0u;
+                        }
+                    }
+                    if (i + 1 == my_ov) {   // this warp's share of the overlap is out of TMEM
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
+                    }
+                    // pairs of features to 32-bit stores: even lanes rows 0-15,
+                    // odd lanes rows 16-31 of the block
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float v = __uint_as_float(fodd ? r[j] : r[16 + j]);
+                        const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+                        const int rl = fodd ? 16 + j : j;
+                        const int pr = __shfl_sync(0xffffffffu, prow[i], rl);
+                        const uint32_t word =
+                            fodd ? pack_bf16x2(other, __uint_as_float(r[16 + j]))
+                                 : pack_bf16x2(__uint_as_float(r[j]), other);
+                        if (pr >= 0)
+                            *reinterpret_cast<uint32_t*>(ob + static_cast<long long>(pr) * p.ldo) = word;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(fdone_c0 + end * 8u);
+                continue;
+            }
             if (!mbar_wait(&tfull[end], static_cast<uint32_t>(k >> 1) & 1u, abort_flag, p.status))
                 break;
             tc_fence_after();
-            const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                static_cast<uint32_t>(base);
             // column c of the tile is the group's row row0 + c (chunk 0 is full)
             const int unit = t.mb * 128 + static_cast<int>(crank) * 64 + q * 16 + (y & ~1);
-            uint16_t* hb = p.h + (static_cast<long long>(t.e) * p.c_recv + t.row0) * p.H + unit;
+            uint16_t* hb = p.out + (static_cast<long long>(t.e) * p.c_recv + t.row0) * p.ldo + unit;
             int drained = 0;
 #pragma unroll 1
             for (int pos = grp; pos < nblk; pos += 2) {
@@ -671,7 +747,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_gateup_kernel(const __grid
                     const int row = rb + (odd ? 8 + j : j);
                     const uint32_t word = odd ? pack_bf16x2(other, hv[8 + j]) : pack_bf16x2(hv[j], other);
                     if (row < t.rows)
-                        *reinterpret_cast<uint32_t*>(hb + static_cast<long long>(row) * p.H) = word;
+                        *reinterpret_cast<uint32_t*>(hb + static_cast<long long>(row) * p.ldo) = word;
                 }
             }
             tc_fence_before();
@@ -888,8 +964,9 @@ int map_gateup_il(CUtensorMap* m, const void* Wg, const void* Wu, int E, int H, 
     return MOE_OK;
 }
 
-int launch_gateup(const GParams& p, int sms, cudaStream_t st, const char* name) {
-    auto kern = expert_gateup_kernel;
+template <int EPI>
+int launch_group(const GParams& p, int sms, cudaStream_t st, const char* name) {
+    auto kern = expert_group_kernel<EPI>;
     if (ensure_smem_attr(reinterpret_cast<const void*>(kern), GSMEM) != MOE_OK) return MOE_ECUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
@@ -909,11 +986,36 @@ int launch_gateup(const GParams& p, int sms, cudaStream_t st, const char* name) 
     return MOE_OK;
 }
 
-// The down product over the chunk list.
+// The down product: over the row groups (expert_group_kernel), or with
+// MOE_XPAIR_DGROUP=0 over the chunk list (expert_pair_kernel).
+#ifndef MOE_XPAIR_DGROUP
+#define MOE_XPAIR_DGROUP 1
+#endif
 int launch_down(int E, int c_recv, int L, int H, const uint16_t* Wd, const int4* chunks,
-                const int32_t* nchunks, uint16_t* h, const int32_t* expert_rows, uint16_t* ypool,
-                int64_t pool_rows, int32_t* status, int sms, cudaStream_t st) {
+                const int32_t* nchunks, const int4* groups, const int32_t* ngroups, uint16_t* h,
+                const int32_t* expert_rows, uint16_t* ypool, int64_t pool_rows, int32_t* status,
+                int sms, cudaStream_t st) {
     int rc;
+    if (MOE_XPAIR_DGROUP) {
+        GParams g;
+        std::memset(&g, 0, sizeof(g));
+        if ((rc = map3(&g.mapW, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
+        for (int i = 0; i < XNMAP; ++i)
+            if ((rc = map3(&g.mapX[i], h, H, c_recv, E, H, static_cast<uint64_t>(c_recv) * H,
+                           XHSTEP * (i + 1))))
+                return rc;
+        g.groups = groups;
+        g.ngroups = ngroups;
+        g.n_mb = L / 256;
+        g.kb = H / XBK;
+        g.c_recv = c_recv;
+        g.out = ypool;
+        g.ldo = L;
+        g.rowmap = expert_rows;
+        g.out_rows = pool_rows;
+        g.status = status;
+        return launch_group<EPI_SCATTER>(g, sms, st, "gemm_expert_down");
+    }
     XParams b;
     std::memset(&b, 0, sizeof(b));
     if ((rc = map3(&b.mapW0, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
@@ -988,12 +1090,12 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
             g.zpe = H / 16;
             g.kb = L / XBK;
             g.c_recv = c_recv;
-            g.H = H;
-            g.h = h;
+            g.out = h;
+            g.ldo = H;
             g.status = status;
-            if ((rc = launch_gateup(g, sms, st, "gemm_expert_gateup"))) return rc;
-            return launch_down(E, c_recv, L, H, Wd, chunks, nchunks, h, expert_rows, ypool, pool_rows,
-                               status, sms, st);
+            if ((rc = launch_group<EPI_SWIGLU>(g, sms, st, "gemm_expert_gateup"))) return rc;
+            return launch_down(E, c_recv, L, H, Wd, chunks, nchunks, groups, ngroups, h, expert_rows,
+                               ypool, pool_rows, status, sms, st);
         }
     }
     XParams a;
@@ -1023,8 +1125,8 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
     a.ldo = H;
     a.status = status;
     if ((rc = launch_pair<EPI_SWIGLU>(a, sms, st, "gemm_expert_gateup"))) return rc;
-    return launch_down(E, c_recv, L, H, Wd, chunks, nchunks, h, expert_rows, ypool, pool_rows, status,
-                       sms, st);
+    return launch_down(E, c_recv, L, H, Wd, chunks, nchunks, groups, ngroups, h, expert_rows, ypool,
+                       pool_rows, status, sms, st);
 }
 
 }  // namespace moe
