@@ -148,21 +148,30 @@ def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None, bank=False):
 def expert_mma_rows(counts, c_recv, bank_path):
     """Rows the expert products multiply per weight row.  Gathered path: each
     expert's rows padded to whole 128-row tiles.  Bank path (CTA pairs, rows
-    on the MMA's N axis): an expert's n rows in ceil(n / 256) chunks of even
-    size rounded up to 16, each chunk's width rounded up to 16."""
+    on the MMA's N axis): an expert's n rows in groups of at most 416 sized
+    evenly and rounded up to 16; a group of r rows is one chunk of r rounded
+    up to 16 when r <= 256, else two chunks, the first half of r rounded up
+    to 32 and the rest rounded up to 16."""
+    def up(v, m):
+        return (v + m - 1) // m * m
+
     total = 0
     for n in counts:
         n = max(0, min(int(n), c_recv))
         if not bank_path:
-            total += (n + 127) // 128 * 128
+            total += up(n, 128)
             continue
-        nch = (n + 255) // 256
-        if nch == 0:
+        if n == 0:
             continue
-        per = ((n + nch - 1) // nch + 15) // 16 * 16
-        for i in range(nch):
-            rows = min(per, n - i * per)
-            total += (rows + 15) // 16 * 16
+        ng = (n + 415) // 416
+        per = up((n + ng - 1) // ng, 16)
+        for i in range((n + per - 1) // per):
+            r = min(per, n - i * per)
+            if r <= 256:
+                total += up(r, 16)
+            else:
+                n0 = up((r + 1) // 2, 32)
+                total += n0 + up(r - n0, 16)
     return total
 
 

@@ -66,10 +66,13 @@ def test_expert_mma_rows():
     import bench
     # gathered path: 128-row tiles
     assert bench.expert_mma_rows([0, 1, 128, 129, 316], 393, False) == 0 + 128 + 128 + 256 + 384
-    # bank path: 316 -> two chunks of 160 (158 rows each, rounded to 16);
-    # 393 -> 208 + 185 (-> 192); 250 -> 256; 33 -> 48; 0 -> nothing
+    # bank path: 316 -> one group, chunks 160 (158 rounded to 32) + 160 (156
+    # rounded to 16); 393 -> 224 + 176 (169 -> 176); 250 -> 256; 33 -> 48;
+    # 0 -> nothing
     assert bench.expert_mma_rows([316], 393, True) == 320
-    assert bench.expert_mma_rows([393], 393, True) == 208 + 192
+    assert bench.expert_mma_rows([393], 393, True) == 224 + 176
     assert bench.expert_mma_rows([250, 33, 0], 393, True) == 256 + 48
     # counts past c_recv are clamped
-    assert bench.expert_mma_rows([500], 393, True) == 208 + 192
+    assert bench.expert_mma_rows([500], 393, True) == 224 + 176
+    # 900 rows: three groups of 304, 304, 292 -> chunks 160+144, 160+144, 160+144
+    assert bench.expert_mma_rows([900], 1000, True) == 3 * 304

@@ -1,14 +1,16 @@
-"""The paired expert products at every chunk boundary.
+"""The paired expert products at every chunk and group boundary.
 
-A routing is built so that the experts receive exactly 0, 1, 7, 8, 9, 15,
-16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300 and 393
-(the receiver cap) rows: chunks of every width class from 16 to 256, one and
-two chunks an expert, widths rounded up from one row past a multiple of 16.
+A routing is built so that chosen experts receive exactly the given numbers
+of rows.  With c_recv = 393 (one group an expert): 0, 1, 7, 8, 9, 15, 16,
+17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300 and 393 rows,
+chunks of every width class from 16 to 256, one and two chunks a group,
+widths rounded up from one row past a multiple of 16.  With c_recv = 2356:
+417, 431, 448, 832, 833 and 1100 rows, two and three groups an expert.
 The routing goes straight to moe_dispatch_pooled (no router), once writing
 the per-expert bank and once not, then to moe_expert_ffn_grouped, which takes
 the paired path from the bank or gathers the rows from the pool.  Both must
-give the same bits in every computed row, and a row of each expert must
-match the oracle's SwiGLU expert on the same input row.
+give the same bits in every computed row, and the first and last row of each
+expert must match the oracle's SwiGLU expert on the same input row.
 """
 import numpy as np
 import pytest
@@ -22,26 +24,29 @@ from helpers import check_close
 
 pytestmark = pytest.mark.gpu
 
-# widths that take the paired path (L a multiple of 256, H of 128); c_recv = 393
-CFG = wl.LayerConfig("chunks", T=4096, d_model=256, d_latent=256, n_experts=24, n_ranks=4,
-                     top_k=2, n_waves=3, n_shared=1, h_expert=128, h_shared=128, seed=9)
-TARGETS = [0, 1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300,
-           393]
+# widths that take the paired path (L a multiple of 256, H of 128)
+ONE_GROUP = (wl.LayerConfig("chunks", T=4096, d_model=256, d_latent=256, n_experts=24, n_ranks=4,
+                            top_k=2, n_waves=3, n_shared=1, h_expert=128, h_shared=128, seed=9),
+             [0, 1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300,
+              393])
+MANY_GROUPS = (wl.LayerConfig("groups", T=8192, d_model=256, d_latent=256, n_experts=8, n_ranks=4,
+                              top_k=2, n_waves=2, n_shared=1, h_expert=128, h_shared=128, seed=9),
+               [417, 431, 448, 832, 833, 1100])
 
 
-def _routing(rng):
-    """idx [T, 2] whose receiver-kept counts are TARGETS for experts 0..21;
-    experts 22 and 23 take the remaining assignments (capped by the sender)."""
-    cfg = CFG
-    T, k, S = cfg.T, cfg.top_k, cfg.n_ranks
+def _routing(rng, cfg, targets):
+    """idx [T, 2] whose receiver-kept counts are `targets` for the first
+    experts; the last two experts take the remaining assignments (capped by
+    the sender)."""
+    T, k, S, E = cfg.T, cfg.top_k, cfg.n_ranks, cfg.n_experts
     T_s = T // S
     per_src = []
     for s in range(S):
         a = []
-        for e, n in enumerate(TARGETS):
+        for e, n in enumerate(targets):
             a += [e] * (n // S + (1 if s < n % S else 0))
         fill = T_s * k - len(a)
-        a += [22 + (i % 2) for i in range(fill)]
+        a += [E - 2 + (i % 2) for i in range(fill)]
         a = np.array(a)
         rng.shuffle(a)
         pairs = a.reshape(T_s, k)
@@ -59,8 +64,8 @@ def _routing(rng):
     return idx
 
 
-def _run(idx, z, w, bank):
-    cfg, p = CFG, abi.plan(CFG)
+def _run(cfg, idx, z, w, bank):
+    p = abi.plan(cfg)
     dev = "cuda"
     T, k, E, L = cfg.T, cfg.top_k, cfg.n_experts, cfg.d_latent
     ws = torch.empty(max(1, p.ws_dispatch_bytes), dtype=torch.uint8, device=dev)
@@ -84,17 +89,19 @@ def _run(idx, z, w, bank):
     return o
 
 
-def test_chunk_boundaries():
+@pytest.mark.parametrize("case", [ONE_GROUP, MANY_GROUPS], ids=["one_group", "many_groups"])
+def test_chunk_boundaries(case):
+    cfg, targets = case
     rng = np.random.default_rng(3)
-    idx = _routing(rng)
-    inp = wl.make_inputs(CFG, "cuda")
-    z = torch.randn(CFG.T, CFG.d_latent, generator=torch.Generator(device="cuda").manual_seed(4),
+    idx = _routing(rng, cfg, targets)
+    inp = wl.make_inputs(cfg, "cuda")
+    z = torch.randn(cfg.T, cfg.d_latent, generator=torch.Generator(device="cuda").manual_seed(4),
                     device="cuda").to(torch.bfloat16)
-    a = _run(idx, z, inp, bank=True)
-    b = _run(idx, z, inp, bank=False)
-    d = O.dispatch(idx, O.make_plan(CFG))
+    a = _run(cfg, idx, z, inp, bank=True)
+    b = _run(cfg, idx, z, inp, bank=False)
+    d = O.dispatch(idx, O.make_plan(cfg))
     cnt = a["expert_count"].cpu().numpy()
-    assert cnt[:len(TARGETS)].tolist() == TARGETS, cnt
+    assert cnt[:len(targets)].tolist() == targets, cnt
     assert (cnt == d["count"]).all()
     assert (a["expert_rows"].cpu().numpy() == d["expert_rows"]).all()
     for n in ("slot_of", "drop", "expert_rows", "expert_count"):
@@ -106,7 +113,7 @@ def test_chunk_boundaries():
     token_of = {int(r): int(t) for (t, j), r in np.ndenumerate(d["send_row"]) if r >= 0}
     zh = z.double().cpu().numpy()
     got, want = [], []
-    for e in range(CFG.n_experts):
+    for e in range(cfg.n_experts):
         n = int(d["count"][e])
         if n == 0:
             continue
