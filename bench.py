@@ -145,6 +145,19 @@ def kernel_work(name, cfg, plan, st, pipeline="none", sent_w0=None, bank=False):
     return None, None, "latency"
 
 
+def expert_stream_bytes(name, cfg, st, n_active):
+    """DRAM bytes an expert product must move at least: the weights of the
+    experts with rows, read once, the rows read once and the output written
+    once (gate/up: bank or pool rows of width L in, h out; down: h in, Y
+    rows of width L out).  None for other kernels."""
+    L, H, kept = cfg.d_latent, cfg.h_expert, st["kept"]
+    if name == "gemm_expert_gateup":
+        return (n_active * 2 * H * L * 2 + kept * L * 2 + kept * H * 2) / 1e9
+    if name == "gemm_expert_down":
+        return (n_active * L * H * 2 + kept * H * 2 + kept * L * 2) / 1e9
+    return None
+
+
 def expert_mma_rows(counts, c_recv, bank_path):
     """Rows the expert products multiply per weight row.  Gathered path: each
     expert's rows padded to whole 128-row tiles.  Bank path (CTA pairs, rows
@@ -379,6 +392,7 @@ def run_gb300(args, rank, world, local_rank):
     near_ties = int((m.tie != 0).sum().item())
     # MMA rows the expert GEMMs compute (the padding is work the tensor cores
     # do but the algorithmic flop count leaves out)
+    n_active = int((m.expert_count > 0).sum().item())
     tile_rows = expert_mma_rows(m.expert_count.tolist(), m.plan.c_recv,
                                 m.bank is not None and cfg.d_latent % 256 == 0
                                 and cfg.h_expert % 128 == 0)
@@ -433,6 +447,12 @@ def run_gb300(args, rank, world, local_rank):
             peak = tensor_peak if bound == "tensor" else pk["hbm"]
             e.update({"work_per_launch": work, "unit": unit + "/s", "achieved": round(ach, 2),
                       "frac": round(ach / peak, 4)})
+        sb = expert_stream_bytes(name, cfg, st, n_active)
+        if sb is not None:   # the same launch against its DRAM floor
+            gbs = sb / (ms_l / 1e3)
+            e["hbm"] = {"bytes_per_launch_gb": round(sb, 4), "achieved_gbs": round(gbs, 1),
+                        "frac": round(gbs / pk["hbm"], 4),
+                        "floor_ms": round(sb / pk["hbm"] * 1e3, 4)}
         kernels[name] = e
     top = next(iter(kernels))
     twork, tunit, tbound = kernel_work(top, cfg, m.plan, st, pipeline, sent_w0)
@@ -468,6 +488,8 @@ def run_gb300(args, rank, world, local_rank):
         if top.startswith("gemm_expert") and tile_rows:
             roof["tile_rows"] = tile_rows
             roof["row_util"] = round(st["kept"] / tile_rows, 4)   # kept rows / MMA rows
+        if "hbm" in kernels[top]:   # the weight stream's floor beside the tensor figure
+            roof["hbm"] = kernels[top]["hbm"]
     else:
         roof = {"kernel": top, "bound": "latency", "achieved": None, "peak": None,
                 "unit": None, "frac": None, "traffic": traffic}

@@ -76,3 +76,20 @@ def test_expert_mma_rows():
     assert bench.expert_mma_rows([500], 393, True) == 224 + 176
     # 900 rows: three groups of 304, 304, 292 -> chunks 160+144, 160+144, 160+144
     assert bench.expert_mma_rows([900], 1000, True) == 3 * 304
+
+
+def test_expert_stream_bytes_match_the_traffic_records():
+    """The expert products' DRAM floor (weights of the experts with rows once,
+    rows in once, output once) against the full launch's algorithmic bytes
+    the committed traffic records were scaled to (full workload: 384 experts
+    with rows, 121,556 kept rows)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from moe_routing_capacity_gb300 import workloads as wl
+    recs = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    cfg = wl.CONFIGS["full"]
+    st = {"kept": 121556}
+    for name in ("gemm_expert_gateup", "gemm_expert_down"):
+        got = bench.expert_stream_bytes(name, cfg, st, 384) * 1e9
+        assert round(got) == recs[name]["full_algorithmic_bytes"], name
+    assert bench.expert_stream_bytes("combine", cfg, st, 384) is None
