@@ -432,18 +432,50 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     q.goff = poff;   // ragged: the padded per-expert rows (A and out)
     q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
     if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
-    std::memset(&q, 0, sizeof(q));   // recompute g/u of the received rows, SwiGLU backward
-    // (its epilogue also zeroes each expert's padding rows of dg and du)
-    q.a_mode = A_GATHER; q.epi = EPI_SWIGLU_BWD; q.bn = 256;
-    q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{nullptr, 0, a.Wg, L, L};
-    q.B_up = a.Wu; q.groups = E; q.rows_per_group = cr; q.b_rows = H;
-    q.b_gstride = static_cast<int64_t>(H) * L;
-    q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
-    q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
-    q.goff = poff; q.rmoff = eoff;   // ragged: outputs padded, rows from the flat map
-    q.gather_src = a.pool; q.gather_pitch = pool_pitch(L); q.gather_rows = g.pool_rows;
-    q.aux = dh; q.out = dg; q.out2 = du; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
-    if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
+    // Capped layout: the per-expert contiguous, zero-padded copy of X (which
+    // the weight gradients contract over) and h's unwritten rows zeroed, made
+    // first, so that the SwiGLU backward can read X as whole TMA tiles.
+    bool grouped = false;
+    if (!rag) {
+        const int64_t nw = static_cast<int64_t>(E) * cr;
+        const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
+        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, a.expert_count, E, cr, L, xe);
+        zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "bwd_gather_rows");
+        // recompute g/u and the SwiGLU backward on CTA pairs over row groups;
+        // their list sits at the start of dxpool, which only the dX product
+        // below writes
+        rc = static_cast<size_t>(g.pool_rows) * L * 2 >= expert_pair_chunks_bytes(E, cr)
+                 ? expert_swiglu_bwd_group(E, cr, L, H, xe, a.expert_count, a.Wg, a.Wu, dh, dxp, dg,
+                                           du, a.status, st)
+                 : MOE_EINVAL;
+        if (rc == MOE_OK) {
+            grouped = true;
+            // rows past each expert's count: zeros, which the weight
+            // gradients contract over
+            zero_pad_rows_kernel<<<grid, 256, 0, st>>>(dg, a.expert_count, E, cr, H);
+            zero_pad_rows_kernel<<<grid, 256, 0, st>>>(du, a.expert_count, E, cr, H);
+            if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+            trace_after(st, "bwd_zero_pad");
+        } else if (rc != MOE_EINVAL) {
+            return rc;
+        }
+    }
+    if (!grouped) {
+        std::memset(&q, 0, sizeof(q));   // recompute g/u of the received rows, SwiGLU backward
+        // (its epilogue also zeroes each expert's padding rows of dg and du)
+        q.a_mode = A_GATHER; q.epi = EPI_SWIGLU_BWD; q.bn = 256;
+        q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{nullptr, 0, a.Wg, L, L};
+        q.B_up = a.Wu; q.groups = E; q.rows_per_group = cr; q.b_rows = H;
+        q.b_gstride = static_cast<int64_t>(H) * L;
+        q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
+        q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+        q.goff = poff; q.rmoff = eoff;   // ragged: outputs padded, rows from the flat map
+        q.gather_src = a.pool; q.gather_pitch = pool_pitch(L); q.gather_rows = g.pool_rows;
+        q.aux = dh; q.out = dg; q.out2 = du; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
+        if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
+    }
     std::memset(&q, 0, sizeof(q));   // dX = dg Wg_e + du Wu_e, back to the pool rows
     q.a_mode = A_GROUPED; q.epi = EPI_SCATTER; q.bn = 256; q.b_mn = 1;
     q.N = L; q.nseg = 2;
@@ -462,13 +494,6 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
                                                 a.expert_count, poff, L, xe);
         gather_ragged_kernel<<<E, 256, 0, st>>>(a.h, H, nullptr, eoff, a.expert_count, poff, H,
                                                 hp);
-        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
-        trace_after(st, "bwd_gather_rows");
-    } else {   // per-expert contiguous, zero-padded copy of X; h's unwritten rows zeroed
-        const int64_t nw = static_cast<int64_t>(E) * cr;
-        const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
-        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, a.expert_count, E, cr, L, xe);
-        zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_gather_rows");
     }

@@ -411,7 +411,10 @@ struct GParams {
     int gate_hi;               // gate/up: the gate tensor is the higher-addressed one
     int kb;                    // K blocks
     int c_recv;
-    uint16_t* out;             // h [E, c_recv, H] (gate/up) or ypool [pool_rows, L] (down)
+    uint16_t* out;             // h [E, c_recv, H] (gate/up), ypool [pool_rows, L] (down),
+                               // dg [E, c_recv, H] (SwiGLU backward)
+    uint16_t* out2;            // SwiGLU backward: du [E, c_recv, H]
+    const uint16_t* aux;       // SwiGLU backward: dh [E, c_recv, H]
     long long ldo;             // H or L
     const int* rowmap;         // down: expert_rows [E, c_recv]
     long long out_rows;        // down: pool rows (checked builds)
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     const uint32_t a_dst = smem_u32(sStage + s * GSTAGE);
                     const uint32_t b_dst = a_dst + XA_BYTES;
                     const int kx = kb * XBK;
-                    if (EPI == EPI_SWIGLU)
+                    if (EPI != EPI_SCATTER)
                         tma_load_4d_pair(a_dst, &p.mapW, fb, kx, 0, 0, z);
                     else
                         tma_load_3d_pair(a_dst, &p.mapW, fb, kx,
@@ -727,6 +730,57 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
                 }
+                if (EPI == EPI_SWIGLU_BWD) {
+                    // recomputed g, u of this lane's unit for rows 0-15 (lanes < 16)
+                    // or 16-31 of the block, then pairs of units per lane: even
+                    // lanes rows 0-7, odd lanes 8-15; incoming dh, dg = dh u
+                    // silu'(g), du = dh silu(g); 32-bit loads and stores
+                    float gv[16], uv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t mine = hi ? r[16 + j] : r[j];
+                        const uint32_t give = hi ? r[j] : r[16 + j];
+                        const float oth = __uint_as_float(__shfl_xor_sync(0xffffffffu, give, 16));
+                        const float own = __uint_as_float(mine);
+                        const float lo_t = hi ? oth : own, hi_t = hi ? own : oth;
+                        gv[j] = p.gate_hi ? hi_t : lo_t;
+                        uv[j] = p.gate_hi ? lo_t : hi_t;
+                    }
+                    const long long gbase =
+                        (static_cast<long long>(t.e) * p.c_recv + t.row0) * p.ldo + unit;
+                    const int rb = 32 * b + (hi ? 16 : 0) + (odd ? 8 : 0);   // this lane's first row
+                    // the eight rows' dh first (independent loads), then the
+                    // partner's g, u, then the arithmetic
+                    uint32_t hw[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        hw[j] = rb + j < t.rows
+                                    ? *reinterpret_cast<const uint32_t*>(
+                                          p.aux + gbase + static_cast<long long>(rb + j) * p.ldo)
+                                    : 0u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float og = __shfl_xor_sync(0xffffffffu, odd ? gv[j] : gv[8 + j], 1);
+                        const float ou = __shfl_xor_sync(0xffffffffu, odd ? uv[j] : uv[8 + j], 1);
+                        const int row = rb + j;
+                        if (row < t.rows) {
+                            const float g2[2] = {odd ? og : gv[j], odd ? gv[8 + j] : og};
+                            const float u2[2] = {odd ? ou : uv[j], odd ? uv[8 + j] : ou};
+                            const long long off = gbase + static_cast<long long>(row) * p.ldo;
+                            float dg2[2], du2[2];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const float gg = g2[e2], uu = u2[e2];
+                                const float dh = e2 ? bf16_hi(hw[j]) : bf16_lo(hw[j]);
+                                const float sig = 1.0f / (1.0f + expf(-gg));
+                                dg2[e2] = dh * uu * (sig * (1.0f + gg * (1.0f - sig)));
+                                du2[e2] = dh * (gg * sig);
+                            }
+                            *reinterpret_cast<uint32_t*>(p.out + off) = pack_bf16x2(dg2[0], dg2[1]);
+                            *reinterpret_cast<uint32_t*>(p.out2 + off) = pack_bf16x2(du2[0], du2[1]);
+                        }
+                    }
+                } else {
                 // lanes < 16 finish rows 0-15 of the block, lanes >= 16 rows 16-31
                 float hv[16];
 #pragma unroll
@@ -748,6 +802,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     const uint32_t word = odd ? pack_bf16x2(other, hv[8 + j]) : pack_bf16x2(hv[j], other);
                     if (row < t.rows)
                         *reinterpret_cast<uint32_t*>(hb + static_cast<long long>(row) * p.ldo) = word;
+                }
                 }
             }
             tc_fence_before();
@@ -1041,6 +1096,49 @@ int launch_down(int E, int c_recv, int L, int H, const uint16_t* Wd, const int4*
 int check_status_expert_pair() { return moe_check_read_reset(); }
 
 // Chunk list, group list, then the two counts (16 bytes).
+static size_t chunk_list_bytes(int E, int c_recv);
+
+int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
+                            const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                            const uint16_t* dh, void* list_ws, uint16_t* dg, uint16_t* du,
+                            int32_t* status, cudaStream_t st) {
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    if (!MOE_XPAIR_TM || sms < 2 || E <= 0 || c_recv <= 0 || L % 256 || H % 128) return MOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(list_ws) & 15) || (reinterpret_cast<uintptr_t>(xe) & 15) ||
+        (reinterpret_cast<uintptr_t>(dh) & 15) || (reinterpret_cast<uintptr_t>(dg) & 15) ||
+        (reinterpret_cast<uintptr_t>(du) & 15))
+        return MOE_EINVAL;
+    GParams g;
+    std::memset(&g, 0, sizeof(g));
+    if (map_gateup_il(&g.mapW, Wg, Wu, E, H, L, &g.gate_hi) != MOE_OK) return MOE_EINVAL;
+    for (int i = 0; i < XNMAP; ++i)
+        if ((rc = map3(&g.mapX[i], xe, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
+                       XHSTEP * (i + 1))))
+            return rc;
+    uint8_t* ws = static_cast<uint8_t*>(list_ws);
+    int4* chunks = reinterpret_cast<int4*>(ws);
+    int4* groups = reinterpret_cast<int4*>(ws + chunk_list_bytes(E, c_recv));
+    int32_t* nchunks = reinterpret_cast<int32_t*>(ws + expert_pair_chunks_bytes(E, c_recv) - 16);
+    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, c_recv, chunks, nchunks, groups,
+                                          nchunks + 1);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "bwd_build_groups");
+    g.groups = groups;
+    g.ngroups = nchunks + 1;
+    g.n_mb = H / 128;
+    g.zpe = H / 16;
+    g.kb = L / XBK;
+    g.c_recv = c_recv;
+    g.out = dg;
+    g.out2 = du;
+    g.aux = dh;
+    g.ldo = H;
+    g.status = status;
+    return launch_group<EPI_SWIGLU_BWD>(g, sms, st, "bwd_gemm_expert_swiglu");
+}
+
 static size_t chunk_list_bytes(int E, int c_recv) {
     const size_t per = static_cast<size_t>((c_recv + XCHUNK - 1) / XCHUNK);
     return static_cast<size_t>(E) * (per > 0 ? per : 1) * sizeof(int4);

@@ -192,6 +192,18 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
                     uint16_t* ypool, int64_t pool_rows, int32_t* status, cudaStream_t stream);
 int check_status_expert_pair();
 
+// The backward's recomputed gate/up and SwiGLU backward of the routed experts
+// over row groups on CTA pairs (expert_pair.cu): X rows from xe [E, c_recv,
+// L], dh [E, c_recv, H] in, dg and du [E, c_recv, H] out for each expert's
+// first expert_count rows (the rest untouched).  list_ws: at least
+// expert_pair_chunks_bytes(E, c_recv) bytes of scratch, 16-byte aligned.
+// MOE_EINVAL when the widths or the weight tensors do not allow this path
+// (the caller then takes the gathered one).
+int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
+                            const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                            const uint16_t* dh, void* list_ws, uint16_t* dg, uint16_t* du,
+                            int32_t* status, cudaStream_t stream);
+
 // Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
 // Checked builds: the site code recorded by each translation unit's index
 // checks since the last call (0: none), reset on reading.

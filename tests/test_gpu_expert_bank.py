@@ -89,3 +89,25 @@ def test_mid_bank_path_equals_gathered_rows():
     kept = a.slot_of[a.slot_of >= 0].long()
     assert torch.equal(a.ypool[kept].view(torch.int16), b.ypool[kept].view(torch.int16))
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def test_same_tensor_for_gate_and_up():
+    """One tensor passed as both Wg and Wu.  The gate/up product reads the two
+    through one tensor map that interleaves them by 16 rows, with the distance
+    between the tensors as a stride; at distance 0 no such map exists and the
+    product takes the one-chunk-a-tile kernel with two weight boxes a stage.
+    It must still match the oracle, and the path that gathers the rows from
+    the pool bit for bit."""
+    cfg = PAIRS
+    inp = wl.make_inputs(cfg, "cuda")
+    inp["Wu"] = inp["Wg"]
+    # h = silu(g) g is never negative, so Y grows past the range where one
+    # bf16 step of Y stays within c's tolerance; a power-of-two scale of Wd
+    # (exact in bf16) keeps Y in the usual range
+    inp["Wd"] = inp["Wd"] * 0.25
+    m, ref, rep = compare_full(cfg, inp, expert_bank=True)
+    assert m.w["Wg"].data_ptr() == m.w["Wu"].data_ptr()
+    b = run_gpu(cfg, inp, expert_bank=False)
+    kept = m.slot_of[m.slot_of >= 0].long()
+    assert torch.equal(m.ypool[kept].view(torch.int16), b.ypool[kept].view(torch.int16))
+    print(rep)
