@@ -421,17 +421,35 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     const int max_mt = rag ? static_cast<int>(g.pool_rows / 128 + E) : E * ((cr + 127) / 128);
     int32_t* tile_count = tiles + 2 * max_mt;
     if ((rc = launch_build_tiles(a.expert_count, E, 128, tiles, tile_count, st))) return rc;
-    std::memset(&q, 0, sizeof(q));   // dh = dY_e Wd_e (per-expert rows by TMA)
-    q.a_mode = A_GROUPED; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
-    q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{dye, L, a.Wd, H, L};
-    q.groups = E; q.rows_per_group = rag ? static_cast<int>(PE) : cr;
-    q.a_gstride = static_cast<int64_t>(cr) * L;
-    q.b_rows = H; q.b_gstride = static_cast<int64_t>(L) * H;
-    q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
-    q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
-    q.goff = poff;   // ragged: the padded per-expert rows (A and out)
-    q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
-    if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
+    // Capped layout, widths in whole blocks: the three expert products on CTA
+    // pairs over row groups, whose list sits at the start of dz (written only
+    // by the return of dX below); each falls back to the grouped GEMM where
+    // its path is not open.
+    ExpertGroups gl{};
+    bool groups = false;
+    if (!rag && static_cast<size_t>(T) * L * 2 >= expert_pair_chunks_bytes(E, cr)) {
+        rc = expert_group_list(E, cr, a.expert_count, dz, &gl, st);
+        if (rc == MOE_OK)
+            groups = true;
+        else if (rc != MOE_EINVAL)
+            return rc;
+    }
+    rc = groups ? expert_dh_group(E, cr, L, H, dye, a.Wd, gl, dh, a.status, st) : MOE_EINVAL;
+    if (rc == MOE_EINVAL) {
+        std::memset(&q, 0, sizeof(q));   // dh = dY_e Wd_e (per-expert rows by TMA)
+        q.a_mode = A_GROUPED; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
+        q.N = H; q.nseg = 1; q.seg[0] = GemmSeg{dye, L, a.Wd, H, L};
+        q.groups = E; q.rows_per_group = rag ? static_cast<int>(PE) : cr;
+        q.a_gstride = static_cast<int64_t>(cr) * L;
+        q.b_rows = H; q.b_gstride = static_cast<int64_t>(L) * H;
+        q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
+        q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+        q.goff = poff;   // ragged: the padded per-expert rows (A and out)
+        q.out = dh; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
+        if ((rc = mm(q, "bwd_gemm_dh"))) return rc;
+    } else if (rc) {
+        return rc;
+    }
     // Capped layout: the per-expert contiguous, zero-padded copy of X (which
     // the weight gradients contract over) and h's unwritten rows zeroed, made
     // first, so that the SwiGLU backward can read X as whole TMA tiles.
@@ -443,13 +461,10 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_gather_rows");
-        // recompute g/u and the SwiGLU backward on CTA pairs over row groups;
-        // their list sits at the start of dxpool, which only the dX product
-        // below writes
-        rc = static_cast<size_t>(g.pool_rows) * L * 2 >= expert_pair_chunks_bytes(E, cr)
-                 ? expert_swiglu_bwd_group(E, cr, L, H, xe, a.expert_count, a.Wg, a.Wu, dh, dxp, dg,
-                                           du, a.status, st)
-                 : MOE_EINVAL;
+        // recompute g/u and the SwiGLU backward over row groups
+        rc = groups ? expert_swiglu_bwd_group(E, cr, L, H, xe, a.Wg, a.Wu, dh, gl, dg, du, a.status,
+                                              st)
+                    : MOE_EINVAL;
         if (rc == MOE_OK) {
             grouped = true;
             // rows past each expert's count: zeros, which the weight
@@ -476,19 +491,26 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         q.aux = dh; q.out = dg; q.out2 = du; q.ldo = H; q.out_gstride = static_cast<int64_t>(cr) * H;
         if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
     }
-    std::memset(&q, 0, sizeof(q));   // dX = dg Wg_e + du Wu_e, back to the pool rows
-    q.a_mode = A_GROUPED; q.epi = EPI_SCATTER; q.bn = 256; q.b_mn = 1;
-    q.N = L; q.nseg = 2;
-    q.seg[0] = GemmSeg{dg, H, a.Wg, L, H};
-    q.seg[1] = GemmSeg{du, H, a.Wu, L, H};
-    q.groups = E; q.rows_per_group = rag ? static_cast<int>(PE) : cr;
-    q.a_gstride = static_cast<int64_t>(cr) * H;
-    q.b_rows = L; q.b_gstride = static_cast<int64_t>(H) * L;
-    q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
-    q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
-    q.goff = poff; q.rmoff = eoff;
-    q.out = dxp; q.ldo = L; q.gather_rows = g.pool_rows;
-    if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
+    rc = groups ? expert_dx_group(E, cr, L, H, dg, du, a.Wg, a.Wu, gl, a.expert_rows, dxp,
+                                  g.pool_rows, a.status, st)
+                : MOE_EINVAL;
+    if (rc == MOE_EINVAL) {
+        std::memset(&q, 0, sizeof(q));   // dX = dg Wg_e + du Wu_e, back to the pool rows
+        q.a_mode = A_GROUPED; q.epi = EPI_SCATTER; q.bn = 256; q.b_mn = 1;
+        q.N = L; q.nseg = 2;
+        q.seg[0] = GemmSeg{dg, H, a.Wg, L, H};
+        q.seg[1] = GemmSeg{du, H, a.Wu, L, H};
+        q.groups = E; q.rows_per_group = rag ? static_cast<int>(PE) : cr;
+        q.a_gstride = static_cast<int64_t>(cr) * H;
+        q.b_rows = L; q.b_gstride = static_cast<int64_t>(H) * L;
+        q.tile_list = tiles; q.tile_count = tile_count; q.max_tiles = max_mt;
+        q.rowmap = a.expert_rows; q.counts = a.expert_count; q.rowmap_ld = cr;
+        q.goff = poff; q.rmoff = eoff;
+        q.out = dxp; q.ldo = L; q.gather_rows = g.pool_rows;
+        if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
+    } else if (rc) {
+        return rc;
+    }
     if (rag) {   // padded per-expert copies of X and of h
         gather_ragged_kernel<<<E, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, eoff,
                                                 a.expert_count, poff, L, xe);

@@ -416,8 +416,15 @@ struct GParams {
     uint16_t* out2;            // SwiGLU backward: du [E, c_recv, H]
     const uint16_t* aux;       // SwiGLU backward: dh [E, c_recv, H]
     long long ldo;             // H or L
-    const int* rowmap;         // down: expert_rows [E, c_recv]
-    long long out_rows;        // down: pool rows (checked builds)
+    const int* rowmap;         // scatter: the output row of each group row, [E, c_recv]
+                               // (NULL: row e * c_recv + r, the per-expert layout)
+    long long out_rows;        // scatter: output rows (checked builds)
+    int a_mn;                  // scatter: the weights are MN-major (stored [K, M]): two
+                               // 64 x 64 boxes a stage, 8 KB apart
+    int kseg;                  // scatter: K in two segments of this many (0: one); mapW
+                               // and mapX then have a 4th dimension stepping between two
+                               // tensors, aseg / bseg giving each segment's index in it
+    int aseg[2], bseg[2];
     int* status;
 };
 
@@ -525,15 +532,31 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     const uint32_t a_dst = smem_u32(sStage + s * GSTAGE);
                     const uint32_t b_dst = a_dst + XA_BYTES;
                     const int kx = kb * XBK;
-                    if (EPI != EPI_SCATTER)
+                    const int m0 = t.mb * 256 + static_cast<int>(crank) * 128;
+                    const int sg = p.kseg ? kx / p.kseg : 0, kin = kx - sg * p.kseg;
+                    if (EPI != EPI_SCATTER) {
                         tma_load_4d_pair(a_dst, &p.mapW, fb, kx, 0, 0, z);
-                    else
-                        tma_load_3d_pair(a_dst, &p.mapW, fb, kx,
-                                         t.mb * 256 + static_cast<int>(crank) * 128, t.e);
-                    tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, xrow0, t.e);
-                    if (h1)
-                        tma_load_3d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kx,
-                                         xrow1, t.e);
+                    } else if (!p.a_mn) {
+                        tma_load_3d_pair(a_dst, &p.mapW, fb, kx, m0, t.e);
+                    } else if (p.kseg) {
+                        tma_load_4d_pair(a_dst, &p.mapW, fb, m0, kin, t.e, p.aseg[sg]);
+                        tma_load_4d_pair(a_dst + 8192, &p.mapW, fb, m0 + 64, kin, t.e, p.aseg[sg]);
+                    } else {
+                        tma_load_3d_pair(a_dst, &p.mapW, fb, m0, kx, t.e);
+                        tma_load_3d_pair(a_dst + 8192, &p.mapW, fb, m0 + 64, kx, t.e);
+                    }
+                    if (p.kseg) {
+                        tma_load_4d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kin, xrow0, t.e,
+                                         p.bseg[sg]);
+                        if (h1)
+                            tma_load_4d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kin,
+                                             xrow1, t.e, p.bseg[sg]);
+                    } else {
+                        tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, xrow0, t.e);
+                        if (h1)
+                            tma_load_3d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kx,
+                                             xrow1, t.e);
+                    }
                     if (++s == GST) {
                         s = 0;
                         ph ^= 1u;
@@ -571,9 +594,13 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + static_cast<uint32_t>(gate_base(k, t.n0 + t.n1));
                 const uint32_t d1 = d0 + static_cast<uint32_t>(t.n0);
-                const uint32_t id0 = idesc_bf16_f32(256, t.n0);
-                const uint32_t id1 = idesc_bf16_f32(256, t.n1 ? t.n1 : 16);
+                const bool amn = EPI == EPI_SCATTER && p.a_mn;
+                const uint32_t id0 = idesc_bf16_f32(256, t.n0, amn);
+                const uint32_t id1 = idesc_bf16_f32(256, t.n1 ? t.n1 : 16, amn);
                 const uint32_t boff1 = static_cast<uint32_t>(t.n0 >> 1) * XBK * 2;
+                // descriptor step per 16-wide K slice: 32 B along a K-major row,
+                // 16 rows of 128 B down an MN-major box
+                const uint32_t a_step = amn ? (2048u >> 4) : (32u >> 4);
                 for (int kb = 0; kb < p.kb; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, p.status)) {
                         ok = false;
@@ -581,14 +608,14 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     }
                     tc_fence_after();
                     const uint32_t a_s = smem_u32(sStage + s * GSTAGE);
-                    const uint64_t ad = sdesc_k_sw128(a_s);
+                    const uint64_t ad = amn ? sdesc_mn_sw128(a_s) : sdesc_k_sw128(a_s);
                     const uint64_t bd0 = sdesc_k_sw128(a_s + XA_BYTES);
                     const uint64_t bd1 = sdesc_k_sw128(a_s + XA_BYTES + boff1);
 #pragma unroll
                     for (int kk = 0; kk < XBK / 16; ++kk) {
                         const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-                        mma_bf16_pair(d0, ad + 2u * kk, bd0 + 2u * kk, id0, acc);
-                        if (t.n1) mma_bf16_pair(d1, ad + 2u * kk, bd1 + 2u * kk, id1, acc);
+                        mma_bf16_pair(d0, ad + a_step * kk, bd0 + 2u * kk, id0, acc);
+                        if (t.n1) mma_bf16_pair(d1, ad + a_step * kk, bd1 + 2u * kk, id1, acc);
                     }
                     mma_commit_pair(&empty[s]);
                     if (++s == GST) {
@@ -651,7 +678,8 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     const int rr = 32 * b + lane;
                     prow[i] = -1;
                     if (pos < nblk && rr < t.rows) {
-                        const int v = p.rowmap[static_cast<long long>(t.e) * p.c_recv + t.row0 + rr];
+                        const int r = t.e * p.c_recv + t.row0 + rr;
+                        const int v = p.rowmap ? p.rowmap[r] : r;
                         if (moe_check(v >= 0 && v < p.out_rows, 1102)) prow[i] = v;
                     }
                 }
@@ -945,6 +973,25 @@ int map3(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
 }
 
+// bf16 4-D map of dims {d0, d1, d2, d3} (d0 contiguous) with byte strides
+// {s1, s2, s3} of dims 1..3, box {64, box1, 1, 1}, 128-byte swizzle: two
+// tensors of the same shape as the two values of the outermost dimension,
+// s3 the distance from the lower-addressed to the other.  MOE_EINVAL when the
+// driver refuses it (a distance of 0, not a multiple of 16, ...).
+int map4(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+         uint64_t s1, uint64_t s2, uint64_t s3, uint32_t box1) {
+    EncodeTiledFnX enc = encode_x();
+    if (!enc) return MOE_ECUDA;
+    if (s3 == 0 || (s3 & 15) || s3 >= (1ull << 40)) return MOE_EINVAL;
+    const cuuint64_t gdim[4] = {d0, d1, d2, d3};
+    const cuuint64_t gstr[3] = {s1, s2, s3};
+    const cuuint32_t box[4] = {XBK, box1, 1, 1}, est[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gdim, gstr,
+                     box, est, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_EINVAL;
+}
+
 // One map over both gate/up weight tensors, so that one box brings a CTA's
 // 64 gate rows and the 64 up rows of the same units: dims {L, 64, E*H/64,
 // 2}, the outermost one stepping from the lower-addressed tensor to the
@@ -1095,20 +1142,67 @@ int launch_down(int E, int c_recv, int L, int H, const uint16_t* Wd, const int4*
 
 int check_status_expert_pair() { return moe_check_read_reset(); }
 
-// Chunk list, group list, then the two counts (16 bytes).
 static size_t chunk_list_bytes(int E, int c_recv);
 
-int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
-                            const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
-                            const uint16_t* dh, void* list_ws, uint16_t* dg, uint16_t* du,
-                            int32_t* status, cudaStream_t st) {
+int expert_group_list(int E, int c_recv, const int32_t* expert_count, void* ws, ExpertGroups* out,
+                      cudaStream_t st) {
+    if (E <= 0 || c_recv <= 0 || (reinterpret_cast<uintptr_t>(ws) & 15)) return MOE_EINVAL;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int4* chunks = reinterpret_cast<int4*>(w);
+    int4* groups = reinterpret_cast<int4*>(w + chunk_list_bytes(E, c_recv));
+    int32_t* counts = reinterpret_cast<int32_t*>(w + expert_pair_chunks_bytes(E, c_recv) - 16);
+    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, c_recv, chunks, counts, groups,
+                                          counts + 1);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "bwd_build_groups");
+    out->groups = groups;
+    out->ngroups = counts + 1;
+    return MOE_OK;
+}
+
+static bool pair_widths(int sms, int E, int c_recv) { return sms >= 2 && E > 0 && c_recv > 0; }
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const uint16_t* Wd,
+                    const ExpertGroups& gl, uint16_t* dh, int32_t* status, cudaStream_t st) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
     if (rc) return rc;
-    if (!MOE_XPAIR_TM || sms < 2 || E <= 0 || c_recv <= 0 || L % 256 || H % 128) return MOE_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(list_ws) & 15) || (reinterpret_cast<uintptr_t>(xe) & 15) ||
-        (reinterpret_cast<uintptr_t>(dh) & 15) || (reinterpret_cast<uintptr_t>(dg) & 15) ||
-        (reinterpret_cast<uintptr_t>(du) & 15))
+    if (!MOE_XPAIR_TM || !pair_widths(sms, E, c_recv) || H % 256 || L % 64 || !al16(dye) ||
+        !al16(Wd) || !al16(dh))
+        return MOE_EINVAL;
+    GParams g;
+    std::memset(&g, 0, sizeof(g));
+    // Wd [E, L, H] is the weights' [K, M]: MN-major boxes of 64 units x 64 K
+    if ((rc = map3(&g.mapW, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 64))) return rc;
+    for (int i = 0; i < XNMAP; ++i)
+        if ((rc = map3(&g.mapX[i], dye, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
+                       XHSTEP * (i + 1))))
+            return rc;
+    g.groups = gl.groups;
+    g.ngroups = gl.ngroups;
+    g.n_mb = H / 256;
+    g.kb = L / XBK;
+    g.c_recv = c_recv;
+    g.out = dh;
+    g.ldo = H;
+    g.rowmap = nullptr;   // dh in the per-expert layout
+    g.out_rows = static_cast<long long>(E) * c_recv;
+    g.a_mn = 1;
+    g.status = status;
+    return launch_group<EPI_SCATTER>(g, sms, st, "bwd_gemm_dh");
+}
+
+int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
+                            const uint16_t* Wg, const uint16_t* Wu, const uint16_t* dh,
+                            const ExpertGroups& gl, uint16_t* dg, uint16_t* du, int32_t* status,
+                            cudaStream_t st) {
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    if (!MOE_XPAIR_TM || !pair_widths(sms, E, c_recv) || L % 256 || H % 128 || !al16(xe) ||
+        !al16(dh) || !al16(dg) || !al16(du))
         return MOE_EINVAL;
     GParams g;
     std::memset(&g, 0, sizeof(g));
@@ -1117,16 +1211,8 @@ int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
         if ((rc = map3(&g.mapX[i], xe, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
                        XHSTEP * (i + 1))))
             return rc;
-    uint8_t* ws = static_cast<uint8_t*>(list_ws);
-    int4* chunks = reinterpret_cast<int4*>(ws);
-    int4* groups = reinterpret_cast<int4*>(ws + chunk_list_bytes(E, c_recv));
-    int32_t* nchunks = reinterpret_cast<int32_t*>(ws + expert_pair_chunks_bytes(E, c_recv) - 16);
-    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, c_recv, chunks, nchunks, groups,
-                                          nchunks + 1);
-    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
-    trace_after(st, "bwd_build_groups");
-    g.groups = groups;
-    g.ngroups = nchunks + 1;
+    g.groups = gl.groups;
+    g.ngroups = gl.ngroups;
     g.n_mb = H / 128;
     g.zpe = H / 16;
     g.kb = L / XBK;
@@ -1137,6 +1223,53 @@ int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
     g.ldo = H;
     g.status = status;
     return launch_group<EPI_SWIGLU_BWD>(g, sms, st, "bwd_gemm_expert_swiglu");
+}
+
+int expert_dx_group(int E, int c_recv, int L, int H, const uint16_t* dg, const uint16_t* du,
+                    const uint16_t* Wg, const uint16_t* Wu, const ExpertGroups& gl,
+                    const int32_t* expert_rows, uint16_t* dxpool, int64_t pool_rows,
+                    int32_t* status, cudaStream_t st) {
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    if (!MOE_XPAIR_TM || !pair_widths(sms, E, c_recv) || L % 256 || H % 64 || !al16(dg) ||
+        !al16(du) || !al16(Wg) || !al16(Wu) || !al16(dxpool))
+        return MOE_EINVAL;
+    GParams g;
+    std::memset(&g, 0, sizeof(g));
+    // K in two segments, gate then up: the weights Wg, Wu [E, H, L] as [K, M]
+    // (MN-major), the rows dg, du [E, c_recv, H]; each pair through one 4-D
+    // map whose outer dimension steps from the lower-addressed tensor to the
+    // other
+    const uintptr_t wg = reinterpret_cast<uintptr_t>(Wg), wu = reinterpret_cast<uintptr_t>(Wu);
+    const uintptr_t xg = reinterpret_cast<uintptr_t>(dg), xu = reinterpret_cast<uintptr_t>(du);
+    const void* wlo = reinterpret_cast<const void*>(wg < wu ? wg : wu);
+    const void* xlo = reinterpret_cast<const void*>(xg < xu ? xg : xu);
+    if ((rc = map4(&g.mapW, wlo, L, H, E, 2, static_cast<uint64_t>(L) * 2,
+                   static_cast<uint64_t>(H) * L * 2, wg < wu ? wu - wg : wg - wu, 64)))
+        return rc;
+    for (int i = 0; i < XNMAP; ++i)
+        if ((rc = map4(&g.mapX[i], xlo, H, c_recv, E, 2, static_cast<uint64_t>(H) * 2,
+                       static_cast<uint64_t>(c_recv) * H * 2, xg < xu ? xu - xg : xg - xu,
+                       XHSTEP * (i + 1))))
+            return rc;
+    g.aseg[0] = wg < wu ? 0 : 1;
+    g.aseg[1] = 1 - g.aseg[0];
+    g.bseg[0] = xg < xu ? 0 : 1;
+    g.bseg[1] = 1 - g.bseg[0];
+    g.kseg = H;
+    g.groups = gl.groups;
+    g.ngroups = gl.ngroups;
+    g.n_mb = L / 256;
+    g.kb = 2 * H / XBK;
+    g.c_recv = c_recv;
+    g.out = dxpool;
+    g.ldo = L;
+    g.rowmap = expert_rows;
+    g.out_rows = pool_rows;
+    g.a_mn = 1;
+    g.status = status;
+    return launch_group<EPI_SCATTER>(g, sms, st, "bwd_gemm_dX");
 }
 
 static size_t chunk_list_bytes(int E, int c_recv) {

@@ -192,17 +192,35 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
                     uint16_t* ypool, int64_t pool_rows, int32_t* status, cudaStream_t stream);
 int check_status_expert_pair();
 
-// The backward's recomputed gate/up and SwiGLU backward of the routed experts
-// over row groups on CTA pairs (expert_pair.cu): X rows from xe [E, c_recv,
-// L], dh [E, c_recv, H] in, dg and du [E, c_recv, H] out for each expert's
-// first expert_count rows (the rest untouched).  list_ws: at least
-// expert_pair_chunks_bytes(E, c_recv) bytes of scratch, 16-byte aligned.
-// MOE_EINVAL when the widths or the weight tensors do not allow this path
-// (the caller then takes the gathered one).
+// The routed experts' products of the backward over row groups on CTA pairs
+// (expert_pair.cu), capped layout, per-expert row layouts [E, c_recv, .]:
+//  expert_group_list: the row groups of every expert from expert_count, in
+//    `ws` (expert_pair_chunks_bytes(E, c_recv) bytes, 16-byte aligned; kept
+//    until the products below have run);
+//  expert_dh_group: dh = dY Wd_e (dY rows from dye, zero past each count);
+//  expert_swiglu_bwd_group: g, u recomputed from X (xe), dg = dh u silu'(g),
+//    du = dh silu(g), each expert's first expert_count rows (the rest
+//    untouched);
+//  expert_dx_group: dX = dg Wg_e + du Wu_e, each row to its pool row of
+//    dxpool (expert_rows).
+// Each returns MOE_EINVAL, having enqueued nothing, when the widths or the
+// tensors do not allow its path (the caller then takes the grouped GEMM).
+struct ExpertGroups {
+    const int4* groups;
+    const int32_t* ngroups;
+};
+int expert_group_list(int E, int c_recv, const int32_t* expert_count, void* ws, ExpertGroups* out,
+                      cudaStream_t stream);
+int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const uint16_t* Wd,
+                    const ExpertGroups& groups, uint16_t* dh, int32_t* status, cudaStream_t stream);
 int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
-                            const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
-                            const uint16_t* dh, void* list_ws, uint16_t* dg, uint16_t* du,
+                            const uint16_t* Wg, const uint16_t* Wu, const uint16_t* dh,
+                            const ExpertGroups& groups, uint16_t* dg, uint16_t* du,
                             int32_t* status, cudaStream_t stream);
+int expert_dx_group(int E, int c_recv, int L, int H, const uint16_t* dg, const uint16_t* du,
+                    const uint16_t* Wg, const uint16_t* Wu, const ExpertGroups& groups,
+                    const int32_t* expert_rows, uint16_t* dxpool, int64_t pool_rows,
+                    int32_t* status, cudaStream_t stream);
 
 // Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
 // Checked builds: the site code recorded by each translation unit's index
