@@ -728,8 +728,16 @@ def run_gb300(args, rank, world, local_rank):
         # recomputes (routed and shared)
         fwd_tf = sum(kernel_work(n, cfg, m.plan, st)[0] or 0.0 for n in per
                      if kernel_work(n, cfg, m.plan, st)[2] == "tensor")
+        # the backward's launches, ms a step each (a name launched several
+        # times a step is summed)
+        bk = {}
+        for n, ms in ttr:
+            if n.startswith("bwd_"):
+                bk[n] = bk.get(n, 0.0) + ms / nt
         train = {"value": tv, "unit": UNIT, "ms_per_step": tms, "steps": nt,
                  "backward_ms": round(bwd, 4),
+                 "backward_kernels_ms": {n: round(v, 4) for n, v in
+                                         sorted(bk.items(), key=lambda kv: -kv[1])},
                  "forward_tflop": round(fwd_tf, 3),
                  "note": "forward + backward of the layer; weight gradients fp32"}
 
