@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -96,12 +97,23 @@ def source_group(kernel: str, bank_path: bool = True) -> str:
     return "gemm" if kernel.startswith("gemm") else "route"
 
 
+def code_text(text):
+    """C++/CUDA source with its comments removed and whitespace collapsed:
+    what a source hash should change with (string literals in these sources
+    hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(kernel="gemm", bank_path=True):
+    """Hash of the code (comments and layout left out) of a kernel's
+    translation unit, the shared device headers and the entry points."""
     files = KERNEL_SOURCES[source_group(kernel, bank_path)]
     h = hashlib.sha256()
     src = os.path.join(ROOT, "moe_routing_capacity_gb300", "csrc")
     for f in files:
-        h.update(open(os.path.join(src, f), "rb").read())
+        h.update(code_text(open(os.path.join(src, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -378,14 +378,18 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
 // the rest.  The MMA issuer waits for the overlap of the tile before and for
 // the whole of the tile two before (the same end).
 //
-// Gate/up: a CTA's 128 weight rows arrive by one TMA box that interleaves the
-// two tensors by 16 rows: lanes 32q .. 32q+15 hold 16 hidden units of the
-// lower-addressed tensor, lanes 32q+16 .. 32q+31 the same units of the other,
-// so a lane's SwiGLU partner is lane ^ 16 of its own warp (one shuffle, no
-// shared-memory exchange).  Down: a CTA's 128 rows of Wd are 128 output
-// features; lanes pair adjacent features by a shuffle into 32-bit stores
-// scattered to the rows' pool rows.  Eight epilogue warps, two a lane
-// quarter, take alternate 32-column blocks.
+// Gate/up (forward, and its recomputation in the backward): a CTA's 128
+// weight rows arrive by one TMA box that interleaves the two tensors by 16
+// rows: lanes 32q .. 32q+15 hold 16 hidden units of the lower-addressed
+// tensor, lanes 32q+16 .. 32q+31 the same units of the other, so a lane's
+// SwiGLU partner is lane ^ 16 of its own warp (one shuffle, no shared-memory
+// exchange); the forward writes h, the backward reads dh and writes dg, du.
+// Scatter (the forward's down product; the backward's dh and dX): a CTA's
+// 128 weight rows are 128 output features; lanes pair adjacent features by a
+// shuffle into 32-bit stores to each row's output row (its pool row, or its
+// row of the per-expert layout).  The backward's products read their weights
+// MN-major (stored [K, M]), dX's K in two segments (gate, then up).  Eight
+// epilogue warps, two a lane quarter, take alternate 32-column blocks.
 constexpr int GACC = 416;                      // most rows (accumulator columns) a group
 constexpr int GB_BYTES = GACC / 2 * XBK * 2;   // this CTA's rows a stage: at most 208
 constexpr int GSTAGE = XA_BYTES + GB_BYTES;    // 42 KB

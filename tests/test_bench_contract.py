@@ -93,3 +93,15 @@ def test_expert_stream_bytes_match_the_traffic_records():
         got = bench.expert_stream_bytes(name, cfg, st, 384) * 1e9
         assert round(got) == recs[name]["full_algorithmic_bytes"], name
     assert bench.expert_stream_bytes("combine", cfg, st, 384) is None
+
+
+def test_source_hash_follows_code_not_comments():
+    """A traffic record stays valid through comment and layout edits of the
+    kernel's sources, and not through a change of code."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) {  // the same\n  return x + 1; /* block\n comment */ }\n"
+    b = "int f(int x) {\n    return x + 1;\n}\n// another comment\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
