@@ -2,7 +2,8 @@
 kernel computes is verified before use, failures recorded in a device word
 and the access skipped) on the layer's forward and backward, capped and
 dropless, and on the overlapped pool fills (copy warps inside the shared
-or the expert gate/up launch): no check fires, and the results equal the
+or the expert gate/up launch), at the tiny and mid sizes and on the full
+workload in the bench's schedule: no check fires, and the results equal the
 normal build's bit for bit.  This stands in for a memory checker, which is
 not available here."""
 import os
@@ -71,3 +72,20 @@ def test_checked_build_overlapped_fill(checked_lib, name, pipeline):
     assert code == 0, f"index check site {code} fired"
     for key, v in want.items():
         assert torch.equal(v.contiguous().view(torch.uint8), got[key].contiguous().view(torch.uint8)), key
+
+
+def test_checked_build_full_workload(checked_lib):
+    """The full workload in the bench's schedule (pool fill inside the shared
+    gate/up, the expert products on CTA pairs over row groups, and the
+    backward's grouped expert products), forward and backward, through the
+    checked build: no index check fires and every output and gradient equals
+    the normal build's bit for bit."""
+    cfg = wl.CONFIGS["full"]
+    want, code0 = _run(cfg, False, pipeline="shared")
+    assert code0 == 0
+    got, code = _run(cfg, False, checked_lib, pipeline="shared")
+    assert code == 0, f"index check site {code} fired"
+    for key in list(want):
+        a, b = want.pop(key), got.pop(key)
+        assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8)), key
+        del a, b
