@@ -245,16 +245,24 @@ int moe_dispatch_pooled_noalloc(const moe_config_t* cfg, const uint16_t* z, cons
  *   expert_offsets [E+1] int32: expert e's rows are
  *   expert_rows[expert_offsets[e] .. expert_offsets[e+1]) (flat [T*k] int32,
  *   priority order); expert_count [E] = the differences; drop is all 0 and
- *   slot_of >= 0 everywhere.
+ *   slot_of >= 0 everywhere.  bank: optional (NULL: not written) [T*k, L]
+ *   bf16, 16-byte aligned, L a multiple of 8: bank[i] = z[t] for the
+ *   assignment in expert_rows[i], i.e. every expert's rows contiguous from
+ *   row expert_offsets[e], in the row list's order.
  * moe_expert_ffn_ragged: moe_expert_ffn_grouped over those row lists; h
  *   [T*k, H] sits at plan.h_offset_bytes of ws with expert e's rows from
- *   expert_offsets[e].  ypool [T*k, L].  moe_combine applies unchanged. */
+ *   expert_offsets[e].  ypool [T*k, L].  moe_combine applies unchanged.
+ *   bank: optional, the one moe_dispatch_ragged wrote (16-byte aligned); with
+ *   L a multiple of 256 and H of 128 the products then load each expert's
+ *   rows from it as whole tiles (same h and ypool, bit for bit, as without
+ *   it); otherwise it is not read. */
 int moe_plan_ragged(const moe_config_t* cfg, moe_plan_t* plan);
 int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
                         void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
                         uint8_t* drop, int32_t* expert_offsets, int32_t* expert_rows,
-                        int32_t* expert_count, moe_drop_stats_t* stats, void* stream);
-int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
+                        int32_t* expert_count, moe_drop_stats_t* stats, uint16_t* bank,
+                        void* stream);
+int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool, const uint16_t* bank,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
                           const uint16_t* Wd, void* ws, size_t ws_bytes, uint16_t* ypool,
@@ -557,8 +565,9 @@ int moe_trace_event(int i, const char** name, float* ms_since_prev);
 /* Human-readable name of a MOE_* code (static string). */
 const char* moe_strerror(int code);
 
-/* ABI version: 3 (2: the optional per-expert bank of the dispatch and the
- * expert FFN; 3: the whole-layer forward and the host-memory pipeline). */
+/* ABI version: 4 (2: the optional per-expert bank of the dispatch and the
+ * expert FFN; 3: the whole-layer forward and the host-memory pipeline; 4: the
+ * optional bank of the dropless dispatch and expert FFN). */
 int moe_abi_version(void);
 
 #ifdef __cplusplus

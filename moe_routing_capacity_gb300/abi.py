@@ -131,8 +131,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.moe_balance_update.argtypes = [pc, vp, vp, ctypes.c_float, vp, vp]
     L.moe_balance_update_window.argtypes = [pc, vp, vp, vp, i32, vp, ctypes.c_float, vp, vp]
     L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
-    L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp]
-    L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.moe_backward_plan.argtypes = [pc, ctypes.POINTER(BackwardWs)]
     L.moe_layer_backward.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
     L.moe_backward_plan_ragged.argtypes = [pc, ctypes.POINTER(BackwardWs)]
@@ -315,18 +315,19 @@ def dispatch_shared_overlap(cfg, z, idx, ws, pool, slot_of, drop, expert_rows, e
 
 
 def dispatch_ragged(cfg, z, idx, ws, pool, slot_of, drop, expert_offsets, expert_rows,
-                    expert_count, stats, stream=None):
+                    expert_count, stats, stream=None, bank=None):
     _check("moe_dispatch_ragged", lib().moe_dispatch_ragged(
         ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
         ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
         _ptr(expert_offsets, i32), _ptr(expert_rows, i32), _ptr(expert_count, i32),
-        _ptr(stats, torch.int64), _stream(stream)))
+        _ptr(stats, torch.int64), _ptr(bank, bf16, allow_none=True), _stream(stream)))
 
 
 def expert_ffn_ragged(cfg, pool, expert_offsets, expert_rows, expert_count, Wg, Wu, Wd, ws,
-                      ypool, status, stream=None):
+                      ypool, status, stream=None, bank=None):
     _check("moe_expert_ffn_ragged", lib().moe_expert_ffn_ragged(
-        ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16), _ptr(expert_offsets, i32),
+        ctypes.byref(make_config(cfg)), _ptr(pool, torch.int16),
+        _ptr(bank, bf16, allow_none=True), _ptr(expert_offsets, i32),
         _ptr(expert_rows, i32), _ptr(expert_count, i32), _ptr(Wg, bf16), _ptr(Wu, bf16),
         _ptr(Wd, bf16), _ptr(ws, u8), ws.numel(), _ptr(ypool, bf16), _ptr(status, i32),
         _stream(stream)))

@@ -187,11 +187,16 @@ static int make_geom_ragged(const moe_config_t* c, Geom* out) {
     p.pool_rows = n;
     p.ws_dispatch_bytes = static_cast<int64_t>(dispatch_ws_layout(g).total);
     const size_t max_mt = static_cast<size_t>(n / 128 + g.E);
-    const size_t tiles_bytes = align_up(max_mt * 8 + 16, 1024);
+    // the tile list of the gathered path or the group lists of the bank path
+    const size_t tiles_bytes =
+        align_up(std::max(max_mt * 8 + 16, expert_pair_lists_bytes_ragged(g.E, n)), 1024);
     p.h_offset_bytes = static_cast<int64_t>(tiles_bytes);
     p.ws_ffn_bytes = static_cast<int64_t>(tiles_bytes + static_cast<size_t>(n) * out->H * 2);
     return MOE_OK;
 }
+
+// The row-group expert kernels take these widths (else the gathered GEMMs).
+static bool pair_path_fits(const Geom& G) { return G.g.L % 256 == 0 && G.H % 128 == 0; }
 
 }  // namespace moe
 
@@ -199,7 +204,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 3; }
+int moe_abi_version(void) { return 4; }
 
 int moe_check_status(void) {
     const int v[4] = {check_status_route(), check_status_gemm(), check_status_backward(),
@@ -442,7 +447,7 @@ int moe_plan_ragged(const moe_config_t* cfg, moe_plan_t* plan) {
 int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx, void* ws,
                         size_t ws_bytes, uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                         int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
-                        moe_drop_stats_t* stats, void* stream) {
+                        moe_drop_stats_t* stats, uint16_t* bank, void* stream) {
     MOE_NVTX_RANGE();
     Geom G;
     int rc = make_geom_ragged(cfg, &G);
@@ -450,16 +455,18 @@ int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_
     if (!stats || !expert_count || !expert_offsets || !ws ||
         (G.g.T > 0 && (!z || !idx || !slot_of || !drop || !pool || !expert_rows)))
         return MOE_EINVAL;
-    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || !aligned16(ws)) return MOE_EINVAL;
+    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || !aligned16(ws) ||
+        (bank && (!aligned16(bank) || G.g.L % 8)))
+        return MOE_EINVAL;
     if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
     int dev, sms;
     if ((rc = current_device(&dev, &sms))) return rc;
     return launch_dispatch_ragged(G.g, z, idx, ws, pool, slot_of, drop, expert_offsets,
-                                  expert_rows, expert_count, stats,
+                                  expert_rows, expert_count, stats, bank,
                                   static_cast<cudaStream_t>(stream));
 }
 
-int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
+int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool, const uint16_t* bank,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
                           const uint16_t* Wd, void* ws, size_t ws_bytes, uint16_t* ypool,
@@ -477,12 +484,18 @@ int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool,
         !aligned16(ypool) || !aligned16(ws))
         return MOE_EINVAL;
     if (ws_bytes < static_cast<size_t>(G.plan.ws_ffn_bytes)) return MOE_ENOSPC;
+    if (bank && !aligned16(bank)) return MOE_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
+    uint16_t* h = reinterpret_cast<uint16_t*>(wsb + G.plan.h_offset_bytes);
+    if (bank && pair_path_fits(G)) {
+        rc = expert_ffn_pair_ragged(g.E, g.pool_rows, g.L, G.H, bank, expert_offsets, expert_rows,
+                                    expert_count, Wg, Wu, Wd, ws, h, ypool, status, st);
+        if (rc != MOE_EINVAL) return rc;   // else: the gathered products below
+    }
     int32_t* tiles = reinterpret_cast<int32_t*>(wsb);
     const int max_mt = static_cast<int>(g.pool_rows / 128 + g.E);
     int32_t* tile_count = reinterpret_cast<int32_t*>(wsb + static_cast<size_t>(max_mt) * 8);
-    uint16_t* h = reinterpret_cast<uint16_t*>(wsb + G.plan.h_offset_bytes);
     if ((rc = launch_build_tiles(expert_count, g.E, 128, tiles, tile_count, st))) return rc;
     const int L = g.L, H = G.H;
     const int n = static_cast<int>(g.pool_rows);
@@ -550,8 +563,6 @@ struct WavePipe {
 
 // The per-expert bank path (CTA pairs, rows on the MMA's N axis) takes
 // widths that are whole 256-column output blocks and 128-unit hidden blocks.
-static bool pair_path_fits(const Geom& G) { return G.g.L % 256 == 0 && G.H % 128 == 0; }
-
 static int expert_ffn_capped(const Geom& G, uint16_t* pool, const int32_t* expert_rows,
                              const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
                              const uint16_t* Wd, void* ws, uint16_t* ypool, int32_t* status,

@@ -429,11 +429,15 @@ struct GParams {
                                // and mapX then have a 4th dimension stepping between two
                                // tensors, aseg / bseg giving each segment's index in it
     int aseg[2], bseg[2];
+    const int32_t* roff;       // dropless layout: expert e's rows start at row roff[e] of the
+                               // flat bank, h and row list (mapX one group of all rows);
+                               // NULL: at e * c_recv, mapX [E, c_recv, K]
     int* status;
 };
 
 struct GTile {
     int e, row0, rows, n0, n1, mb;
+    long long rbase;   // the expert's first row in the flat row space (e * c_recv or roff[e])
 };
 
 __device__ __forceinline__ GTile gate_tile(const GParams& p, int tile) {
@@ -446,6 +450,8 @@ __device__ __forceinline__ GTile gate_tile(const GParams& p, int tile) {
     t.n0 = g.w & 0xffff;
     t.n1 = static_cast<int>(static_cast<uint32_t>(g.w) >> 16);
     t.mb = tile - gi * p.n_mb;
+    t.rbase = p.roff ? static_cast<long long>(p.roff[t.e])
+                     : static_cast<long long>(t.e) * p.c_recv;
     return t;
 }
 
@@ -556,10 +562,13 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                             tma_load_4d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kin,
                                              xrow1, t.e, p.bseg[sg]);
                     } else {
-                        tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, xrow0, t.e);
+                        // rows: [E, c_recv] by expert, or (dropless) one flat group
+                        const int by = p.roff ? static_cast<int>(t.rbase) : 0;
+                        const int bz = p.roff ? 0 : t.e;
+                        tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, by + xrow0, bz);
                         if (h1)
                             tma_load_3d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kx,
-                                             xrow1, t.e);
+                                             by + xrow1, bz);
                     }
                     if (++s == GST) {
                         s = 0;
@@ -682,7 +691,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     const int rr = 32 * b + lane;
                     prow[i] = -1;
                     if (pos < nblk && rr < t.rows) {
-                        const int r = t.e * p.c_recv + t.row0 + rr;
+                        const int r = static_cast<int>(t.rbase) + t.row0 + rr;
                         const int v = p.rowmap ? p.rowmap[r] : r;
                         if (moe_check(v >= 0 && v < p.out_rows, 1102)) prow[i] = v;
                     }
@@ -740,7 +749,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
             tc_fence_after();
             // column c of the tile is the group's row row0 + c (chunk 0 is full)
             const int unit = t.mb * 128 + static_cast<int>(crank) * 64 + q * 16 + (y & ~1);
-            uint16_t* hb = p.out + (static_cast<long long>(t.e) * p.c_recv + t.row0) * p.ldo + unit;
+            uint16_t* hb = p.out + (t.rbase + t.row0) * p.ldo + unit;
             int drained = 0;
 #pragma unroll 1
             for (int pos = grp; pos < nblk; pos += 2) {
@@ -778,8 +787,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                         gv[j] = p.gate_hi ? hi_t : lo_t;
                         uv[j] = p.gate_hi ? lo_t : hi_t;
                     }
-                    const long long gbase =
-                        (static_cast<long long>(t.e) * p.c_recv + t.row0) * p.ldo + unit;
+                    const long long gbase = (t.rbase + t.row0) * p.ldo + unit;
                     const int rb = 32 * b + (hi ? 16 : 0) + (odd ? 8 : 0);   // this lane's first row
                     // the eight rows' dh first (independent loads), then the
                     // partner's g, u, then the arithmetic
@@ -1148,6 +1156,74 @@ int check_status_expert_pair() { return moe_check_read_reset(); }
 
 static size_t chunk_list_bytes(int E, int c_recv);
 
+static bool pair_widths(int sms, int E, int c_recv) { return sms >= 2 && E > 0 && c_recv > 0; }
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t expert_pair_lists_bytes_ragged(int E, int64_t rows) {
+    // every expert's chunks and groups: at most E + rows / 256 and E + rows / 416
+    const size_t nc = static_cast<size_t>(E) + static_cast<size_t>(rows / XCHUNK) + 1;
+    const size_t ng = static_cast<size_t>(E) + static_cast<size_t>(rows / GACC) + 1;
+    return (nc + ng) * sizeof(int4) + 16;
+}
+
+int expert_ffn_pair_ragged(int E, int64_t rows, int L, int H, const uint16_t* bank,
+                           const int32_t* expert_offsets, const int32_t* expert_rows,
+                           const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                           const uint16_t* Wd, void* list_ws, uint16_t* h, uint16_t* ypool,
+                           int32_t* status, cudaStream_t st) {
+    int dev, sms;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    if (!MOE_XPAIR_TM || sms < 2 || E <= 0 || rows <= 0 || rows > INT32_MAX / 2 || L % 256 ||
+        H % 128 || !al16(bank) || !al16(h) || !al16(list_ws))
+        return MOE_EINVAL;
+    GParams g;
+    std::memset(&g, 0, sizeof(g));
+    if (map_gateup_il(&g.mapW, Wg, Wu, E, H, L, &g.gate_hi) != MOE_OK) return MOE_EINVAL;
+    for (int i = 0; i < XNMAP; ++i)   // the flat bank [rows, L] as one group
+        if ((rc = map3(&g.mapX[i], bank, L, rows, 1, L, static_cast<uint64_t>(rows) * L,
+                       XHSTEP * (i + 1))))
+            return rc;
+    const size_t nc = static_cast<size_t>(E) + static_cast<size_t>(rows / XCHUNK) + 1;
+    uint8_t* w = static_cast<uint8_t*>(list_ws);
+    int4* chunks = reinterpret_cast<int4*>(w);
+    int4* groups = chunks + nc;
+    int32_t* counts = reinterpret_cast<int32_t*>(w + expert_pair_lists_bytes_ragged(E, rows) - 16);
+    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, INT32_MAX, chunks, counts, groups,
+                                          counts + 1);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "build_chunks");
+    g.groups = groups;
+    g.ngroups = counts + 1;
+    g.n_mb = H / 128;
+    g.zpe = H / 16;
+    g.kb = L / XBK;
+    g.out = h;
+    g.ldo = H;
+    g.roff = expert_offsets;
+    g.status = status;
+    if ((rc = launch_group<EPI_SWIGLU>(g, sms, st, "gemm_expert_gateup"))) return rc;
+    GParams d;
+    std::memset(&d, 0, sizeof(d));
+    if ((rc = map3(&d.mapW, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 128))) return rc;
+    for (int i = 0; i < XNMAP; ++i)   // the flat h [rows, H] as one group
+        if ((rc = map3(&d.mapX[i], h, H, rows, 1, H, static_cast<uint64_t>(rows) * H,
+                       XHSTEP * (i + 1))))
+            return rc;
+    d.groups = groups;
+    d.ngroups = counts + 1;
+    d.n_mb = L / 256;
+    d.kb = H / XBK;
+    d.out = ypool;
+    d.ldo = L;
+    d.rowmap = expert_rows;
+    d.out_rows = rows;
+    d.roff = expert_offsets;
+    d.status = status;
+    return launch_group<EPI_SCATTER>(d, sms, st, "gemm_expert_down");
+}
+
 int expert_group_list(int E, int c_recv, const int32_t* expert_count, void* ws, ExpertGroups* out,
                       cudaStream_t st) {
     if (E <= 0 || c_recv <= 0 || (reinterpret_cast<uintptr_t>(ws) & 15)) return MOE_EINVAL;
@@ -1163,10 +1239,6 @@ int expert_group_list(int E, int c_recv, const int32_t* expert_count, void* ws, 
     out->ngroups = counts + 1;
     return MOE_OK;
 }
-
-static bool pair_widths(int sms, int E, int c_recv) { return sms >= 2 && E > 0 && c_recv > 0; }
-
-static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const uint16_t* Wd,
                     const ExpertGroups& gl, uint16_t* dh, int32_t* status, cudaStream_t st) {

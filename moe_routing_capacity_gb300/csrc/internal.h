@@ -176,10 +176,12 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
                     int32_t* expert_count, moe_drop_stats_t* stats, cudaStream_t stream,
                     int copy_wave = -1, bool run_pack = true, uint16_t* bank = nullptr);
 
+// bank (optional): [T*k, L], each row also written at its position in the
+// flat expert row list.
 int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                            uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                            int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
-                           moe_drop_stats_t* stats, cudaStream_t stream);
+                           moe_drop_stats_t* stats, uint16_t* bank, cudaStream_t stream);
 
 // The capped layout's expert FFN on CTA pairs with the expert's rows on the
 // MMA's N axis (expert_pair.cu): chunk list, gate/up from the per-expert
@@ -191,6 +193,19 @@ int expert_ffn_pair(int E, int c_recv, int L, int H, const uint16_t* bank,
                     const uint16_t* Wu, const uint16_t* Wd, void* chunk_ws, uint16_t* h,
                     uint16_t* ypool, int64_t pool_rows, int32_t* status, cudaStream_t stream);
 int check_status_expert_pair();
+
+// The dropless layout's expert FFN on CTA pairs over row groups
+// (expert_pair.cu): gate/up from the flat bank [rows, L] (expert e's rows at
+// expert_offsets[e]) into the flat h [rows, H], down from h scattered to the
+// pool rows of ypool (expert_rows, flat).  list_ws:
+// expert_pair_lists_bytes_ragged(E, rows), 16-byte aligned.  MOE_EINVAL,
+// having enqueued nothing, when the widths or tensors do not allow it.
+size_t expert_pair_lists_bytes_ragged(int E, int64_t rows);
+int expert_ffn_pair_ragged(int E, int64_t rows, int L, int H, const uint16_t* bank,
+                           const int32_t* expert_offsets, const int32_t* expert_rows,
+                           const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
+                           const uint16_t* Wd, void* list_ws, uint16_t* h, uint16_t* ypool,
+                           int32_t* status, cudaStream_t stream);
 
 // The routed experts' products of the backward over row groups on CTA pairs
 // (expert_pair.cu), capped layout, per-expert row layouts [E, c_recv, .]:

@@ -14,8 +14,9 @@ namespace moe {
 // 1 dropped by the sender, 2 by the receiver).  copy_wave: copy the latent
 // row and write the tag into the pool rows of every sender-kept assignment
 // (-1), of those of one wave (>= 0), or of none (< -1); with a bank and
-// decide, each receiver-kept row copied is also written to the bank row of
-// its expert and receiver rank.  The latent row is read once, CH 16-byte
+// decide, each receiver-kept row copied is also written to the bank at its
+// position in its expert's row list (e * c_recv + r capped, offset[e] + r
+// ragged).  The latent row is read once, CH 16-byte
 // chunks a lane at a time, and written to each row.
 // STREAM: streaming (evict-first) loads and stores, for a copy that runs
 // beside a product whose tiles should stay in L2.
@@ -25,7 +26,7 @@ __device__ __forceinline__ void pack_token(const DispatchGeom& g, const PackArgs
     const int64_t s = t / g.T_s;
     const int64_t pitch = pool_pitch(g.L);
     int64_t row = -1;
-    int64_t brow = -1;   // bank row (expert e, receiver rank r) of a receiver-kept row
+    int64_t brow = -1;   // bank row of a receiver-kept row: its expert row list position
     int e = 0;
     if (lane < g.k) {
         const int64_t a = t * g.k + lane;
@@ -43,11 +44,12 @@ __device__ __forceinline__ void pack_token(const DispatchGeom& g, const PackArgs
                                                 : static_cast<int64_t>(e) * g.c_recv + r;
                     if (moe_check(at >= 0 && at < (g.ragged ? g.T * g.k
                                                             : static_cast<int64_t>(g.E) * g.c_recv),
-                                  1002))
+                                  1002)) {
                         P.expert_rows[at] = static_cast<int32_t>(row);
+                        if (P.bank) brow = at;
+                    }
                     so = static_cast<int32_t>(row);
                     dr = 0;
-                    if (P.bank && !g.ragged) brow = static_cast<int64_t>(e) * g.c_recv + r;
                 } else {
                     dr = 2;
                 }

@@ -32,9 +32,10 @@ class PooledWaveMoE:
     waves' pool rows copied while wave 0's experts run) or "shared" (the
     pool rows copied while the shared experts' gate/up runs); the capped
     layout only.  ``expert_bank``: the dispatch also writes the received
-    rows grouped by expert (``self.bank``), from which the expert products
-    load whole tiles (capped layout, calls one after another or "shared");
-    False gathers each expert's rows from the pool instead."""
+    rows grouped by expert (``self.bank``: [E, c_recv, L] capped, [T*k, L]
+    dropless in the flat row list's order), from which the expert products
+    load whole tiles (either layout, except the "waves" pipeline); False
+    gathers each expert's rows from the pool instead."""
 
     PIPELINES = (None, "waves", "shared")
 
@@ -73,8 +74,12 @@ class PooledWaveMoE:
         self.stats = torch.zeros(abi.STATS_WORDS, dtype=torch.int64, device=dev)
         self.ws_ffn = e(max(1, p.ws_ffn_bytes), dt=torch.uint8)
         # the received rows grouped by local expert (written by the pack)
-        self.bank = (e(E, max(1, p.c_recv), L, dt=torch.bfloat16)
-                     if expert_bank and not dropless and pipeline != "waves" else None)
+        if not expert_bank or pipeline == "waves":
+            self.bank = None
+        elif dropless:
+            self.bank = e(max(1, T * k), L, dt=torch.bfloat16)
+        else:
+            self.bank = e(E, max(1, p.c_recv), L, dt=torch.bfloat16)
         self.ypool = e(p.pool_rows, L, dt=torch.bfloat16)
         self.c = e(T, L, dt=torch.bfloat16)
         self.a = e(T, max(1, cfg.n_shared * cfg.h_shared), dt=torch.bfloat16)
@@ -102,7 +107,7 @@ class PooledWaveMoE:
         if self.dropless:
             abi.dispatch_ragged(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
                                 self.slot_of, self.drop, self.expert_offsets, self.expert_rows,
-                                self.expert_count, self.stats, stream)
+                                self.expert_count, self.stats, stream, bank=self.bank)
         else:
             abi.dispatch_pooled(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
                                 self.slot_of, self.drop, self.expert_rows, self.expert_count,
@@ -112,7 +117,7 @@ class PooledWaveMoE:
         if self.dropless:
             abi.expert_ffn_ragged(self.cfg, self.pool, self.expert_offsets, self.expert_rows,
                                   self.expert_count, self.w["Wg"], self.w["Wu"], self.w["Wd"],
-                                  self.ws_ffn, self.ypool, self.status, stream)
+                                  self.ws_ffn, self.ypool, self.status, stream, bank=self.bank)
         else:
             abi.expert_ffn_grouped(self.cfg, self.pool, self.expert_rows, self.expert_count,
                                    self.w["Wg"], self.w["Wu"], self.w["Wd"], self.ws_ffn,

@@ -149,3 +149,60 @@ def test_ragged_full_size_sampled(name):
     a_o = O.shared_act(xh[toks], inp["Wsg"].double().cpu().numpy(), inp["Wsu"].double().cpu().numpy())
     out_o = O.output(c_o, a_o, inp["W_lu"].double().cpu().numpy(), inp["Wsd"].double().cpu().numpy())
     check_close("out", m.out[toks].double().cpu().numpy(), out_o)
+
+
+# Widths the row-group expert kernels take (L a multiple of 256, H of 128);
+# a Zipf bias gives experts of several hundred rows (two- and three-group
+# experts) next to near-empty ones.
+PAIR_SMALL = wl.LayerConfig("ragged-pair", T=3072, d_model=256, d_latent=256, n_experts=24,
+                            n_ranks=4, top_k=2, n_waves=3, n_shared=1, h_expert=128,
+                            h_shared=128, seed=47, bias_kind="zipf")
+
+
+def _bank_vs_gathered(cfg, inp):
+    x = inp["x"].cuda()
+    a = PooledWaveMoE(cfg, inp, "cuda", dropless=True)
+    b = PooledWaveMoE(cfg, inp, "cuda", dropless=True, expert_bank=False)
+    a.forward(x)
+    b.forward(x)
+    torch.cuda.synchronize()
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    assert a.bank is not None and b.bank is None
+    # the bank holds each row of the flat row list's token in that order
+    tok = a.pool_tags()[a.expert_rows.long(), 1].long()
+    assert torch.equal(a.bank.view(torch.int16), a.z[tok].view(torch.int16))
+    assert torch.equal(a.ypool.view(torch.int16), b.ypool.view(torch.int16))
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    return a
+
+
+@pytest.mark.parametrize("name", ["ragged-pair", "mid", "skew"])
+def test_ragged_bank_equals_gathered(name):
+    cfg = PAIR_SMALL if name == "ragged-pair" else wl.CONFIGS[name]
+    m = _bank_vs_gathered(cfg, wl.make_inputs(cfg, "cuda"))
+    counts = m.expert_count.cpu()
+    if name != "mid":   # the skewed routings reach the multi-group experts
+        assert int(counts.max()) > 416
+
+
+def test_ragged_bank_small_parity():
+    m = compare(PAIR_SMALL, wl.make_inputs(PAIR_SMALL, "cpu"))
+    assert m.bank is not None
+
+
+def test_ragged_bank_equals_capped_bank_without_caps():
+    """Both layouts through the row-group kernels: with unbounded factors each
+    expert's rows, their order and the row groups are the same, so are the
+    bits."""
+    cfg = PAIR_SMALL.with_(seed=48, cf_send=float("inf"), cf_recv=float("inf"))
+    inp = wl.make_inputs(cfg, "cpu")
+    a = PooledWaveMoE(cfg, inp, "cuda")
+    b = PooledWaveMoE(cfg, inp, "cuda", dropless=True)
+    assert a.bank is not None and b.bank is not None
+    x = inp["x"].cuda()
+    a.forward(x)
+    b.forward(x)
+    torch.cuda.synchronize()
+    assert a.drop_stats()["kept"] == cfg.T * cfg.top_k
+    assert torch.equal(a.c.view(torch.int16), b.c.view(torch.int16))
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
