@@ -87,7 +87,14 @@ LONG = FULL.with_(name="long", T=65536, seed=3, x_kind="ar1", n_seqs=1)
 # device memory, small enough for multi-pass profiler captures.
 SLICE = FULL.with_(name="full_slice", T=4096, n_experts=96, n_ranks=16, seed=4, n_seqs=1)
 
-CONFIGS = {c.name: c for c in (TINY, MID, FULL, SKEW, LONG, SLICE)}
+# The full layer's routing (T=16384, 384 experts on 64 ranks, top-8, three
+# waves, the same capacity factors) at narrow widths (d=512, L=256, H=128):
+# the router top-k, dispatch and combine kernels see the full routing's
+# shapes and launch sizes on a few hundred MB of device memory.
+ROUTE_SLICE = FULL.with_(name="route_slice", d_model=512, d_latent=256, h_expert=128,
+                         h_shared=128, seed=5)
+
+CONFIGS = {c.name: c for c in (TINY, MID, FULL, SKEW, LONG, SLICE, ROUTE_SLICE)}
 
 # Inputs with fewer elements than this are drawn on the host (so CPU-only and
 # GPU test runs see identical values); larger ones are drawn on the target
