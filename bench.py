@@ -466,6 +466,20 @@ def run_gb300(args, rank, world, local_rank):
                         "frac": round(gbs / pk["hbm"], 4),
                         "floor_ms": round(sb / pk["hbm"] * 1e3, 4)}
         kernels[name] = e
+    # the grouped expert FFN as a whole: both products of every expert
+    expert_ffn = None
+    gu, dn = kernels.get("gemm_expert_gateup", {}), kernels.get("gemm_expert_down", {})
+    if "work_per_launch" in gu and "work_per_launch" in dn:
+        w_ffn = gu["work_per_launch"] + dn["work_per_launch"]
+        ms_ffn = gu["ms_per_launch"] + dn["ms_per_launch"]
+        ach = w_ffn / (ms_ffn / 1e3)
+        expert_ffn = {"ms": round(ms_ffn, 4), "work": w_ffn, "unit": "TFLOP/s",
+                      "achieved": round(ach, 2), "frac": round(ach / tensor_peak, 4),
+                      "peak_source": pk["source"] + f" {tensor_state} bf16"}
+        if "hbm" in gu and "hbm" in dn:
+            gb = gu["hbm"]["bytes_per_launch_gb"] + dn["hbm"]["bytes_per_launch_gb"]
+            expert_ffn["hbm"] = {"bytes_gb": round(gb, 4),
+                                 "frac": round(gb / (ms_ffn / 1e3) / pk["hbm"], 4)}
     top = next(iter(kernels))
     twork, tunit, tbound = kernel_work(top, cfg, m.plan, st, pipeline, sent_w0)
     # DRAM bytes per launch from the committed ncu record, where it was taken
@@ -788,7 +802,8 @@ def run_gb300(args, rank, world, local_rank):
                       "dropped_recv": st["dropped_recv"],
                       "drop_rate": (st["dropped_send"] + st["dropped_recv"]) / max(1, st["assignments"])},
             "gpu_launches": sum(v[1] for v in per.values()),
-            "roofline": roof, "kernels": kernels, "clocks": clk, "e2e": e2e,
+            "roofline": roof, "kernels": kernels, "expert_ffn": expert_ffn, "clocks": clk,
+            "e2e": e2e,
             "graph_replay": graph, "pipelines": pipes, "dropless": dropless, "train_step": train,
             "workloads": others,
             "cpu_baseline": cpu,

@@ -388,8 +388,9 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
 // 128 weight rows are 128 output features; lanes pair adjacent features by a
 // shuffle into 32-bit stores to each row's output row (its pool row, or its
 // row of the per-expert layout).  The backward's products read their weights
-// MN-major (stored [K, M]), dX's K in two segments (gate, then up).  Eight
-// epilogue warps, two a lane quarter, take alternate 32-column blocks.
+// MN-major (stored [K, M]), dX's K in two segments (gate, then up).  Sixteen
+// epilogue warps, four a lane quarter, take every fourth 32-column block, so
+// the columns the next tile needs drain in a quarter of the blocks' time.
 constexpr int GACC = 416;                      // most rows (accumulator columns) a group
 constexpr int GB_BYTES = GACC / 2 * XBK * 2;   // this CTA's rows a stage: at most 208
 constexpr int GSTAGE = XA_BYTES + GB_BYTES;    // 42 KB
@@ -400,8 +401,10 @@ constexpr int GST = MOE_XGATE_STAGES;
 constexpr int GBAR_BYTES = ((2 * GST + 7) * 8 + 2 * 4 + 63) / 64 * 64;
 constexpr int GSMEM = 1024 + GST * GSTAGE + GBAR_BYTES;
 static_assert(GSMEM <= 232448, "shared memory budget");
-constexpr int GEPI_WARPS = 8;
-constexpr int GMAXB = (GACC / 32 + 2) / 2;      // most 32-column blocks a warp drains a tile
+constexpr int GEPI_WARPS = 16;                    // epilogue warps, GEPQ a TMEM lane quarter
+constexpr int GEPQ = GEPI_WARPS / 4;
+static_assert(GEPI_WARPS % 4 == 0, "whole lane quarters");
+constexpr int GMAXB = (GACC / 32 + GEPQ - 1) / GEPQ;   // most 32-column blocks a warp drains a tile
 constexpr int GTHREADS = 128 + 32 * GEPI_WARPS;
 
 struct GParams {
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 4;
         const int q = ew & 3;                     // TMEM lane quarter (= warp % 4)
-        const int grp = ew >> 2;                  // order positions grp, grp + 2, ...
+        const int grp = ew >> 2;                  // order positions grp, grp + GEPQ, ...
         const bool hi = lane >= 16;               // lanes of the higher-addressed tensor
         const int y = lane & 15;
         const bool odd = (y & 1) != 0;
@@ -672,7 +675,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     n_ov = end ? (hi_c - base + 31) >> 5                 // ascending: blocks below hi_c
                                : nblk - ((lo - base) >> 5);              // descending: blocks from lo up
             }
-            const int my_ov = n_ov > grp ? (n_ov - grp + 1) >> 1 : 0;
+            const int my_ov = n_ov > grp ? (n_ov - grp + GEPQ - 1) / GEPQ : 0;
             if (my_ov == 0) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                 int prow[GMAXB];
 #pragma unroll
                 for (int i = 0; i < GMAXB; ++i) {
-                    const int pos = grp + 2 * i;
+                    const int pos = grp + GEPQ * i;
                     const int b = end ? pos : nblk - 1 - pos;
                     const int rr = 32 * b + lane;
                     prow[i] = -1;
@@ -704,7 +707,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                 const bool fodd = (lane & 1) != 0;
 #pragma unroll
                 for (int i = 0; i < GMAXB; ++i) {
-                    const int pos = grp + 2 * i;
+                    const int pos = grp + GEPQ * i;
                     if (pos >= nblk) break;   // warp-uniform
                     const int b = end ? pos : nblk - 1 - pos;
                     uint32_t r[32];
@@ -752,7 +755,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
             uint16_t* hb = p.out + (t.rbase + t.row0) * p.ldo + unit;
             int drained = 0;
 #pragma unroll 1
-            for (int pos = grp; pos < nblk; pos += 2) {
+            for (int pos = grp; pos < nblk; pos += GEPQ) {
                 const int b = end ? pos : nblk - 1 - pos;
                 uint32_t r[32];
                 if (S - 32 * b >= 32) {
