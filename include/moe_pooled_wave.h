@@ -477,6 +477,12 @@ typedef struct moe_backward_args {
     int32_t* status;
     const int32_t* expert_offsets;   /* dropless layout: [E + 1], from moe_dispatch_ragged;
                                         NULL for the capped layout */
+    uint16_t* bank;                  /* capped layout, optional (NULL: not used): the
+                                        forward dispatch's per-expert bank [E, c_recv, L];
+                                        X is then read from it instead of copied out of
+                                        the pool rows (the same values), and its rows past
+                                        each expert's count are set to zero.  Ignored by
+                                        the dropless backward. */
 } moe_backward_args_t;
 
 int moe_backward_plan(const moe_config_t* cfg, moe_backward_ws_t* layout);
@@ -565,9 +571,10 @@ int moe_trace_event(int i, const char** name, float* ms_since_prev);
 /* Human-readable name of a MOE_* code (static string). */
 const char* moe_strerror(int code);
 
-/* ABI version: 4 (2: the optional per-expert bank of the dispatch and the
+/* ABI version: 5 (2: the optional per-expert bank of the dispatch and the
  * expert FFN; 3: the whole-layer forward and the host-memory pipeline; 4: the
- * optional bank of the dropless dispatch and expert FFN). */
+ * optional bank of the dropless dispatch and expert FFN; 5: the optional bank
+ * as the backward's source of X). */
 int moe_abi_version(void);
 
 #ifdef __cplusplus

@@ -82,7 +82,7 @@ BWD_ARG_FIELDS = ("x", "Wr", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Ws
 class BackwardArgs(ctypes.Structure):
     _fields_ = ([(f, ctypes.c_void_p) for f in BWD_ARG_FIELDS] +
                 [("ws_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p),
-                 ("expert_offsets", ctypes.c_void_p)])
+                 ("expert_offsets", ctypes.c_void_p), ("bank", ctypes.c_void_p)])
 
 LAYER_BUFFER_FIELDS = ("Wr", "bias", "W_ld", "Wg", "Wu", "Wd", "W_lu", "Wsg", "Wsu", "Wsd",
                        "logits", "idx", "w", "tie", "z", "ws_dispatch", "ws_dispatch_bytes",
@@ -473,6 +473,8 @@ def layer_backward(cfg, tensors: dict, ws, status, stream=None):
     args.status = status.data_ptr()
     eoff = tensors.get("expert_offsets")
     args.expert_offsets = None if eoff is None else eoff.data_ptr()
+    bank = tensors.get("bank")
+    args.bank = None if bank is None else bank.data_ptr()
     fn = "moe_layer_backward" if eoff is None else "moe_layer_backward_ragged"
     _check(fn, getattr(lib(), fn)(ctypes.byref(make_config(cfg)), ctypes.byref(args),
                                   _stream(stream)))

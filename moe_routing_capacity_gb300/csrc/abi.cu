@@ -204,7 +204,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 4; }
+int moe_abi_version(void) { return 5; }
 
 int moe_check_status(void) {
     const int v[4] = {check_status_route(), check_status_gemm(), check_status_backward(),
@@ -865,6 +865,7 @@ static int layer_backward(const Geom& G, const moe_backward_args_t* a, void* str
                           a->dWd, a->dW_lu, a->ws};
     for (const void* ptr : al16)
         if (!aligned16(ptr)) return MOE_EINVAL;
+    if (a->bank && !aligned16(a->bank)) return MOE_EINVAL;
     if (G.g.pool_rows == 0 || G.g.c_recv == 0) return MOE_EINVAL;
     const BackwardWs w = backward_ws_layout(G.g, G.d, G.H, G.Hs, G.ns);
     if (a->ws_bytes < w.total) return MOE_ENOSPC;

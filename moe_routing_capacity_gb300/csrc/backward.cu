@@ -450,14 +450,23 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     } else if (rc) {
         return rc;
     }
-    // Capped layout: the per-expert contiguous, zero-padded copy of X (which
+    // Capped layout: X in per-expert contiguous rows with zero padding (which
     // the weight gradients contract over) and h's unwritten rows zeroed, made
-    // first, so that the SwiGLU backward can read X as whole TMA tiles.
+    // first, so that the SwiGLU backward can read X as whole TMA tiles.  X
+    // is the forward's bank when the caller passes it (its kept rows are the
+    // pool rows' payloads; only its padding rows need zeroing), else a copy
+    // gathered from the pool rows.
     bool grouped = false;
     if (!rag) {
         const int64_t nw = static_cast<int64_t>(E) * cr;
         const unsigned grid = static_cast<unsigned>((nw + 7) / 8);
-        gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, a.expert_count, E, cr, L, xe);
+        if (a.bank) {
+            xe = a.bank;
+            zero_pad_rows_kernel<<<grid, 256, 0, st>>>(xe, a.expert_count, E, cr, L);
+        } else {
+            gather_expert_rows_kernel<<<grid, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows,
+                                                            a.expert_count, E, cr, L, xe);
+        }
         zero_pad_rows_kernel<<<grid, 256, 0, st>>>(a.h, a.expert_count, E, cr, H);
         if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
         trace_after(st, "bwd_gather_rows");

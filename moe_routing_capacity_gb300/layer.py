@@ -215,7 +215,8 @@ class PooledWaveMoE:
                        dW_ld=g["W_ld"], dWg=g["Wg"], dWu=g["Wu"], dWd=g["Wd"], dW_lu=g["W_lu"],
                        dWsg=g["Wsg"] if ns else None, dWsu=g["Wsu"] if ns else None,
                        dWsd=g["Wsd"] if ns else None,
-                       expert_offsets=self.expert_offsets if self.dropless else None)
+                       expert_offsets=self.expert_offsets if self.dropless else None,
+                       bank=None if self.dropless else self.bank)
         abi.layer_backward(cfg, tensors, self.bwd_ws, self.status, stream)
         return g
 

@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     L = abi.lib()
     for name in _declared():
         assert hasattr(L, name), name
-    assert L.moe_abi_version() == 4
+    assert L.moe_abi_version() == 5
 
 
 def test_every_export_declares_its_signature():
@@ -78,6 +78,38 @@ def test_struct_sizes():
     assert ctypes.sizeof(abi.Plan) == 64
     assert ctypes.sizeof(abi.DropStats) == 48
     assert abi.STATS_WORDS == 6
+
+
+def _c_layout(struct, fields, tmp_path):
+    """sizeof and each field's offset of a header struct, from a C program
+    compiled against the header."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe_pooled_wave.h"',
+             "int main(void) {", f'  printf("%zu\\n", sizeof({struct}));']
+    lines += [f'  printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    lines += ["  return 0;", "}"]
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    return vals[0], vals[1:]
+
+
+@pytest.mark.parametrize("struct,cls", [("moe_backward_args_t", abi.BackwardArgs),
+                                        ("moe_layer_buffers_t", abi.LayerBuffers)])
+def test_struct_mirrors_match_header(struct, cls, tmp_path):
+    """The binding's ctypes mirrors of the argument structs have the header's
+    size and field offsets, field by field."""
+    names = [f for f, _ in cls._fields_]
+    size, offs = _c_layout(struct, names, tmp_path)
+    assert ctypes.sizeof(cls) == size
+    assert [getattr(cls, f).offset for f in names] == offs
 
 
 def test_strerror_names_every_code():

@@ -111,3 +111,36 @@ def test_same_tensor_for_gate_and_up():
     kept = m.slot_of[m.slot_of >= 0].long()
     assert torch.equal(m.ypool[kept].view(torch.int16), b.ypool[kept].view(torch.int16))
     print(rep)
+
+
+def _train_grads(cfg, inp, bank, pipeline):
+    from moe_routing_capacity_gb300.layer import PooledWaveMoE
+    m = PooledWaveMoE(cfg, inp, "cuda", pipeline=pipeline, expert_bank=bank)
+    x = inp["x"].cuda()
+    m.forward(x)
+    g = torch.Generator().manual_seed(11)
+    dout = torch.randn(cfg.T, cfg.d_model, generator=g).to(torch.bfloat16).cuda()
+    grads = m.backward(x, dout)
+    torch.cuda.synchronize()
+    assert int(m.status.item()) == 0
+    return m, {k: v.clone() for k, v in grads.items()}
+
+
+@pytest.mark.parametrize("kind", ["uniform", "skew"])
+def test_backward_reads_x_from_the_bank(kind):
+    """The backward with the forward's bank as its X (only the padding rows
+    zeroed) gives the gradients of the one that copies X out of the pool
+    rows, bit for bit; the bank's kept rows are left as the forward wrote
+    them and its padding rows are zero."""
+    cfg, inp = _inputs(kind)
+    mb, ga = _train_grads(cfg, inp, True, "shared")
+    _, gb = _train_grads(cfg, inp, False, None)
+    for k in ga:
+        w = torch.int32 if ga[k].dtype == torch.float32 else torch.int16
+        assert torch.equal(ga[k].view(w), gb[k].view(w)), k
+    _bank_matches_pool(mb, cfg)
+    cnt = mb.expert_count.long()
+    r_idx = torch.arange(mb.bank.shape[1], device=cnt.device)[None, :]
+    pad = r_idx >= cnt[:, None]
+    assert int(pad.sum()) > 0
+    assert (mb.bank.view(torch.int16)[pad] == 0).all()
