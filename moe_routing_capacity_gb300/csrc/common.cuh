@@ -82,6 +82,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrival on this CTA's mbarrier without release semantics (the same use as
+// mbar_arrive_cluster_relaxed below).
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -374,8 +381,13 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // One arrival on an mbarrier given by its cluster address (possibly the peer's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+// Arrival on an mbarrier of either CTA of the pair, without release
+// semantics: the barriers it serves only hand over TMEM columns this thread
+// has finished reading (tcgen05.wait::ld done), so the arrival need not wait
+// for the thread's earlier global stores to become visible (a release
+// arrival measured 8 % slower on the expert down product for that wait).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 

@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(256, 1) expert_pair_kernel(const __grid_consta
                 }
             }
             tc_fence_before();
-            mbar_arrive_cluster(tempty_c0 + acc * 8u);
+            mbar_arrive_cluster_relaxed(tempty_c0 + acc * 8u);
             if (++acc == 2) {
                 acc = 0;
                 acc_ph ^= 1u;
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
             const int my_ov = n_ov > grp ? (n_ov - grp + GEPQ - 1) / GEPQ : 0;
             if (my_ov == 0) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
+                if (lane == 0) mbar_arrive_cluster_relaxed(bar_c0 + end * 8u);
             }
             const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                 static_cast<uint32_t>(base);
@@ -725,7 +725,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     if (i + 1 == my_ov) {   // this warp's share of the overlap is out of TMEM
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
+                        if (lane == 0) mbar_arrive_cluster_relaxed(bar_c0 + end * 8u);
                     }
                     // pairs of features to 32-bit stores: even lanes rows 0-15,
                     // odd lanes rows 16-31 of the block
@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(fdone_c0 + end * 8u);
+                if (lane == 0) mbar_arrive_cluster_relaxed(fdone_c0 + end * 8u);
                 continue;
             }
             if (!mbar_wait(&tfull[end], static_cast<uint32_t>(k >> 1) & 1u, abort_flag, p.status))
@@ -772,7 +772,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                 if (++drained == my_ov) {   // this warp's share of the overlap is out of TMEM
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(bar_c0 + end * 8u);
+                    if (lane == 0) mbar_arrive_cluster_relaxed(bar_c0 + end * 8u);
                 }
                 if (EPI == EPI_SWIGLU_BWD) {
                     // recomputed g, u of this lane's unit for rows 0-15 (lanes < 16)
@@ -850,7 +850,7 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(fdone_c0 + end * 8u);
+            if (lane == 0) mbar_arrive_cluster_relaxed(fdone_c0 + end * 8u);
         }
     }
 

@@ -879,11 +879,13 @@ __global__ void __launch_bounds__(AMODE == A_GATHER ? 512 : 384, 1)
                     }
                 }
             }
+            // the accumulator's columns are read (tcgen05.wait::ld): hand them
+            // back without waiting for this tile's stores to be visible
             tc_fence_before();
             if constexpr (CG2)
-                mbar_arrive_cluster(tempty_c0 + acc * 8u);
+                mbar_arrive_cluster_relaxed(tempty_c0 + acc * 8u);
             else
-                mbar_arrive(&tempty[acc]);
+                mbar_arrive_relaxed(&tempty[acc]);
             if (++acc == C::NACC) {
                 acc = 0;
                 acc_phase ^= 1u;
