@@ -663,7 +663,10 @@ def run_gb300(args, rank, world, local_rank):
     # ---- the dropless ragged variant on the same batch: the cost of removing drops
     dropless = None
     if not args.no_dropless:
-        md = PooledWaveMoE(cfg, inp, dev, dropless=True)
+        # the same pool-fill schedule as the main line (the wave pipeline is
+        # built for the capped layout only)
+        dpipe = "shared" if pipeline == "shared" else None
+        md = PooledWaveMoE(cfg, inp, dev, dropless=True, pipeline=dpipe)
         for _ in range(args.warmup):
             md.forward(x)
         torch.cuda.synchronize()
@@ -686,7 +689,7 @@ def run_gb300(args, rank, world, local_rank):
                 dper.setdefault(name, []).append(ms)
         dst = md.drop_stats()
         dropless = {"value": world * cfg.T / (dms / 1e3), "unit": UNIT, "ms_per_step": dms,
-                    "steps": nd, "pool_rows": md.plan.pool_rows,
+                    "steps": nd, "pool_rows": md.plan.pool_rows, "pool_fill": dpipe or "none",
                     "kept": dst["kept"], "capped_kept": st["kept"],
                     "expert_ffn_ms": round(sum(sum(v) for k2, v in dper.items()
                                                if k2.startswith("gemm_expert")) / nd, 4)}

@@ -262,6 +262,23 @@ int moe_dispatch_ragged(const moe_config_t* cfg, const uint16_t* z, const int32_
                         uint8_t* drop, int32_t* expert_offsets, int32_t* expert_rows,
                         int32_t* expert_count, moe_drop_stats_t* stats, uint16_t* bank,
                         void* stream);
+/* moe_dispatch_ragged overlapped with the shared experts, as
+ * moe_dispatch_shared_overlap does for the capped layout: the same outputs,
+ * bit for bit, as moe_dispatch_ragged (the optional bank included) followed
+ * by moe_combine's shared step, which writes a [T, n_s*Hs]; the sender
+ * stage, the receiver counts and the ragged offsets run as kernels of their
+ * own, the final decisions, row lists, payload rows and tags (and the
+ * bank's rows) in four extra warps per CTA of the shared gate/up launch.
+ * Pass Wsg = Wsu = NULL to moe_combine afterwards.  With n_s = 0 or no
+ * tokens it is moe_dispatch_ragged. */
+int moe_dispatch_ragged_shared_overlap(const moe_config_t* cfg, const uint16_t* z,
+                                       const int32_t* idx, void* ws, size_t ws_bytes,
+                                       uint16_t* pool, int32_t* slot_of, uint8_t* drop,
+                                       int32_t* expert_offsets, int32_t* expert_rows,
+                                       int32_t* expert_count, moe_drop_stats_t* stats,
+                                       uint16_t* bank, const uint16_t* x, const uint16_t* Wsg,
+                                       const uint16_t* Wsu, uint16_t* a, int32_t* status,
+                                       void* stream);
 int moe_expert_ffn_ragged(const moe_config_t* cfg, const uint16_t* pool, const uint16_t* bank,
                           const int32_t* expert_offsets, const int32_t* expert_rows,
                           const int32_t* expert_count, const uint16_t* Wg, const uint16_t* Wu,
@@ -571,10 +588,11 @@ int moe_trace_event(int i, const char** name, float* ms_since_prev);
 /* Human-readable name of a MOE_* code (static string). */
 const char* moe_strerror(int code);
 
-/* ABI version: 5 (2: the optional per-expert bank of the dispatch and the
+/* ABI version: 6 (2: the optional per-expert bank of the dispatch and the
  * expert FFN; 3: the whole-layer forward and the host-memory pipeline; 4: the
  * optional bank of the dropless dispatch and expert FFN; 5: the optional bank
- * as the backward's source of X). */
+ * as the backward's source of X; 6: the dropless dispatch overlapped with the
+ * shared experts). */
 int moe_abi_version(void);
 
 #ifdef __cplusplus

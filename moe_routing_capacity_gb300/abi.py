@@ -23,7 +23,8 @@ EXPORTS = ("moe_plan", "moe_router_topk", "moe_latent_proj", "moe_route_project"
            "moe_dispatch_pooled",
            "moe_dispatch_pooled_noalloc", "moe_expert_ffn_grouped", "moe_dispatch_expert_waves",
            "moe_dispatch_shared_overlap", "moe_balance_update", "moe_balance_update_window",
-           "moe_plan_ragged", "moe_dispatch_ragged", "moe_expert_ffn_ragged",
+           "moe_plan_ragged", "moe_dispatch_ragged", "moe_dispatch_ragged_shared_overlap",
+           "moe_expert_ffn_ragged",
            "moe_backward_plan", "moe_layer_backward", "moe_backward_plan_ragged",
            "moe_layer_backward_ragged", "moe_combine", "moe_trace_begin", "moe_trace_mark",
            "moe_trace_end", "moe_trace_event", "moe_check_status", "moe_strerror",
@@ -132,6 +133,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.moe_balance_update_window.argtypes = [pc, vp, vp, vp, i32, vp, ctypes.c_float, vp, vp]
     L.moe_plan_ragged.argtypes = [pc, ctypes.POINTER(Plan)]
     L.moe_dispatch_ragged.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_ragged_shared_overlap.argtypes = [pc, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp,
+                                                     vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_expert_ffn_ragged.argtypes = [pc, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.moe_backward_plan.argtypes = [pc, ctypes.POINTER(BackwardWs)]
     L.moe_layer_backward.argtypes = [pc, ctypes.POINTER(BackwardArgs), vp]
@@ -321,6 +324,21 @@ def dispatch_ragged(cfg, z, idx, ws, pool, slot_of, drop, expert_offsets, expert
         ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
         _ptr(expert_offsets, i32), _ptr(expert_rows, i32), _ptr(expert_count, i32),
         _ptr(stats, torch.int64), _ptr(bank, bf16, allow_none=True), _stream(stream)))
+
+
+def dispatch_ragged_shared_overlap(cfg, z, idx, ws, pool, slot_of, drop, expert_offsets,
+                                   expert_rows, expert_count, stats, x, Wsg, Wsu, a, status,
+                                   stream=None, bank=None):
+    """dispatch_ragged plus the shared experts' activations a, the pack run
+    inside the shared gate/up product; then call combine with Wsg = Wsu = None."""
+    _check("moe_dispatch_ragged_shared_overlap", lib().moe_dispatch_ragged_shared_overlap(
+        ctypes.byref(make_config(cfg)), _ptr(z, bf16), _ptr(idx, i32), _ptr(ws, u8),
+        ws.numel(), _ptr(pool, torch.int16), _ptr(slot_of, i32), _ptr(drop, u8),
+        _ptr(expert_offsets, i32), _ptr(expert_rows, i32), _ptr(expert_count, i32),
+        _ptr(stats, torch.int64), _ptr(bank, bf16, allow_none=True),
+        _ptr(x, bf16, allow_none=True), _ptr(Wsg, bf16, allow_none=True),
+        _ptr(Wsu, bf16, allow_none=True), _ptr(a, bf16, allow_none=True), _ptr(status, i32),
+        _stream(stream)))
 
 
 def expert_ffn_ragged(cfg, pool, expert_offsets, expert_rows, expert_count, Wg, Wu, Wd, ws,

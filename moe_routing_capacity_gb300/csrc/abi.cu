@@ -204,7 +204,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 5; }
+int moe_abi_version(void) { return 6; }
 
 int moe_check_status(void) {
     const int v[4] = {check_status_route(), check_status_gemm(), check_status_backward(),
@@ -722,6 +722,73 @@ int moe_dispatch_expert_waves(const moe_config_t* cfg, const uint16_t* z, const 
                              status, st, pipe ? &wp : nullptr);
 }
 
+}  // extern "C"
+
+// The shared experts' gate/up; with pack, its extra warps also carry the
+// dispatch's pack (final decisions, row lists, copies, tags) of the layout
+// g describes.
+static int shared_gateup(const Geom& G, const PackArgs* pack, const uint16_t* x,
+                         const uint16_t* Wsg, const uint16_t* Wsu, uint16_t* a, int32_t* status,
+                         cudaStream_t st) {
+    const DispatchGeom& g = G.g;
+    const int d = G.d, hs_all = G.ns * G.Hs;
+    GemmDesc s1;
+    std::memset(&s1, 0, sizeof(s1));
+    s1.a_mode = A_DENSE;
+    s1.epi = EPI_SWIGLU;
+    s1.bn = 256;
+    s1.M = g.T;
+    s1.N = hs_all;
+    s1.nseg = 1;
+    s1.seg[0] = GemmSeg{x, d, Wsg, d, d};
+    s1.B_up = Wsu;
+    s1.b_rows = hs_all;
+    s1.out = a;
+    s1.ldo = hs_all;
+    s1.status = status;
+    s1.name = "gemm_shared_gateup";
+    if (pack) {
+        s1.wp_g = g;
+        s1.wp_a = *pack;
+    }
+    return gemm_launch(s1, st);
+}
+
+static PackArgs pack_args(const DispatchGeom& g, void* ws, const uint16_t* z, const int32_t* idx,
+                          uint16_t* pool, int32_t* slot_of, uint8_t* drop, int32_t* expert_rows,
+                          const int32_t* expert_offsets, uint16_t* bank) {
+    const DispatchWs Lw = dispatch_ws_layout(g);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    PackArgs P;
+    std::memset(&P, 0, sizeof(P));
+    P.z = z;
+    P.idx = idx;
+    P.send_row = reinterpret_cast<const int64_t*>(w + Lw.send_row_off);
+    P.rloc = reinterpret_cast<const int32_t*>(w + Lw.rloc_off);
+    P.base_se = reinterpret_cast<const int32_t*>(w + Lw.base_se_off);
+    P.pool = pool;
+    P.slot_of = slot_of;
+    P.drop = drop;
+    P.expert_rows = expert_rows;
+    if (g.ragged) {
+        P.blk_off = reinterpret_cast<const int32_t*>(w + Lw.blk_off_off);
+        P.eoff = expert_offsets;
+    }
+    P.bank = bank;
+    return P;
+}
+
+static int check_shared_args(const Geom& G, const uint16_t* x, const uint16_t* Wsg,
+                             const uint16_t* Wsu, const uint16_t* a) {
+    if (G.ns > 0 && G.g.T > 0 &&
+        (!x || !Wsg || !Wsu || !a || !aligned16(x) || !aligned16(Wsg) || !aligned16(Wsu) ||
+         !aligned16(a)))
+        return MOE_EINVAL;
+    return MOE_OK;
+}
+
+extern "C" {
+
 int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, const int32_t* idx,
                                 void* ws, size_t ws_bytes, uint16_t* pool, int32_t* slot_of,
                                 uint8_t* drop, int32_t* expert_rows, int32_t* expert_count,
@@ -741,11 +808,7 @@ int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, cons
     if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || (ws && !aligned16(ws)))
         return MOE_EINVAL;
     if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
-    const int d = G.d, hs_all = G.ns * G.Hs;
-    if (G.ns > 0 && g.T > 0 &&
-        (!x || !Wsg || !Wsu || !a || !aligned16(x) || !aligned16(Wsg) || !aligned16(Wsu) ||
-         !aligned16(a)))
-        return MOE_EINVAL;
+    if ((rc = check_shared_args(G, x, Wsg, Wsu, a))) return rc;
     int dev, sms;
     if ((rc = current_device(&dev, &sms))) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -755,37 +818,42 @@ int moe_dispatch_shared_overlap(const moe_config_t* cfg, const uint16_t* z, cons
                               st, -1, !overlap, bank)))
         return rc;
     if (G.ns == 0 || g.T == 0) return MOE_OK;
-    const DispatchWs Lw = dispatch_ws_layout(g);
-    GemmDesc s1;
-    std::memset(&s1, 0, sizeof(s1));
-    s1.a_mode = A_DENSE;
-    s1.epi = EPI_SWIGLU;
-    s1.bn = 256;
-    s1.M = g.T;
-    s1.N = hs_all;
-    s1.nseg = 1;
-    s1.seg[0] = GemmSeg{x, d, Wsg, d, d};
-    s1.B_up = Wsu;
-    s1.b_rows = hs_all;
-    s1.out = a;
-    s1.ldo = hs_all;
-    s1.status = status;
-    s1.name = "gemm_shared_gateup";
-    if (overlap) {   // the whole pack: final decisions, row lists, copies, tags
-        uint8_t* w = static_cast<uint8_t*>(ws);
-        s1.wp_g = g;
-        s1.wp_a.z = z;
-        s1.wp_a.idx = idx;
-        s1.wp_a.send_row = reinterpret_cast<const int64_t*>(w + Lw.send_row_off);
-        s1.wp_a.rloc = reinterpret_cast<const int32_t*>(w + Lw.rloc_off);
-        s1.wp_a.base_se = reinterpret_cast<const int32_t*>(w + Lw.base_se_off);
-        s1.wp_a.pool = pool;
-        s1.wp_a.slot_of = slot_of;
-        s1.wp_a.drop = drop;
-        s1.wp_a.expert_rows = expert_rows;
-        s1.wp_a.bank = bank;
-    }
-    return gemm_launch(s1, st);
+    const PackArgs P = pack_args(g, ws, z, idx, pool, slot_of, drop, expert_rows, nullptr, bank);
+    return shared_gateup(G, overlap ? &P : nullptr, x, Wsg, Wsu, a, status, st);
+}
+
+int moe_dispatch_ragged_shared_overlap(const moe_config_t* cfg, const uint16_t* z,
+                                       const int32_t* idx, void* ws, size_t ws_bytes,
+                                       uint16_t* pool, int32_t* slot_of, uint8_t* drop,
+                                       int32_t* expert_offsets, int32_t* expert_rows,
+                                       int32_t* expert_count, moe_drop_stats_t* stats,
+                                       uint16_t* bank, const uint16_t* x, const uint16_t* Wsg,
+                                       const uint16_t* Wsu, uint16_t* a, int32_t* status,
+                                       void* stream) {
+    MOE_NVTX_RANGE();
+    Geom G;
+    int rc = make_geom_ragged(cfg, &G);
+    if (rc) return rc;
+    const DispatchGeom& g = G.g;
+    if (!stats || !expert_count || !expert_offsets || !ws || !status ||
+        (g.T > 0 && (!z || !idx || !slot_of || !drop || !pool || !expert_rows)))
+        return MOE_EINVAL;
+    if ((z && !aligned16(z)) || (pool && !aligned16(pool)) || !aligned16(ws) ||
+        (bank && (!aligned16(bank) || g.L % 8)))
+        return MOE_EINVAL;
+    if (ws_bytes < static_cast<size_t>(G.plan.ws_dispatch_bytes)) return MOE_ENOSPC;
+    if ((rc = check_shared_args(G, x, Wsg, Wsu, a))) return rc;
+    int dev, sms;
+    if ((rc = current_device(&dev, &sms))) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool overlap = G.ns > 0 && g.T > 0;
+    if ((rc = launch_dispatch_ragged(g, z, idx, ws, pool, slot_of, drop, expert_offsets,
+                                     expert_rows, expert_count, stats, bank, st, !overlap)))
+        return rc;
+    if (G.ns == 0 || g.T == 0) return MOE_OK;
+    const PackArgs P =
+        pack_args(g, ws, z, idx, pool, slot_of, drop, expert_rows, expert_offsets, bank);
+    return shared_gateup(G, &P, x, Wsg, Wsu, a, status, st);
 }
 
 int moe_balance_update(const moe_config_t* cfg, const int32_t* idx, int64_t* hist, float alpha,

@@ -1280,7 +1280,10 @@ int gemm_launch(const GemmDesc& d, cudaStream_t st) {
     if (d.epi == EPI_SWIGLU_BWD) p.out2 = d.out2;
     if (d.wp_a.pool) {   // the dispatch's pack rides along (waves pipeline or dense overlap)
         const DispatchGeom& g = d.wp_g;
-        if (!d.wp_a.z || !d.wp_a.idx || !d.wp_a.send_row || g.ragged || g.k < 1 || g.k > 32 ||
+        // the dropless layout rides along only with the dense overlap, with
+        // its block and expert offsets
+        if (g.ragged && (d.wp_ready || !d.wp_a.blk_off || !d.wp_a.eoff)) return MOE_EINVAL;
+        if (!d.wp_a.z || !d.wp_a.idx || !d.wp_a.send_row || g.k < 1 || g.k > 32 ||
             g.W < 1 || g.W > 32 || g.E_w < 1 || g.E_l != g.E_w * g.W || g.E % g.E_l || g.L < 8 ||
             g.L % 8 || (reinterpret_cast<uintptr_t>(d.wp_a.z) & 15) ||
             (reinterpret_cast<uintptr_t>(d.wp_a.pool) & 15))

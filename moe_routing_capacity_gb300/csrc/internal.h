@@ -177,11 +177,13 @@ int launch_dispatch(const DispatchGeom& g, const uint16_t* z, const int32_t* idx
                     int copy_wave = -1, bool run_pack = true, uint16_t* bank = nullptr);
 
 // bank (optional): [T*k, L], each row also written at its position in the
-// flat expert row list.
+// flat expert row list.  run_pack = false stops after the offsets (the pack
+// then runs inside the shared experts' gate/up launch).
 int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                            uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                            int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
-                           moe_drop_stats_t* stats, uint16_t* bank, cudaStream_t stream);
+                           moe_drop_stats_t* stats, uint16_t* bank, cudaStream_t stream,
+                           bool run_pack = true);
 
 // The capped layout's expert FFN on CTA pairs with the expert's rows on the
 // MMA's N axis (expert_pair.cu): chunk list, gate/up from the per-expert

@@ -567,7 +567,8 @@ __global__ void __launch_bounds__(1024) ragged_offsets_kernel(DispatchGeom g,
 int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32_t* idx, void* ws,
                            uint16_t* pool, int32_t* slot_of, uint8_t* drop,
                            int32_t* expert_offsets, int32_t* expert_rows, int32_t* expert_count,
-                           moe_drop_stats_t* stats, uint16_t* bank, cudaStream_t st) {
+                           moe_drop_stats_t* stats, uint16_t* bank, cudaStream_t st,
+                           bool run_pack) {
     const DispatchWs L = dispatch_ws_layout(g);
     uint8_t* w = static_cast<uint8_t*>(ws);
     int64_t* send_row = reinterpret_cast<int64_t*>(w + L.send_row_off);
@@ -599,7 +600,7 @@ int launch_dispatch_ragged(const DispatchGeom& g, const uint16_t* z, const int32
     ragged_offsets_kernel<<<1, 1024, 0, st>>>(g, demand, expert_count, blk_off, expert_offsets);
     if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
     trace_after(st, "ragged_offsets");
-    if (g.T == 0) return MOE_OK;
+    if (g.T == 0 || !run_pack) return MOE_OK;
     const unsigned grid = static_cast<unsigned>((g.T + 7) / 8);
     if (g.L / 8 <= 32 * 4)
         dispatch_pack_kernel<4><<<grid, 256, 0, st>>>(g, z, idx, send_row, rloc, base_se, pool,

@@ -9,8 +9,9 @@ once through PyTorch's caching allocator) and runs the layer as
 (``pipeline="waves"``: the middle two are the single wave-pipelined call
 moe_dispatch_expert_waves; ``pipeline="shared"``: moe_dispatch_shared_overlap
 copies the pool rows while the shared experts' gate/up runs, then
-moe_expert_ffn_grouped and moe_combine with the shared activations given;
-same results either way)
+moe_expert_ffn_grouped and moe_combine with the shared activations given,
+moe_dispatch_ragged_shared_overlap likewise for the dropless layout; same
+results either way)
 
 on one CUDA stream, with no host synchronisation, so the whole forward can be
 captured in a CUDA graph.  Intermediates stay readable as attributes.
@@ -29,9 +30,9 @@ class PooledWaveMoE:
     next batch on; with ``balance_window`` = N the histogram spans exactly
     the past N batches.  ``pipeline``: None (the calls one after another),
     "waves" (dispatch and experts as one wave-pipelined call: the later
-    waves' pool rows copied while wave 0's experts run) or "shared" (the
-    pool rows copied while the shared experts' gate/up runs); the capped
-    layout only.  ``expert_bank``: the dispatch also writes the received
+    waves' pool rows copied while wave 0's experts run; capped layout only)
+    or "shared" (the pool rows copied while the shared experts' gate/up
+    runs; either layout).  ``expert_bank``: the dispatch also writes the received
     rows grouped by expert (``self.bank``: [E, c_recv, L] capped, [T*k, L]
     dropless in the flat row list's order), from which the expert products
     load whole tiles (either layout, except the "waves" pipeline); False
@@ -45,8 +46,8 @@ class PooledWaveMoE:
         self.dropless = dropless
         if pipeline not in self.PIPELINES:
             raise ValueError(f"pipeline must be one of {self.PIPELINES}")
-        if pipeline and dropless:
-            raise ValueError("the overlapped dispatch is built for the capped layout")
+        if pipeline == "waves" and dropless:
+            raise ValueError("the wave pipeline is built for the capped layout")
         self.pipeline = pipeline
         self.plan = abi.plan_ragged(cfg) if dropless else abi.plan(cfg)
         self.device = torch.device(device)
@@ -152,11 +153,18 @@ class PooledWaveMoE:
                                       self.w["Wd"], self.ws_ffn, self.ypool, self.status, stream)
             self.combine(x, out, stream)
         elif self.pipeline == "shared" and self.cfg.n_shared:
-            abi.dispatch_shared_overlap(self.cfg, self.z, self.idx, self.ws_dispatch, self.pool,
-                                        self.slot_of, self.drop, self.expert_rows,
-                                        self.expert_count, self.stats, x, self.w["Wsg"],
-                                        self.w["Wsu"], self.a, self.status, stream,
-                                        bank=self.bank)
+            if self.dropless:
+                abi.dispatch_ragged_shared_overlap(
+                    self.cfg, self.z, self.idx, self.ws_dispatch, self.pool, self.slot_of,
+                    self.drop, self.expert_offsets, self.expert_rows, self.expert_count,
+                    self.stats, x, self.w["Wsg"], self.w["Wsu"], self.a, self.status, stream,
+                    bank=self.bank)
+            else:
+                abi.dispatch_shared_overlap(self.cfg, self.z, self.idx, self.ws_dispatch,
+                                            self.pool, self.slot_of, self.drop, self.expert_rows,
+                                            self.expert_count, self.stats, x, self.w["Wsg"],
+                                            self.w["Wsu"], self.a, self.status, stream,
+                                            bank=self.bank)
             self.experts(stream)
             abi.combine(self.cfg, self.ypool, self.slot_of, self.gate_w, self.w["W_lu"], None,
                         None, None, self.w["Wsd"], self.c, self.a,

@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     L = abi.lib()
     for name in _declared():
         assert hasattr(L, name), name
-    assert L.moe_abi_version() == 5
+    assert L.moe_abi_version() == 6
 
 
 def test_every_export_declares_its_signature():

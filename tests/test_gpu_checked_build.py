@@ -62,13 +62,14 @@ def test_checked_build_clean_and_identical(checked_lib, name, dropless):
         assert torch.equal(a, b), key
 
 
-@pytest.mark.parametrize("pipeline", ["waves", "shared"])
+@pytest.mark.parametrize("pipeline,dropless", [("waves", False), ("shared", False),
+                                               ("shared", True)])
 @pytest.mark.parametrize("name", ["tiny", "mid"])
-def test_checked_build_overlapped_fill(checked_lib, name, pipeline):
+def test_checked_build_overlapped_fill(checked_lib, name, pipeline, dropless):
     cfg = wl.CONFIGS[name]
-    want, code0 = _run(cfg, False, pipeline=pipeline)
+    want, code0 = _run(cfg, dropless, pipeline=pipeline)
     assert code0 == 0
-    got, code = _run(cfg, False, checked_lib, pipeline=pipeline)
+    got, code = _run(cfg, dropless, checked_lib, pipeline=pipeline)
     assert code == 0, f"index check site {code} fired"
     for key, v in want.items():
         assert torch.equal(v.contiguous().view(torch.uint8), got[key].contiguous().view(torch.uint8)), key

@@ -17,8 +17,8 @@ def _host(inp):
     return {k: (v.float().cpu().numpy() if v is not None else None) for k, v in inp.items()}
 
 
-def run(cfg, inp):
-    m = PooledWaveMoE(cfg, inp, "cuda", dropless=True)
+def run(cfg, inp, pipeline=None):
+    m = PooledWaveMoE(cfg, inp, "cuda", dropless=True, pipeline=pipeline)
     m.forward(inp["x"].cuda())
     torch.cuda.synchronize()
     assert int(m.status.item()) == 0
@@ -28,9 +28,9 @@ def run(cfg, inp):
     return m
 
 
-def compare(cfg, inp):
+def compare(cfg, inp, pipeline=None):
     ref = O.layer_ragged(cfg, _host(inp))
-    m = run(cfg, inp)
+    m = run(cfg, inp, pipeline)
     idx = m.idx.cpu().numpy()
     assert np.abs(m.logits.cpu().numpy() - ref["logits"]).max() <= LOGIT_ATOL
     clear = ref["tie"] == 0
@@ -206,3 +206,38 @@ def test_ragged_bank_equals_capped_bank_without_caps():
     assert a.drop_stats()["kept"] == cfg.T * cfg.top_k
     assert torch.equal(a.c.view(torch.int16), b.c.view(torch.int16))
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def _state(m):
+    """Every output of the dropless layer's forward, as raw bits."""
+    out = {"out": m.out, "c": m.c, "a": m.a, "ypool": m.ypool, "slot_of": m.slot_of,
+           "drop": m.drop, "expert_rows": m.expert_rows, "expert_offsets": m.expert_offsets,
+           "expert_count": m.expert_count, "tags": m.pool_tags(), "payload": m.pool_payload()}
+    if m.bank is not None:
+        out["bank"] = m.bank
+    return {k: v.contiguous().view(torch.uint8).clone() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged-pair", "mid", "full"])
+def test_ragged_shared_schedule_equals_sequential(name):
+    """The pack inside the shared experts' gate/up launch: every output of the
+    dropless forward (decisions, row lists, offsets, pool rows and tags, the
+    bank, Y, c, a, out) bit for bit as with the pack as a kernel of its own."""
+    cfg = PAIR_SMALL if name == "ragged-pair" else wl.CONFIGS[name]
+    inp = wl.make_inputs(cfg, "cuda" if name == "full" else "cpu")
+    x = inp["x"].cuda()
+    got = {}
+    for pipe in (None, "shared"):
+        m = PooledWaveMoE(cfg, inp, "cuda", dropless=True, pipeline=pipe)
+        m.forward(x)
+        torch.cuda.synchronize()
+        assert int(m.status.item()) == 0 and m.drop_stats()["status"] == 0
+        got[pipe] = _state(m)
+        del m
+    for k, v in got[None].items():
+        assert torch.equal(v, got["shared"][k]), k
+
+
+def test_ragged_shared_schedule_parity():
+    m = compare(PAIR_SMALL, wl.make_inputs(PAIR_SMALL, "cpu"), pipeline="shared")
+    assert m.bank is not None
