@@ -213,6 +213,35 @@ def test_entry_points_validate_before_touching_the_gpu():
                                          n) == abi.MOE_EINVAL   # no a
     assert L.moe_balance_update_window(cp, fake, fake, fake, 0, fake, ctypes.c_float(1.0), fake,
                                        n) == abi.MOE_EINVAL   # window < 1
+    # the dropless entry points: null pointers, short scratch, a misaligned
+    # bank, the overlapped dispatch without a
+    pr = abi.plan_ragged(_small())
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert L.moe_dispatch_ragged(cp, *([n] * 3), sz(0), *([n] * 10)) == abi.MOE_EINVAL
+    assert L.moe_dispatch_ragged(cp, fake, fake, fake, sz(pr.ws_dispatch_bytes - 1),
+                                 *([fake] * 7), n, n) == abi.MOE_ENOSPC
+    assert L.moe_dispatch_ragged(cp, fake, fake, fake, sz(pr.ws_dispatch_bytes),
+                                 *([fake] * 7), odd, n) == abi.MOE_EINVAL
+    assert L.moe_dispatch_ragged_shared_overlap(cp, *([n] * 3), sz(0),
+                                                *([n] * 15)) == abi.MOE_EINVAL
+    assert L.moe_dispatch_ragged_shared_overlap(cp, fake, fake, fake,
+                                                sz(pr.ws_dispatch_bytes - 1), *([fake] * 7), n,
+                                                *([fake] * 5), n) == abi.MOE_ENOSPC
+    assert L.moe_dispatch_ragged_shared_overlap(cp, fake, fake, fake, sz(pr.ws_dispatch_bytes),
+                                                *([fake] * 7), n, *([fake] * 3), n, fake,
+                                                n) == abi.MOE_EINVAL   # no a
+    assert L.moe_expert_ffn_ragged(cp, fake, n, *([fake] * 7), sz(pr.ws_ffn_bytes - 1), fake,
+                                   fake, n) == abi.MOE_ENOSPC
+    assert L.moe_expert_ffn_ragged(cp, fake, odd, *([fake] * 7), sz(pr.ws_ffn_bytes), fake,
+                                   fake, n) == abi.MOE_EINVAL
+    # the backward refuses a bank that is not 16-byte aligned
+    args = abi.BackwardArgs()
+    for f, _ in abi.BackwardArgs._fields_:
+        if f not in ("ws_bytes", "expert_offsets", "bank"):
+            setattr(args, f, 1 << 20)
+    args.ws_bytes = 1 << 40
+    args.bank = (1 << 20) + 8
+    assert L.moe_layer_backward(cp, ctypes.byref(args), n) == abi.MOE_EINVAL
     bad = abi.make_config(_small(T=63))
     assert L.moe_plan(ctypes.byref(bad), ctypes.byref(abi.Plan())) == abi.MOE_EINVAL
 

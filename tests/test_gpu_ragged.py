@@ -241,3 +241,35 @@ def test_ragged_shared_schedule_equals_sequential(name):
 def test_ragged_shared_schedule_parity():
     m = compare(PAIR_SMALL, wl.make_inputs(PAIR_SMALL, "cpu"), pipeline="shared")
     assert m.bank is not None
+
+
+@pytest.mark.parametrize("kw", [dict(n_shared=0), dict(T=0)], ids=["no-shared", "no-tokens"])
+def test_ragged_shared_overlap_degenerate(kw):
+    """Without shared experts, or without tokens, the overlapped dropless
+    dispatch is the plain one: same outputs bit for bit."""
+    from moe_routing_capacity_gb300 import abi
+    cfg = wl.TINY.with_(seed=49, **kw)
+    inp = wl.make_inputs(cfg, "cpu")
+    x = inp["x"].cuda()
+    got = []
+    for overlap in (False, True):
+        m = PooledWaveMoE(cfg, inp, "cuda", dropless=True)
+        m.route_and_latent(x)
+        if overlap:
+            ns = cfg.n_shared
+            abi.dispatch_ragged_shared_overlap(
+                cfg, m.z, m.idx, m.ws_dispatch, m.pool, m.slot_of, m.drop, m.expert_offsets,
+                m.expert_rows, m.expert_count, m.stats, x if ns else None,
+                m.w["Wsg"] if ns else None, m.w["Wsu"] if ns else None, m.a if ns else None,
+                m.status, bank=m.bank)
+        else:
+            m.dispatch()
+        torch.cuda.synchronize()
+        assert int(m.status.item()) == 0 and m.drop_stats()["status"] == 0
+        st = {"offsets": m.expert_offsets, "count": m.expert_count, "stats": m.stats}
+        if cfg.T:
+            st.update(slot_of=m.slot_of, drop=m.drop, rows=m.expert_rows, tags=m.pool_tags(),
+                      payload=m.pool_payload(), bank=m.bank)
+        got.append({k: v.contiguous().view(torch.uint8).clone() for k, v in st.items()})
+    for k in got[0]:
+        assert torch.equal(got[0][k], got[1][k]), k
