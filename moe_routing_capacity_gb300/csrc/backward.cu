@@ -427,14 +427,20 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
     // its path is not open.
     ExpertGroups gl{};
     bool groups = false;
-    if (!rag && static_cast<size_t>(T) * L * 2 >= expert_pair_chunks_bytes(E, cr)) {
-        rc = expert_group_list(E, cr, a.expert_count, dz, &gl, st);
+    const size_t list_bytes = rag ? expert_pair_lists_bytes_ragged(E, g.pool_rows)
+                                  : expert_pair_chunks_bytes(E, cr);
+    if (static_cast<size_t>(T) * L * 2 >= list_bytes) {
+        rc = rag ? expert_group_list_ragged(E, g.pool_rows, a.expert_count, dz, &gl, st)
+                 : expert_group_list(E, cr, a.expert_count, dz, &gl, st);
         if (rc == MOE_OK)
             groups = true;
         else if (rc != MOE_EINVAL)
             return rc;
     }
-    rc = groups ? expert_dh_group(E, cr, L, H, dye, a.Wd, gl, dh, a.status, st) : MOE_EINVAL;
+    // dropless: the per-expert buffers' rows at the padded offsets poff
+    const int32_t* roff = rag ? poff : nullptr;
+    rc = groups ? expert_dh_group(E, cr, L, H, dye, a.Wd, gl, dh, a.status, st, roff, PE)
+                : MOE_EINVAL;
     if (rc == MOE_EINVAL) {
         std::memset(&q, 0, sizeof(q));   // dh = dY_e Wd_e (per-expert rows by TMA)
         q.a_mode = A_GROUPED; q.epi = EPI_BF16; q.bn = 256; q.b_mn = 1;
@@ -485,6 +491,27 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         } else if (rc != MOE_EINVAL) {
             return rc;
         }
+    } else {
+        // dropless: padded per-expert copies of X and of h (zero padding),
+        // then the SwiGLU backward over row groups from X
+        gather_ragged_kernel<<<E, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, eoff,
+                                                a.expert_count, poff, L, xe);
+        gather_ragged_kernel<<<E, 256, 0, st>>>(a.h, H, nullptr, eoff, a.expert_count, poff, H,
+                                                hp);
+        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+        trace_after(st, "bwd_gather_rows");
+        rc = groups ? expert_swiglu_bwd_group(E, cr, L, H, xe, a.Wg, a.Wu, dh, gl, dg, du,
+                                              a.status, st, roff, PE)
+                    : MOE_EINVAL;
+        if (rc == MOE_OK) {
+            grouped = true;
+            zero_pad_ragged_kernel<<<E, 256, 0, st>>>(dg, a.expert_count, poff, H);
+            zero_pad_ragged_kernel<<<E, 256, 0, st>>>(du, a.expert_count, poff, H);
+            if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+            trace_after(st, "bwd_zero_pad");
+        } else if (rc != MOE_EINVAL) {
+            return rc;
+        }
     }
     if (!grouped) {
         std::memset(&q, 0, sizeof(q));   // recompute g/u of the received rows, SwiGLU backward
@@ -501,7 +528,7 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         if ((rc = mm(q, "bwd_gemm_expert_swiglu"))) return rc;
     }
     rc = groups ? expert_dx_group(E, cr, L, H, dg, du, a.Wg, a.Wu, gl, a.expert_rows, dxp,
-                                  g.pool_rows, a.status, st)
+                                  g.pool_rows, a.status, st, roff, PE, rag ? eoff : nullptr)
                 : MOE_EINVAL;
     if (rc == MOE_EINVAL) {
         std::memset(&q, 0, sizeof(q));   // dX = dg Wg_e + du Wu_e, back to the pool rows
@@ -519,14 +546,6 @@ int launch_backward(const DispatchGeom& g, int d, int H, int Hs, int ns,
         if ((rc = mm(q, "bwd_gemm_dX"))) return rc;
     } else if (rc) {
         return rc;
-    }
-    if (rag) {   // padded per-expert copies of X and of h
-        gather_ragged_kernel<<<E, 256, 0, st>>>(a.pool, pool_pitch(L), a.expert_rows, eoff,
-                                                a.expert_count, poff, L, xe);
-        gather_ragged_kernel<<<E, 256, 0, st>>>(a.h, H, nullptr, eoff, a.expert_count, poff, H,
-                                                hp);
-        if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
-        trace_after(st, "bwd_gather_rows");
     }
     auto wgrad = [&](const uint16_t* A, int M, const uint16_t* B, int N, float* out, const char* nm) {
         std::memset(&q, 0, sizeof(q));   // out_e[M, N] = A_e^T B_e over the expert's rows

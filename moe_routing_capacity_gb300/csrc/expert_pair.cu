@@ -435,6 +435,9 @@ struct GParams {
     const int32_t* roff;       // dropless layout: expert e's rows start at row roff[e] of the
                                // flat bank, h and row list (mapX one group of all rows);
                                // NULL: at e * c_recv, mapX [E, c_recv, K]
+    const int32_t* rmoff;      // scatter, dropless backward: expert e's first entry in
+                               // rowmap, where it differs from roff[e] (padded operands,
+                               // unpadded row list); NULL: the same row as the operand
     int* status;
 };
 
@@ -558,16 +561,16 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                         tma_load_3d_pair(a_dst, &p.mapW, fb, m0, kx, t.e);
                         tma_load_3d_pair(a_dst + 8192, &p.mapW, fb, m0 + 64, kx, t.e);
                     }
+                    // rows: [E, c_recv] by expert, or (dropless) one flat group
+                    const int by = p.roff ? static_cast<int>(t.rbase) : 0;
+                    const int bz = p.roff ? 0 : t.e;
                     if (p.kseg) {
-                        tma_load_4d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kin, xrow0, t.e,
+                        tma_load_4d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kin, by + xrow0, bz,
                                          p.bseg[sg]);
                         if (h1)
                             tma_load_4d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kin,
-                                             xrow1, t.e, p.bseg[sg]);
+                                             by + xrow1, bz, p.bseg[sg]);
                     } else {
-                        // rows: [E, c_recv] by expert, or (dropless) one flat group
-                        const int by = p.roff ? static_cast<int>(t.rbase) : 0;
-                        const int bz = p.roff ? 0 : t.e;
                         tma_load_3d_pair(b_dst, &p.mapX[h0 / XHSTEP - 1], fb, kx, by + xrow0, bz);
                         if (h1)
                             tma_load_3d_pair(b_dst + h0 * XBK * 2, &p.mapX[h1 / XHSTEP - 1], fb, kx,
@@ -694,8 +697,9 @@ __global__ void __launch_bounds__(GTHREADS, 1) expert_group_kernel(const __grid_
                     const int rr = 32 * b + lane;
                     prow[i] = -1;
                     if (pos < nblk && rr < t.rows) {
-                        const int r = static_cast<int>(t.rbase) + t.row0 + rr;
-                        const int v = p.rowmap ? p.rowmap[r] : r;
+                        const int rm = p.rmoff ? p.rmoff[t.e] : static_cast<int>(t.rbase);
+                        const int r = rm + t.row0 + rr;
+                        const int v = p.rowmap ? p.rowmap[r] : static_cast<int>(t.rbase) + t.row0 + rr;
                         if (moe_check(v >= 0 && v < p.out_rows, 1102)) prow[i] = v;
                     }
                 }
@@ -1159,8 +1163,6 @@ int check_status_expert_pair() { return moe_check_read_reset(); }
 
 static size_t chunk_list_bytes(int E, int c_recv);
 
-static bool pair_widths(int sms, int E, int c_recv) { return sms >= 2 && E > 0 && c_recv > 0; }
-
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 size_t expert_pair_lists_bytes_ragged(int E, int64_t rows) {
@@ -1243,22 +1245,53 @@ int expert_group_list(int E, int c_recv, const int32_t* expert_count, void* ws, 
     return MOE_OK;
 }
 
+int expert_group_list_ragged(int E, int64_t rows, const int32_t* expert_count, void* ws,
+                             ExpertGroups* out, cudaStream_t st) {
+    if (E <= 0 || rows <= 0 || rows > INT32_MAX / 2 || (reinterpret_cast<uintptr_t>(ws) & 15))
+        return MOE_EINVAL;
+    const size_t nc = static_cast<size_t>(E) + static_cast<size_t>(rows / XCHUNK) + 1;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int4* chunks = reinterpret_cast<int4*>(w);
+    int4* groups = chunks + nc;
+    int32_t* counts = reinterpret_cast<int32_t*>(w + expert_pair_lists_bytes_ragged(E, rows) - 16);
+    chunk_list_kernel<<<1, 1024, 0, st>>>(expert_count, E, INT32_MAX, chunks, counts, groups,
+                                          counts + 1);
+    if (cudaPeekAtLastError() != cudaSuccess) return MOE_ECUDA;
+    trace_after(st, "bwd_build_groups");
+    out->groups = groups;
+    out->ngroups = counts + 1;
+    return MOE_OK;
+}
+
+// The rows of a backward product's operand X [K wide]: per expert [E, c_recv,
+// K], or (roff) one flat group of `rows`, expert e's from row roff[e].
+static int map_rows(CUtensorMap* m, const void* X, int K, int c_recv, int E,
+                    const int32_t* roff, int64_t rows, int i) {
+    if (roff)
+        return map3(m, X, K, rows, 1, K, static_cast<uint64_t>(rows) * K, XHSTEP * (i + 1));
+    return map3(m, X, K, c_recv, E, K, static_cast<uint64_t>(c_recv) * K, XHSTEP * (i + 1));
+}
+
+static bool bwd_rows_ok(int sms, int E, int c_recv, const int32_t* roff, int64_t rows) {
+    return sms >= 2 && E > 0 && (roff ? rows > 0 && rows <= INT32_MAX / 2 : c_recv > 0);
+}
+
 int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const uint16_t* Wd,
-                    const ExpertGroups& gl, uint16_t* dh, int32_t* status, cudaStream_t st) {
+                    const ExpertGroups& gl, uint16_t* dh, int32_t* status, cudaStream_t st,
+                    const int32_t* roff, int64_t rows) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
     if (rc) return rc;
-    if (!MOE_XPAIR_TM || !pair_widths(sms, E, c_recv) || H % 256 || L % 64 || !al16(dye) ||
-        !al16(Wd) || !al16(dh))
+    if (!MOE_XPAIR_TM || !bwd_rows_ok(sms, E, c_recv, roff, rows) || H % 256 || L % 64 ||
+        !al16(dye) || !al16(Wd) || !al16(dh))
         return MOE_EINVAL;
     GParams g;
     std::memset(&g, 0, sizeof(g));
     // Wd [E, L, H] is the weights' [K, M]: MN-major boxes of 64 units x 64 K
     if ((rc = map3(&g.mapW, Wd, H, L, E, H, static_cast<uint64_t>(L) * H, 64))) return rc;
     for (int i = 0; i < XNMAP; ++i)
-        if ((rc = map3(&g.mapX[i], dye, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
-                       XHSTEP * (i + 1))))
-            return rc;
+        if ((rc = map_rows(&g.mapX[i], dye, L, c_recv, E, roff, rows, i))) return rc;
+    g.roff = roff;
     g.groups = gl.groups;
     g.ngroups = gl.ngroups;
     g.n_mb = H / 256;
@@ -1266,8 +1299,8 @@ int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const 
     g.c_recv = c_recv;
     g.out = dh;
     g.ldo = H;
-    g.rowmap = nullptr;   // dh in the per-expert layout
-    g.out_rows = static_cast<long long>(E) * c_recv;
+    g.rowmap = nullptr;   // dh in the operand's row layout
+    g.out_rows = roff ? rows : static_cast<long long>(E) * c_recv;
     g.a_mn = 1;
     g.status = status;
     return launch_group<EPI_SCATTER>(g, sms, st, "bwd_gemm_dh");
@@ -1276,20 +1309,19 @@ int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const 
 int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
                             const uint16_t* Wg, const uint16_t* Wu, const uint16_t* dh,
                             const ExpertGroups& gl, uint16_t* dg, uint16_t* du, int32_t* status,
-                            cudaStream_t st) {
+                            cudaStream_t st, const int32_t* roff, int64_t rows) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
     if (rc) return rc;
-    if (!MOE_XPAIR_TM || !pair_widths(sms, E, c_recv) || L % 256 || H % 128 || !al16(xe) ||
-        !al16(dh) || !al16(dg) || !al16(du))
+    if (!MOE_XPAIR_TM || !bwd_rows_ok(sms, E, c_recv, roff, rows) || L % 256 || H % 128 ||
+        !al16(xe) || !al16(dh) || !al16(dg) || !al16(du))
         return MOE_EINVAL;
     GParams g;
     std::memset(&g, 0, sizeof(g));
     if (map_gateup_il(&g.mapW, Wg, Wu, E, H, L, &g.gate_hi) != MOE_OK) return MOE_EINVAL;
     for (int i = 0; i < XNMAP; ++i)
-        if ((rc = map3(&g.mapX[i], xe, L, c_recv, E, L, static_cast<uint64_t>(c_recv) * L,
-                       XHSTEP * (i + 1))))
-            return rc;
+        if ((rc = map_rows(&g.mapX[i], xe, L, c_recv, E, roff, rows, i))) return rc;
+    g.roff = roff;
     g.groups = gl.groups;
     g.ngroups = gl.ngroups;
     g.n_mb = H / 128;
@@ -1307,12 +1339,13 @@ int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
 int expert_dx_group(int E, int c_recv, int L, int H, const uint16_t* dg, const uint16_t* du,
                     const uint16_t* Wg, const uint16_t* Wu, const ExpertGroups& gl,
                     const int32_t* expert_rows, uint16_t* dxpool, int64_t pool_rows,
-                    int32_t* status, cudaStream_t st) {
+                    int32_t* status, cudaStream_t st, const int32_t* roff, int64_t rows,
+                    const int32_t* rmoff) {
     int dev, sms;
     int rc = current_device(&dev, &sms);
     if (rc) return rc;
-    if (!MOE_XPAIR_TM || !pair_widths(sms, E, c_recv) || L % 256 || H % 64 || !al16(dg) ||
-        !al16(du) || !al16(Wg) || !al16(Wu) || !al16(dxpool))
+    if (!MOE_XPAIR_TM || !bwd_rows_ok(sms, E, c_recv, roff, rows) || L % 256 || H % 64 ||
+        !al16(dg) || !al16(du) || !al16(Wg) || !al16(Wu) || !al16(dxpool))
         return MOE_EINVAL;
     GParams g;
     std::memset(&g, 0, sizeof(g));
@@ -1327,11 +1360,14 @@ int expert_dx_group(int E, int c_recv, int L, int H, const uint16_t* dg, const u
     if ((rc = map4(&g.mapW, wlo, L, H, E, 2, static_cast<uint64_t>(L) * 2,
                    static_cast<uint64_t>(H) * L * 2, wg < wu ? wu - wg : wg - wu, 64)))
         return rc;
+    const uint64_t xrows = roff ? static_cast<uint64_t>(rows) : static_cast<uint64_t>(c_recv);
+    const uint64_t xgroups = roff ? 1u : static_cast<uint64_t>(E);
     for (int i = 0; i < XNMAP; ++i)
-        if ((rc = map4(&g.mapX[i], xlo, H, c_recv, E, 2, static_cast<uint64_t>(H) * 2,
-                       static_cast<uint64_t>(c_recv) * H * 2, xg < xu ? xu - xg : xg - xu,
-                       XHSTEP * (i + 1))))
+        if ((rc = map4(&g.mapX[i], xlo, H, xrows, xgroups, 2, static_cast<uint64_t>(H) * 2,
+                       xrows * H * 2, xg < xu ? xu - xg : xg - xu, XHSTEP * (i + 1))))
             return rc;
+    g.roff = roff;
+    g.rmoff = rmoff;
     g.aseg[0] = wg < wu ? 0 : 1;
     g.aseg[1] = 1 - g.aseg[0];
     g.bseg[0] = xg < xu ? 0 : 1;

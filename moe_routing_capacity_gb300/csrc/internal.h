@@ -220,6 +220,11 @@ int expert_ffn_pair_ragged(int E, int64_t rows, int L, int H, const uint16_t* ba
 //    untouched);
 //  expert_dx_group: dX = dg Wg_e + du Wu_e, each row to its pool row of
 //    dxpool (expert_rows).
+// The dropless layout (roff given, c_recv ignored): the per-expert buffers
+// are flat [rows, .] with expert e's rows from row roff[e] (padded to whole
+// 64-row blocks), the group list from expert_group_list_ragged (its `ws`:
+// expert_pair_lists_bytes_ragged(E, kept rows) bytes), and dX's row list is
+// the flat one with expert e's entries from rmoff[e].
 // Each returns MOE_EINVAL, having enqueued nothing, when the widths or the
 // tensors do not allow its path (the caller then takes the grouped GEMM).
 struct ExpertGroups {
@@ -228,16 +233,21 @@ struct ExpertGroups {
 };
 int expert_group_list(int E, int c_recv, const int32_t* expert_count, void* ws, ExpertGroups* out,
                       cudaStream_t stream);
+int expert_group_list_ragged(int E, int64_t rows, const int32_t* expert_count, void* ws,
+                             ExpertGroups* out, cudaStream_t stream);
 int expert_dh_group(int E, int c_recv, int L, int H, const uint16_t* dye, const uint16_t* Wd,
-                    const ExpertGroups& groups, uint16_t* dh, int32_t* status, cudaStream_t stream);
+                    const ExpertGroups& groups, uint16_t* dh, int32_t* status, cudaStream_t stream,
+                    const int32_t* roff = nullptr, int64_t rows = 0);
 int expert_swiglu_bwd_group(int E, int c_recv, int L, int H, const uint16_t* xe,
                             const uint16_t* Wg, const uint16_t* Wu, const uint16_t* dh,
                             const ExpertGroups& groups, uint16_t* dg, uint16_t* du,
-                            int32_t* status, cudaStream_t stream);
+                            int32_t* status, cudaStream_t stream, const int32_t* roff = nullptr,
+                            int64_t rows = 0);
 int expert_dx_group(int E, int c_recv, int L, int H, const uint16_t* dg, const uint16_t* du,
                     const uint16_t* Wg, const uint16_t* Wu, const ExpertGroups& groups,
                     const int32_t* expert_rows, uint16_t* dxpool, int64_t pool_rows,
-                    int32_t* status, cudaStream_t stream);
+                    int32_t* status, cudaStream_t stream, const int32_t* roff = nullptr,
+                    int64_t rows = 0, const int32_t* rmoff = nullptr);
 
 // Tile list {expert, m0} of the grouped expert GEMMs, from the expert counts.
 // Checked builds: the site code recorded by each translation unit's index
