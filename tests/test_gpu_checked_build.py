@@ -75,16 +75,17 @@ def test_checked_build_overlapped_fill(checked_lib, name, pipeline, dropless):
         assert torch.equal(v.contiguous().view(torch.uint8), got[key].contiguous().view(torch.uint8)), key
 
 
-def test_checked_build_full_workload(checked_lib):
+@pytest.mark.parametrize("dropless", [False, True], ids=["capped", "dropless"])
+def test_checked_build_full_workload(checked_lib, dropless):
     """The full workload in the bench's schedule (pool fill inside the shared
     gate/up, the expert products on CTA pairs over row groups, and the
-    backward's grouped expert products), forward and backward, through the
-    checked build: no index check fires and every output and gradient equals
-    the normal build's bit for bit."""
+    backward's grouped expert products), forward and backward, in either
+    layout, through the checked build: no index check fires and every output
+    and gradient equals the normal build's bit for bit."""
     cfg = wl.CONFIGS["full"]
-    want, code0 = _run(cfg, False, pipeline="shared")
+    want, code0 = _run(cfg, dropless, pipeline="shared")
     assert code0 == 0
-    got, code = _run(cfg, False, checked_lib, pipeline="shared")
+    got, code = _run(cfg, dropless, checked_lib, pipeline="shared")
     assert code == 0, f"index check site {code} fired"
     for key in list(want):
         a, b = want.pop(key), got.pop(key)
