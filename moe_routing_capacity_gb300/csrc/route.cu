@@ -1,5 +1,6 @@
 // route.cu -- the bandwidth- and latency-bound steps of the layer:
-//   router top-k        one warp per token, warp-shuffle arg-max rounds
+//   router top-k        one warp per token, rounds of warp max / min
+//                       reductions over each lane's earliest entries
 //   dispatch            sender slots and receiver ranks (warp-aggregated
 //                       counting, deterministic prefix sums), drops counted,
 //                       payload rows packed into the fixed pools
@@ -20,40 +21,19 @@ namespace moe {
 
 constexpr float kTieEps = 1e-4f;
 
-// Routing order: the larger logit first, the lower expert id on equal logits.
-__device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb) {
-    return va > vb || (va == vb && ea < eb);
-}
-
-// Bitonic sort of one (logit, id) pair per lane across the warp, in routing
-// order (lane 0 first); empty slots are (-inf, INT_MAX) and sort last.
-__device__ __forceinline__ void warp_sort_routing(float& v, int& e, int lane) {
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
-            const int oe = __shfl_xor_sync(0xffffffffu, e, stride);
-            // the lower lane of a pair keeps the earlier entry in the blocks
-            // sorted first-to-last (lane & size == 0), the later one otherwise
-            const bool keep_earlier = ((lane & size) == 0) == ((lane & stride) == 0);
-            if (keep_earlier ? ranks_before(ov, oe, v, e) : ranks_before(v, e, ov, oe)) {
-                v = ov;
-                e = oe;
-            }
-        }
-    }
+// The routing order on the logit alone as an unsigned key: a larger logit,
+// a larger key (-0 taken as +0, so equal logits give equal keys); 0 marks no
+// entry.  Among equal keys the lower expert id ranks first.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 template <int PER>   // logits per lane: E <= 32 * PER
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int64_t T,
-                                                   int E, int k, int32_t* __restrict__ idx,
-                                                   float* __restrict__ w,
-                                                   uint8_t* __restrict__ tie) {
-    __shared__ float cand_v[8][32];
-    __shared__ int cand_e[8][32];
+__global__ void __launch_bounds__(256, PER > 16 ? 2 : 5)
+    topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
+                int32_t* __restrict__ idx, float* __restrict__ w, uint8_t* __restrict__ tie) {
     const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float* row = logits + t * E;
@@ -63,96 +43,64 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
         const int e = lane + 32 * i;
         v[i] = e < E ? __ldg(row + e) : 0.0f;
     }
-
+    // This lane's entries are experts lane + 32 i.  Its two earliest in
+    // routing order: head (hk, hi, hv) and second (sk, si, sv); ids ascend
+    // with i, so a strict comparison keeps the lower id first on equal keys.
+    uint32_t hk = 0, sk = 0;
+    int hi = -1, si = -1;
+    float hv = 0.0f, sv = 0.0f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        if (lane + 32 * i < E) {
+            const uint32_t kk = logit_key(v[i]);
+            if (kk > hk) {
+                sk = hk; si = hi; sv = hv;
+                hk = kk; hi = i; hv = v[i];
+            } else if (kk > sk) {
+                sk = kk; si = i; sv = v[i];
+            }
+        }
+    }
+    // Rounds of selection across the warp: the largest head key, the lowest
+    // expert id among the heads that hold it; the winning lane moves on to its
+    // second entry, or rescans its unused ones after two wins.
     float my_v = 0.0f;   // lane j holds the j-th entry in routing order
     int my_e = 0;
     float next_v = 0.0f; // the (k+1)-th largest logit
+    uint32_t used = 0;   // bit i: entry i of this lane already ranked
     const int rounds = k < E ? k + 1 : k;   // entries to rank
-    bool ranked = false;
-    if (rounds <= 32) {
-        // Candidates: the n = rounds largest lane maxima are n distinct
-        // entries, so every entry of the top n ranks at or before the n-th
-        // of them, (tv, te).  Usually few entries do; gathered one per lane
-        // and sorted, they give the top n directly.
-        float lm = -INFINITY;
-        int le = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-            if (lane + 32 * i < E && (le == INT_MAX || v[i] > lm)) {
-                lm = v[i];
-                le = lane + 32 * i;
-            }
-        warp_sort_routing(lm, le, lane);
-        const float tv = __shfl_sync(0xffffffffu, lm, rounds - 1);
-        const int te = __shfl_sync(0xffffffffu, le, rounds - 1);
-        int cnt = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && (v[i] > tv || (v[i] == tv && e <= te))) ++cnt;
-        }
-        int incl = cnt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total <= 32) {   // warp-uniform
-            int pos = incl - cnt;
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && (v[i] > tv || (v[i] == tv && e <= te))) {
-                    cand_v[wib][pos] = v[i];
-                    cand_e[wib][pos] = e;
-                    ++pos;
-                }
-            }
-            __syncwarp();
-            float cv = lane < total ? cand_v[wib][lane] : -INFINITY;
-            int ce = lane < total ? cand_e[wib][lane] : INT_MAX;
-            warp_sort_routing(cv, ce, lane);
-            my_v = cv;
-            my_e = ce;
-            next_v = __shfl_sync(0xffffffffu, cv, k < 31 ? k : 31);
-            ranked = true;
-        }
-    }
-    // otherwise rounds of warp arg-max over the entries still in play
-    uint32_t live = 0;   // bit i: entry i still a candidate
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-        if (lane + 32 * i < E) live |= 1u << i;
-    for (int rd = 0; !ranked && rd < rounds; ++rd) {
-        // best live entry of this lane: largest value, lowest expert id on ties
-        float bv = -INFINITY;
-        int be = INT_MAX;
-        int bi = -1;
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-            if ((live >> i & 1u) && (bi < 0 || v[i] > bv)) {
-                bv = v[i];
-                be = lane + 32 * i;
-                bi = i;
-            }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
-                bv = ov;
-                be = oe;
-            }
-        }
+    for (int rd = 0; rd < rounds; ++rd) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t mine =
+            (hi >= 0 && hk == m) ? static_cast<uint32_t>(lane + 32 * hi) : 0xffffffffu;
+        const uint32_t we = __reduce_min_sync(0xffffffffu, mine);
+        const int wl = static_cast<int>(we & 31u);
+        const float vr = __shfl_sync(0xffffffffu, hv, wl);
         if (rd < k) {
             if (lane == rd) {
-                my_v = bv;
-                my_e = be;
+                my_v = vr;
+                my_e = static_cast<int>(we);
             }
-            if ((be & 31) == lane) live &= ~(1u << (be >> 5));
         } else {
-            next_v = bv;
+            next_v = vr;
+        }
+        if (lane == wl) {
+            used |= 1u << hi;
+            if (si >= 0) {
+                hk = sk; hi = si; hv = sv;
+                sk = 0; si = -1;
+            } else {
+                hk = 0; hi = -1;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    if (lane + 32 * i < E && !(used >> i & 1u)) {
+                        const uint32_t kk = logit_key(v[i]);
+                        if (kk > hk) {
+                            hk = kk; hi = i; hv = v[i];
+                        }
+                    }
+                }
+            }
         }
     }
     // softmax over the selected logits (lane 0 holds the largest)
