@@ -131,6 +131,24 @@ def test_plan_matches_oracle(cfg):
     assert p.ws_ffn_bytes >= p.h_offset_bytes + cfg.n_experts * p.c_recv * cfg.h_expert * 2
 
 
+@pytest.mark.parametrize("cfg", list(wl.CONFIGS.values()), ids=lambda c: c.name)
+def test_ragged_plan_leaves_room_for_the_row_groups(cfg):
+    """The dropless plan: a pool of exactly T*k rows, and below h room for
+    the expert products' work lists in the worst case, whatever the routing:
+    the gathered path's 128-row tiles (at most rows/128 + E entries of 8
+    bytes) and the row-group path's lists (every expert's chunks of at most
+    256 rows and groups of at most 416: at most E + rows/256 + 1 and
+    E + rows/416 + 1 entries of 16 bytes, plus two counters)."""
+    p = abi.plan_ragged(cfg)
+    rows, E = cfg.T * cfg.top_k, cfg.n_experts
+    assert p.pool_rows == rows and p.c_send == 0 and p.c_recv == 0
+    tiles = (rows // 128 + E) * 8 + 16
+    lists = (E + rows // 256 + 1 + E + rows // 416 + 1) * 16 + 16
+    assert p.h_offset_bytes >= max(tiles, lists)
+    assert p.h_offset_bytes % 16 == 0
+    assert p.ws_ffn_bytes >= p.h_offset_bytes + rows * cfg.h_expert * 2
+
+
 def _small(**kw):
     base = dict(name="s", T=64, d_model=64, d_latent=32, n_experts=12, n_ranks=2, top_k=2,
                 n_waves=3, n_shared=1, h_expert=32, h_shared=32)
