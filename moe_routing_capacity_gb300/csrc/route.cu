@@ -23,7 +23,10 @@ constexpr float kTieEps = 1e-4f;
 
 // The routing order on the logit alone as an unsigned key: a larger logit,
 // a larger key (-0 taken as +0, so equal logits give equal keys); 0 marks no
-// entry.  Among equal keys the lower expert id ranks first.
+// entry.  Among equal keys the lower expert id ranks first.  Logits are
+// finite here (a product of finite inputs); a NaN ranks where its bits put
+// it, the one whose bits are all ones as no entry, and routing with NaN
+// logits is left unspecified, as for the oracle.
 __device__ __forceinline__ uint32_t logit_key(float v) {
     const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
