@@ -9,7 +9,6 @@ rows, experts with none).  The bank itself is compared with the pool rows
 it groups, and the whole layer with the path that gathers each expert's
 rows from the pool, for each pool-fill schedule.
 """
-import numpy as np
 import pytest
 import torch
 

@@ -236,7 +236,6 @@ def test_host_pipeline_matches_forward():
 def test_route_project_equals_separate_calls(E):
     """The one-pass router + latent projection gives the same bits as
     moe_router_topk followed by moe_latent_proj."""
-    from moe_routing_capacity_gb300 import abi
     cfg = wl.TINY.with_(seed=28, T=640, n_ranks=4, d_model=384, d_latent=512, n_experts=E,
                         top_k=8 if E > 48 else 4, bias_kind="zipf")
     inp = wl.make_inputs(cfg, "cuda")
