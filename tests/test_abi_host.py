@@ -186,6 +186,16 @@ def test_plan_rejects_invalid(kw):
     assert ei.value.code == abi.MOE_EINVAL
 
 
+def test_plans_refuse_rows_past_32_bit_indices():
+    """Row lists and slots are int32: a batch whose pool would hold more rows
+    than they index is refused by both layouts' plans."""
+    cfg = _small(T=2**28, top_k=8)
+    for fn in (abi.plan, abi.plan_ragged):
+        with pytest.raises(abi.MoeError) as ei:
+            fn(cfg)
+        assert ei.value.code == abi.MOE_EINVAL
+
+
 def test_entry_points_validate_before_touching_the_gpu():
     """Null pointers and short scratch are refused on the host, before any
     device call (these run without a GPU)."""
